@@ -1,0 +1,124 @@
+"""Plant plausible mistakes in a copy of the oracle (on the CPU) and check that
+the pin battery catches every one of them.
+
+Each mutant is the oracle's C source with one textual change (a dropped term, a
+wrong sign or index, a swapped operand), compiled to a temporary library.  The
+merge operator's mutants replace ``oracle.merge`` for the duration of a check.
+"""
+import os
+import subprocess
+import tempfile
+
+import numpy as np
+import pytest
+
+import oracle
+from tests import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "tree_attn_oracle.c")
+
+C_MUTANTS = {
+    "gqa_index_modulo": ("const int g = h / G;", "const int g = h % Hkv;"),
+    "dropped_scale": ("s[t] = scale * acc;", "s[t] = acc;"),
+    "value_from_keys": ("o[i] += w * widen(v, kv_dtype, kvoff + t * d + i);",
+                        "o[i] += w * widen(k, kv_dtype, kvoff + t * d + i);"),
+    "exp_sign_flipped": ("double w = exp(s[t] - M);", "double w = exp(M - s[t]);"),
+    "lse_missing_max": ("lse[bh] = M + log(L);", "lse[bh] = log(L);"),
+    "not_normalised": ("o[i] = o[i] / L;", "o[i] = o[i];"),
+    "first_token_dropped": ("double w = exp(s[t] - M);\n            L += w;",
+                            "double w = exp(s[t] - M);\n            if (t == 0) continue;\n            L += w;"),
+    "bf16_widen_shift": ("((uint32_t)bits) << 16", "((uint32_t)bits) << 15"),
+    "query_head_zero": ("widen(q, q_dtype, qoff + i) * widen(k, kv_dtype, kvoff + t * d + i)",
+                        "widen(q, q_dtype, (int64_t)b * Hq * d + i) * widen(k, kv_dtype, kvoff + t * d + i)"),
+    "partial_no_max_shift": ("double e = exp(s[t] - m);", "double e = exp(s[t]);"),
+    "partial_l_counts_tokens": ("l += e;", "l += 1.0;"),
+    "partial_value_from_keys": ("o[i] += e * widen(v, kv_dtype, kvoff + (t0 + t) * d + i);",
+                                "o[i] += e * widen(k, kv_dtype, kvoff + (t0 + t) * d + i);"),
+}
+
+
+def _build_mutant(name, old, new, tmpdir):
+    src = open(SRC).read()
+    assert src.count(old) >= 1, f"mutation site for {name} not found"
+    mutated = src.replace(old, new, 1)
+    path = os.path.join(tmpdir, f"mut_{name}.c")
+    with open(path, "w") as f:
+        f.write(mutated)
+    so = os.path.join(tmpdir, f"libmut_{name}.so")
+    subprocess.run(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", path, "-o", so, "-lm"], check=True,
+                   capture_output=True)
+    return oracle._load(so)
+
+
+def _battery_fails(lib_handle):
+    for check in pins.BATTERY:
+        try:
+            with np.errstate(all="ignore"):
+                check(lib_handle=lib_handle)
+        except (AssertionError, ValueError, FloatingPointError):
+            return check.__name__
+    return None
+
+
+@pytest.fixture(scope="module")
+def tmpdir():
+    with tempfile.TemporaryDirectory() as d:
+        yield d
+
+
+def test_unmutated_copy_passes(tmpdir):
+    lib = _build_mutant("none", "#include <math.h>", "#include <math.h>", tmpdir)
+    assert _battery_fails(lib) is None
+
+
+@pytest.mark.parametrize("name", sorted(C_MUTANTS))
+def test_c_mutant_is_caught(name, tmpdir):
+    old, new = C_MUTANTS[name]
+    lib = _build_mutant(name, old, new, tmpdir)
+    caught_by = _battery_fails(lib)
+    assert caught_by is not None, f"mutant {name} survived every pin"
+
+
+def _merge_beta_uses_a(a, b):
+    o_a, l_a, m_a = a
+    o_b, l_b, m_b = b
+    m_new = np.maximum(m_a, m_b)
+    m_ref = np.where(np.isneginf(m_new), 0.0, m_new)
+    alpha = np.exp(m_a - m_ref)
+    beta = np.exp(m_a - m_ref)
+    return alpha[..., None] * o_a + beta[..., None] * o_b, alpha * l_a + beta * l_b, m_new
+
+
+def _merge_min_instead_of_max(a, b):
+    o_a, l_a, m_a = a
+    o_b, l_b, m_b = b
+    m_new = np.minimum(m_a, m_b)
+    m_ref = np.where(np.isneginf(m_new), 0.0, m_new)
+    alpha = np.exp(np.where(np.isneginf(m_a), -np.inf, m_a - m_ref))
+    beta = np.exp(np.where(np.isneginf(m_b), -np.inf, m_b - m_ref))
+    return alpha[..., None] * o_a + beta[..., None] * o_b, alpha * l_a + beta * l_b, m_new
+
+
+def _merge_l_not_rescaled(a, b):
+    o_a, l_a, m_a = a
+    o_b, l_b, m_b = b
+    m_new = np.maximum(m_a, m_b)
+    m_ref = np.where(np.isneginf(m_new), 0.0, m_new)
+    alpha = np.exp(m_a - m_ref)
+    beta = np.exp(m_b - m_ref)
+    return alpha[..., None] * o_a + beta[..., None] * o_b, l_a + l_b, m_new
+
+
+@pytest.mark.parametrize("mutant", [_merge_beta_uses_a, _merge_min_instead_of_max, _merge_l_not_rescaled],
+                         ids=lambda f: f.__name__)
+def test_merge_mutant_is_caught(mutant, monkeypatch):
+    monkeypatch.setattr(oracle, "merge", mutant)
+    caught = None
+    for check in (pins.check_tree_shapes, pins.test_merge_closed_form):
+        try:
+            with np.errstate(all="ignore"):
+                check()
+        except AssertionError:
+            caught = check.__name__
+            break
+    assert caught is not None
