@@ -1,0 +1,420 @@
+#!/usr/bin/env python3
+"""Decode-attention benchmark: KV-cache HBM GB/s of one tree-attention decode step.
+
+One step = one ``tree_attn_decode`` call (split-KV kernel + tree combine) for
+one attention layer of the Llama-3.1-8B-shaped decode workload (B1, 32 query /
+8 KV heads, d128, 131072 BF16 KV tokens).  Metric: algorithmic KV bytes
+(every valid K and V element once) per second.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--num-splits P] [--kernel auto|mma|fma]
+
+Rank 0 prints one JSON line.  For N > 1 (torchrun, one rank per GPU) every
+rank runs its own replica -- the path has no cross-GPU step -- and the value is
+the bytes all ranks processed divided by the slowest rank's time.
+``--impl reference`` times the float64 CPU oracle instead, on rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode-attention KV HBM GB/s (fraction of GB300 peak) and us/step vs context len"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+
+# DRAM traffic per launch of the dominant kernel, from one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by kernel family and
+# workload, with the SHA-256 of the kernel source it was taken on; reported
+# only while that source is unchanged.  Summaries live in profiles/.
+NCU_TRAFFIC = {}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama3.1-8b-decode-layer")
+    ap.add_argument("--num-splits", type=int, default=0, help="<= 0: the library's heuristic")
+    ap.add_argument("--kernel", choices=["auto", "mma", "fma"], default="auto")
+    ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--ref-tokens", type=int, default=8192,
+                    help="reference arm: tokens per row in each step's sample")
+    return ap.parse_args(argv)
+
+
+# --------------------------------------------------------------- helpers
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash(kernel):
+    name = {"mma": "split_kv_mma.cu", "fma": "split_kv_fma.cuh"}[kernel]
+    h = hashlib.sha256()
+    for f in (name, "common.cuh", "emit.cuh"):
+        with open(os.path.join(ROOT, "softmax_tree_reduction_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled in the background."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id=None, interval_ms=50):
+        self.gpu_id = gpu_id
+        self.interval_ms = interval_ms
+        self.proc = None
+        self.lines = []
+        self.t_start = self.t_stop = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu=timestamp,{self.FIELDS}", "--format=csv,noheader,nounits",
+               f"-lms={self.interval_ms}"]
+        if self.gpu_id:
+            cmd.insert(1, f"--id={self.gpu_id}")
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._reader, daemon=True)
+        self.thread.start()
+
+    def _reader(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark_start(self):
+        self.t_start = time.time()
+
+    def mark_stop(self):
+        self.t_stop = time.time()
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for t, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append((t, parts))
+        inside = [r for r in rows if self.t_start and self.t_stop and self.t_start <= r[0] <= self.t_stop + 0.05]
+        used = inside if inside else rows[-3:]
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for _, p in used if num(p[1]) is not None]
+        mx = [num(p[2]) for _, p in used if num(p[2]) is not None]
+        reasons = set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for _, p in used:
+            for name, val in zip(names, p[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(used),
+                "samples_inside_timed_region": len(inside)}
+
+
+def gpu_uuid(device):
+    import torch
+    try:
+        u = torch.cuda.get_device_properties(device).uuid
+        s = str(u)
+        return s if s.startswith("GPU-") else "GPU-" + s
+    except Exception:
+        return None
+
+
+def max_over_ranks(value, world):
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------- CPU oracle
+def oracle_baseline(w, inp, target_s, max_s=30.0):
+    """Time the float64 oracle as it stands on the host's cores.
+
+    Sample: the whole workload (every head, every token), repeated until
+    ``target_s`` seconds of CPU work; value = KV bytes processed / time."""
+    import oracle
+    threads = oracle.max_threads()
+    kv_bytes = w.kv_bytes(inp["seqlens"])
+    reps, elapsed = 0, 0.0
+    while elapsed < target_s and elapsed < max_s:
+        t0 = time.perf_counter()
+        oracle.attention(inp["q"], inp["k"], inp["v"], inp["seqlens"], w.softmax_scale, threads=threads)
+        elapsed += time.perf_counter() - t0
+        reps += 1
+        if reps == 1 and elapsed * 2 > max_s:
+            break
+    return {"value": kv_bytes * reps / elapsed / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"whole workload ({w.name}), {reps} pass(es), {elapsed:.1f} s, float64 C oracle "
+                      f"with {threads} OpenMP threads on {os.cpu_count()} host cores"}
+
+
+# ------------------------------------------------------------ our GPU arm
+def run_ours(args, rank, world, local):
+    import torch
+    import softmax_tree_reduction_gb300 as ta
+    from softmax_tree_reduction_gb300 import workloads
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    ta.load()
+    w = workloads.WORKLOADS[args.workload]
+    inp = workloads.make_inputs(w)
+    kv_bytes = w.kv_bytes(inp["seqlens"])
+    dev = {k: inp[k].cuda() for k in ("q", "k", "v", "seqlens")}
+    # two copies of the KV cache, alternated step to step (each far larger than L2)
+    copies = [dev, {"q": dev["q"], "k": dev["k"].clone(), "v": dev["v"].clone(), "seqlens": dev["seqlens"]}]
+    shape = ta.make_shape(dev["q"], dev["k"])
+    P = args.num_splits if args.num_splits > 0 else ta.tree_attn_pick_splits(shape)
+    kernel_used = args.kernel
+    if kernel_used == "auto":
+        kernel_used = "mma" if (w.kv_dtype == torch.bfloat16 and w.q_dtype == torch.bfloat16
+                                and w.group <= 8) else "fma"
+    B, Hq, d = dev["q"].shape
+    out = torch.empty(B, Hq, d, dtype=torch.float32, device="cuda")
+    lse = torch.empty(B, Hq, dtype=torch.float32, device="cuda")
+    nbytes = ta.tree_attn_workspace_bytes(shape, P)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(i, events=None):
+        c = copies[i & 1]
+        ta.tree_attn_decode(c["q"], c["k"], c["v"], c["seqlens"], out=out, lse=lse, num_splits=P,
+                            workspace=ws, kernel=args.kernel, split_events=events)
+
+    for i in range(max(args.warmup, 3)):
+        step(i)
+    torch.cuda.synchronize()
+    assert ta.tree_attn_get_device_error() == 0
+
+    sampler = ClockSampler(gpu_uuid(local))
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.3)
+    # ---- timed region A: the API call as a user makes it
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.mark_start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark_stop()
+    barrier(world)
+    elapsed_ms = e0.elapsed_time(e1)
+    # ---- timed region B: same steps, split-KV kernel bracketed by events
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        step(i, events=evs[i])
+    torch.cuda.synchronize()
+    barrier(world)
+    split_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    if rank == 0:
+        time.sleep(0.1)
+        sampler.stop()
+    assert ta.tree_attn_get_device_error() == 0
+
+    elapsed_ms = max_over_ranks(elapsed_ms, world)
+    split_ms_max = max_over_ranks(split_ms, world)
+    ms_per_step = elapsed_ms / args.steps
+    value = kv_bytes * args.steps * world / (elapsed_ms / 1e3) / 1e9
+
+    # ---- end to end: pinned host inputs -> device, decode, results -> host
+    e2e = None
+    if not args.no_e2e:
+        n_e2e = max(1, min(args.e2e_steps, args.steps))
+        host = {k: inp[k].pin_memory() for k in ("q", "k", "v", "seqlens")}
+        dbuf = {k: torch.empty_like(host[k], device="cuda") for k in host}
+        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = h_out.numel() * 4 + h_lse.numel() * 4
+
+        def e2e_step():
+            for k in host:
+                dbuf[k].copy_(host[k], non_blocking=True)
+            ta.tree_attn_decode(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["seqlens"], out=out, lse=lse,
+                                num_splits=P, workspace=ws, kernel=args.kernel)
+            h_out.copy_(out, non_blocking=True)
+            h_lse.copy_(lse, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(a.elapsed_time(b), world)
+        e2e = {"value": kv_bytes * n_e2e * world / (e2e_ms / 1e3) / 1e9, "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": n_e2e,
+               "ms_per_step": e2e_ms / n_e2e}
+        del dbuf, host
+
+    if rank != 0:
+        return None
+    peak, peak_kind = load_peaks()
+    achieved = kv_bytes / (split_ms_max / 1e3) / 1e9
+    tr = NCU_TRAFFIC.get((kernel_used, w.name))
+    traffic = None
+    if tr and tr.get("src_sha256") == kernel_source_hash(kernel_used) and tr.get("num_splits") == P:
+        traffic = tr["bytes_per_launch"]
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = oracle_baseline(w, inp, args.cpu_seconds)
+    return {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
+        "us_per_step": round(ms_per_step * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) Llama-shaped KV cache; no weights or datasets)",
+        "config": {"workload": f"{w.name}: {w.description}", "batch": w.batch,
+                   "seq_len": int(max(inp['seqlens'])), "num_q_heads": w.num_q_heads,
+                   "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "num_splits": P,
+                   "kernel": kernel_used, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2: two 512 MiB K+V copies alternated step to step"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "kernel": f"split_kv_{kernel_used}", "kernel_us": round(split_ms_max * 1e3, 3),
+                     "bytes_per_launch": int(kv_bytes), "traffic": traffic,
+                     "frac_of_8TBps": round(achieved / 8000.0, 4)},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": int(args.steps * (2 if P > 1 else 1)),
+        "clocks": sampler.summary(),
+    }
+
+
+# ------------------------------------------------------- reference arm
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import numpy as np
+    import torch
+    import oracle
+    from softmax_tree_reduction_gb300 import workloads
+
+    w = workloads.WORKLOADS[args.workload]
+    inp = workloads.make_inputs(w)
+    n = min(args.ref_tokens, int(inp["seqlens"].min()))
+    sub_len = torch.full_like(inp["seqlens"], n)
+    kv_bytes = w.kv_bytes(sub_len)
+    threads = oracle.max_threads()
+    k_sub = inp["k"][:, :, :n].contiguous()
+    v_sub = inp["v"][:, :, :n].contiguous()
+
+    def step():
+        oracle.attention(inp["q"], k_sub, v_sub, sub_len, w.softmax_scale, threads=threads)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    value = kv_bytes * args.steps / el / 1e9
+    sample = (f"first {n} tokens of every (row, head) of {w.name} per step; float64 C oracle, "
+              f"{threads} OpenMP threads on {os.cpu_count()} host cores")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) Llama-shaped KV cache)",
+        "config": {"workload": f"{w.name}: {w.description}", "batch": w.batch, "seq_len": n,
+                   "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        res = run_ours(args, rank, world, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        if dist.is_initialized():
+            dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,191 @@
+/*
+ * tree_attn.h -- C ABI of libtreeattn.so: exact single-query (decode) softmax
+ * attention over a long KV cache, computed Tree Attention's way on one GPU.
+ *
+ * The method (web pages on Tree Attention, arXiv:2408.04093; "Tree Attention
+ * Guide: Topology-Aware LLM Decoding"):
+ *  - "Local Independent Partial Attention": the sequence axis is cut into P
+ *    slices; each slice i yields a partial state T_i = (o_i, l_i, m_i) with
+ *    m_i = max(q K_i^T), l_i = sum exp(q K_i^T - m_i),
+ *    o_i = sum exp(q K_i^T - m_i) V_i (logits scaled by 1/sqrt(d), as in the
+ *    page's implementation listing).
+ *  - "The Tree Reduction Merge Operator": states merge by
+ *    m = max(m_A, m_B), alpha = exp(m_A - m), beta = exp(m_B - m),
+ *    l = alpha l_A + beta l_B, o = alpha o_A + beta o_B; the operator is
+ *    associative and commutative, so any tree shape gives the same result.
+ *  - Root normalisation: O = o_root / l_root.
+ * Here the P slices become P thread blocks per (batch row, KV head) and the
+ * tree is an on-chip reduction (lanes -> warps -> blocks) instead of a
+ * reduction across devices.
+ *
+ * Conventions for every entry point:
+ *  - All pointers named "device" are CUDA device (or managed) memory owned by
+ *    the caller.  The library allocates nothing and frees nothing.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Work is enqueued asynchronously on it; no call synchronises
+ *    except tree_attn_get_device_error.
+ *  - Argument errors are detected on the host, before anything is enqueued,
+ *    and returned as a negative ta_status.  A launch failure returns
+ *    TA_ERR_CUDA.  Invalid data found on the device (a sequence length outside
+ *    [0, max_seqlen]) never traps: the affected rows become NaN and an error
+ *    word is set, reported by tree_attn_get_device_error.
+ *  - Outputs `out` and `lse` are fully overwritten; inputs are never written.
+ */
+#ifndef TREE_ATTN_H
+#define TREE_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TREE_ATTN_VERSION 1
+
+/* Status codes (0 = success). */
+typedef enum {
+    TA_OK = 0,
+    TA_ERR_NULL = -1,          /* a required pointer is NULL */
+    TA_ERR_ALIGN = -2,         /* a pointer or stride breaks the 16-byte rule */
+    TA_ERR_SHAPE = -3,         /* unsupported or inconsistent sizes */
+    TA_ERR_DTYPE = -4,         /* unsupported dtype combination */
+    TA_ERR_SPLITS = -5,        /* num_splits outside [1, TA_MAX_SPLITS] */
+    TA_ERR_WORKSPACE = -6,     /* workspace missing or too small */
+    TA_ERR_CUDA = -7,          /* a CUDA runtime/driver call failed */
+    TA_ERR_DEVICE_DATA = -8,   /* device found a sequence length outside [0, max_seqlen] */
+    TA_ERR_DEVICE_TIMEOUT = -9 /* a bounded on-chip wait gave up (outputs are NaN) */
+} ta_status;
+
+/* Element types. */
+typedef enum {
+    TA_F32 = 0,   /* IEEE binary32 */
+    TA_BF16 = 1   /* bfloat16 (upper half of a binary32) */
+} ta_dtype;
+
+/* Largest accepted num_splits. */
+#define TA_MAX_SPLITS 4096
+
+/* Sizes and layout of one decode-attention call.
+ *
+ *  q       [batch][num_q_heads][head_dim], dense, dtype q_dtype.
+ *  k_cache, v_cache: element (b, g, t, i) of KV head g, token t, channel i is
+ *          at  b*kv_stride_b + g*kv_stride_h + t*kv_stride_t + i  (elements,
+ *          dtype kv_dtype).  All three strides 0 selects the dense layout
+ *          [batch][num_kv_heads][max_seqlen][head_dim].  A token-major layout
+ *          [batch][max_seqlen][num_kv_heads][head_dim] is expressed with
+ *          kv_stride_t = num_kv_heads*head_dim, kv_stride_h = head_dim.
+ *          Every stride times the element size must be a multiple of 16 bytes.
+ *  Query head h reads KV head h / (num_q_heads / num_kv_heads).
+ */
+typedef struct {
+    int32_t batch;          /* B >= 1 */
+    int32_t num_q_heads;    /* Hq >= 1 */
+    int32_t num_kv_heads;   /* Hkv >= 1, Hq % Hkv == 0, Hq/Hkv in {1,2,4,8,16} */
+    int32_t head_dim;       /* d: 64 or 128 */
+    int32_t max_seqlen;     /* S: cache capacity per sequence, tokens (>= 1) */
+    int32_t q_dtype;        /* ta_dtype */
+    int32_t kv_dtype;       /* ta_dtype */
+    float scale;            /* logit scale; 0 selects 1/sqrt(head_dim) */
+    int64_t kv_stride_b;    /* elements; see above */
+    int64_t kv_stride_h;
+    int64_t kv_stride_t;
+} ta_shape;
+
+/* Kernel family for the per-slice step. */
+typedef enum {
+    TA_KERNEL_AUTO = 0,  /* tensor-core path when it applies, else FMA */
+    TA_KERNEL_FMA = 1,   /* FP32 FMA on CUDA cores; every dtype combination */
+    TA_KERNEL_MMA = 2    /* BF16 tensor-core mma; needs q and kv in BF16, Hq/Hkv <= 8 */
+} ta_kernel;
+
+/* Optional per-call settings (pass NULL for defaults). */
+typedef struct {
+    int32_t kernel;            /* ta_kernel */
+    int32_t reserved;          /* must be 0 */
+    void *split_start_event;   /* optional cudaEvent_t recorded on `stream` just before the
+                                  per-slice kernel is enqueued */
+    void *split_end_event;     /* optional cudaEvent_t recorded just after it (before the combine) */
+} ta_options;
+
+/* Text for a status code (static storage; never NULL). */
+const char *tree_attn_status_string(int status);
+
+/* Library ABI version (TREE_ATTN_VERSION). */
+int tree_attn_version(void);
+
+/* Validate a shape (sizes, dtypes, strides) without touching any pointer.
+ * Returns TA_OK or the error tree_attn_decode would return for it. */
+int tree_attn_check_shape(const ta_shape *shape);
+
+/* Bytes of device workspace tree_attn_decode needs for `num_splits` slices:
+ * partial o [B][Hq][P][d], partial m and l [B][Hq][P], FP32, each region
+ * 256-byte aligned.  0 when num_splits == 1 (no partial states are stored)
+ * and 0 for an invalid shape or num_splits (see tree_attn_check_shape). */
+size_t tree_attn_workspace_bytes(const ta_shape *shape, int num_splits);
+
+/* Split-count heuristic ("Core Innovation 1": the P-way partition of the
+ * sequence axis).  Picks P so that the B*Hkv*P thread blocks fill the GPU's
+ * `num_sms` multiprocessors in whole waves with slices of >= 256 tokens,
+ * trading the combine's cost against wave quantisation.  `host_seqlens`
+ * ([batch], host memory) may be NULL, in which case every row is assumed to
+ * hold max_seqlen tokens.  num_sms <= 0 queries the current CUDA device.
+ * Returns P in [1, TA_MAX_SPLITS], or a negative ta_status. */
+int tree_attn_pick_splits(const ta_shape *shape, const int32_t *host_seqlens, int num_sms);
+
+/* One decode-attention step: out[b][h][:] = softmax(scale q K^T) V over the
+ * tokens [0, seqlens[b]) of row b, and lse[b][h] = log sum exp of the scaled
+ * logits (natural log).  The sequence axis of each (b, KV head) is cut into
+ * `num_splits` contiguous slices; every slice yields a partial state and the
+ * states are merged by the operator above (partial m in natural-log units),
+ * then normalised.  A row with seqlens[b] == 0 gives out = 0, lse = -inf.
+ *
+ *  shape       sizes/layout (host memory, read during the call only)
+ *  q, k_cache, v_cache   device, 16-byte aligned; strides as in ta_shape
+ *  seqlens     device int32 [batch], each in [0, max_seqlen]
+ *  out         device float32 [batch][num_q_heads][head_dim]
+ *  lse         device float32 [batch][num_q_heads], or NULL to skip it
+ *  num_splits  P >= 1, or <= 0 to use tree_attn_pick_splits(shape, NULL, 0)
+ *  workspace   device, >= tree_attn_workspace_bytes(shape, P) bytes, 16-byte
+ *              aligned; may be NULL when P == 1.  Contents on entry are
+ *              ignored; calls sharing one workspace must be ordered on the GPU.
+ *  stream      cudaStream_t as void*
+ */
+int tree_attn_decode(const ta_shape *shape, const void *q, const void *k_cache,
+                     const void *v_cache, const int32_t *seqlens, float *out, float *lse,
+                     int num_splits, void *workspace, size_t workspace_bytes, void *stream);
+
+/* tree_attn_decode with per-call options (kernel family, timing events). */
+int tree_attn_decode_ex(const ta_shape *shape, const void *q, const void *k_cache,
+                        const void *v_cache, const int32_t *seqlens, float *out, float *lse,
+                        int num_splits, void *workspace, size_t workspace_bytes,
+                        const ta_options *options, void *stream);
+
+/* The tree combine on its own ("The Tree Reduction Merge Operator" applied to
+ * P states per (b, h), then the root normalisation O = o / l):
+ *
+ *  partial_o  device float32 [batch][num_q_heads][num_splits][head_dim],
+ *             unnormalised numerators
+ *  partial_m  device float32 [batch][num_q_heads][num_splits], maxima in
+ *             natural-log units of the scaled logits (-inf for an empty slice)
+ *  partial_l  device float32 [batch][num_q_heads][num_splits], denominators
+ *             (0 for an empty slice)
+ *  out        device float32 [batch][num_q_heads][head_dim]
+ *  lse        device float32 [batch][num_q_heads] or NULL
+ * Only batch, num_q_heads and head_dim of `shape` are used; head_dim must be
+ * 64 or 128.  All pointers 16-byte aligned.  All-empty rows give out = 0,
+ * lse = -inf. */
+int tree_attn_combine(const ta_shape *shape, const float *partial_o, const float *partial_m,
+                      const float *partial_l, int num_splits, float *out, float *lse,
+                      void *stream);
+
+/* Synchronise `stream`, then read and clear the current device's error word.
+ * Returns TA_OK, TA_ERR_DEVICE_DATA or TA_ERR_DEVICE_TIMEOUT (or TA_ERR_CUDA
+ * when the synchronisation itself fails). */
+int tree_attn_get_device_error(void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TREE_ATTN_H */

@@ -1,1 +1,11 @@
-"""GB300-native split-KV decode attention with an intra-GPU log-sum-exp tree combine."""
+"""GB300-native split-KV decode attention with an on-chip log-sum-exp tree combine.
+
+The computation lives in ``libtreeattn.so`` (C ABI in ``include/tree_attn.h``);
+this package only binds it (``_binding``), builds it (``build``) and draws
+seeded synthetic inputs (``workloads``).
+"""
+from ._binding import (  # noqa: F401
+    LIB_PATH, TA_BF16, TA_F32, TA_KERNEL, TA_MAX_SPLITS, TaOptions, TaShape, TreeAttnError, load,
+    make_shape, tree_attn_check_shape, tree_attn_combine, tree_attn_decode,
+    tree_attn_get_device_error, tree_attn_pick_splits, tree_attn_status_string,
+    tree_attn_version, tree_attn_workspace_bytes)

@@ -1,0 +1,239 @@
+"""ctypes binding of libtreeattn.so (include/tree_attn.h), same names as the C ABI.
+
+Argument marshalling only: tensors are checked and turned into pointers,
+outputs and workspace are allocated with torch when the caller passes none,
+and the call is enqueued on torch's current CUDA stream.  Every step of the
+computation runs in the library's CUDA kernels; there is no CPU fallback, and
+a missing library raises immediately.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtreeattn.so")
+
+TA_OK = 0
+TA_F32, TA_BF16 = 0, 1
+TA_KERNEL = {"auto": 0, "fma": 1, "mma": 2}
+TA_MAX_SPLITS = 4096
+
+_EXPORTS = ["tree_attn_status_string", "tree_attn_version", "tree_attn_check_shape",
+            "tree_attn_workspace_bytes", "tree_attn_pick_splits", "tree_attn_decode",
+            "tree_attn_decode_ex", "tree_attn_combine", "tree_attn_get_device_error"]
+
+
+class TaShape(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("max_seqlen", ctypes.c_int32), ("q_dtype", ctypes.c_int32),
+                ("kv_dtype", ctypes.c_int32), ("scale", ctypes.c_float),
+                ("kv_stride_b", ctypes.c_int64), ("kv_stride_h", ctypes.c_int64),
+                ("kv_stride_t", ctypes.c_int64)]
+
+
+class TaOptions(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("split_start_event", ctypes.c_void_p), ("split_end_event", ctypes.c_void_p)]
+
+
+class TreeAttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {tree_attn_status_string(status)} (status {status})")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libtreeattn.so once; raise if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with "
+                               "`python -m softmax_tree_reduction_gb300.build`")
+        lib = ctypes.CDLL(path)
+        P, SP, I32, SZ = ctypes.c_void_p, ctypes.POINTER(TaShape), ctypes.c_int, ctypes.c_size_t
+        lib.tree_attn_status_string.argtypes = [I32]
+        lib.tree_attn_status_string.restype = ctypes.c_char_p
+        lib.tree_attn_version.argtypes = []
+        lib.tree_attn_version.restype = I32
+        lib.tree_attn_check_shape.argtypes = [SP]
+        lib.tree_attn_check_shape.restype = I32
+        lib.tree_attn_workspace_bytes.argtypes = [SP, I32]
+        lib.tree_attn_workspace_bytes.restype = SZ
+        lib.tree_attn_pick_splits.argtypes = [SP, P, I32]
+        lib.tree_attn_pick_splits.restype = I32
+        lib.tree_attn_decode.argtypes = [SP, P, P, P, P, P, P, I32, P, SZ, P]
+        lib.tree_attn_decode.restype = I32
+        lib.tree_attn_decode_ex.argtypes = [SP, P, P, P, P, P, P, I32, P, SZ,
+                                            ctypes.POINTER(TaOptions), P]
+        lib.tree_attn_decode_ex.restype = I32
+        lib.tree_attn_combine.argtypes = [SP, P, P, P, I32, P, P, P]
+        lib.tree_attn_combine.restype = I32
+        lib.tree_attn_get_device_error.argtypes = [P]
+        lib.tree_attn_get_device_error.restype = I32
+        _lib = lib
+        return lib
+
+
+def _dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.float32:
+        return TA_F32
+    if dt == torch.bfloat16:
+        return TA_BF16
+    raise TypeError(f"unsupported dtype {dt}; use float32 or bfloat16")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def make_shape(q: torch.Tensor, k_cache: torch.Tensor, scale: Optional[float] = None) -> TaShape:
+    """Shape descriptor for q [B, Hq, d] and a K/V cache viewed as [B, Hkv, S, d]
+    (any strides with a unit channel stride)."""
+    if q.dim() != 3 or k_cache.dim() != 4:
+        raise ValueError("q must be [B, Hq, d] and k_cache [B, Hkv, S, d]")
+    B, Hq, d = q.shape
+    Bk, Hkv, S, dk = k_cache.shape
+    if Bk != B or dk != d:
+        raise ValueError("q and k_cache disagree on batch or head_dim")
+    if k_cache.stride(3) != 1:
+        raise ValueError("k_cache channels must be contiguous")
+    sb, sh, st, _ = k_cache.stride()
+    dense = k_cache.is_contiguous()
+    return TaShape(B, Hq, Hkv, d, S, _dtype_code(q.dtype), _dtype_code(k_cache.dtype),
+                   float(scale or 0.0), 0 if dense else sb, 0 if dense else sh, 0 if dense else st)
+
+
+def tree_attn_status_string(status: int) -> str:
+    return load().tree_attn_status_string(int(status)).decode()
+
+
+def tree_attn_version() -> int:
+    return int(load().tree_attn_version())
+
+
+def tree_attn_check_shape(shape: TaShape) -> int:
+    return int(load().tree_attn_check_shape(ctypes.byref(shape)))
+
+
+def tree_attn_workspace_bytes(shape: TaShape, num_splits: int) -> int:
+    return int(load().tree_attn_workspace_bytes(ctypes.byref(shape), int(num_splits)))
+
+
+def tree_attn_pick_splits(shape: TaShape, host_seqlens=None, num_sms: int = 0) -> int:
+    arr = None
+    if host_seqlens is not None:
+        arr = torch.as_tensor(host_seqlens, dtype=torch.int32).cpu().contiguous()
+        if arr.numel() != shape.batch:
+            raise ValueError("host_seqlens must have one entry per batch row")
+    r = int(load().tree_attn_pick_splits(ctypes.byref(shape), _ptr(arr), int(num_sms)))
+    if r < 0:
+        raise TreeAttnError(r, "tree_attn_pick_splits")
+    return r
+
+
+def _check_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("tensors must live on a CUDA device")
+
+
+def tree_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                     seqlens: torch.Tensor, out: Optional[torch.Tensor] = None,
+                     lse: Optional[torch.Tensor] = None, num_splits: int = 0,
+                     workspace: Optional[torch.Tensor] = None, kernel: str = "auto",
+                     scale: Optional[float] = None, stream=None, split_events=None,
+                     want_lse: bool = True):
+    """Decode attention through the C ABI; returns (out [B,Hq,d] fp32, lse [B,Hq] fp32 or None).
+
+    ``num_splits`` <= 0 uses the library's heuristic (picked on the host so the
+    workspace can be sized).  ``split_events`` = (start, end) torch.cuda.Event
+    pair recorded around the per-slice kernel.
+    """
+    lib = load()
+    _check_cuda(q, k_cache, v_cache, seqlens, out, lse, workspace)
+    if v_cache.shape != k_cache.shape or v_cache.stride() != k_cache.stride():
+        raise ValueError("k_cache and v_cache must have the same shape and strides")
+    if v_cache.dtype != k_cache.dtype:
+        raise ValueError("k_cache and v_cache must share a dtype")
+    if not q.is_contiguous():
+        raise ValueError("q must be contiguous")
+    if seqlens.dtype != torch.int32 or not seqlens.is_contiguous():
+        raise ValueError("seqlens must be a contiguous int32 tensor")
+    shape = make_shape(q, k_cache, scale)
+    B, Hq, d = q.shape
+    if out is None:
+        out = torch.empty(B, Hq, d, dtype=torch.float32, device=q.device)
+    if lse is None and want_lse:
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
+    P = int(num_splits)
+    if P <= 0:
+        P = tree_attn_pick_splits(shape)
+    nbytes = tree_attn_workspace_bytes(shape, P)
+    if nbytes and workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = _stream(stream)
+    if kernel == "auto" and split_events is None:
+        rc = lib.tree_attn_decode(ctypes.byref(shape), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                  _ptr(seqlens), _ptr(out), _ptr(lse), P, _ptr(workspace),
+                                  ws_bytes, st)
+    else:
+        opts = TaOptions(TA_KERNEL[kernel], 0, None, None)
+        if split_events is not None:
+            opts.split_start_event = split_events[0].cuda_event
+            opts.split_end_event = split_events[1].cuda_event
+        rc = lib.tree_attn_decode_ex(ctypes.byref(shape), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                     _ptr(seqlens), _ptr(out), _ptr(lse), P, _ptr(workspace),
+                                     ws_bytes, ctypes.byref(opts), st)
+    if rc != TA_OK:
+        raise TreeAttnError(rc, "tree_attn_decode")
+    return out, lse
+
+
+def tree_attn_combine(partial_o: torch.Tensor, partial_m: torch.Tensor, partial_l: torch.Tensor,
+                      out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                      stream=None):
+    """Tree combine of partial states [B,Hq,P,d] / [B,Hq,P] (fp32) -> (out, lse)."""
+    lib = load()
+    _check_cuda(partial_o, partial_m, partial_l, out, lse)
+    for t in (partial_o, partial_m, partial_l):
+        if t.dtype != torch.float32 or not t.is_contiguous():
+            raise ValueError("partial states must be contiguous float32")
+    B, Hq, P, d = partial_o.shape
+    if partial_m.shape != (B, Hq, P) or partial_l.shape != (B, Hq, P):
+        raise ValueError("partial_m / partial_l must be [B, Hq, P]")
+    if out is None:
+        out = torch.empty(B, Hq, d, dtype=torch.float32, device=partial_o.device)
+    if lse is None:
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=partial_o.device)
+    shape = TaShape(B, Hq, 1, d, 1, TA_F32, TA_F32, 0.0, 0, 0, 0)
+    rc = lib.tree_attn_combine(ctypes.byref(shape), _ptr(partial_o), _ptr(partial_m),
+                               _ptr(partial_l), P, _ptr(out), _ptr(lse), _stream(stream))
+    if rc != TA_OK:
+        raise TreeAttnError(rc, "tree_attn_combine")
+    return out, lse
+
+
+def tree_attn_get_device_error(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error status."""
+    return int(load().tree_attn_get_device_error(_stream(stream)))

@@ -1,0 +1,431 @@
+// C ABI of libtreeattn.so (declared in include/tree_attn.h): argument
+// validation, the split-count heuristic, TMA descriptors, kernel dispatch and
+// the device error word.  Every step of the computation runs in the kernels
+// of this library; this file only checks, plans and enqueues.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <queue>
+#include <vector>
+
+#include "../../include/tree_attn.h"
+#include "kernels.h"
+
+namespace {
+
+using ta::Geometry;
+
+__device__ int g_error_word;  // bits ta::kErrBadSeqlen | ta::kErrTimeout
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool ready = false;
+    int num_sms = 0;
+    int* err = nullptr;  // device address of g_error_word on this device
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+// Per-device set-up, once, with that device current.
+int device_state(DeviceState** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return TA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState& s = g_dev[dev];
+    if (!s.ready) {
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return TA_ERR_CUDA;
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return TA_ERR_CUDA;
+        s.num_sms = sms;
+        s.err = static_cast<int*>(p);
+        s.ready = true;
+    }
+    *out = &s;
+    return TA_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int elem_bytes(int dtype) { return dtype == TA_BF16 ? 2 : 4; }
+
+struct Strides {
+    int64_t b, h, t;
+};
+
+// Validate the shape; on success fill the resolved KV strides (elements).
+int check_shape(const ta_shape* s, Strides* st) {
+    if (!s) return TA_ERR_NULL;
+    if (s->batch < 1 || s->num_q_heads < 1 || s->num_kv_heads < 1 || s->max_seqlen < 1)
+        return TA_ERR_SHAPE;
+    if (s->num_q_heads % s->num_kv_heads != 0) return TA_ERR_SHAPE;
+    const int G = s->num_q_heads / s->num_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return TA_ERR_SHAPE;
+    if (s->head_dim != 64 && s->head_dim != 128) return TA_ERR_SHAPE;
+    if ((s->q_dtype != TA_F32 && s->q_dtype != TA_BF16) ||
+        (s->kv_dtype != TA_F32 && s->kv_dtype != TA_BF16))
+        return TA_ERR_DTYPE;
+    if (!(s->scale >= 0.f) || std::isinf(s->scale)) return TA_ERR_SHAPE;
+    Strides r;
+    const int64_t d = s->head_dim, S = s->max_seqlen, H = s->num_kv_heads;
+    if (s->kv_stride_b == 0 && s->kv_stride_h == 0 && s->kv_stride_t == 0) {
+        r.t = d;
+        r.h = S * d;
+        r.b = H * S * d;
+    } else {
+        r.b = s->kv_stride_b;
+        r.h = s->kv_stride_h;
+        r.t = s->kv_stride_t;
+        if (r.b <= 0 || r.h <= 0 || r.t <= 0) return TA_ERR_SHAPE;
+    }
+    const int64_t es = elem_bytes(s->kv_dtype);
+    const int64_t lim = int64_t(1) << 40;
+    for (int64_t x : {r.b, r.h, r.t}) {
+        if ((x * es) % 16 != 0) return TA_ERR_ALIGN;
+        if (x * es >= lim) return TA_ERR_SHAPE;
+    }
+    if (st) *st = r;
+    return TA_OK;
+}
+
+int resolve_kernel(const ta_shape* s, int requested) {
+    const bool mma_ok = s->q_dtype == TA_BF16 && s->kv_dtype == TA_BF16 &&
+                        (s->num_q_heads / s->num_kv_heads) <= 8;
+    switch (requested) {
+        case TA_KERNEL_AUTO: return mma_ok ? TA_KERNEL_MMA : TA_KERNEL_FMA;
+        case TA_KERNEL_FMA: return TA_KERNEL_FMA;
+        case TA_KERNEL_MMA: return mma_ok ? static_cast<int>(TA_KERNEL_MMA) : static_cast<int>(TA_ERR_DTYPE);
+        default: return TA_ERR_SHAPE;
+    }
+}
+
+Geometry geometry_of(const ta_shape* s, int kernel) {
+    return kernel == TA_KERNEL_MMA ? ta::mma_geometry(s->head_dim)
+                                   : ta::fma_geometry(elem_bytes(s->kv_dtype), s->head_dim);
+}
+
+// Resident thread blocks per SM of each kernel family (shared memory bound:
+// the MMA kernel's ring is ~145 KB at d = 128 and ~105 KB at d = 64; the FMA
+// kernel's ~113 KB with 288 threads of ~170 registers).
+int blocks_per_sm(const ta_shape* s, int kernel) {
+    if (kernel == TA_KERNEL_MMA) return s->head_dim == 64 ? 2 : 1;
+    return 1;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct WsLayout {
+    size_t o, m, l, total;
+};
+
+WsLayout workspace_layout(const ta_shape* s, int P) {
+    const size_t rows = static_cast<size_t>(s->batch) * s->num_q_heads * P;
+    WsLayout w;
+    w.o = 0;
+    w.m = round256(rows * s->head_dim * sizeof(float));
+    w.l = w.m + round256(rows * sizeof(float));
+    w.total = w.l + round256(rows * sizeof(float));
+    return w;
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// ------------------------------------------------------------ heuristic
+// Estimated step time for P slices, in units of "one block streaming one
+// token": a block's fixed cost (pipeline fill, epilogue) is worth
+// kBlockCost tokens; a second (combine) launch kBlockCost more plus its
+// traffic (partials written and read back) spread over the whole GPU.
+constexpr double kBlockCost = 256.0;
+
+double estimate(const ta_shape* s, const std::vector<int64_t>& lens, bool uniform, int P,
+                int tile, int slots) {
+    const int Hkv = s->num_kv_heads;
+    const double bytes_per_token = 2.0 * s->head_dim * elem_bytes(s->kv_dtype);
+    double comb = 0.0;
+    if (P > 1) {
+        const double comb_bytes =
+            2.0 * s->batch * s->num_q_heads * static_cast<double>(P) * (s->head_dim + 2) * 4;
+        comb = kBlockCost + comb_bytes / bytes_per_token / slots;
+    }
+    if (uniform) {
+        const int64_t N = lens[0];
+        const int64_t c = ceil_div(ceil_div(N, P), tile) * tile;
+        const int64_t blocks = static_cast<int64_t>(s->batch) * Hkv * P;
+        const int64_t waves = ceil_div(blocks, slots);
+        return static_cast<double>(waves) * (static_cast<double>(std::min<int64_t>(c, N)) + kBlockCost) +
+               comb;
+    }
+    // Ragged rows: list-schedule the blocks in launch order (slice fastest,
+    // then KV head, then batch row) onto the earliest free slot.
+    std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
+    for (int i = 0; i < slots; ++i) free_at.push(0.0);
+    double makespan = 0.0;
+    for (int b = 0; b < s->batch; ++b) {
+        const int64_t N = lens[b];
+        const int64_t c = N > 0 ? ceil_div(ceil_div(N, P), tile) * tile : 0;
+        for (int g = 0; g < Hkv; ++g) {
+            for (int p = 0; p < P; ++p) {
+                const int64_t a = c * p;
+                const int64_t len = (a >= N) ? 0 : std::min<int64_t>(c, N - a);
+                const double t = free_at.top() + static_cast<double>(len) + kBlockCost;
+                free_at.pop();
+                free_at.push(t);
+                makespan = std::max(makespan, t);
+            }
+        }
+    }
+    return makespan + comb;
+}
+
+int pick_splits_impl(const ta_shape* s, const int32_t* host_seqlens, int num_sms, int kernel) {
+    const int tile = geometry_of(s, kernel).tile_tokens;
+    const int slots = std::max(1, num_sms) * blocks_per_sm(s, kernel);
+    std::vector<int64_t> lens(s->batch);
+    bool uniform = true;
+    int64_t maxN = 0;
+    for (int b = 0; b < s->batch; ++b) {
+        int64_t n = host_seqlens ? host_seqlens[b] : s->max_seqlen;
+        n = std::max<int64_t>(0, std::min<int64_t>(n, s->max_seqlen));
+        lens[b] = n;
+        maxN = std::max(maxN, n);
+        if (n != lens[0]) uniform = false;
+    }
+    if (maxN == 0) return 1;
+    // slices of at least 256 tokens; no more than 64 waves of blocks
+    int64_t pmax = std::max<int64_t>(1, ceil_div(maxN, 256));
+    pmax = std::min<int64_t>(pmax, TA_MAX_SPLITS);
+    const int64_t rows = static_cast<int64_t>(s->batch) * s->num_kv_heads;
+    pmax = std::min<int64_t>(pmax, std::max<int64_t>(1, 64 * static_cast<int64_t>(slots) / rows));
+    int best = 1;
+    double best_t = estimate(s, lens, uniform, 1, tile, slots);
+    for (int P = 2; P <= pmax; ++P) {
+        const double t = estimate(s, lens, uniform, P, tile, slots);
+        if (t < best_t * (1.0 - 1e-9)) {
+            best_t = t;
+            best = P;
+        }
+    }
+    return best;
+}
+
+int encode_kv_map(CUtensorMap* map, const void* base, const ta_shape* s, const Strides& st,
+                  const Geometry& geo) {
+    auto fn = encode_fn();
+    if (!fn) return TA_ERR_CUDA;
+    const int64_t es = elem_bytes(s->kv_dtype);
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(s->head_dim),
+                          static_cast<cuuint64_t>(s->max_seqlen),
+                          static_cast<cuuint64_t>(s->num_kv_heads),
+                          static_cast<cuuint64_t>(s->batch)};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(st.t * es), static_cast<cuuint64_t>(st.h * es),
+                             static_cast<cuuint64_t>(st.b * es)};
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(geo.box_x),
+                         static_cast<cuuint32_t>(geo.tile_tokens), 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUresult r = fn(map,
+                          s->kv_dtype == TA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                          4, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          geo.swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? TA_OK : TA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* tree_attn_status_string(int status) {
+    switch (status) {
+        case TA_OK: return "ok";
+        case TA_ERR_NULL: return "a required pointer is NULL";
+        case TA_ERR_ALIGN: return "a pointer or stride is not 16-byte aligned";
+        case TA_ERR_SHAPE: return "unsupported or inconsistent sizes";
+        case TA_ERR_DTYPE: return "unsupported dtype combination";
+        case TA_ERR_SPLITS: return "num_splits outside [1, TA_MAX_SPLITS]";
+        case TA_ERR_WORKSPACE: return "workspace missing or too small";
+        case TA_ERR_CUDA: return "a CUDA call failed";
+        case TA_ERR_DEVICE_DATA: return "a sequence length outside [0, max_seqlen] was found on the device";
+        case TA_ERR_DEVICE_TIMEOUT: return "an on-chip wait timed out";
+        default: return "unknown status";
+    }
+}
+
+int tree_attn_version(void) { return TREE_ATTN_VERSION; }
+
+int tree_attn_check_shape(const ta_shape* shape) { return check_shape(shape, nullptr); }
+
+size_t tree_attn_workspace_bytes(const ta_shape* shape, int num_splits) {
+    if (check_shape(shape, nullptr) != TA_OK) return 0;
+    if (num_splits <= 1 || num_splits > TA_MAX_SPLITS) return 0;
+    return workspace_layout(shape, num_splits).total;
+}
+
+int tree_attn_pick_splits(const ta_shape* shape, const int32_t* host_seqlens, int num_sms) {
+    const int rc = check_shape(shape, nullptr);
+    if (rc != TA_OK) return rc;
+    if (num_sms <= 0) {
+        DeviceState* ds = nullptr;
+        const int r = device_state(&ds);
+        if (r != TA_OK) return r;
+        num_sms = ds->num_sms;
+    }
+    const int kernel = resolve_kernel(shape, TA_KERNEL_AUTO);
+    return pick_splits_impl(shape, host_seqlens, num_sms, kernel);
+}
+
+int tree_attn_decode_ex(const ta_shape* shape, const void* q, const void* k_cache,
+                        const void* v_cache, const int32_t* seqlens, float* out, float* lse,
+                        int num_splits, void* workspace, size_t workspace_bytes,
+                        const ta_options* options, void* stream_ptr) {
+    Strides st;
+    int rc = check_shape(shape, &st);
+    if (rc != TA_OK) return rc;
+    if (!q || !k_cache || !v_cache || !seqlens || !out) return TA_ERR_NULL;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+        !aligned(seqlens, 4) || (lse && !aligned(lse, 4)))
+        return TA_ERR_ALIGN;
+    if (options && options->reserved != 0) return TA_ERR_SHAPE;
+    const int kernel = resolve_kernel(shape, options ? options->kernel : TA_KERNEL_AUTO);
+    if (kernel < 0) return kernel;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+
+    if (num_splits > TA_MAX_SPLITS) return TA_ERR_SPLITS;
+    auto check_ws = [&](int P) {
+        if (P <= 1) return static_cast<int>(TA_OK);
+        if (!workspace || workspace_bytes < workspace_layout(shape, P).total)
+            return static_cast<int>(TA_ERR_WORKSPACE);
+        if (!aligned(workspace, 16)) return static_cast<int>(TA_ERR_ALIGN);
+        return static_cast<int>(TA_OK);
+    };
+    // With an explicit split count every argument is checked before any CUDA call.
+    if (num_splits > 0 && (rc = check_ws(num_splits)) != TA_OK) return rc;
+
+    DeviceState* ds = nullptr;
+    rc = device_state(&ds);
+    if (rc != TA_OK) return rc;
+
+    int P = num_splits;
+    if (P <= 0) {
+        P = pick_splits_impl(shape, nullptr, ds->num_sms, kernel);
+        if (P < 1 || P > TA_MAX_SPLITS) return TA_ERR_SPLITS;
+        if ((rc = check_ws(P)) != TA_OK) return rc;
+    }
+    const WsLayout ws = workspace_layout(shape, P);
+
+    const Geometry geo = geometry_of(shape, kernel);
+    CUtensorMap tk, tv;
+    rc = encode_kv_map(&tk, k_cache, shape, st, geo);
+    if (rc != TA_OK) return rc;
+    rc = encode_kv_map(&tv, v_cache, shape, st, geo);
+    if (rc != TA_OK) return rc;
+
+    ta::SplitParams p;
+    std::memset(&p, 0, sizeof p);
+    p.q = q;
+    p.q_is_bf16 = shape->q_dtype == TA_BF16;
+    p.seqlens = seqlens;
+    p.err = ds->err;
+    p.B = shape->batch;
+    p.Hq = shape->num_q_heads;
+    p.Hkv = shape->num_kv_heads;
+    p.G = shape->num_q_heads / shape->num_kv_heads;
+    p.S = shape->max_seqlen;
+    p.P = P;
+    const float scale = shape->scale > 0.f ? shape->scale
+                                           : 1.0f / std::sqrt(static_cast<float>(shape->head_dim));
+    p.scale_log2 = scale * ta::kLog2e;
+    if (P == 1) {
+        p.out = out;
+        p.lse = lse;
+    } else {
+        char* w = static_cast<char*>(workspace);
+        p.part_o = reinterpret_cast<float*>(w + ws.o);
+        p.part_m = reinterpret_cast<float*>(w + ws.m);
+        p.part_l = reinterpret_cast<float*>(w + ws.l);
+    }
+
+    if (options && options->split_start_event &&
+        cudaEventRecord(static_cast<cudaEvent_t>(options->split_start_event), stream) != cudaSuccess)
+        return TA_ERR_CUDA;
+    cudaError_t e;
+    if (kernel == TA_KERNEL_MMA)
+        e = ta::launch_split_mma(shape->head_dim, tk, tv, p, stream);
+    else if (shape->kv_dtype == TA_BF16)
+        e = ta::launch_split_fma_bf16(shape->head_dim, tk, tv, p, stream);
+    else
+        e = ta::launch_split_fma_f32(shape->head_dim, tk, tv, p, stream);
+    if (e != cudaSuccess) return TA_ERR_CUDA;
+    if (options && options->split_end_event &&
+        cudaEventRecord(static_cast<cudaEvent_t>(options->split_end_event), stream) != cudaSuccess)
+        return TA_ERR_CUDA;
+    if (P > 1) {
+        e = ta::launch_combine(shape->head_dim, p.part_o, p.part_m, p.part_l, out, lse,
+                               shape->batch, shape->num_q_heads, P, /*dependent=*/true, stream);
+        if (e != cudaSuccess) return TA_ERR_CUDA;
+    }
+    return TA_OK;
+}
+
+int tree_attn_decode(const ta_shape* shape, const void* q, const void* k_cache,
+                     const void* v_cache, const int32_t* seqlens, float* out, float* lse,
+                     int num_splits, void* workspace, size_t workspace_bytes, void* stream) {
+    return tree_attn_decode_ex(shape, q, k_cache, v_cache, seqlens, out, lse, num_splits,
+                               workspace, workspace_bytes, nullptr, stream);
+}
+
+int tree_attn_combine(const ta_shape* shape, const float* partial_o, const float* partial_m,
+                      const float* partial_l, int num_splits, float* out, float* lse,
+                      void* stream) {
+    if (!shape) return TA_ERR_NULL;
+    if (shape->batch < 1 || shape->num_q_heads < 1) return TA_ERR_SHAPE;
+    if (shape->head_dim != 64 && shape->head_dim != 128) return TA_ERR_SHAPE;
+    if (num_splits < 1 || num_splits > TA_MAX_SPLITS) return TA_ERR_SPLITS;
+    if (!partial_o || !partial_m || !partial_l || !out) return TA_ERR_NULL;
+    if (!aligned(partial_o, 16) || !aligned(out, 16) || !aligned(partial_m, 4) ||
+        !aligned(partial_l, 4) || (lse && !aligned(lse, 4)))
+        return TA_ERR_ALIGN;
+    if (shape->batch > 65535) return TA_ERR_SHAPE;
+    const cudaError_t e =
+        ta::launch_combine(shape->head_dim, partial_o, partial_m, partial_l, out, lse, shape->batch,
+                           shape->num_q_heads, num_splits, false, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TA_OK : TA_ERR_CUDA;
+}
+
+int tree_attn_get_device_error(void* stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return TA_ERR_CUDA;
+    DeviceState* ds = nullptr;
+    const int rc = device_state(&ds);
+    if (rc != TA_OK) return rc;
+    int h = 0;
+    if (cudaMemcpy(&h, ds->err, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess) return TA_ERR_CUDA;
+    if (h == 0) return TA_OK;
+    const int zero = 0;
+    if (cudaMemcpy(ds->err, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+        return TA_ERR_CUDA;
+    return (h & ta::kErrTimeout) ? TA_ERR_DEVICE_TIMEOUT : TA_ERR_DEVICE_DATA;
+}
+
+}  // extern "C"

@@ -1,0 +1,157 @@
+// Device-side building blocks shared by the split-KV kernels and the combine:
+// mbarrier waits with a time limit, TMA tile loads, base-2 exponentials and
+// the parameter block every per-slice kernel receives.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ta {
+
+// Error bits of the device error word.
+constexpr int kErrBadSeqlen = 1;  // a sequence length outside [0, max_seqlen]
+constexpr int kErrTimeout = 2;    // a bounded barrier wait gave up
+
+// log2(e) and ln(2): the kernels evaluate exp(x) as 2^(x * log2 e).
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// A bounded wait gives up after this many nanoseconds of %globaltimer.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+// Parameters of one per-slice launch.  Grid: (num_splits, Hkv, B).
+struct SplitParams {
+    const void* q;          // [B][Hq][d]
+    int q_is_bf16;          // 1: q is BF16, 0: FP32
+    const int32_t* seqlens; // [B]
+    float* out;             // [B][Hq][d]      (num_splits == 1)
+    float* lse;             // [B][Hq] or null (num_splits == 1)
+    float* part_o;          // [B][Hq][P][d]   (num_splits > 1)
+    float* part_m;          // [B][Hq][P]
+    float* part_l;          // [B][Hq][P]
+    int* err;               // device error word
+    int B, Hq, Hkv, G, S, P;
+    float scale_log2;       // logit scale * log2(e)
+};
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile(
+        "{\n\t.reg .b64 st;\n\t"
+        "mbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, unsigned bytes) {
+    asm volatile(
+        "{\n\t.reg .b64 st;\n\t"
+        "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+        "r"(bytes)
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete.  Returns false (and
+// sets the timeout bit of *err) if that takes longer than kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity, int* err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer() - t0 > kWaitLimitNs) {
+            atomicOr(err, kErrTimeout);
+            return false;
+        }
+    }
+}
+
+// ------------------------------------------------------------------- TMA
+// 4-D tiled load (x = channel, y = token, z = KV head, w = batch row) into
+// shared memory, completing `bytes` of the mbarrier's transaction count.
+__device__ __forceinline__ void tma_load_4d(void* smem_dst, const CUtensorMap* map, int x, int y,
+                                            int z, int w, uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar)),
+        "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Named barrier over the consumer warps only (id 1; id 0 is __syncthreads).
+__device__ __forceinline__ void consumer_sync(int nthreads) {
+    asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
+// Programmatic dependent launch: let the combine grid start its launch early.
+__device__ __forceinline__ void allow_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void wait_primary() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Slice p of a row of N tokens: [p*c, min((p+1)*c, N)) with c = ceil(N/P)
+// rounded up to `align` tokens (so every slice but a row's last starts and
+// ends on a tile boundary).  Returns false for an empty slice.
+__device__ __forceinline__ bool slice_bounds(int N, int P, int p, int align, int& t0, int& t1) {
+    long long c = (static_cast<long long>(N) + P - 1) / P;
+    c = (c + align - 1) / align * align;
+    long long a = c * p, e = a + c;
+    if (a >= N) {
+        t0 = t1 = N;
+        return false;
+    }
+    t0 = static_cast<int>(a);
+    t1 = static_cast<int>(e < N ? e : N);
+    return true;
+}
+
+}  // namespace ta

@@ -1,0 +1,37 @@
+// Host-side view of the kernels: tile geometry and launchers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace ta {
+
+// How a split-KV kernel wants its K/V tiles delivered by TMA.
+struct Geometry {
+    int tile_tokens;   // tokens per pipeline stage (slices are cut at multiples of this)
+    int box_x;         // channels per TMA box (64 with 128-byte swizzle, else head_dim)
+    int swizzle128;    // 1: CU_TENSOR_MAP_SWIZZLE_128B, 0: no swizzle
+};
+
+Geometry mma_geometry(int head_dim);
+Geometry fma_geometry(int kv_elem_bytes, int head_dim);
+
+// Per-slice kernels.  Grid (P, Hkv, B); `tk`/`tv` are 4-D tensor maps over
+// (channel, token, KV head, batch row) with the box of the kernel's Geometry.
+cudaError_t launch_split_mma(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv,
+                             const SplitParams& p, cudaStream_t stream);
+cudaError_t launch_split_fma_bf16(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv,
+                                  const SplitParams& p, cudaStream_t stream);
+cudaError_t launch_split_fma_f32(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv,
+                                 const SplitParams& p, cudaStream_t stream);
+
+// Cross-block tree combine of P partial states per (b, h) plus normalisation.
+// With `dependent` set it is launched as a programmatic dependent of the
+// previous kernel on the stream (it waits for that grid before reading).
+cudaError_t launch_combine(int head_dim, const float* po, const float* pm, const float* pl,
+                           float* out, float* lse, int B, int Hq, int P, bool dependent,
+                           cudaStream_t stream);
+
+}  // namespace ta

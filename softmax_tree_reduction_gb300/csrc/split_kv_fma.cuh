@@ -1,0 +1,315 @@
+// Split-KV partial attention on the CUDA cores (FP32 FMA), for any dtype
+// combination.  Same block decomposition and pipeline as the tensor-core
+// kernel: grid (slice p, KV head g, batch row b); warp 0 streams K/V tiles
+// (unswizzled TMA boxes of tile x head_dim) into a ring of stages; the other
+// 8 warps compute.
+//
+// Consumer layout: a warp is split into 4 groups of 8 lanes; a group owns one
+// token per step and each lane holds head_dim/8 channels of it (16-byte
+// shared-memory reads, conflict-free).  q.k is a per-lane FMA chain reduced
+// over the group by three shuffles.  Every group keeps its own running state
+// (m, l, o) per head -- the leaves of the block's merge tree -- which are
+// merged inside the warp by shuffles and across warps in shared memory.
+// With G > 4 query heads per KV head the warps also split the heads.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "emit.cuh"
+#include "kernels.h"
+
+namespace ta {
+namespace fma_detail {
+
+template <typename KV, int D>
+struct FmaCfg {
+    static constexpr int kES = sizeof(KV);
+    static constexpr int kWarps = 8;                        // consumer warps
+    static constexpr int kRowBytes = D * kES;
+    static constexpr int kTile = 32768 / (2 * kRowBytes);   // tokens per stage (32 KB of K+V)
+    static constexpr int kKBytes = kTile * kRowBytes;
+    static constexpr int kStageBytes = 2 * kKBytes;
+    static constexpr int kStages = 3;
+    static constexpr int kCPL = kRowBytes / 128;            // 16-byte chunks per lane per row
+    static constexpr int kEPC = 16 / kES;                   // elements per chunk
+    static constexpr int kEPL = kCPL * kEPC;                // channels per lane (= D / 8)
+    static constexpr int kMergeFloats = kWarps * 4 * D + 2 * 64;
+    static constexpr int kBarBytes = 2 * kStages * 8 + 16;
+    static constexpr int kSmem = 1024 + kStages * kStageBytes + kMergeFloats * 4 + kBarBytes;
+    static constexpr int kThreads = 32 * (kWarps + 1);
+    static_assert(kTile >= 32, "a stage must hold at least 32 tokens");
+};
+
+template <typename KV>
+__device__ __forceinline__ void unpack16(const uint4& raw, float* f);
+
+template <>
+__device__ __forceinline__ void unpack16<__nv_bfloat16>(const uint4& raw, float* f) {
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+template <>
+__device__ __forceinline__ void unpack16<float>(const uint4& raw, float* f) {
+    f[0] = __uint_as_float(raw.x);
+    f[1] = __uint_as_float(raw.y);
+    f[2] = __uint_as_float(raw.z);
+    f[3] = __uint_as_float(raw.w);
+}
+
+template <typename KV, int D, int GC>
+__global__ void __launch_bounds__(FmaCfg<KV, D>::kThreads, 1)
+    split_kv_fma_kernel(const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const SplitParams p) {
+    using C = FmaCfg<KV, D>;
+    constexpr int EPL = C::kEPL, EPC = C::kEPC, CPL = C::kCPL;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* stages = smem;
+    float* mg_o = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes);
+    float* mg_m = mg_o + C::kWarps * 4 * D;   // [NTS][G] (NTS*G <= 64)
+    float* mg_l = mg_m + 64;
+    uint64_t* full = reinterpret_cast<uint64_t*>(mg_l + 64);
+    uint64_t* empty = full + C::kStages;
+    int* abort_flag = reinterpret_cast<int*>(empty + C::kStages);
+
+    const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    int N = p.seqlens[b];
+    const bool bad = (N < 0) || (N > p.S);
+    if (bad) {
+        if (threadIdx.x == 0) atomicOr(p.err, kErrBadSeqlen);
+        N = 0;
+    }
+    int t0, t1;
+    slice_bounds(N, p.P, split, C::kTile, t0, t1);
+    const int ntiles = (t1 - t0 + C::kTile - 1) / C::kTile;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], C::kWarps);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        if (lane == 0 && ntiles > 0) {
+            prefetch_tensormap(&tmK);
+            prefetch_tensormap(&tmV);
+            const uint64_t pol = l2_policy_evict_first();
+            int issued = 0;
+            for (int it = 0; it < ntiles; ++it) {
+                const int s = it % C::kStages;
+                if (it >= C::kStages &&
+                    !mbar_wait(&empty[s], ((it / C::kStages) - 1) & 1, p.err))
+                    break;
+                mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+                uint8_t* st = stages + s * C::kStageBytes;
+                const int y = t0 + it * C::kTile;
+                tma_load_4d(st, &tmK, 0, y, g, b, &full[s], pol);
+                tma_load_4d(st + C::kKBytes, &tmV, 0, y, g, b, &full[s], pol);
+                issued = it + 1;
+            }
+            for (int it = issued > C::kStages ? issued - C::kStages : 0; it < issued; ++it)
+                mbar_wait(&full[it % C::kStages], (it / C::kStages) & 1, p.err);
+        }
+        allow_dependents();
+        return;
+    }
+
+    // ---------------------------------------------------------- consumers
+    const int G = p.G;
+    const int NHC = G / GC;                  // head chunks (1, 2 or 4)
+    const int NTS = C::kWarps / NHC;         // token slices of a stage
+    const int cw = warp - 1;
+    const int hc = cw % NHC, ts = cw / NHC;
+    const int grp = lane >> 3, j = lane & 7;
+    const int tok_per_slice = C::kTile / NTS;
+    const int steps = tok_per_slice / 4;
+
+    // this lane's channels: chunk (j + 8c), element e -> (j + 8c) * EPC + e
+    float qf[GC][EPL];
+    {
+        const size_t qrow = static_cast<size_t>(b) * p.Hq + g * G + hc * GC;
+#pragma unroll
+        for (int i = 0; i < GC; ++i)
+#pragma unroll
+            for (int c = 0; c < CPL; ++c)
+#pragma unroll
+                for (int e = 0; e < EPC; ++e) {
+                    const size_t idx = (qrow + i) * D + (j + 8 * c) * EPC + e;
+                    const float qv =
+                        p.q_is_bf16
+                            ? __bfloat162float(static_cast<const __nv_bfloat16*>(p.q)[idx])
+                            : static_cast<const float*>(p.q)[idx];
+                    qf[i][c * EPC + e] = qv * p.scale_log2;
+                }
+    }
+    float m[GC], l[GC], o[GC][EPL];
+#pragma unroll
+    for (int i = 0; i < GC; ++i) {
+        m[i] = -INFINITY;
+        l[i] = 0.f;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) o[i][e] = 0.f;
+    }
+    bool timed_out = false;
+
+    for (int it = 0; it < ntiles; ++it) {
+        const int s = it % C::kStages;
+        if (!mbar_wait(&full[s], (it / C::kStages) & 1, p.err)) {
+            timed_out = true;
+            break;
+        }
+        const uint8_t* kst = stages + s * C::kStageBytes;
+        const uint8_t* vst = kst + C::kKBytes;
+        const int tile0 = t0 + it * C::kTile;
+        for (int step = 0; step < steps; ++step) {
+            const int row = ts * tok_per_slice + step * 4 + grp;
+            const bool valid = tile0 + row < t1;
+            float kf[EPL];
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) {
+                const uint4 raw =
+                    *reinterpret_cast<const uint4*>(kst + row * C::kRowBytes + (j + 8 * c) * 16);
+                unpack16<KV>(raw, &kf[c * EPC]);
+            }
+            float pv[GC];
+#pragma unroll
+            for (int i = 0; i < GC; ++i) {
+                float dot = 0.f;
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) dot = fmaf(qf[i][e], kf[e], dot);
+                dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+                dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+                dot += __shfl_xor_sync(0xffffffffu, dot, 4);
+                const float sc = valid ? dot : -INFINITY;
+                if (sc > m[i]) {
+                    const float al = ex2(m[i] - sc);
+                    m[i] = sc;
+                    l[i] *= al;
+#pragma unroll
+                    for (int e = 0; e < EPL; ++e) o[i][e] *= al;
+                }
+                pv[i] = valid ? ex2(sc - m[i]) : 0.f;
+                l[i] += pv[i];
+            }
+            if (valid) {
+                float vf[EPL];
+#pragma unroll
+                for (int c = 0; c < CPL; ++c) {
+                    const uint4 raw = *reinterpret_cast<const uint4*>(vst + row * C::kRowBytes +
+                                                                      (j + 8 * c) * 16);
+                    unpack16<KV>(raw, &vf[c * EPC]);
+                }
+#pragma unroll
+                for (int i = 0; i < GC; ++i)
+#pragma unroll
+                    for (int e = 0; e < EPL; ++e) o[i][e] = fmaf(pv[i], vf[e], o[i][e]);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    if (timed_out) atomicOr(abort_flag, 1);
+
+    // merge the four groups of the warp (lanes j, j+8, j+16, j+24)
+#pragma unroll
+    for (int i = 0; i < GC; ++i) {
+        float M = fmaxf(m[i], __shfl_xor_sync(0xffffffffu, m[i], 8));
+        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 16));
+        const float w = (M == -INFINITY) ? 0.f : ex2(m[i] - M);
+        float li = l[i] * w;
+        li += __shfl_xor_sync(0xffffffffu, li, 8);
+        li += __shfl_xor_sync(0xffffffffu, li, 16);
+        l[i] = li;
+        m[i] = M;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+            float oe = o[i][e] * w;
+            oe += __shfl_xor_sync(0xffffffffu, oe, 8);
+            oe += __shfl_xor_sync(0xffffffffu, oe, 16);
+            o[i][e] = oe;
+        }
+    }
+    if (grp == 0) {
+#pragma unroll
+        for (int i = 0; i < GC; ++i) {
+            const int h = hc * GC + i;
+#pragma unroll
+            for (int c = 0; c < CPL; ++c)
+#pragma unroll
+                for (int e = 0; e < EPC; ++e)
+                    mg_o[(ts * G + h) * D + (j + 8 * c) * EPC + e] = o[i][c * EPC + e];
+            if (j == 0) {
+                mg_m[ts * G + h] = m[i];
+                mg_l[ts * G + h] = l[i];
+            }
+        }
+    }
+    consumer_sync(C::kWarps * 32);
+    const bool poison = bad || (*abort_flag != 0);
+    const int ct = threadIdx.x - 32;
+    for (int idx = ct; idx < G * D; idx += C::kWarps * 32) {
+        const int h = idx / D, dd = idx - h * D;
+        float M = -INFINITY;
+        for (int t = 0; t < NTS; ++t) M = fmaxf(M, mg_m[t * G + h]);
+        const float Ms = (M == -INFINITY) ? 0.f : M;
+        float ov = 0.f, lv = 0.f;
+        for (int t = 0; t < NTS; ++t) {
+            const float wt = ex2(mg_m[t * G + h] - Ms);
+            ov += wt * mg_o[(t * G + h) * D + dd];
+            lv += wt * mg_l[t * G + h];
+        }
+        emit_state(p, b, g * G + h, split, D, dd, ov, lv, M, poison);
+    }
+    allow_dependents();
+}
+
+template <typename KV, int D, int GC>
+cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& p,
+                       cudaStream_t stream) {
+    using C = FmaCfg<KV, D>;
+    cudaError_t e = cudaFuncSetAttribute(split_kv_fma_kernel<KV, D, GC>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(p.P, p.Hkv, p.B);
+    split_kv_fma_kernel<KV, D, GC><<<grid, C::kThreads, C::kSmem, stream>>>(tk, tv, p);
+    return cudaGetLastError();
+}
+
+template <typename KV, int D>
+cudaError_t launch_d(const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& p,
+                     cudaStream_t stream) {
+    switch (p.G) {
+        case 1: return launch_one<KV, D, 1>(tk, tv, p, stream);
+        case 2: return launch_one<KV, D, 2>(tk, tv, p, stream);
+        case 4:
+        case 8:
+        case 16: return launch_one<KV, D, 4>(tk, tv, p, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <typename KV>
+cudaError_t launch_fma(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const SplitParams& p, cudaStream_t stream) {
+    switch (head_dim) {
+        case 64: return launch_d<KV, 64>(tk, tv, p, stream);
+        case 128: return launch_d<KV, 128>(tk, tv, p, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace fma_detail
+}  // namespace ta

@@ -1,0 +1,177 @@
+"""Host-side checks of libtreeattn.so that need no GPU: the library loads, exports
+every entry point its header declares, validates arguments before touching
+CUDA, sizes the workspace and picks split counts."""
+import ctypes
+import math
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tree_attn.h")
+
+
+@pytest.fixture(scope="module")
+def ta():
+    from softmax_tree_reduction_gb300 import build
+    build.build()
+    import softmax_tree_reduction_gb300 as mod
+    mod.load()
+    return mod
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^[A-Za-z_][\w\s\*]*?\b(tree_attn_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("tree_attn_decode", "tree_attn_combine", "tree_attn_workspace_bytes",
+              "tree_attn_pick_splits", "tree_attn_get_device_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(ta):
+    lib = ctypes.CDLL(ta.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_version_and_status_strings(ta):
+    assert ta.tree_attn_version() == 1
+    for code in range(0, -10, -1):
+        s = ta.tree_attn_status_string(code)
+        assert s and s != "unknown status"
+    assert ta.tree_attn_status_string(-77) == "unknown status"
+
+
+def shape(ta, **kw):
+    base = dict(batch=1, num_q_heads=32, num_kv_heads=8, head_dim=128, max_seqlen=131072,
+                q_dtype=1, kv_dtype=1, scale=0.0, kv_stride_b=0, kv_stride_h=0, kv_stride_t=0)
+    base.update(kw)
+    return ta.TaShape(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(), 0),
+    (dict(num_q_heads=12, num_kv_heads=8), -3),      # Hq % Hkv != 0
+    (dict(num_q_heads=24, num_kv_heads=8), -3),      # G = 3 unsupported
+    (dict(num_q_heads=128, num_kv_heads=4), -3),     # G = 32 unsupported
+    (dict(head_dim=96), -3),
+    (dict(batch=0), -3),
+    (dict(max_seqlen=0), -3),
+    (dict(q_dtype=2), -4),
+    (dict(kv_dtype=7), -4),
+    (dict(scale=-1.0), -3),
+    (dict(scale=float("nan")), -3),
+    (dict(kv_stride_b=131072 * 8 * 128, kv_stride_h=128, kv_stride_t=8 * 128), 0),  # token-major
+    (dict(kv_stride_b=104, kv_stride_h=128, kv_stride_t=1024), 0),
+    (dict(kv_stride_b=100, kv_stride_h=128, kv_stride_t=1024), -2),  # 200 B not 16-aligned
+    (dict(kv_stride_b=1000, kv_stride_h=129, kv_stride_t=1024), -2),   # 258 B not 16-aligned
+    (dict(kv_stride_b=1, kv_stride_h=0, kv_stride_t=1024), -3),
+])
+def test_check_shape(ta, kw, code):
+    assert ta.tree_attn_check_shape(shape(ta, **kw)) == code
+
+
+def test_workspace_bytes_layout(ta):
+    s = shape(ta)
+    assert ta.tree_attn_workspace_bytes(s, 1) == 0
+    assert ta.tree_attn_workspace_bytes(s, 0) == 0
+    assert ta.tree_attn_workspace_bytes(s, 5000) == 0
+    for P in (2, 19, 64, 4096):
+        rows = 1 * 32 * P
+        r256 = lambda x: (x + 255) // 256 * 256
+        assert ta.tree_attn_workspace_bytes(s, P) == r256(rows * 128 * 4) + 2 * r256(rows * 4)
+
+
+def test_pick_splits_fills_whole_waves(ta):
+    # 8 (b, kv-head) rows on 152 SMs: 19 slices give exactly one wave of 152 blocks
+    assert ta.tree_attn_pick_splits(shape(ta), None, 152) == 19
+    # 32 rows (4 x 8): 19 slices give 608 blocks = 4 full waves
+    assert ta.tree_attn_pick_splits(shape(ta, batch=4, num_q_heads=64, max_seqlen=262144), None, 152) == 19
+    # a different SM count moves the choice with it: the largest single wave
+    for sms in (132, 148, 160):
+        assert ta.tree_attn_pick_splits(shape(ta), None, sms) == sms // 8
+
+
+def test_pick_splits_bounds(ta):
+    for n in (1, 100, 255, 256, 257, 4096, 65536, 1 << 20):
+        P = ta.tree_attn_pick_splits(shape(ta, max_seqlen=n), None, 152)
+        assert 1 <= P <= max(1, math.ceil(n / 256))
+    assert ta.tree_attn_pick_splits(shape(ta, max_seqlen=64), [0], 152) == 1
+
+
+def test_pick_splits_ragged_uses_lengths(ta):
+    from softmax_tree_reduction_gb300 import workloads
+    sl = workloads.seqlens_of(workloads.BATCHED_RAGGED)
+    s = shape(ta, batch=16, max_seqlen=65536)
+    P = ta.tree_attn_pick_splits(s, sl, 152)
+    assert 1 <= P <= 256
+    # all rows at the shortest length: the uniform model applies
+    P2 = ta.tree_attn_pick_splits(s, np.full(16, 8192), 152)
+    assert 1 <= P2 <= 32
+
+
+def test_pick_splits_rejects_bad_shape(ta):
+    with pytest.raises(ta.TreeAttnError):
+        ta.tree_attn_pick_splits(shape(ta, head_dim=80), None, 152)
+
+
+def _decode_raw(ta, s, q=0x1000, k=0x2000, v=0x3000, sl=0x4000, out=0x5000, lse=0x6000, P=1,
+                ws=0, wsb=0, opts=None):
+    lib = ta.load()
+    vp = ctypes.c_void_p
+    if opts is None:
+        return lib.tree_attn_decode(ctypes.byref(s) if s is not None else None, vp(q), vp(k), vp(v),
+                                    vp(sl), vp(out), vp(lse), P, vp(ws), wsb, vp(0))
+    return lib.tree_attn_decode_ex(ctypes.byref(s), vp(q), vp(k), vp(v), vp(sl), vp(out), vp(lse),
+                                   P, vp(ws), wsb, ctypes.byref(opts), vp(0))
+
+
+def test_decode_argument_errors_before_any_cuda_call(ta):
+    s = shape(ta)
+    assert _decode_raw(ta, None) == -1
+    assert _decode_raw(ta, s, q=0) == -1
+    assert _decode_raw(ta, s, out=0) == -1
+    assert _decode_raw(ta, s, sl=0) == -1
+    assert _decode_raw(ta, s, k=0x2001) == -2
+    assert _decode_raw(ta, s, out=0x5004) == -2
+    assert _decode_raw(ta, s, P=5000) == -5
+    assert _decode_raw(ta, s, P=4, ws=0, wsb=0) == -6
+    need = ta.tree_attn_workspace_bytes(s, 4)
+    assert _decode_raw(ta, s, P=4, ws=0x7000, wsb=need - 1) == -6
+    assert _decode_raw(ta, s, P=4, ws=0x7008, wsb=need) == -2
+    assert _decode_raw(ta, shape(ta, head_dim=32)) == -3
+    f32 = shape(ta, q_dtype=0, kv_dtype=0)
+    assert _decode_raw(ta, f32, opts=ta.TaOptions(2, 0, None, None)) == -4   # mma needs bf16
+    assert _decode_raw(ta, shape(ta, num_q_heads=128, num_kv_heads=8),
+                       opts=ta.TaOptions(2, 0, None, None)) == -4          # mma needs G <= 8
+    assert _decode_raw(ta, s, opts=ta.TaOptions(0, 1, None, None)) == -3  # reserved != 0
+    assert _decode_raw(ta, s, opts=ta.TaOptions(9, 0, None, None)) == -3  # unknown kernel
+
+
+def test_combine_argument_errors(ta):
+    lib = ta.load()
+    vp = ctypes.c_void_p
+    s = shape(ta)
+    call = lambda s_, po=0x1000, pm=0x2000, pl=0x3000, P=4, out=0x4000, lse=0x5000: \
+        lib.tree_attn_combine(ctypes.byref(s_), vp(po), vp(pm), vp(pl), P, vp(out), vp(lse), vp(0))
+    assert call(s, po=0) == -1
+    assert call(s, out=0) == -1
+    assert call(s, P=0) == -5
+    assert call(s, P=4097) == -5
+    assert call(shape(ta, head_dim=100)) == -3
+    assert call(s, po=0x1004) == -2
+    assert call(s, pm=0x2002) == -2
+
+
+def test_binding_refuses_cpu_tensors(ta):
+    import torch
+    q = torch.zeros(1, 1, 64)
+    k = torch.zeros(1, 1, 8, 64)
+    with pytest.raises(ValueError):
+        ta.tree_attn_decode(q, k, k, torch.zeros(1, dtype=torch.int32))
