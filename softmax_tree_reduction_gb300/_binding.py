@@ -200,6 +200,11 @@ def tree_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
     else:
         opts = TaOptions(TA_KERNEL[kernel], 0, None, None)
         if split_events is not None:
+            # torch creates the CUDA event on its first record; record once so the
+            # handle exists (the library's own record then replaces this one)
+            torch_stream = stream if isinstance(stream, torch.cuda.Stream) else torch.cuda.current_stream()
+            for ev in split_events:
+                ev.record(torch_stream)
             opts.split_start_event = split_events[0].cuda_event
             opts.split_end_event = split_events[1].cuda_event
         rc = lib.tree_attn_decode_ex(ctypes.byref(shape), _ptr(q), _ptr(k_cache), _ptr(v_cache),
