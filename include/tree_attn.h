@@ -54,7 +54,9 @@ typedef enum {
     TA_ERR_WORKSPACE = -6,     /* workspace missing or too small */
     TA_ERR_CUDA = -7,          /* a CUDA runtime/driver call failed */
     TA_ERR_DEVICE_DATA = -8,   /* device found a sequence length outside [0, max_seqlen] */
-    TA_ERR_DEVICE_TIMEOUT = -9 /* a bounded on-chip wait gave up (outputs are NaN) */
+    TA_ERR_DEVICE_TIMEOUT = -9, /* a bounded on-chip wait gave up (outputs are NaN) */
+    TA_ERR_SCRATCH_LIMIT = -10  /* tree_attn_decode_noalloc: the partial states need more than
+                                   TA_NOALLOC_SCRATCH_BYTES */
 } ta_status;
 
 /* Element types. */
@@ -178,6 +180,36 @@ int tree_attn_decode_ex(const ta_shape *shape, const void *q, const void *k_cach
 int tree_attn_combine(const ta_shape *shape, const float *partial_o, const float *partial_m,
                       const float *partial_l, int num_splits, float *out, float *lse,
                       void *stream);
+
+/* Size of the fixed device buffer behind tree_attn_decode_noalloc (8 MiB per
+ * GPU that loads the library, held until the process exits). */
+#define TA_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* tree_attn_decode for callers that must not allocate device memory.  The
+ * Tree Attention pages have no counterpart to this; it is a deployment aid.
+ *
+ * Some callers cannot call cudaMalloc at decode time: an inference engine's
+ * plugin whose device memory is planned before serving starts and whose
+ * enqueue must not allocate, or a serving loop that cannot afford
+ * cudaMalloc's implicit device-wide synchronisation.  This entry point takes
+ * the same inputs and outputs as tree_attn_decode but keeps the partial states
+ * in a buffer of TA_NOALLOC_SCRATCH_BYTES that the library reserves statically
+ * on each device, so the caller passes no workspace and nothing is allocated.
+ *
+ *  - The first call on a device looks up that buffer's device address (a
+ *    one-time set-up with that device current); make that first call before
+ *    any stream capture begins.
+ *  - Returns TA_ERR_SCRATCH_LIMIT, with nothing enqueued, when
+ *    tree_attn_workspace_bytes(shape, P) exceeds TA_NOALLOC_SCRATCH_BYTES
+ *    (P = num_splits, or the heuristic's choice when num_splits <= 0).
+ *  - Every call on a device shares the one buffer and it keeps the previous
+ *    call's contents.  Nothing in it needs to start at zero (every partial
+ *    state is written before it is read), but calls whose work overlaps on
+ *    the GPU (different streams without ordering) race on it: order them.
+ * Other arguments, errors and results are as for tree_attn_decode. */
+int tree_attn_decode_noalloc(const ta_shape *shape, const void *q, const void *k_cache,
+                             const void *v_cache, const int32_t *seqlens, float *out, float *lse,
+                             int num_splits, void *stream);
 
 /* Synchronise `stream`, then read and clear the current device's error word.
  * Returns TA_OK, TA_ERR_DEVICE_DATA or TA_ERR_DEVICE_TIMEOUT (or TA_ERR_CUDA

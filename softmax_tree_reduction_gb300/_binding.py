@@ -22,10 +22,12 @@ TA_OK = 0
 TA_F32, TA_BF16 = 0, 1
 TA_KERNEL = {"auto": 0, "fma": 1, "mma": 2}
 TA_MAX_SPLITS = 4096
+TA_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 _EXPORTS = ["tree_attn_status_string", "tree_attn_version", "tree_attn_check_shape",
             "tree_attn_workspace_bytes", "tree_attn_pick_splits", "tree_attn_decode",
-            "tree_attn_decode_ex", "tree_attn_combine", "tree_attn_get_device_error"]
+            "tree_attn_decode_ex", "tree_attn_combine", "tree_attn_get_device_error",
+            "tree_attn_decode_noalloc"]
 
 
 class TaShape(ctypes.Structure):
@@ -80,6 +82,8 @@ def load(path: str = LIB_PATH):
         lib.tree_attn_decode_ex.restype = I32
         lib.tree_attn_combine.argtypes = [SP, P, P, P, I32, P, P, P]
         lib.tree_attn_combine.restype = I32
+        lib.tree_attn_decode_noalloc.argtypes = [SP, P, P, P, P, P, P, I32, P]
+        lib.tree_attn_decode_noalloc.restype = I32
         lib.tree_attn_get_device_error.argtypes = [P]
         lib.tree_attn_get_device_error.restype = I32
         _lib = lib
@@ -242,3 +246,24 @@ def tree_attn_combine(partial_o: torch.Tensor, partial_m: torch.Tensor, partial_
 def tree_attn_get_device_error(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device error status."""
     return int(load().tree_attn_get_device_error(_stream(stream)))
+
+
+def tree_attn_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                             seqlens: torch.Tensor, out: torch.Tensor, lse: Optional[torch.Tensor] = None,
+                             num_splits: int = 0, scale: Optional[float] = None, stream=None):
+    """Decode attention that allocates nothing: for callers that cannot allocate
+    device memory while decoding (for example an engine plugin whose memory is
+    planned in advance).  The caller passes every output; the partial states go
+    to the library's fixed per-device scratch buffer (TA_NOALLOC_SCRATCH_BYTES).
+    Calls that overlap on the GPU share that buffer and must be ordered."""
+    lib = load()
+    _check_cuda(q, k_cache, v_cache, seqlens, out, lse)
+    if v_cache.shape != k_cache.shape or v_cache.stride() != k_cache.stride():
+        raise ValueError("k_cache and v_cache must have the same shape and strides")
+    shape = make_shape(q, k_cache, scale)
+    rc = lib.tree_attn_decode_noalloc(ctypes.byref(shape), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                      _ptr(seqlens), _ptr(out), _ptr(lse), int(num_splits),
+                                      _stream(stream))
+    if rc != TA_OK:
+        raise TreeAttnError(rc, "tree_attn_decode_noalloc")
+    return out, lse

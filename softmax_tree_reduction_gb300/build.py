@@ -19,7 +19,8 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libtreeattn.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["api.cu", "combine.cu", "split_kv_mma.cu", "split_kv_fma_bf16.cu", "split_kv_fma_f32.cu"]
+SOURCES = ["api.cu", "combine.cu", "split_kv_mma.cu", "split_kv_fma_bf16.cu", "split_kv_fma_f32.cu",
+           "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", "-I", CSRC, "-I", INCLUDE]

@@ -269,6 +269,9 @@ const char* tree_attn_status_string(int status) {
         case TA_ERR_CUDA: return "a CUDA call failed";
         case TA_ERR_DEVICE_DATA: return "a sequence length outside [0, max_seqlen] was found on the device";
         case TA_ERR_DEVICE_TIMEOUT: return "an on-chip wait timed out";
+        case TA_ERR_SCRATCH_LIMIT:
+            return "the partial states need more than the no-allocation scratch buffer holds "
+                   "(TA_NOALLOC_SCRATCH_BYTES); use fewer splits or tree_attn_decode with a workspace";
         default: return "unknown status";
     }
 }
