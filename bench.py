@@ -27,6 +27,8 @@ import sys
 import threading
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
@@ -39,7 +41,12 @@ FALLBACK_HBM_GBS = 6800.0
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by kernel family and
 # workload, with the SHA-256 of the kernel source it was taken on; reported
 # only while that source is unchanged.  Summaries live in profiles/.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # profiles/split_kv_mma_llama31_8b_131k.md
+    ("mma", "llama3.1-8b-decode-layer"): {
+        "bytes_per_launch": 536914944 + 2909184, "num_splits": 19,
+        "src_sha256": "d17b0918223c1a8d648c0b788c31c9dc1645b9e53a8a212f579b5f86daab9ded"},
+}
 
 
 def parse_args(argv=None):
@@ -58,6 +65,12 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--ref-tokens", type=int, default=8192,
                     help="reference arm: tokens per row in each step's sample")
+    ap.add_argument("--sweep-splits", default="",
+                    help="comma list of split counts: print one JSON line per count and kernel, then exit")
+    ap.add_argument("--sweep-context", default="",
+                    help="comma list of context lengths for the workload's head shape (heuristic splits): "
+                         "print one JSON line per length, then exit")
+    ap.add_argument("--sweep-kernels", default="mma,fma")
     return ap.parse_args(argv)
 
 
@@ -357,6 +370,106 @@ def run_ours(args, rank, world, local):
     }
 
 
+# ----------------------------------------------------------------- sweeps
+def _time_steps(ta, torch, copies, P, kernel, steps, warmup, out, lse, ws):
+    """(ms per step, mean split-kernel ms) over ``steps`` decode calls."""
+    def step(i, events=None):
+        c = copies[i % len(copies)]
+        ta.tree_attn_decode(c["q"], c["k"], c["v"], c["seqlens"], out=out, lse=lse, num_splits=P,
+                            workspace=ws, kernel=kernel, split_events=events)
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(s)
+    for i in range(steps):
+        step(i)
+    b.record(s)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for i in range(steps):
+        step(i, events=evs[i])
+    torch.cuda.synchronize()
+    split = statistics.mean(x.elapsed_time(y) for x, y in evs)
+    assert ta.tree_attn_get_device_error() == 0
+    return ms, split
+
+
+def run_sweeps(args):
+    """Sweep modes: seeded inputs drawn on the device (timing only; parity is
+    covered by the tests), two KV copies alternated when they fit."""
+    import torch
+    import softmax_tree_reduction_gb300 as ta
+    from softmax_tree_reduction_gb300 import workloads
+
+    torch.cuda.set_device(0)
+    ta.load()
+    w = workloads.WORKLOADS[args.workload]
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(w.seed)
+
+    def draw(N):
+        B, Hq, Hkv, d = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim
+        q = torch.randn(B, Hq, d, generator=gen, device="cuda").to(w.q_dtype)
+        copies = []
+        per_copy = 2 * B * Hkv * N * d * torch.empty((), dtype=w.kv_dtype).element_size()
+        n_copies = 2 if per_copy <= (8 << 30) else 1
+        for _ in range(n_copies):
+            k = (torch.randn(B, Hkv, N, d, generator=gen, device="cuda") * w.k_scale).to(w.kv_dtype)
+            v = torch.randn(B, Hkv, N, d, generator=gen, device="cuda").to(w.kv_dtype)
+            copies.append({"q": q, "k": k, "v": v,
+                           "seqlens": torch.full((B,), N, dtype=torch.int32, device="cuda")})
+        return copies
+
+    peak, _ = load_peaks()
+    lines = []
+    if args.sweep_splits:
+        copies = draw(w.max_seqlen)
+        shape = ta.make_shape(copies[0]["q"], copies[0]["k"])
+        kv_bytes = w.kv_bytes(np.full(w.batch, w.max_seqlen))
+        B, Hq, d = copies[0]["q"].shape
+        out = torch.empty(B, Hq, d, device="cuda")
+        lse = torch.empty(B, Hq, device="cuda")
+        heur = ta.tree_attn_pick_splits(shape)
+        for kern in args.sweep_kernels.split(","):
+            for P in [int(x) for x in args.sweep_splits.split(",")]:
+                ws = torch.empty(max(16, ta.tree_attn_workspace_bytes(shape, P)), dtype=torch.uint8,
+                                 device="cuda")
+                ms, split = _time_steps(ta, torch, copies, P, kern, args.steps, args.warmup, out, lse, ws)
+                lines.append({"sweep": "splits", "workload": w.name, "kernel": kern, "num_splits": P,
+                              "heuristic": P == heur, "us_per_step": round(ms * 1e3, 3),
+                              "split_kernel_us": round(split * 1e3, 3),
+                              "step_gbs": round(kv_bytes / (ms / 1e3) / 1e9, 1),
+                              "kernel_gbs": round(kv_bytes / (split / 1e3) / 1e9, 1),
+                              "frac_of_measured_peak": round(kv_bytes / (split / 1e3) / 1e9 / peak, 4)})
+                print(json.dumps(lines[-1]), flush=True)
+        del copies
+        torch.cuda.empty_cache()
+    if args.sweep_context:
+        for N in [int(x) for x in args.sweep_context.split(",")]:
+            copies = draw(N)
+            shape = ta.make_shape(copies[0]["q"], copies[0]["k"])
+            P = ta.tree_attn_pick_splits(shape)
+            kv_bytes = w.kv_bytes(np.full(w.batch, N))
+            B, Hq, d = copies[0]["q"].shape
+            out = torch.empty(B, Hq, d, device="cuda")
+            lse = torch.empty(B, Hq, device="cuda")
+            ws = torch.empty(max(16, ta.tree_attn_workspace_bytes(shape, P)), dtype=torch.uint8,
+                             device="cuda")
+            ms, split = _time_steps(ta, torch, copies, P, args.kernel, args.steps, args.warmup, out, lse, ws)
+            lines.append({"sweep": "context", "workload": w.name, "context": N, "num_splits": P,
+                          "us_per_step": round(ms * 1e3, 3), "split_kernel_us": round(split * 1e3, 3),
+                          "step_gbs": round(kv_bytes / (ms / 1e3) / 1e9, 1),
+                          "frac_of_measured_peak": round(kv_bytes / (ms / 1e3) / 1e9 / peak, 4)})
+            print(json.dumps(lines[-1]), flush=True)
+            del copies
+            torch.cuda.empty_cache()
+    return lines
+
+
 # ------------------------------------------------------- reference arm
 def run_reference(args, rank, world):
     if rank != 0:
@@ -403,6 +516,9 @@ def run_reference(args, rank, world):
 def main(argv=None):
     args = parse_args(argv)
     rank, world, local = dist_env()
+    if args.sweep_splits or args.sweep_context:
+        run_sweeps(args)
+        return 0
     if args.impl == "reference":
         res = run_reference(args, rank, world)
     else:
