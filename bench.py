@@ -71,6 +71,8 @@ def parse_args(argv=None):
                     help="comma list of context lengths for the workload's head shape (heuristic splits): "
                          "print one JSON line per length, then exit")
     ap.add_argument("--sweep-kernels", default="mma,fma")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="fixed chunk assignment (bitwise reproducible) instead of run-time balancing")
     return ap.parse_args(argv)
 
 
@@ -280,16 +282,21 @@ def run_ours(args, rank, world, local):
     sampler.mark_stop()
     barrier(world)
     elapsed_ms = e0.elapsed_time(e1)
-    # ---- timed region B: same steps, split-KV kernel bracketed by events
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    barrier(world)
-    torch.cuda.synchronize()
-    for i in range(args.steps):
-        step(i, events=evs[i])
-    torch.cuda.synchronize()
-    barrier(world)
-    split_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    launches = ta.tree_attn_launch_count(shape, P, args.kernel)
+    if launches == 1:
+        # the step is the split-KV kernel alone: its launch duration is the step time
+        split_ms = elapsed_ms / args.steps
+    else:
+        # ---- timed region B: same steps, split-KV kernel bracketed by events
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        barrier(world)
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            step(i, events=evs[i])
+        torch.cuda.synchronize()
+        barrier(world)
+        split_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
     if rank == 0:
         time.sleep(0.1)
         sampler.stop()
@@ -365,18 +372,20 @@ def run_ours(args, rank, world, local):
                      "frac_of_8TBps": round(achieved / 8000.0, 4)},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": int(args.steps * (2 if P > 1 else 1)),
+        "gpu_launches": int(args.steps * launches),
         "clocks": sampler.summary(),
     }
 
 
 # ----------------------------------------------------------------- sweeps
-def _time_steps(ta, torch, copies, P, kernel, steps, warmup, out, lse, ws):
-    """(ms per step, mean split-kernel ms) over ``steps`` decode calls."""
+def _time_steps(ta, torch, copies, P, kernel, steps, warmup, out, lse, ws, deterministic=False):
+    """(ms per step, split-kernel ms) over ``steps`` decode calls; when the step
+    is a single kernel the two are the same number."""
     def step(i, events=None):
         c = copies[i % len(copies)]
         ta.tree_attn_decode(c["q"], c["k"], c["v"], c["seqlens"], out=out, lse=lse, num_splits=P,
-                            workspace=ws, kernel=kernel, split_events=events)
+                            workspace=ws, kernel=kernel, split_events=events,
+                            deterministic=deterministic)
     for i in range(warmup):
         step(i)
     torch.cuda.synchronize()
@@ -388,6 +397,10 @@ def _time_steps(ta, torch, copies, P, kernel, steps, warmup, out, lse, ws):
     b.record(s)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / steps
+    shape = ta.make_shape(copies[0]["q"], copies[0]["k"])
+    if ta.tree_attn_launch_count(shape, P, kernel, deterministic) == 1:
+        assert ta.tree_attn_get_device_error() == 0
+        return ms, ms
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(steps)]
     for i in range(steps):
@@ -438,8 +451,10 @@ def run_sweeps(args):
             for P in [int(x) for x in args.sweep_splits.split(",")]:
                 ws = torch.empty(max(16, ta.tree_attn_workspace_bytes(shape, P)), dtype=torch.uint8,
                                  device="cuda")
-                ms, split = _time_steps(ta, torch, copies, P, kern, args.steps, args.warmup, out, lse, ws)
+                ms, split = _time_steps(ta, torch, copies, P, kern, args.steps, args.warmup, out, lse, ws,
+                                        args.deterministic)
                 lines.append({"sweep": "splits", "workload": w.name, "kernel": kern, "num_splits": P,
+                              "deterministic": args.deterministic,
                               "heuristic": P == heur, "us_per_step": round(ms * 1e3, 3),
                               "split_kernel_us": round(split * 1e3, 3),
                               "step_gbs": round(kv_bytes / (ms / 1e3) / 1e9, 1),
@@ -459,7 +474,8 @@ def run_sweeps(args):
             lse = torch.empty(B, Hq, device="cuda")
             ws = torch.empty(max(16, ta.tree_attn_workspace_bytes(shape, P)), dtype=torch.uint8,
                              device="cuda")
-            ms, split = _time_steps(ta, torch, copies, P, args.kernel, args.steps, args.warmup, out, lse, ws)
+            ms, split = _time_steps(ta, torch, copies, P, args.kernel, args.steps, args.warmup, out, lse, ws,
+                                    args.deterministic)
             lines.append({"sweep": "context", "workload": w.name, "context": N, "num_splits": P,
                           "us_per_step": round(ms * 1e3, 3), "split_kernel_us": round(split * 1e3, 3),
                           "step_gbs": round(kv_bytes / (ms / 1e3) / 1e9, 1),

@@ -101,10 +101,16 @@ typedef enum {
     TA_KERNEL_MMA = 2    /* BF16 tensor-core mma; needs q and kv in BF16, Hq/Hkv <= 8 */
 } ta_kernel;
 
+/* Bits of ta_options.flags. */
+#define TA_FLAG_DETERMINISTIC 1  /* assign each slice a fixed, strided set of chunks instead of
+                                    balancing chunks between a row's blocks at run time: results
+                                    are then bitwise reproducible for a given num_splits (the
+                                    default balancing changes the rounding order run to run) */
+
 /* Optional per-call settings (pass NULL for defaults). */
 typedef struct {
     int32_t kernel;            /* ta_kernel */
-    int32_t reserved;          /* must be 0 */
+    int32_t flags;             /* TA_FLAG_* bits; other bits must be 0 */
     void *split_start_event;   /* optional cudaEvent_t recorded on `stream` just before the
                                   per-slice kernel is enqueued */
     void *split_end_event;     /* optional cudaEvent_t recorded just after it (before the combine) */
@@ -156,6 +162,13 @@ int tree_attn_pick_splits(const ta_shape *shape, const int32_t *host_seqlens, in
 int tree_attn_decode(const ta_shape *shape, const void *q, const void *k_cache,
                      const void *v_cache, const int32_t *seqlens, float *out, float *lse,
                      int num_splits, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Number of kernels tree_attn_decode_ex enqueues for this shape, split count
+ * and options: 1 when the partial states are merged inside the per-slice
+ * kernel (num_splits == 1, or num_splits * Hq/Hkv <= 8192), else 2 (the
+ * per-slice kernel, then the combine).  num_splits <= 0 queries the current
+ * device for the heuristic's choice.  Negative ta_status on invalid input. */
+int tree_attn_launch_count(const ta_shape *shape, int num_splits, const ta_options *options);
 
 /* tree_attn_decode with per-call options (kernel family, timing events). */
 int tree_attn_decode_ex(const ta_shape *shape, const void *q, const void *k_cache,

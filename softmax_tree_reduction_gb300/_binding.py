@@ -22,12 +22,13 @@ TA_OK = 0
 TA_F32, TA_BF16 = 0, 1
 TA_KERNEL = {"auto": 0, "fma": 1, "mma": 2}
 TA_MAX_SPLITS = 4096
+TA_FLAG_DETERMINISTIC = 1
 TA_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 _EXPORTS = ["tree_attn_status_string", "tree_attn_version", "tree_attn_check_shape",
             "tree_attn_workspace_bytes", "tree_attn_pick_splits", "tree_attn_decode",
             "tree_attn_decode_ex", "tree_attn_combine", "tree_attn_get_device_error",
-            "tree_attn_decode_noalloc"]
+            "tree_attn_decode_noalloc", "tree_attn_launch_count"]
 
 
 class TaShape(ctypes.Structure):
@@ -40,7 +41,7 @@ class TaShape(ctypes.Structure):
 
 
 class TaOptions(ctypes.Structure):
-    _fields_ = [("kernel", ctypes.c_int32), ("reserved", ctypes.c_int32),
+    _fields_ = [("kernel", ctypes.c_int32), ("flags", ctypes.c_int32),
                 ("split_start_event", ctypes.c_void_p), ("split_end_event", ctypes.c_void_p)]
 
 
@@ -84,6 +85,8 @@ def load(path: str = LIB_PATH):
         lib.tree_attn_combine.restype = I32
         lib.tree_attn_decode_noalloc.argtypes = [SP, P, P, P, P, P, P, I32, P]
         lib.tree_attn_decode_noalloc.restype = I32
+        lib.tree_attn_launch_count.argtypes = [SP, I32, ctypes.POINTER(TaOptions)]
+        lib.tree_attn_launch_count.restype = I32
         lib.tree_attn_get_device_error.argtypes = [P]
         lib.tree_attn_get_device_error.restype = I32
         _lib = lib
@@ -155,6 +158,16 @@ def tree_attn_pick_splits(shape: TaShape, host_seqlens=None, num_sms: int = 0) -
     return r
 
 
+def tree_attn_launch_count(shape: TaShape, num_splits: int, kernel: str = "auto",
+                           deterministic: bool = False) -> int:
+    """Kernels one tree_attn_decode call enqueues (1 when the merge is fused)."""
+    opts = TaOptions(TA_KERNEL[kernel], TA_FLAG_DETERMINISTIC if deterministic else 0, None, None)
+    r = int(load().tree_attn_launch_count(ctypes.byref(shape), int(num_splits), ctypes.byref(opts)))
+    if r < 0:
+        raise TreeAttnError(r, "tree_attn_launch_count")
+    return r
+
+
 def _check_cuda(*ts):
     for t in ts:
         if t is not None and not t.is_cuda:
@@ -166,12 +179,13 @@ def tree_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
                      lse: Optional[torch.Tensor] = None, num_splits: int = 0,
                      workspace: Optional[torch.Tensor] = None, kernel: str = "auto",
                      scale: Optional[float] = None, stream=None, split_events=None,
-                     want_lse: bool = True):
+                     want_lse: bool = True, deterministic: bool = False):
     """Decode attention through the C ABI; returns (out [B,Hq,d] fp32, lse [B,Hq] fp32 or None).
 
     ``num_splits`` <= 0 uses the library's heuristic (picked on the host so the
     workspace can be sized).  ``split_events`` = (start, end) torch.cuda.Event
-    pair recorded around the per-slice kernel.
+    pair recorded around the per-slice kernel.  ``deterministic`` selects the
+    fixed chunk assignment (bitwise reproducible results for a given split count).
     """
     lib = load()
     _check_cuda(q, k_cache, v_cache, seqlens, out, lse, workspace)
@@ -197,12 +211,12 @@ def tree_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     st = _stream(stream)
-    if kernel == "auto" and split_events is None:
+    if kernel == "auto" and split_events is None and not deterministic:
         rc = lib.tree_attn_decode(ctypes.byref(shape), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                   _ptr(seqlens), _ptr(out), _ptr(lse), P, _ptr(workspace),
                                   ws_bytes, st)
     else:
-        opts = TaOptions(TA_KERNEL[kernel], 0, None, None)
+        opts = TaOptions(TA_KERNEL[kernel], TA_FLAG_DETERMINISTIC if deterministic else 0, None, None)
         if split_events is not None:
             # torch creates the CUDA event on its first record; record once so the
             # handle exists (the library's own record then replaces this one)

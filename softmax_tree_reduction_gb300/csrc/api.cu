@@ -21,12 +21,26 @@ using ta::Geometry;
 
 __device__ int g_error_word;  // bits ta::kErrBadSeqlen | ta::kErrTimeout
 
+// Scheduling counters (chunk claims and row tickets) of the split kernels.
+// Zero at load; each call reserves 2*B*Hkv consecutive slots and leaves them
+// at zero when it completes, so slots are reused as the cursor wraps.
+constexpr unsigned kRingSlots = 1u << 20;
+__device__ unsigned g_sched_ring[kRingSlots];
+
+// Tiles per scheduled chunk of a row (128 tokens with 64-token tiles).
+constexpr int kChunkTiles = 2;
+// The row's last block merges the partial states itself when G*P states fit
+// in its (then idle) stage buffers; otherwise the combine kernel runs.
+constexpr int kFusedMaxStates = 8192;
+
 constexpr int kMaxDevices = 64;
 
 struct DeviceState {
     bool ready = false;
     int num_sms = 0;
-    int* err = nullptr;  // device address of g_error_word on this device
+    int* err = nullptr;        // device address of g_error_word on this device
+    unsigned* ring = nullptr;  // device address of g_sched_ring on this device
+    unsigned cursor = 0;       // next free ring slot
 };
 
 std::mutex g_mu;
@@ -44,12 +58,25 @@ int device_state(DeviceState** out) {
             return TA_ERR_CUDA;
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return TA_ERR_CUDA;
+        void* r = nullptr;
+        if (cudaGetSymbolAddress(&r, g_sched_ring) != cudaSuccess) return TA_ERR_CUDA;
         s.num_sms = sms;
         s.err = static_cast<int*>(p);
+        s.ring = static_cast<unsigned*>(r);
         s.ready = true;
     }
     *out = &s;
     return TA_OK;
+}
+
+// Reserve `n` consecutive counter slots for one call (nullptr if n exceeds the ring).
+unsigned* reserve_slots(DeviceState* s, unsigned n) {
+    if (n == 0 || n > kRingSlots) return nullptr;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (s->cursor + n > kRingSlots) s->cursor = 0;
+    unsigned* r = s->ring + s->cursor;
+    s->cursor += n;
+    return r;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -310,7 +337,8 @@ int tree_attn_decode_ex(const ta_shape* shape, const void* q, const void* k_cach
     if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
         !aligned(seqlens, 4) || (lse && !aligned(lse, 4)))
         return TA_ERR_ALIGN;
-    if (options && options->reserved != 0) return TA_ERR_SHAPE;
+    if (options && (options->flags & ~TA_FLAG_DETERMINISTIC) != 0) return TA_ERR_SHAPE;
+    const bool deterministic = options && (options->flags & TA_FLAG_DETERMINISTIC);
     const int kernel = resolve_kernel(shape, options ? options->kernel : TA_KERNEL_AUTO);
     if (kernel < 0) return kernel;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
@@ -360,14 +388,23 @@ int tree_attn_decode_ex(const ta_shape* shape, const void* q, const void* k_cach
     const float scale = shape->scale > 0.f ? shape->scale
                                            : 1.0f / std::sqrt(static_cast<float>(shape->head_dim));
     p.scale_log2 = scale * ta::kLog2e;
-    if (P == 1) {
-        p.out = out;
-        p.lse = lse;
-    } else {
+    p.chunk_tiles = kChunkTiles;
+    p.out = out;
+    p.lse = lse;
+    bool fused = false;
+    if (P > 1) {
         char* w = static_cast<char*>(workspace);
         p.part_o = reinterpret_cast<float*>(w + ws.o);
         p.part_m = reinterpret_cast<float*>(w + ws.m);
         p.part_l = reinterpret_cast<float*>(w + ws.l);
+        const unsigned rows = static_cast<unsigned>(shape->batch) * shape->num_kv_heads;
+        unsigned* slots = reserve_slots(ds, 2 * rows);
+        if (slots) {
+            if (!deterministic) p.claim = slots;
+            fused = static_cast<int64_t>(p.G) * P <= kFusedMaxStates;
+            p.fuse = fused ? 1 : 0;
+            if (p.claim || fused) p.done = slots + rows;
+        }
     }
 
     if (options && options->split_start_event &&
@@ -384,12 +421,32 @@ int tree_attn_decode_ex(const ta_shape* shape, const void* q, const void* k_cach
     if (options && options->split_end_event &&
         cudaEventRecord(static_cast<cudaEvent_t>(options->split_end_event), stream) != cudaSuccess)
         return TA_ERR_CUDA;
-    if (P > 1) {
+    if (P > 1 && !fused) {
         e = ta::launch_combine(shape->head_dim, p.part_o, p.part_m, p.part_l, out, lse,
                                shape->batch, shape->num_q_heads, P, /*dependent=*/true, stream);
         if (e != cudaSuccess) return TA_ERR_CUDA;
     }
     return TA_OK;
+}
+
+int tree_attn_launch_count(const ta_shape* shape, int num_splits, const ta_options* options) {
+    int rc = check_shape(shape, nullptr);
+    if (rc != TA_OK) return rc;
+    if (options && (options->flags & ~TA_FLAG_DETERMINISTIC) != 0) return TA_ERR_SHAPE;
+    const int kernel = resolve_kernel(shape, options ? options->kernel : TA_KERNEL_AUTO);
+    if (kernel < 0) return kernel;
+    int P = num_splits;
+    if (P > TA_MAX_SPLITS) return TA_ERR_SPLITS;
+    if (P <= 0) {
+        DeviceState* ds = nullptr;
+        if ((rc = device_state(&ds)) != TA_OK) return rc;
+        P = pick_splits_impl(shape, nullptr, ds->num_sms, kernel);
+    }
+    if (P == 1) return 1;
+    const int64_t G = shape->num_q_heads / shape->num_kv_heads;
+    const unsigned rows = static_cast<unsigned>(shape->batch) * shape->num_kv_heads;
+    const bool have_slots = 2 * static_cast<uint64_t>(rows) <= kRingSlots;
+    return (have_slots && G * P <= kFusedMaxStates) ? 1 : 2;
 }
 
 int tree_attn_decode(const ta_shape* shape, const void* q, const void* k_cache,
@@ -428,7 +485,13 @@ int tree_attn_get_device_error(void* stream) {
     const int zero = 0;
     if (cudaMemcpy(ds->err, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
         return TA_ERR_CUDA;
-    return (h & ta::kErrTimeout) ? TA_ERR_DEVICE_TIMEOUT : TA_ERR_DEVICE_DATA;
+    if (h & ta::kErrTimeout) {
+        // a block that gave up may have left scheduling counters mid-count
+        if (cudaMemset(ds->ring, 0, sizeof(unsigned) * kRingSlots) != cudaSuccess) return TA_ERR_CUDA;
+        if (cudaDeviceSynchronize() != cudaSuccess) return TA_ERR_CUDA;
+        return TA_ERR_DEVICE_TIMEOUT;
+    }
+    return TA_ERR_DEVICE_DATA;
 }
 
 }  // extern "C"

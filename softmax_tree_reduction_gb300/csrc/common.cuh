@@ -32,7 +32,11 @@ struct SplitParams {
     float* part_m;          // [B][Hq][P]
     float* part_l;          // [B][Hq][P]
     int* err;               // device error word
+    unsigned* claim;        // [B*Hkv] chunk counters (null: static chunk assignment)
+    unsigned* done;         // [B*Hkv] row tickets (null: no ticket is taken)
+    int fuse;               // the row's last block merges the partial states
     int B, Hq, Hkv, G, S, P;
+    int chunk_tiles;        // tiles per scheduled chunk
     float scale_log2;       // logit scale * log2(e)
 };
 
@@ -136,22 +140,6 @@ __device__ __forceinline__ void allow_dependents() {
 }
 __device__ __forceinline__ void wait_primary() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-
-// Slice p of a row of N tokens: [p*c, min((p+1)*c, N)) with c = ceil(N/P)
-// rounded up to `align` tokens (so every slice but a row's last starts and
-// ends on a tile boundary).  Returns false for an empty slice.
-__device__ __forceinline__ bool slice_bounds(int N, int P, int p, int align, int& t0, int& t1) {
-    long long c = (static_cast<long long>(N) + P - 1) / P;
-    c = (c + align - 1) / align * align;
-    long long a = c * p, e = a + c;
-    if (a >= N) {
-        t0 = t1 = N;
-        return false;
-    }
-    t0 = static_cast<int>(a);
-    t1 = static_cast<int>(e < N ? e : N);
-    return true;
 }
 
 }  // namespace ta

@@ -1,0 +1,235 @@
+// Work distribution inside a (batch row, KV head) sequence and the row's
+// final merge, shared by the split-KV kernels.
+//
+// Scheduling.  With run-time balancing (the default) each of a row's P blocks
+// first streams a contiguous slice holding 7/8 of its fair share of the row
+// (contiguous streaming keeps DRAM pages and translations local); the last
+// eighth of the row is cut into chunks of `chunk_tiles` tiles that blocks
+// claim from a per-row counter as they run dry, so blocks on SMs that receive
+// more bandwidth stream more and a row's blocks finish together.  Each block
+// ends with one partial state over the tokens it streamed; the merge operator
+// is commutative, so this changes nothing in the result.  Without balancing
+// (P == 1, or the deterministic flag) block p streams the contiguous slice
+// [p*c, (p+1)*c), c = ceil(N/P) rounded up to a tile.
+//
+// Counters start at zero.  Claims are atomicAdds issued up to two ahead, when
+// the block has at most two chunks of work left in hand, so their latency
+// hides behind streaming; a block stops at its first claim past the pool
+// (later ones fail too: the counter only grows).  Every block then takes the
+// row's ticket (an acquire-release atomicInc wrapping after P tickets); the
+// block holding the last ticket -- when every claim of the row has been made
+// -- resets the claim counter, so a completed call leaves both counters at
+// zero.
+//
+// The producer lane publishes each stage's token range in shared memory
+// before arming the stage's full barrier; consumers read it after the wait.
+// A stage whose `nvalid` is negative marks the end of the block's work.
+#pragma once
+
+#include "common.cuh"
+
+namespace ta {
+
+struct StageMeta {
+    int tok0;    // first token of the tile
+    int nvalid;  // valid tokens in the tile (1..tile); < 0: no more tiles
+};
+
+// Producer lane: stream this block's tiles into the stage ring.  `issue(s, t)`
+// enqueues the TMA copies of the tile starting at token t into stage s (the
+// full barrier is already armed with `stage_bytes`).  Returns false if a wait
+// timed out (the error word is set; the caller still drains).
+template <int kStages, typename Issue>
+__device__ bool produce_row(const SplitParams& p, int row, int N, int split, int tile,
+                            uint64_t* full, uint64_t* empty, volatile StageMeta* meta,
+                            volatile unsigned* sink, unsigned stage_bytes, Issue&& issue) {
+    const int P = p.P;
+    const int C = tile * p.chunk_tiles;  // tokens per claimed chunk
+    const bool dynamic = p.claim != nullptr;
+    long long slice;
+    if (dynamic) {
+        slice = (static_cast<long long>(N) * 7 / 8) / P / C * C;
+    } else {
+        slice = (static_cast<long long>(N) + P - 1) / P;
+        slice = (slice + tile - 1) / tile * tile;
+    }
+    int t = static_cast<int>(min(static_cast<long long>(split) * slice, static_cast<long long>(N)));
+    int t_end = static_cast<int>(min(static_cast<long long>(split + 1) * slice, static_cast<long long>(N)));
+    const int base = dynamic ? static_cast<int>(min(static_cast<long long>(P) * slice,
+                                                    static_cast<long long>(N)))
+                             : N;
+    const int npool = dynamic ? (N - base + C - 1) / C : 0;  // chunks handed out by the counter
+    bool exhausted = (npool == 0);
+    unsigned pend0 = 0, pend1 = 0;  // claims in flight, oldest first
+    int npend = 0;
+    bool claimed = false;
+    int it = 0;
+    bool ok = true;
+    while (true) {
+        if (t >= t_end) {
+            if (exhausted) break;
+            if (npend == 0) {
+                pend0 = atomicAdd(p.claim + row, 1u);
+                npend = 1;
+                claimed = true;
+            }
+            const unsigned j = pend0;
+            pend0 = pend1;
+            --npend;
+            if (static_cast<int>(j) >= npool) {
+                exhausted = true;
+                break;
+            }
+            t = base + static_cast<int>(j) * C;
+            t_end = min(t + C, N);
+        }
+        if (!exhausted && npend < 2 && t_end - t <= 2 * C) {
+            const unsigned v = atomicAdd(p.claim + row, 1u);
+            if (npend == 0) pend0 = v; else pend1 = v;
+            ++npend;
+            claimed = true;
+        }
+        const int s = it % kStages;
+        if (it >= kStages && !mbar_wait(&empty[s], ((it / kStages) - 1) & 1, p.err)) {
+            ok = false;
+            break;
+        }
+        meta[s].tok0 = t;
+        meta[s].nvalid = min(tile, t_end - t);
+        mbar_arrive_expect_tx(&full[s], stage_bytes);
+        issue(s, t);
+        ++it;
+        t += tile;
+    }
+    // Every claim must have been performed before the block takes its ticket
+    // (the last ticket resets the counter): consume the outstanding results.
+    if (claimed) *sink = pend0 + pend1;
+    int first_pending = it > kStages ? it - kStages : 0;
+    if (ok) {
+        // end-of-work marker in the next stage
+        const int s = it % kStages;
+        if (it < kStages || mbar_wait(&empty[s], ((it / kStages) - 1) & 1, p.err)) {
+            meta[s].tok0 = 0;
+            meta[s].nvalid = -1;
+            mbar_arrive(&full[s]);
+            first_pending = it >= kStages ? it - kStages + 1 : 0;
+        } else {
+            ok = false;
+        }
+    }
+    // Do not leave while copies into this block's shared memory are in flight.
+    for (int j = first_pending; j < it; ++j) mbar_wait(&full[j % kStages], (j / kStages) & 1, p.err);
+    return ok;
+}
+
+// Take the row's ticket after this block's partial state is written.  The
+// block holding the last ticket resets the row's claim counter and, when
+// `fuse` is set, merges the row's P partial states for its G query heads
+// ("The Tree Reduction Merge Operator" with the root maximum resolved first,
+// then O = o / l) and writes out / lse.
+// `scratch` holds >= 2*G*P + 2*G floats of shared memory no longer in use.
+// Ticket with acquire-release semantics at GPU scope: the block's partial
+// writes (ordered before it by the preceding block barrier) are published,
+// and the last taker sees every other block's writes.
+__device__ __forceinline__ unsigned ticket_acq_rel(unsigned* p, unsigned limit) {
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.inc.u32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "l"(p), "r"(limit)
+                 : "memory");
+    return old;
+}
+
+template <int D>
+__device__ void finish_row(const SplitParams& p, int b, int g, float* scratch, int* flag, int tid,
+                           int nthr) {
+    consumer_sync(nthr);
+    if (tid == 0) {
+        const int row = b * p.Hkv + g;
+        const unsigned t = ticket_acq_rel(p.done + row, static_cast<unsigned>(p.P - 1));
+        const bool last = (t == static_cast<unsigned>(p.P - 1));
+        if (last && p.claim) atomicExch(p.claim + row, 0u);
+        *flag = last;
+    }
+    consumer_sync(nthr);
+    if (!*flag || !p.fuse) return;
+    const int G = p.G, P = p.P;
+    const size_t row0 = static_cast<size_t>(b) * p.Hq + static_cast<size_t>(g) * G;
+    float* sw = scratch;           // [G][P]  maxima, then leaf weights
+    float* sl = scratch + G * P;   // [G][P]  denominators
+    float* sr = sl + G * P;        // [G] root maxima, [G] root denominators
+    constexpr int D4 = D / 4;
+    constexpr int kBatch = 20;     // leaf numerators in flight per thread
+    // The first batch of each thread's numerators is loaded together with the
+    // maxima and denominators, so the merge costs one round trip to L2.
+    const int idx0 = tid;
+    const bool has0 = idx0 < G * D4;
+    const int h0 = has0 ? idx0 / D4 : 0, d40 = has0 ? idx0 - h0 * D4 : 0;
+    const float4* o0 = reinterpret_cast<const float4*>(p.part_o + (row0 + h0) * P * D) + d40;
+    float4 v[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k)
+        v[k] = (has0 && k < P) ? __ldcg(o0 + static_cast<size_t>(k) * D4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = tid; i < G * P; i += nthr) {
+        sw[i] = __ldcg(p.part_m + row0 * P + i);
+        sl[i] = __ldcg(p.part_l + row0 * P + i);
+    }
+    consumer_sync(nthr);
+    const int warp = tid >> 5, lane = tid & 31, nw = nthr >> 5;
+    for (int h = warp; h < G; h += nw) {
+        float M = -INFINITY;
+        for (int q = lane; q < P; q += 32) M = fmaxf(M, sw[h * P + q]);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        const float Ms = (M == -INFINITY) ? 0.f : M;
+        float L = 0.f;
+        for (int q = lane; q < P; q += 32) {
+            const float mq = sw[h * P + q];
+            const float w = (mq == -INFINITY) ? 0.f : ex2((mq - Ms) * kLog2e);
+            sw[h * P + q] = w;
+            L = fmaf(w, sl[h * P + q], L);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+        if (lane == 0) {
+            sr[h] = M;
+            sr[G + h] = L;
+        }
+    }
+    consumer_sync(nthr);
+    for (int idx = tid; idx < G * D4; idx += nthr) {
+        const int h = idx / D4, d4 = idx - h * D4;
+        const float4* o = reinterpret_cast<const float4*>(p.part_o + (row0 + h) * P * D) + d4;
+        const float* w = sw + h * P;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int q0 = 0; q0 < P; q0 += kBatch) {
+            if (idx != idx0 || q0 != 0) {
+#pragma unroll
+                for (int k = 0; k < kBatch; ++k)
+                    v[k] = (q0 + k < P) ? __ldcg(o + static_cast<size_t>(q0 + k) * D4)
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                const float wk = (q0 + k < P) ? w[q0 + k] : 0.f;
+                acc.x = fmaf(wk, v[k].x, acc.x);
+                acc.y = fmaf(wk, v[k].y, acc.y);
+                acc.z = fmaf(wk, v[k].z, acc.z);
+                acc.w = fmaf(wk, v[k].w, acc.w);
+            }
+        }
+        const float L = sr[G + h];
+        if (L == 0.f) {
+            acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {  // NaN inputs propagate
+            acc.x /= L;
+            acc.y /= L;
+            acc.z /= L;
+            acc.w /= L;
+        }
+        reinterpret_cast<float4*>(p.out + (row0 + h) * D)[d4] = acc;
+        if (d4 == 0 && p.lse) p.lse[row0 + h] = (L > 0.f) ? sr[h] + logf(L) : (L == 0.f ? -INFINITY : L);
+    }
+}
+
+}  // namespace ta

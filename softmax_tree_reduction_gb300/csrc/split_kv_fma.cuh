@@ -18,6 +18,7 @@
 #include "common.cuh"
 #include "emit.cuh"
 #include "kernels.h"
+#include "sched.cuh"
 
 namespace ta {
 namespace fma_detail {
@@ -35,7 +36,7 @@ struct FmaCfg {
     static constexpr int kEPC = 16 / kES;                   // elements per chunk
     static constexpr int kEPL = kCPL * kEPC;                // channels per lane (= D / 8)
     static constexpr int kMergeFloats = kWarps * 4 * D + 2 * 64;
-    static constexpr int kBarBytes = 2 * kStages * 8 + 16;
+    static constexpr int kBarBytes = 2 * kStages * 8 + kStages * 8 + 32;
     static constexpr int kSmem = 1024 + kStages * kStageBytes + kMergeFloats * 4 + kBarBytes;
     static constexpr int kThreads = 32 * (kWarps + 1);
     static_assert(kTile >= 32, "a stage must hold at least 32 tokens");
@@ -77,20 +78,13 @@ __global__ void __launch_bounds__(FmaCfg<KV, D>::kThreads, 1)
     float* mg_l = mg_m + 64;
     uint64_t* full = reinterpret_cast<uint64_t*>(mg_l + 64);
     uint64_t* empty = full + C::kStages;
-    int* abort_flag = reinterpret_cast<int*>(empty + C::kStages);
+    volatile StageMeta* meta = reinterpret_cast<volatile StageMeta*>(empty + C::kStages);
+    int* abort_flag = const_cast<int*>(reinterpret_cast<volatile int*>(meta + C::kStages));
+    int* last_flag = abort_flag + 1;
+    volatile unsigned* claim_sink = reinterpret_cast<volatile unsigned*>(abort_flag + 2);
 
     const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    int N = p.seqlens[b];
-    const bool bad = (N < 0) || (N > p.S);
-    if (bad) {
-        if (threadIdx.x == 0) atomicOr(p.err, kErrBadSeqlen);
-        N = 0;
-    }
-    int t0, t1;
-    slice_bounds(N, p.P, split, C::kTile, t0, t1);
-    const int ntiles = (t1 - t0 + C::kTile - 1) / C::kTile;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
@@ -100,28 +94,31 @@ __global__ void __launch_bounds__(FmaCfg<KV, D>::kThreads, 1)
         *abort_flag = 0;
         fence_barrier_init();
     }
+    if (threadIdx.x == 32) {
+        prefetch_tensormap(&tmK);
+        prefetch_tensormap(&tmV);
+    }
     __syncthreads();
+    // Launched as a programmatic dependent: nothing an earlier kernel may
+    // write is touched before this.
+    wait_primary();
+
+    int N = p.seqlens[b];
+    const bool bad = (N < 0) || (N > p.S);
+    if (bad) {
+        if (threadIdx.x == 0) atomicOr(p.err, kErrBadSeqlen);
+        N = 0;
+    }
 
     if (warp == 0) {
-        if (lane == 0 && ntiles > 0) {
-            prefetch_tensormap(&tmK);
-            prefetch_tensormap(&tmV);
+        if (lane == 0) {
             const uint64_t pol = l2_policy_evict_first();
-            int issued = 0;
-            for (int it = 0; it < ntiles; ++it) {
-                const int s = it % C::kStages;
-                if (it >= C::kStages &&
-                    !mbar_wait(&empty[s], ((it / C::kStages) - 1) & 1, p.err))
-                    break;
-                mbar_arrive_expect_tx(&full[s], C::kStageBytes);
-                uint8_t* st = stages + s * C::kStageBytes;
-                const int y = t0 + it * C::kTile;
-                tma_load_4d(st, &tmK, 0, y, g, b, &full[s], pol);
-                tma_load_4d(st + C::kKBytes, &tmV, 0, y, g, b, &full[s], pol);
-                issued = it + 1;
-            }
-            for (int it = issued > C::kStages ? issued - C::kStages : 0; it < issued; ++it)
-                mbar_wait(&full[it % C::kStages], (it / C::kStages) & 1, p.err);
+            produce_row<C::kStages>(p, b * p.Hkv + g, N, split, C::kTile, full, empty, meta,
+                                    claim_sink, C::kStageBytes, [&](int s, int y) {
+                                        uint8_t* st = stages + s * C::kStageBytes;
+                                        tma_load_4d(st, &tmK, 0, y, g, b, &full[s], pol);
+                                        tma_load_4d(st + C::kKBytes, &tmV, 0, y, g, b, &full[s], pol);
+                                    });
         }
         allow_dependents();
         return;
@@ -165,18 +162,19 @@ __global__ void __launch_bounds__(FmaCfg<KV, D>::kThreads, 1)
     }
     bool timed_out = false;
 
-    for (int it = 0; it < ntiles; ++it) {
+    for (int it = 0;; ++it) {
         const int s = it % C::kStages;
         if (!mbar_wait(&full[s], (it / C::kStages) & 1, p.err)) {
             timed_out = true;
             break;
         }
+        const int tile_valid = meta[s].nvalid;
+        if (tile_valid < 0) break;  // end of this block's work
         const uint8_t* kst = stages + s * C::kStageBytes;
         const uint8_t* vst = kst + C::kKBytes;
-        const int tile0 = t0 + it * C::kTile;
         for (int step = 0; step < steps; ++step) {
             const int row = ts * tok_per_slice + step * 4 + grp;
-            const bool valid = tile0 + row < t1;
+            const bool valid = row < tile_valid;
             float kf[EPL];
 #pragma unroll
             for (int c = 0; c < CPL; ++c) {
@@ -273,6 +271,7 @@ __global__ void __launch_bounds__(FmaCfg<KV, D>::kThreads, 1)
         }
         emit_state(p, b, g * G + h, split, D, dd, ov, lv, M, poison);
     }
+    if (p.done) finish_row<D>(p, b, g, reinterpret_cast<float*>(stages), last_flag, ct, C::kWarps * 32);
     allow_dependents();
 }
 
@@ -283,9 +282,17 @@ cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const Split
     cudaError_t e = cudaFuncSetAttribute(split_kv_fma_kernel<KV, D, GC>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
-    dim3 grid(p.P, p.Hkv, p.B);
-    split_kv_fma_kernel<KV, D, GC><<<grid, C::kThreads, C::kSmem, stream>>>(tk, tv, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.P, p.Hkv, p.B);
+    cfg.blockDim = dim3(C::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, split_kv_fma_kernel<KV, D, GC>, tk, tv, p);
 }
 
 template <typename KV, int D>

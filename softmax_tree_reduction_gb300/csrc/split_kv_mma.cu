@@ -24,6 +24,7 @@
 #include "common.cuh"
 #include "emit.cuh"
 #include "kernels.h"
+#include "sched.cuh"
 
 namespace ta {
 namespace {
@@ -38,7 +39,7 @@ struct MmaCfg {
     static constexpr int kStageBytes = 2 * kKBytes;  // K and V
     static constexpr int kStages = (D == 128) ? 4 : 6;
     static constexpr int kMergeBytes = kWarps * 8 * (D + 2) * 4;
-    static constexpr int kBarBytes = 2 * kStages * 8 + 16;
+    static constexpr int kBarBytes = 2 * kStages * 8 + kStages * 8 + 32;
     static constexpr int kSmem = 1024 + kStages * kStageBytes + kMergeBytes + kBarBytes;
     static constexpr int kThreads = 32 * (kWarps + 1);
 };
@@ -89,20 +90,13 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
     float* mg_l = mg_m + C::kWarps * 8;                                            // [W][8]
     uint64_t* full = reinterpret_cast<uint64_t*>(mg_l + C::kWarps * 8);
     uint64_t* empty = full + C::kStages;
-    int* abort_flag = reinterpret_cast<int*>(empty + C::kStages);
+    volatile StageMeta* meta = reinterpret_cast<volatile StageMeta*>(empty + C::kStages);
+    int* abort_flag = const_cast<int*>(reinterpret_cast<volatile int*>(meta + C::kStages));
+    int* last_flag = abort_flag + 1;
+    volatile unsigned* claim_sink = reinterpret_cast<volatile unsigned*>(abort_flag + 2);
 
     const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    int N = p.seqlens[b];
-    const bool bad = (N < 0) || (N > p.S);
-    if (bad) {
-        if (threadIdx.x == 0) atomicOr(p.err, kErrBadSeqlen);
-        N = 0;
-    }
-    int t0, t1;
-    slice_bounds(N, p.P, split, C::kTile, t0, t1);
-    const int ntiles = (t1 - t0 + C::kTile - 1) / C::kTile;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
@@ -112,34 +106,37 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
         *abort_flag = 0;
         fence_barrier_init();
     }
+    if (threadIdx.x == 32) {
+        prefetch_tensormap(&tmK);
+        prefetch_tensormap(&tmV);
+    }
     __syncthreads();
+    // Launched as a programmatic dependent: nothing an earlier kernel may
+    // write (q, the caches, the lengths, the outputs) is touched before this.
+    wait_primary();
+
+    int N = p.seqlens[b];
+    const bool bad = (N < 0) || (N > p.S);
+    if (bad) {
+        if (threadIdx.x == 0) atomicOr(p.err, kErrBadSeqlen);
+        N = 0;
+    }
 
     if (warp == 0) {
         // ------------------------------------------------------ producer
-        if (lane == 0 && ntiles > 0) {
-            prefetch_tensormap(&tmK);
-            prefetch_tensormap(&tmV);
+        if (lane == 0) {
             const uint64_t pol = l2_policy_evict_first();
-            int issued = 0;
-            for (int it = 0; it < ntiles; ++it) {
-                const int s = it % C::kStages;
-                if (it >= C::kStages &&
-                    !mbar_wait(&empty[s], ((it / C::kStages) - 1) & 1, p.err))
-                    break;
-                mbar_arrive_expect_tx(&full[s], C::kStageBytes);
-                uint8_t* st = stages + s * C::kStageBytes;
-                const int y = t0 + it * C::kTile;
+            produce_row<C::kStages>(p, b * p.Hkv + g, N, split, C::kTile, full, empty, meta,
+                                    claim_sink, C::kStageBytes, [&](int s, int y) {
+                                        uint8_t* st = stages + s * C::kStageBytes;
 #pragma unroll
-                for (int h = 0; h < C::kHalves; ++h) {
-                    tma_load_4d(st + h * C::kBoxBytes, &tmK, h * 64, y, g, b, &full[s], pol);
-                    tma_load_4d(st + C::kKBytes + h * C::kBoxBytes, &tmV, h * 64, y, g, b,
-                                &full[s], pol);
-                }
-                issued = it + 1;
-            }
-            // Do not leave while copies into this block's shared memory are in flight.
-            for (int it = issued > C::kStages ? issued - C::kStages : 0; it < issued; ++it)
-                mbar_wait(&full[it % C::kStages], (it / C::kStages) & 1, p.err);
+                                        for (int h = 0; h < C::kHalves; ++h) {
+                                            tma_load_4d(st + h * C::kBoxBytes, &tmK, h * 64, y, g, b,
+                                                        &full[s], pol);
+                                            tma_load_4d(st + C::kKBytes + h * C::kBoxBytes, &tmV,
+                                                        h * 64, y, g, b, &full[s], pol);
+                                        }
+                                    });
         }
         allow_dependents();
         return;
@@ -179,15 +176,17 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
     const float sl2 = p.scale_log2;
     bool timed_out = false;
 
-    for (int it = 0; it < ntiles; ++it) {
+    for (int it = 0;; ++it) {
         const int s = it % C::kStages;
         if (!mbar_wait(&full[s], (it / C::kStages) & 1, p.err)) {
             timed_out = true;
             break;
         }
+        const int tile_valid = meta[s].nvalid;
+        if (tile_valid < 0) break;  // end of this block's work
         const uint32_t kbase = smem_u32(stages + s * C::kStageBytes);
         const uint32_t vbase = kbase + C::kKBytes;
-        const int nvalid = t1 - (t0 + it * C::kTile + cw * 16);  // valid tokens of this block
+        const int nvalid = tile_valid - cw * 16;  // valid tokens of this warp's 16-token block
 
         if (nvalid > 0) {
             // S^T = K_blk Q^T (two accumulators to shorten the dependency chain)
@@ -312,6 +311,7 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
         const float l = (lw[0] + lw[1]) + (lw[2] + lw[3]);
         emit_state(p, b, g * p.G + h, split, D, dd, o, l, M, poison);
     }
+    if (p.done) finish_row<D>(p, b, g, reinterpret_cast<float*>(stages), last_flag, ct, C::kWarps * 32);
     allow_dependents();
 }
 
@@ -322,9 +322,17 @@ cudaError_t launch_impl(const CUtensorMap& tk, const CUtensorMap& tv, const Spli
     cudaError_t e = cudaFuncSetAttribute(split_kv_mma_kernel<D>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
-    dim3 grid(p.P, p.Hkv, p.B);
-    split_kv_mma_kernel<D><<<grid, C::kThreads, C::kSmem, stream>>>(tk, tv, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.P, p.Hkv, p.B);
+    cfg.blockDim = dim3(C::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<D>, tk, tv, p);
 }
 
 }  // namespace

@@ -150,7 +150,7 @@ def test_decode_argument_errors_before_any_cuda_call(ta):
     assert _decode_raw(ta, f32, opts=ta.TaOptions(2, 0, None, None)) == -4   # mma needs bf16
     assert _decode_raw(ta, shape(ta, num_q_heads=128, num_kv_heads=8),
                        opts=ta.TaOptions(2, 0, None, None)) == -4          # mma needs G <= 8
-    assert _decode_raw(ta, s, opts=ta.TaOptions(0, 1, None, None)) == -3  # reserved != 0
+    assert _decode_raw(ta, s, opts=ta.TaOptions(0, 2, None, None)) == -3  # unknown flag bit
     assert _decode_raw(ta, s, opts=ta.TaOptions(9, 0, None, None)) == -3  # unknown kernel
 
 

@@ -158,23 +158,38 @@ def test_heuristic_split_count_runs():
     assert_close(out, lse, ref_o, ref_l, torch.bfloat16, "heuristic")
 
 
-@pytest.mark.parametrize("kern,P", [("mma", 1), ("mma", 19), ("fma", 19), ("mma", 256)])
+@pytest.mark.parametrize("kern,P", [("mma", 1), ("mma", 19), ("fma", 19), ("mma", 256), ("fma", 3)])
 def test_bitwise_determinism(kern, P):
+    """With the deterministic flag the chunk assignment is fixed: bitwise equal runs."""
     dev = to_dev(_llama_like(seed=3))
-    a = decode(dev, num_splits=P, kernel=kern)
-    b = decode(dev, num_splits=P, kernel=kern)
+    a = decode(dev, num_splits=P, kernel=kern, deterministic=True)
+    b = decode(dev, num_splits=P, kernel=kern, deterministic=True)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("kern", ["mma", "fma"])
+def test_balanced_and_deterministic_schedules_agree(kern):
+    """Run-time chunk balancing only reorders the merge: results agree to rounding."""
+    inp = _llama_like(seed=4)
+    ref_o, ref_l = oracle.attention(inp["q"], inp["k"], inp["v"], inp["seqlens"])
+    dev = to_dev(inp)
+    d_o, d_l = decode(dev, num_splits=19, kernel=kern, deterministic=True)
+    for _ in range(3):
+        o, l = decode(dev, num_splits=19, kernel=kern)
+        assert np.max(np.abs(o - d_o)) <= 1e-5 and np.max(np.abs(l - d_l)) <= 1e-5
+        assert_close(o, l, ref_o, ref_l, torch.bfloat16, f"{kern} balanced")
 
 
 def test_token_major_layout_matches_dense():
     """K/V stored [B, S, Hkv, d] (token-major) and passed with strides."""
     inp = _llama_like(N=5000, B=2, seed=5)
     dev = to_dev(inp)
-    out_d, lse_d = decode(dev, num_splits=7)
+    out_d, lse_d = decode(dev, num_splits=7, deterministic=True)
     km = dev["k"].permute(0, 2, 1, 3).contiguous().permute(0, 2, 1, 3)   # [B,Hkv,S,d] view
     vm = dev["v"].permute(0, 2, 1, 3).contiguous().permute(0, 2, 1, 3)
     assert not km.is_contiguous()
-    out_t, lse_t = ta.tree_attn_decode(dev["q"], km, vm, dev["seqlens"], num_splits=7)
+    out_t, lse_t = ta.tree_attn_decode(dev["q"], km, vm, dev["seqlens"], num_splits=7,
+                                       deterministic=True)
     torch.cuda.synchronize()
     assert np.array_equal(out_t.double().cpu().numpy(), out_d)
     assert np.array_equal(lse_t.double().cpu().numpy(), lse_d)
@@ -275,3 +290,13 @@ def test_full_llama3_70b():
 @pytest.mark.slow
 def test_full_million_token():
     _check_full(workloads.MILLION_TOKEN, [64, 512, 2048], n_groups=2)
+
+
+@pytest.mark.parametrize("P", [64, 1024, 1025, 4096])
+def test_fused_and_launched_combine_paths(P):
+    """G*P <= 8192 merges in the row's last block; above that the combine kernel runs.
+    Many slices here are empty (more blocks than chunks)."""
+    inp = _llama_like(N=16384, G=8, seed=9)
+    ref_o, ref_l = oracle.attention(inp["q"], inp["k"], inp["v"], inp["seqlens"])
+    out, lse = decode(to_dev(inp), num_splits=P)
+    assert_close(out, lse, ref_o, ref_l, torch.bfloat16, f"P={P}")
