@@ -44,8 +44,8 @@ FALLBACK_HBM_GBS = 6800.0
 NCU_TRAFFIC = {
     # profiles/split_kv_mma_llama31_8b_131k.md
     ("mma", "llama3.1-8b-decode-layer"): {
-        "bytes_per_launch": 536914944 + 2909184, "num_splits": 19,
-        "src_sha256": "d17b0918223c1a8d648c0b788c31c9dc1645b9e53a8a212f579b5f86daab9ded"},
+        "bytes_per_launch": 536935168 + 3162368, "num_splits": 19,
+        "src_sha256": "b5542e81ecd09c4d943b901807d4322582c52f57c1874260a222595314c29272"},
 }
 
 
@@ -71,6 +71,8 @@ def parse_args(argv=None):
                     help="comma list of context lengths for the workload's head shape (heuristic splits): "
                          "print one JSON line per length, then exit")
     ap.add_argument("--sweep-kernels", default="mma,fma")
+    ap.add_argument("--graph", action="store_true",
+                    help="sweeps: capture the timed steps in one CUDA graph (removes the host's per-call cost)")
     ap.add_argument("--deterministic", action="store_true",
                     help="fixed chunk assignment (bitwise reproducible) instead of run-time balancing")
     return ap.parse_args(argv)
@@ -97,7 +99,7 @@ def load_peaks():
 def kernel_source_hash(kernel):
     name = {"mma": "split_kv_mma.cu", "fma": "split_kv_fma.cuh"}[kernel]
     h = hashlib.sha256()
-    for f in (name, "common.cuh", "emit.cuh"):
+    for f in (name, "common.cuh", "emit.cuh", "sched.cuh"):
         with open(os.path.join(ROOT, "softmax_tree_reduction_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
@@ -203,6 +205,23 @@ def barrier(world):
         dist.barrier()
 
 
+L2_BYTES = 126.5 * 2**20   # GB300 L2 (the device reports its own size; this is the default)
+
+
+def l2_note(kv_bytes, copies):
+    try:
+        import torch
+        l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+    except Exception:
+        l2 = L2_BYTES
+    mib = kv_bytes / 2**20
+    if kv_bytes > l2:
+        return (f"inputs larger than L2: {copies} K+V copies of {mib:.0f} MiB alternated step to step "
+                f"(L2 {l2 / 2**20:.0f} MiB)")
+    return (f"inputs fit in L2 ({copies} x {mib:.1f} MiB K+V vs {l2 / 2**20:.0f} MiB L2, not flushed): "
+            "a latency figure, not an HBM one")
+
+
 # ------------------------------------------------------------- CPU oracle
 def oracle_baseline(w, inp, target_s, max_s=30.0):
     """Time the float64 oracle as it stands on the host's cores.
@@ -258,7 +277,8 @@ def run_ours(args, rank, world, local):
     def step(i, events=None):
         c = copies[i & 1]
         ta.tree_attn_decode(c["q"], c["k"], c["v"], c["seqlens"], out=out, lse=lse, num_splits=P,
-                            workspace=ws, kernel=args.kernel, split_events=events)
+                            workspace=ws, kernel=args.kernel, split_events=events,
+                            deterministic=args.deterministic)
 
     for i in range(max(args.warmup, 3)):
         step(i)
@@ -282,7 +302,7 @@ def run_ours(args, rank, world, local):
     sampler.mark_stop()
     barrier(world)
     elapsed_ms = e0.elapsed_time(e1)
-    launches = ta.tree_attn_launch_count(shape, P, args.kernel)
+    launches = ta.tree_attn_launch_count(shape, P, args.kernel, args.deterministic)
     if launches == 1:
         # the step is the split-KV kernel alone: its launch duration is the step time
         split_ms = elapsed_ms / args.steps
@@ -362,8 +382,9 @@ def run_ours(args, rank, world, local):
         "config": {"workload": f"{w.name}: {w.description}", "batch": w.batch,
                    "seq_len": int(max(inp['seqlens'])), "num_q_heads": w.num_q_heads,
                    "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "num_splits": P,
-                   "kernel": kernel_used, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": "inputs larger than L2: two 512 MiB K+V copies alternated step to step"},
+                   "kernel": kernel_used, "deterministic": args.deterministic,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": l2_note(kv_bytes, len(copies))},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
@@ -378,9 +399,11 @@ def run_ours(args, rank, world, local):
 
 
 # ----------------------------------------------------------------- sweeps
-def _time_steps(ta, torch, copies, P, kernel, steps, warmup, out, lse, ws, deterministic=False):
+def _time_steps(ta, torch, copies, P, kernel, steps, warmup, out, lse, ws, deterministic=False,
+                graph=False):
     """(ms per step, split-kernel ms) over ``steps`` decode calls; when the step
-    is a single kernel the two are the same number."""
+    is a single kernel the two are the same number.  With ``graph`` the steps
+    are captured once in a CUDA graph and the replay is timed."""
     def step(i, events=None):
         c = copies[i % len(copies)]
         ta.tree_attn_decode(c["q"], c["k"], c["v"], c["seqlens"], out=out, lse=lse, num_splits=P,
@@ -389,14 +412,27 @@ def _time_steps(ta, torch, copies, P, kernel, steps, warmup, out, lse, ws, deter
     for i in range(warmup):
         step(i)
     torch.cuda.synchronize()
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(steps):
+                step(i)
+        g.replay()
+        torch.cuda.synchronize()
     s = torch.cuda.current_stream()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(s)
-    for i in range(steps):
-        step(i)
+    if graph:
+        g.replay()
+    else:
+        for i in range(steps):
+            step(i)
     b.record(s)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / steps
+    if graph:
+        assert ta.tree_attn_get_device_error() == 0
+        return ms, ms
     shape = ta.make_shape(copies[0]["q"], copies[0]["k"])
     if ta.tree_attn_launch_count(shape, P, kernel, deterministic) == 1:
         assert ta.tree_attn_get_device_error() == 0
@@ -452,9 +488,9 @@ def run_sweeps(args):
                 ws = torch.empty(max(16, ta.tree_attn_workspace_bytes(shape, P)), dtype=torch.uint8,
                                  device="cuda")
                 ms, split = _time_steps(ta, torch, copies, P, kern, args.steps, args.warmup, out, lse, ws,
-                                        args.deterministic)
+                                        args.deterministic, args.graph)
                 lines.append({"sweep": "splits", "workload": w.name, "kernel": kern, "num_splits": P,
-                              "deterministic": args.deterministic,
+                              "deterministic": args.deterministic, "graph": args.graph,
                               "heuristic": P == heur, "us_per_step": round(ms * 1e3, 3),
                               "split_kernel_us": round(split * 1e3, 3),
                               "step_gbs": round(kv_bytes / (ms / 1e3) / 1e9, 1),
@@ -475,8 +511,10 @@ def run_sweeps(args):
             ws = torch.empty(max(16, ta.tree_attn_workspace_bytes(shape, P)), dtype=torch.uint8,
                              device="cuda")
             ms, split = _time_steps(ta, torch, copies, P, args.kernel, args.steps, args.warmup, out, lse, ws,
-                                    args.deterministic)
+                                    args.deterministic, args.graph)
             lines.append({"sweep": "context", "workload": w.name, "context": N, "num_splits": P,
+                          "graph": args.graph, "l2": "fits" if w.kv_bytes(np.full(w.batch, N)) * len(copies)
+                          < L2_BYTES else "exceeds",
                           "us_per_step": round(ms * 1e3, 3), "split_kernel_us": round(split * 1e3, 3),
                           "step_gbs": round(kv_bytes / (ms / 1e3) / 1e9, 1),
                           "frac_of_measured_peak": round(kv_bytes / (ms / 1e3) / 1e9 / peak, 4)})

@@ -102,10 +102,12 @@ typedef enum {
 } ta_kernel;
 
 /* Bits of ta_options.flags. */
-#define TA_FLAG_DETERMINISTIC 1  /* assign each slice a fixed, strided set of chunks instead of
-                                    balancing chunks between a row's blocks at run time: results
-                                    are then bitwise reproducible for a given num_splits (the
-                                    default balancing changes the rounding order run to run) */
+#define TA_FLAG_DETERMINISTIC 1  /* give slice p the fixed contiguous range [p*c, (p+1)*c) of
+                                    its row instead of balancing the last eighth of the row
+                                    between the row's blocks at run time: results are then
+                                    bitwise reproducible for a given num_splits (balancing,
+                                    used by default when the grid is at most four waves of
+                                    blocks, changes the rounding order from run to run) */
 
 /* Optional per-call settings (pass NULL for defaults). */
 typedef struct {
@@ -165,8 +167,8 @@ int tree_attn_decode(const ta_shape *shape, const void *q, const void *k_cache,
 
 /* Number of kernels tree_attn_decode_ex enqueues for this shape, split count
  * and options: 1 when the partial states are merged inside the per-slice
- * kernel (num_splits == 1, or num_splits * Hq/Hkv <= 8192), else 2 (the
- * per-slice kernel, then the combine).  num_splits <= 0 queries the current
+ * kernel (num_splits == 1, or num_splits <= 40), else 2 (the per-slice
+ * kernel, then the combine).  num_splits <= 0 queries the current
  * device for the heuristic's choice.  Negative ta_status on invalid input. */
 int tree_attn_launch_count(const ta_shape *shape, int num_splits, const ta_options *options);
 

@@ -29,9 +29,18 @@ __device__ unsigned g_sched_ring[kRingSlots];
 
 // Tiles per scheduled chunk of a row (128 tokens with 64-token tiles).
 constexpr int kChunkTiles = 2;
-// The row's last block merges the partial states itself when G*P states fit
-// in its (then idle) stage buffers; otherwise the combine kernel runs.
+// The row's last block merges the partial states itself when there are few
+// of them (its merge costs about one L2 round trip per 20 states, serially);
+// more splits go to the combine kernel, which spreads the merge over (h, b)
+// blocks.  G*P states must also fit in the block's idle stage buffers.
+constexpr int kFusedMaxSplits = 40;
+// Chunks are balanced at run time only for grids of at most this many waves.
+constexpr int64_t kBalanceMaxWaves = 4;
 constexpr int kFusedMaxStates = 8192;
+
+bool fuse_merge(int G, int P) {
+    return P <= kFusedMaxSplits && static_cast<int64_t>(G) * P <= kFusedMaxStates;
+}
 
 constexpr int kMaxDevices = 64;
 
@@ -400,8 +409,12 @@ int tree_attn_decode_ex(const ta_shape* shape, const void* q, const void* k_cach
         const unsigned rows = static_cast<unsigned>(shape->batch) * shape->num_kv_heads;
         unsigned* slots = reserve_slots(ds, 2 * rows);
         if (slots) {
-            if (!deterministic) p.claim = slots;
-            fused = static_cast<int64_t>(p.G) * P <= kFusedMaxStates;
+            // Run-time balancing pays while the grid is a few waves at most; with
+            // more waves the block scheduler balances and claims only add latency.
+            const int64_t blocks = static_cast<int64_t>(rows) * P;
+            const int64_t resident = static_cast<int64_t>(ds->num_sms) * blocks_per_sm(shape, kernel);
+            if (!deterministic && blocks <= kBalanceMaxWaves * resident) p.claim = slots;
+            fused = fuse_merge(p.G, P);
             p.fuse = fused ? 1 : 0;
             if (p.claim || fused) p.done = slots + rows;
         }
@@ -446,7 +459,7 @@ int tree_attn_launch_count(const ta_shape* shape, int num_splits, const ta_optio
     const int64_t G = shape->num_q_heads / shape->num_kv_heads;
     const unsigned rows = static_cast<unsigned>(shape->batch) * shape->num_kv_heads;
     const bool have_slots = 2 * static_cast<uint64_t>(rows) <= kRingSlots;
-    return (have_slots && G * P <= kFusedMaxStates) ? 1 : 2;
+    return (have_slots && fuse_merge(static_cast<int>(G), P)) ? 1 : 2;
 }
 
 int tree_attn_decode(const ta_shape* shape, const void* q, const void* k_cache,

@@ -1,12 +1,14 @@
 // Cross-block tree combine ("The Tree Reduction Merge Operator" over the P
 // partial states of every (b, h), then the root normalisation O = o / l).
 //
-// One 128-thread block per (h, b).  The root maximum M = max_p m_p is found
-// first (a block max-reduction), so every leaf's rescale factor
-// exp(m_p - M) is applied directly -- the merge tree with its maxima already
-// resolved.  The numerators are then folded by G groups of threads (group r
-// takes p = r, r + G, ...; each thread owns four channels) and the group sums
-// are merged pairwise in shared memory.  An empty slice (m = -inf, l = 0)
+// One block per (h, b): 128 threads for up to 64 states, 512 for more (the
+// fold is bound by loads in flight, so larger P gets more of them).  The root
+// maximum M = max_p m_p is found first (a block max-reduction), so every
+// leaf's rescale factor exp(m_p - M) is applied directly -- the merge tree
+// with its maxima already resolved.  The numerators are then folded by groups
+// of threads (group r takes p = r, r + groups, ...; each thread owns four
+// channels; eight loads in flight per thread) and the group sums are merged
+// pairwise in shared memory.  An empty slice (m = -inf, l = 0)
 // contributes nothing; all-empty rows give out = 0, lse = -inf; NaN inputs
 // propagate to the row's outputs.
 #include "common.cuh"
@@ -15,9 +17,7 @@
 namespace ta {
 namespace {
 
-constexpr int kCombineThreads = 128;
-
-template <int D>
+template <int D, int kCombineThreads>
 __global__ void __launch_bounds__(kCombineThreads)
     combine_kernel(const float* __restrict__ po, const float* __restrict__ pm,
                    const float* __restrict__ pl, float* __restrict__ out, float* __restrict__ lse,
@@ -53,7 +53,7 @@ __global__ void __launch_bounds__(kCombineThreads)
     const int c4 = tid % kTPR, grp = tid / kTPR;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float lacc = 0.f;
-#pragma unroll 4
+#pragma unroll 8
     for (int q = grp; q < P; q += kGroups) {
         const float mq = m[q];
         const float w = (mq == -INFINITY) ? 0.f : ex2((mq - Ms) * kLog2e);
@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(kCombineThreads)
     }
 }
 
-template <int D>
+template <int D, int kCombineThreads>
 cudaError_t launch_impl(const float* po, const float* pm, const float* pl, float* out, float* lse,
                         int B, int Hq, int P, bool dependent, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
@@ -110,7 +110,7 @@ cudaError_t launch_impl(const float* po, const float* pm, const float* pl, float
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = dependent ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, combine_kernel<D>, po, pm, pl, out, lse, Hq, P);
+    return cudaLaunchKernelEx(&cfg, combine_kernel<D, kCombineThreads>, po, pm, pl, out, lse, Hq, P);
 }
 
 }  // namespace
@@ -118,9 +118,14 @@ cudaError_t launch_impl(const float* po, const float* pm, const float* pl, float
 cudaError_t launch_combine(int head_dim, const float* po, const float* pm, const float* pl,
                            float* out, float* lse, int B, int Hq, int P, bool dependent,
                            cudaStream_t stream) {
+    const bool wide = P > 64;
     switch (head_dim) {
-        case 64: return launch_impl<64>(po, pm, pl, out, lse, B, Hq, P, dependent, stream);
-        case 128: return launch_impl<128>(po, pm, pl, out, lse, B, Hq, P, dependent, stream);
+        case 64:
+            return wide ? launch_impl<64, 512>(po, pm, pl, out, lse, B, Hq, P, dependent, stream)
+                        : launch_impl<64, 128>(po, pm, pl, out, lse, B, Hq, P, dependent, stream);
+        case 128:
+            return wide ? launch_impl<128, 512>(po, pm, pl, out, lse, B, Hq, P, dependent, stream)
+                        : launch_impl<128, 128>(po, pm, pl, out, lse, B, Hq, P, dependent, stream);
         default: return cudaErrorInvalidValue;
     }
 }

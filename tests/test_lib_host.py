@@ -175,3 +175,16 @@ def test_binding_refuses_cpu_tensors(ta):
     k = torch.zeros(1, 1, 8, 64)
     with pytest.raises(ValueError):
         ta.tree_attn_decode(q, k, k, torch.zeros(1, dtype=torch.int32))
+
+
+def test_launch_count(ta):
+    s = shape(ta)
+    assert ta.tree_attn_launch_count(s, 1) == 1
+    assert ta.tree_attn_launch_count(s, 19) == 1
+    assert ta.tree_attn_launch_count(s, 40) == 1
+    assert ta.tree_attn_launch_count(s, 41) == 2
+    assert ta.tree_attn_launch_count(s, 4096) == 2
+    with pytest.raises(ta.TreeAttnError):
+        ta.tree_attn_launch_count(s, 5000)
+    with pytest.raises(ta.TreeAttnError):
+        ta.tree_attn_launch_count(shape(ta, head_dim=48), 4)

@@ -292,11 +292,40 @@ def test_full_million_token():
     _check_full(workloads.MILLION_TOKEN, [64, 512, 2048], n_groups=2)
 
 
-@pytest.mark.parametrize("P", [64, 1024, 1025, 4096])
+@pytest.mark.parametrize("P", [40, 41, 64, 1024, 4096])
 def test_fused_and_launched_combine_paths(P):
-    """G*P <= 8192 merges in the row's last block; above that the combine kernel runs.
+    """Up to 40 splits merge in the row's last block; more go to the combine kernel.
     Many slices here are empty (more blocks than chunks)."""
     inp = _llama_like(N=16384, G=8, seed=9)
     ref_o, ref_l = oracle.attention(inp["q"], inp["k"], inp["v"], inp["seqlens"])
-    out, lse = decode(to_dev(inp), num_splits=P)
+    dev = to_dev(inp)
+    assert ta.tree_attn_launch_count(ta.make_shape(dev["q"], dev["k"]), P) == (1 if P <= 40 else 2)
+    out, lse = decode(dev, num_splits=P)
     assert_close(out, lse, ref_o, ref_l, torch.bfloat16, f"P={P}")
+
+
+def test_cuda_graph_capture_and_replay():
+    """tree_attn_decode enqueues only kernels on the caller's stream, so a
+    sequence of calls can be captured once and replayed."""
+    inp = _llama_like(N=8192, seed=12)
+    ref_o, ref_l = oracle.attention(inp["q"], inp["k"], inp["v"], inp["seqlens"])
+    dev = to_dev(inp)
+    out = torch.empty(1, 32, 128, device="cuda")
+    lse = torch.empty(1, 32, device="cuda")
+    shape = ta.make_shape(dev["q"], dev["k"])
+    ws = torch.empty(ta.tree_attn_workspace_bytes(shape, 19), dtype=torch.uint8, device="cuda")
+    ta.tree_attn_decode(dev["q"], dev["k"], dev["v"], dev["seqlens"], out=out, lse=lse, num_splits=19,
+                        workspace=ws)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(3):
+            ta.tree_attn_decode(dev["q"], dev["k"], dev["v"], dev["seqlens"], out=out, lse=lse,
+                                num_splits=19, workspace=ws)
+    for _ in range(2):
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert_close(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_o, ref_l,
+                     torch.bfloat16, "graph replay")
+    assert ta.tree_attn_get_device_error() == 0
