@@ -27,8 +27,8 @@ __device__ int g_error_word;  // bits ta::kErrBadSeqlen | ta::kErrTimeout
 constexpr unsigned kRingSlots = 1u << 20;
 __device__ unsigned g_sched_ring[kRingSlots];
 
-// Tiles per scheduled chunk of a row (128 tokens with 64-token tiles).
-constexpr int kChunkTiles = 2;
+// Tokens per run-time scheduled chunk of a row (rounded to whole tiles).
+constexpr int kChunkTokens = 128;
 // The row's last block merges the partial states itself when there are few
 // of them (its merge costs about one L2 round trip per 20 states, serially);
 // more splits go to the combine kernel, which spreads the merge over (h, b)
@@ -162,10 +162,11 @@ Geometry geometry_of(const ta_shape* s, int kernel) {
 }
 
 // Resident thread blocks per SM of each kernel family (shared memory bound:
-// the MMA kernel's ring is ~145 KB at d = 128 and ~105 KB at d = 64; the FMA
-// kernel's ~113 KB with 288 threads of ~170 registers).
+// the MMA kernel's ring is 192 KB; the FMA kernel's ~113 KB with 288 threads
+// of ~170 registers).
 int blocks_per_sm(const ta_shape* s, int kernel) {
-    if (kernel == TA_KERNEL_MMA) return s->head_dim == 64 ? 2 : 1;
+    (void)s;
+    (void)kernel;
     return 1;
 }
 
@@ -397,7 +398,7 @@ int tree_attn_decode_ex(const ta_shape* shape, const void* q, const void* k_cach
     const float scale = shape->scale > 0.f ? shape->scale
                                            : 1.0f / std::sqrt(static_cast<float>(shape->head_dim));
     p.scale_log2 = scale * ta::kLog2e;
-    p.chunk_tiles = kChunkTiles;
+    p.chunk_tiles = std::max(1, kChunkTokens / geo.tile_tokens);
     p.out = out;
     p.lse = lse;
     bool fused = false;

@@ -6,10 +6,11 @@
 // Attention pages), then merges the states of its warps with the merge
 // operator ("The Tree Reduction Merge Operator").
 //
-//  warp 0      producer: one lane streams K and V tiles (64 tokens x 128 B
+//  warp 0      producer: one lane streams K and V tiles (128 tokens x 128 B
 //              boxes, 128-byte swizzle) HBM -> shared memory with TMA into a
 //              ring of stages guarded by full/empty mbarriers.
-//  warps 1..4  consumers: each owns 16 tokens of every stage.
+//  warps 1..8  consumers: each owns 16 tokens of every 128-token stage (two
+//              warps per SM sub-partition hide each other's latencies).
 //     S^T[16 tok x 8 heads] = K_blk . Q^T      mma.m16n8k16 (A = K via ldmatrix,
 //                                              B = q, resident in registers)
 //     online softmax over the block            FP32, base 2, per head
@@ -31,18 +32,30 @@ namespace {
 
 template <int D>
 struct MmaCfg {
-    static constexpr int kWarps = 4;                 // consumer warps
+    static constexpr int kWarps = 8;                 // consumer warps (two per SM sub-partition)
     static constexpr int kTile = 16 * kWarps;        // tokens per stage
     static constexpr int kHalves = D / 64;           // 128-byte column blocks per row
     static constexpr int kBoxBytes = kTile * 128;    // one TMA box
     static constexpr int kKBytes = kHalves * kBoxBytes;
     static constexpr int kStageBytes = 2 * kKBytes;  // K and V
-    static constexpr int kStages = (D == 128) ? 4 : 6;
-    static constexpr int kMergeBytes = kWarps * 8 * (D + 2) * 4;
+    static constexpr int kStages = (D == 128) ? 3 : 6;
     static constexpr int kBarBytes = 2 * kStages * 8 + kStages * 8 + 32;
-    static constexpr int kSmem = 1024 + kStages * kStageBytes + kMergeBytes + kBarBytes;
+    // the warps' states are merged in the stage buffers once streaming is over
+    static constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes;
     static constexpr int kThreads = 32 * (kWarps + 1);
+    static_assert(kWarps * 8 * (D + 2) * 4 <= kStages * kStageBytes, "merge buffer");
+    static_assert(kTile <= 256, "TMA box height");
 };
+
+// Pairwise tree sum of N values (N a power of two).
+template <int N>
+__device__ __forceinline__ float tree_sum(const float* v) {
+    if constexpr (N == 1) {
+        return v[0];
+    } else {
+        return tree_sum<N / 2>(v) + tree_sum<N / 2>(v + N / 2);
+    }
+}
 
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -85,10 +98,10 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* stages = smem;
-    float* mg_o = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes);  // [W][8][D]
-    float* mg_m = mg_o + C::kWarps * 8 * D;                                        // [W][8]
-    float* mg_l = mg_m + C::kWarps * 8;                                            // [W][8]
-    uint64_t* full = reinterpret_cast<uint64_t*>(mg_l + C::kWarps * 8);
+    float* mg_o = reinterpret_cast<float*>(stages);  // [W][8][D], after streaming
+    float* mg_m = mg_o + C::kWarps * 8 * D;          // [W][8]
+    float* mg_l = mg_m + C::kWarps * 8;              // [W][8]
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
     uint64_t* empty = full + C::kStages;
     volatile StageMeta* meta = reinterpret_cast<volatile StageMeta*>(empty + C::kStages);
     int* abort_flag = const_cast<int*>(reinterpret_cast<volatile int*>(meta + C::kStages));
@@ -272,6 +285,7 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
         l0 += __shfl_xor_sync(0xffffffffu, l0, off);
         l1 += __shfl_xor_sync(0xffffffffu, l1, off);
     }
+    consumer_sync(C::kWarps * 32);  // every warp is done reading the stages
     float* mo = mg_o + cw * 8 * D;
 #pragma unroll
     for (int mt = 0; mt < D / 16; ++mt) {
@@ -306,9 +320,9 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
             ow[w] = wt * mg_o[(w * 8 + h) * D + dd];
             lw[w] = wt * mg_l[w * 8 + h];
         }
-        // pairwise tree over the four warps
-        const float o = (ow[0] + ow[1]) + (ow[2] + ow[3]);
-        const float l = (lw[0] + lw[1]) + (lw[2] + lw[3]);
+        // pairwise tree over the warps
+        const float o = tree_sum<C::kWarps>(ow);
+        const float l = tree_sum<C::kWarps>(lw);
         emit_state(p, b, g * p.G + h, split, D, dd, o, l, M, poison);
     }
     if (p.done) finish_row<D>(p, b, g, reinterpret_cast<float*>(stages), last_flag, ct, C::kWarps * 32);
@@ -339,7 +353,7 @@ cudaError_t launch_impl(const CUtensorMap& tk, const CUtensorMap& tv, const Spli
 
 Geometry mma_geometry(int head_dim) {
     (void)head_dim;
-    return Geometry{16 * 4, 64, 1};
+    return Geometry{MmaCfg<128>::kTile, 64, 1};
 }
 
 cudaError_t launch_split_mma(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv,
