@@ -71,6 +71,10 @@ def parse_args(argv=None):
                     help="comma list of context lengths for the workload's head shape (heuristic splits): "
                          "print one JSON line per length, then exit")
     ap.add_argument("--sweep-kernels", default="mma,fma")
+    ap.add_argument("--paged", type=int, default=0,
+                    help="run through the paged-KV entry point with this page size (pages shuffled in a pool)")
+    ap.add_argument("--paged-layout", choices=["NHD", "HND"], default="NHD",
+                    help="page layout: [pages][page][heads][d] (NHD) or [pages][heads][page][d] (HND)")
     ap.add_argument("--graph", action="store_true",
                     help="sweeps: capture the timed steps in one CUDA graph (removes the host's per-call cost)")
     ap.add_argument("--deterministic", action="store_true",
@@ -244,6 +248,16 @@ def oracle_baseline(w, inp, target_s, max_s=30.0):
                       f"with {threads} OpenMP threads on {os.cpu_count()} host cores"}
 
 
+def _clone_view(t):
+    """A copy with the same strides (clone() of a permuted view keeps its layout)."""
+    return t.clone(memory_format=torch_preserve_format())
+
+
+def torch_preserve_format():
+    import torch
+    return torch.preserve_format
+
+
 # ------------------------------------------------------------ our GPU arm
 def run_ours(args, rank, world, local):
     import torch
@@ -259,9 +273,18 @@ def run_ours(args, rank, world, local):
     inp = workloads.make_inputs(w)
     kv_bytes = w.kv_bytes(inp["seqlens"])
     dev = {k: inp[k].cuda() for k in ("q", "k", "v", "seqlens")}
+    if args.paged:
+        kp, vp, bt = workloads.page_pool(inp["k"], inp["v"], inp["seqlens"], args.paged, seed=w.seed,
+                                         layout=args.paged_layout)
+        dev.update(k=kp.cuda(), v=vp.cuda(), block_table=bt.cuda())
+        del kp, vp
     # two copies of the KV cache, alternated step to step (each far larger than L2)
-    copies = [dev, {"q": dev["q"], "k": dev["k"].clone(), "v": dev["v"].clone(), "seqlens": dev["seqlens"]}]
-    shape = ta.make_shape(dev["q"], dev["k"])
+    copies = [dev, dict(dev, k=_clone_view(dev["k"]), v=_clone_view(dev["v"]))]
+    shape = (ta.make_shape(dev["q"], inp["k"]) if not args.paged else
+             ta.TaShape(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.max_seqlen,
+                        ta.TA_BF16 if w.q_dtype == torch.bfloat16 else ta.TA_F32,
+                        ta.TA_BF16 if w.kv_dtype == torch.bfloat16 else ta.TA_F32, 0.0,
+                        dev["k"].stride(0), dev["k"].stride(2), dev["k"].stride(1)))
     P = args.num_splits if args.num_splits > 0 else ta.tree_attn_pick_splits(shape)
     kernel_used = args.kernel
     if kernel_used == "auto":
@@ -276,6 +299,11 @@ def run_ours(args, rank, world, local):
 
     def step(i, events=None):
         c = copies[i & 1]
+        if args.paged:
+            ta.tree_attn_decode_paged(c["q"], c["k"], c["v"], c["block_table"], c["seqlens"], out=out,
+                                      lse=lse, num_splits=P, workspace=ws, kernel=args.kernel,
+                                      deterministic=args.deterministic, max_seqlen=w.max_seqlen)
+            return
         ta.tree_attn_decode(c["q"], c["k"], c["v"], c["seqlens"], out=out, lse=lse, num_splits=P,
                             workspace=ws, kernel=args.kernel, split_events=events,
                             deterministic=args.deterministic)
@@ -303,7 +331,7 @@ def run_ours(args, rank, world, local):
     barrier(world)
     elapsed_ms = e0.elapsed_time(e1)
     launches = ta.tree_attn_launch_count(shape, P, args.kernel, args.deterministic)
-    if launches == 1:
+    if launches == 1 or args.paged:
         # the step is the split-KV kernel alone: its launch duration is the step time
         split_ms = elapsed_ms / args.steps
     else:
@@ -331,7 +359,8 @@ def run_ours(args, rank, world, local):
     e2e = None
     if not args.no_e2e:
         n_e2e = max(1, min(args.e2e_steps, args.steps))
-        host = {k: inp[k].pin_memory() for k in ("q", "k", "v", "seqlens")}
+        host = {k: (dev[k].cpu() if args.paged and k in ("k", "v", "block_table") else inp[k]).pin_memory()
+                for k in (("q", "k", "v", "seqlens", "block_table") if args.paged else ("q", "k", "v", "seqlens"))}
         dbuf = {k: torch.empty_like(host[k], device="cuda") for k in host}
         h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
@@ -341,8 +370,13 @@ def run_ours(args, rank, world, local):
         def e2e_step():
             for k in host:
                 dbuf[k].copy_(host[k], non_blocking=True)
-            ta.tree_attn_decode(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["seqlens"], out=out, lse=lse,
-                                num_splits=P, workspace=ws, kernel=args.kernel)
+            if args.paged:
+                ta.tree_attn_decode_paged(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["block_table"],
+                                          dbuf["seqlens"], out=out, lse=lse, num_splits=P, workspace=ws,
+                                          kernel=args.kernel, max_seqlen=w.max_seqlen)
+            else:
+                ta.tree_attn_decode(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["seqlens"], out=out, lse=lse,
+                                    num_splits=P, workspace=ws, kernel=args.kernel)
             h_out.copy_(out, non_blocking=True)
             h_lse.copy_(lse, non_blocking=True)
 
@@ -383,6 +417,9 @@ def run_ours(args, rank, world, local):
                    "seq_len": int(max(inp['seqlens'])), "num_q_heads": w.num_q_heads,
                    "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "num_splits": P,
                    "kernel": kernel_used, "deterministic": args.deterministic,
+                   "kv_layout": f"paged ({args.paged_layout}), {args.paged}-token pages shuffled in a pool"
+                   if args.paged
+                   else "dense [B][Hkv][S][d]",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": l2_note(kv_bytes, len(copies))},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",

@@ -178,6 +178,34 @@ int tree_attn_decode_ex(const ta_shape *shape, const void *q, const void *k_cach
                         int num_splits, void *workspace, size_t workspace_bytes,
                         const ta_options *options, void *stream);
 
+/* Paged KV cache: the K and V caches are pools of fixed-size pages, and a
+ * block table maps each sequence's logical pages to physical pages (the
+ * layout of paged-attention serving engines).  Token t of batch row b lives
+ * in physical page block_table[b][t / page_size] at position t % page_size.
+ * With this, ta_shape's strides describe one pool: element (page, t_in_page,
+ * g, i) is at page*kv_stride_b + t_in_page*kv_stride_t + g*kv_stride_h + i;
+ * all three 0 select [num_pages][page_size][num_kv_heads][head_dim]. */
+typedef struct {
+    const int32_t *block_table;  /* device int32 [batch][max_pages_per_seq] */
+    int32_t max_pages_per_seq;   /* columns of block_table; max_seqlen <= this * page_size */
+    int32_t page_size;           /* tokens per page: a power of two in [16, 1024] */
+    int32_t num_pages;           /* pages in each pool */
+    int32_t reserved;            /* must be 0 */
+} ta_paged_kv;
+
+/* tree_attn_decode over a paged KV cache.  `k_pages`, `v_pages`: device,
+ * 16-byte aligned pools of `paged->num_pages` pages laid out as described
+ * above.  Block-table entries of pages that hold valid tokens must be in
+ * [0, num_pages); an entry outside that range reads zeros, sets the device
+ * error word (TA_ERR_DEVICE_DATA from tree_attn_get_device_error) and makes
+ * that row NaN.  Entries past a row's last page are never read.  Results are
+ * those of tree_attn_decode on the gathered cache (bitwise equal with
+ * TA_FLAG_DETERMINISTIC at the same num_splits). */
+int tree_attn_decode_paged(const ta_shape *shape, const ta_paged_kv *paged, const void *q,
+                           const void *k_pages, const void *v_pages, const int32_t *seqlens,
+                           float *out, float *lse, int num_splits, void *workspace,
+                           size_t workspace_bytes, const ta_options *options, void *stream);
+
 /* The tree combine on its own ("The Tree Reduction Merge Operator" applied to
  * P states per (b, h), then the root normalisation O = o / l):
  *

@@ -28,7 +28,7 @@ TA_NOALLOC_SCRATCH_BYTES = 8 << 20
 _EXPORTS = ["tree_attn_status_string", "tree_attn_version", "tree_attn_check_shape",
             "tree_attn_workspace_bytes", "tree_attn_pick_splits", "tree_attn_decode",
             "tree_attn_decode_ex", "tree_attn_combine", "tree_attn_get_device_error",
-            "tree_attn_decode_noalloc", "tree_attn_launch_count"]
+            "tree_attn_decode_noalloc", "tree_attn_launch_count", "tree_attn_decode_paged"]
 
 
 class TaShape(ctypes.Structure):
@@ -43,6 +43,12 @@ class TaShape(ctypes.Structure):
 class TaOptions(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int32), ("flags", ctypes.c_int32),
                 ("split_start_event", ctypes.c_void_p), ("split_end_event", ctypes.c_void_p)]
+
+
+class TaPagedKV(ctypes.Structure):
+    _fields_ = [("block_table", ctypes.c_void_p), ("max_pages_per_seq", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("num_pages", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 class TreeAttnError(RuntimeError):
@@ -85,6 +91,9 @@ def load(path: str = LIB_PATH):
         lib.tree_attn_combine.restype = I32
         lib.tree_attn_decode_noalloc.argtypes = [SP, P, P, P, P, P, P, I32, P]
         lib.tree_attn_decode_noalloc.restype = I32
+        lib.tree_attn_decode_paged.argtypes = [SP, ctypes.POINTER(TaPagedKV), P, P, P, P, P, P, I32, P,
+                                               SZ, ctypes.POINTER(TaOptions), P]
+        lib.tree_attn_decode_paged.restype = I32
         lib.tree_attn_launch_count.argtypes = [SP, I32, ctypes.POINTER(TaOptions)]
         lib.tree_attn_launch_count.restype = I32
         lib.tree_attn_get_device_error.argtypes = [P]
@@ -280,4 +289,55 @@ def tree_attn_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: to
                                       _stream(stream))
     if rc != TA_OK:
         raise TreeAttnError(rc, "tree_attn_decode_noalloc")
+    return out, lse
+
+
+def tree_attn_decode_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor,
+                           block_table: torch.Tensor, seqlens: torch.Tensor,
+                           out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                           num_splits: int = 0, workspace: Optional[torch.Tensor] = None,
+                           kernel: str = "auto", scale: Optional[float] = None, stream=None,
+                           deterministic: bool = False, max_seqlen: Optional[int] = None):
+    """Decode attention over a paged KV cache through the C ABI.
+
+    k_pages, v_pages: [num_pages, page_size, Hkv, d] views (any strides with a unit
+    channel stride; a [num_pages, Hkv, page_size, d] pool is passed as a permuted view);
+    block_table: int32 [B, max_pages_per_seq]; returns (out, lse).
+    """
+    lib = load()
+    _check_cuda(q, k_pages, v_pages, block_table, seqlens, out, lse, workspace)
+    if k_pages.dim() != 4 or v_pages.shape != k_pages.shape or v_pages.stride() != k_pages.stride():
+        raise ValueError("k_pages and v_pages must be [num_pages, page_size, Hkv, d] with equal strides")
+    if k_pages.stride(3) != 1 or not q.is_contiguous():
+        raise ValueError("channels must be contiguous and q dense")
+    if block_table.dtype != torch.int32 or block_table.dim() != 2 or not block_table.is_contiguous():
+        raise ValueError("block_table must be a contiguous int32 [B, max_pages] tensor")
+    if seqlens.dtype != torch.int32 or not seqlens.is_contiguous():
+        raise ValueError("seqlens must be a contiguous int32 tensor")
+    num_pages, page_size, Hkv, d = k_pages.shape
+    B, Hq, dq = q.shape
+    if dq != d or block_table.shape[0] != B:
+        raise ValueError("q, pages and block_table disagree")
+    S = int(max_seqlen) if max_seqlen is not None else block_table.shape[1] * page_size
+    sp, st, sh, _ = k_pages.stride()
+    shape = TaShape(B, Hq, Hkv, d, S, _dtype_code(q.dtype), _dtype_code(k_pages.dtype),
+                    float(scale or 0.0), sp, sh, st)
+    paged = TaPagedKV(block_table.data_ptr(), block_table.shape[1], page_size, num_pages, 0)
+    if out is None:
+        out = torch.empty(B, Hq, d, dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
+    P = int(num_splits)
+    if P <= 0:
+        P = tree_attn_pick_splits(shape)
+    nbytes = tree_attn_workspace_bytes(shape, P)
+    if nbytes and workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    opts = TaOptions(TA_KERNEL[kernel], TA_FLAG_DETERMINISTIC if deterministic else 0, None, None)
+    rc = lib.tree_attn_decode_paged(ctypes.byref(shape), ctypes.byref(paged), _ptr(q), _ptr(k_pages),
+                                    _ptr(v_pages), _ptr(seqlens), _ptr(out), _ptr(lse), P,
+                                    _ptr(workspace), ws_bytes, ctypes.byref(opts), _stream(stream))
+    if rc != TA_OK:
+        raise TreeAttnError(rc, "tree_attn_decode_paged")
     return out, lse

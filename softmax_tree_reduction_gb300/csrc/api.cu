@@ -111,7 +111,9 @@ struct Strides {
 };
 
 // Validate the shape; on success fill the resolved KV strides (elements).
-int check_shape(const ta_shape* s, Strides* st) {
+// `page_size` > 0: the strides describe a page pool whose default layout is
+// [num_pages][page_size][Hkv][d] (kv_stride_b = stride between pages).
+int check_shape(const ta_shape* s, Strides* st, int page_size = 0) {
     if (!s) return TA_ERR_NULL;
     if (s->batch < 1 || s->num_q_heads < 1 || s->num_kv_heads < 1 || s->max_seqlen < 1)
         return TA_ERR_SHAPE;
@@ -126,9 +128,15 @@ int check_shape(const ta_shape* s, Strides* st) {
     Strides r;
     const int64_t d = s->head_dim, S = s->max_seqlen, H = s->num_kv_heads;
     if (s->kv_stride_b == 0 && s->kv_stride_h == 0 && s->kv_stride_t == 0) {
-        r.t = d;
-        r.h = S * d;
-        r.b = H * S * d;
+        if (page_size > 0) {
+            r.h = d;
+            r.t = H * d;
+            r.b = static_cast<int64_t>(page_size) * H * d;
+        } else {
+            r.t = d;
+            r.h = S * d;
+            r.b = H * S * d;
+        }
     } else {
         r.b = s->kv_stride_b;
         r.h = s->kv_stride_h;
@@ -266,20 +274,35 @@ int pick_splits_impl(const ta_shape* s, const int32_t* host_seqlens, int num_sms
     return best;
 }
 
+// 4-D map over (channel, token, KV head, batch row) -- or, for a page pool,
+// (channel, token in page, KV head, physical page).  Box: box_x channels x
+// `rows` tokens.
 int encode_kv_map(CUtensorMap* map, const void* base, const ta_shape* s, const Strides& st,
-                  const Geometry& geo) {
+                  const Geometry& geo, const ta_paged_kv* paged, int rows) {
     auto fn = encode_fn();
     if (!fn) return TA_ERR_CUDA;
     const int64_t es = elem_bytes(s->kv_dtype);
     cuuint64_t dims[4] = {static_cast<cuuint64_t>(s->head_dim),
-                          static_cast<cuuint64_t>(s->max_seqlen),
+                          static_cast<cuuint64_t>(paged ? paged->page_size : s->max_seqlen),
                           static_cast<cuuint64_t>(s->num_kv_heads),
-                          static_cast<cuuint64_t>(s->batch)};
+                          static_cast<cuuint64_t>(paged ? paged->num_pages : s->batch)};
     cuuint64_t strides[3] = {static_cast<cuuint64_t>(st.t * es), static_cast<cuuint64_t>(st.h * es),
                              static_cast<cuuint64_t>(st.b * es)};
-    cuuint32_t box[4] = {static_cast<cuuint32_t>(geo.box_x),
-                         static_cast<cuuint32_t>(geo.tile_tokens), 1, 1};
-    cuuint32_t estr[4] = {1, 1, 1, 1};
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(geo.box_x), static_cast<cuuint32_t>(rows), 1, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    if (geo.swizzle128) {
+        // 5-D view (channel in half, token, half, KV head, row/page): one box
+        // brings every 64-channel half of `rows` tokens, [half][rows][128 B].
+        const cuuint64_t halves = static_cast<cuuint64_t>(s->head_dim / 64);
+        cuuint64_t dims5[5] = {64, dims[1], halves, dims[2], dims[3]};
+        cuuint64_t strides5[4] = {strides[0], 128, strides[1], strides[2]};
+        cuuint32_t box5[5] = {64, static_cast<cuuint32_t>(rows), static_cast<cuuint32_t>(halves), 1, 1};
+        const CUresult r5 = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base),
+                               dims5, strides5, box5, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        return r5 == CUDA_SUCCESS ? TA_OK : TA_ERR_CUDA;
+    }
     const CUresult r = fn(map,
                           s->kv_dtype == TA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
@@ -288,6 +311,143 @@ int encode_kv_map(CUtensorMap* map, const void* base, const ta_shape* s, const S
                           geo.swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? TA_OK : TA_ERR_CUDA;
+}
+
+}  // namespace
+
+namespace {
+
+int check_paged(const ta_shape* shape, const ta_paged_kv* pg) {
+    if (!pg->block_table) return TA_ERR_NULL;
+    if (!aligned(pg->block_table, 4)) return TA_ERR_ALIGN;
+    if (pg->reserved != 0) return TA_ERR_SHAPE;
+    const int ps = pg->page_size;
+    if (ps < 16 || ps > 1024 || (ps & (ps - 1)) != 0) return TA_ERR_SHAPE;
+    if (pg->max_pages_per_seq < 1 || pg->num_pages < 1) return TA_ERR_SHAPE;
+    if (static_cast<int64_t>(shape->max_seqlen) > static_cast<int64_t>(pg->max_pages_per_seq) * ps)
+        return TA_ERR_SHAPE;
+    return TA_OK;
+}
+
+int decode_impl(const ta_shape* shape, const ta_paged_kv* paged, const void* q,
+                const void* k_cache, const void* v_cache, const int32_t* seqlens, float* out,
+                float* lse, int num_splits, void* workspace, size_t workspace_bytes,
+                const ta_options* options, void* stream_ptr) {
+    if (!shape) return TA_ERR_NULL;
+    Strides st;
+    int rc = paged ? check_paged(shape, paged) : TA_OK;
+    if (rc != TA_OK) return rc;
+    rc = check_shape(shape, &st, paged ? paged->page_size : 0);
+    if (rc != TA_OK) return rc;
+    if (!q || !k_cache || !v_cache || !seqlens || !out) return TA_ERR_NULL;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+        !aligned(seqlens, 4) || (lse && !aligned(lse, 4)))
+        return TA_ERR_ALIGN;
+    if (options && (options->flags & ~TA_FLAG_DETERMINISTIC) != 0) return TA_ERR_SHAPE;
+    const bool deterministic = options && (options->flags & TA_FLAG_DETERMINISTIC);
+    const int kernel = resolve_kernel(shape, options ? options->kernel : TA_KERNEL_AUTO);
+    if (kernel < 0) return kernel;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+
+    if (num_splits > TA_MAX_SPLITS) return TA_ERR_SPLITS;
+    auto check_ws = [&](int P) {
+        if (P <= 1) return static_cast<int>(TA_OK);
+        if (!workspace || workspace_bytes < workspace_layout(shape, P).total)
+            return static_cast<int>(TA_ERR_WORKSPACE);
+        if (!aligned(workspace, 16)) return static_cast<int>(TA_ERR_ALIGN);
+        return static_cast<int>(TA_OK);
+    };
+    // With an explicit split count every argument is checked before any CUDA call.
+    if (num_splits > 0 && (rc = check_ws(num_splits)) != TA_OK) return rc;
+
+    DeviceState* ds = nullptr;
+    rc = device_state(&ds);
+    if (rc != TA_OK) return rc;
+
+    int P = num_splits;
+    if (P <= 0) {
+        P = pick_splits_impl(shape, nullptr, ds->num_sms, kernel);
+        if (P < 1 || P > TA_MAX_SPLITS) return TA_ERR_SPLITS;
+        if ((rc = check_ws(P)) != TA_OK) return rc;
+    }
+    const WsLayout ws = workspace_layout(shape, P);
+
+    const Geometry geo = geometry_of(shape, kernel);
+    const int rows = paged ? std::min(geo.tile_tokens, paged->page_size) : geo.tile_tokens;
+    CUtensorMap tk, tv;
+    rc = encode_kv_map(&tk, k_cache, shape, st, geo, paged, rows);
+    if (rc != TA_OK) return rc;
+    rc = encode_kv_map(&tv, v_cache, shape, st, geo, paged, rows);
+    if (rc != TA_OK) return rc;
+
+    ta::SplitParams p;
+    std::memset(&p, 0, sizeof p);
+    p.q = q;
+    p.q_is_bf16 = shape->q_dtype == TA_BF16;
+    p.seqlens = seqlens;
+    p.err = ds->err;
+    p.B = shape->batch;
+    p.Hq = shape->num_q_heads;
+    p.Hkv = shape->num_kv_heads;
+    p.G = shape->num_q_heads / shape->num_kv_heads;
+    p.S = shape->max_seqlen;
+    p.P = P;
+    const float scale = shape->scale > 0.f ? shape->scale
+                                           : 1.0f / std::sqrt(static_cast<float>(shape->head_dim));
+    p.scale_log2 = scale * ta::kLog2e;
+    p.chunk_tiles = std::max(1, kChunkTokens / geo.tile_tokens);
+    p.box_rows = rows;
+    p.num_pages = shape->batch;
+    if (paged) {
+        p.block_table = paged->block_table;
+        p.max_pages = paged->max_pages_per_seq;
+        p.num_pages = paged->num_pages;
+        int sh = 0;
+        while ((1 << sh) < paged->page_size) ++sh;
+        p.page_shift = sh;
+    }
+    p.out = out;
+    p.lse = lse;
+    bool fused = false;
+    if (P > 1) {
+        char* w = static_cast<char*>(workspace);
+        p.part_o = reinterpret_cast<float*>(w + ws.o);
+        p.part_m = reinterpret_cast<float*>(w + ws.m);
+        p.part_l = reinterpret_cast<float*>(w + ws.l);
+        const unsigned rows = static_cast<unsigned>(shape->batch) * shape->num_kv_heads;
+        unsigned* slots = reserve_slots(ds, 2 * rows);
+        if (slots) {
+            // Run-time balancing pays while the grid is a few waves at most; with
+            // more waves the block scheduler balances and claims only add latency.
+            const int64_t blocks = static_cast<int64_t>(rows) * P;
+            const int64_t resident = static_cast<int64_t>(ds->num_sms) * blocks_per_sm(shape, kernel);
+            if (!deterministic && blocks <= kBalanceMaxWaves * resident) p.claim = slots;
+            fused = fuse_merge(p.G, P);
+            p.fuse = fused ? 1 : 0;
+            if (p.claim || fused) p.done = slots + rows;
+        }
+    }
+
+    if (options && options->split_start_event &&
+        cudaEventRecord(static_cast<cudaEvent_t>(options->split_start_event), stream) != cudaSuccess)
+        return TA_ERR_CUDA;
+    cudaError_t e;
+    if (kernel == TA_KERNEL_MMA)
+        e = ta::launch_split_mma(shape->head_dim, tk, tv, p, stream);
+    else if (shape->kv_dtype == TA_BF16)
+        e = ta::launch_split_fma_bf16(shape->head_dim, tk, tv, p, stream);
+    else
+        e = ta::launch_split_fma_f32(shape->head_dim, tk, tv, p, stream);
+    if (e != cudaSuccess) return TA_ERR_CUDA;
+    if (options && options->split_end_event &&
+        cudaEventRecord(static_cast<cudaEvent_t>(options->split_end_event), stream) != cudaSuccess)
+        return TA_ERR_CUDA;
+    if (P > 1 && !fused) {
+        e = ta::launch_combine(shape->head_dim, p.part_o, p.part_m, p.part_l, out, lse,
+                               shape->batch, shape->num_q_heads, P, /*dependent=*/true, stream);
+        if (e != cudaSuccess) return TA_ERR_CUDA;
+    }
+    return TA_OK;
 }
 
 }  // namespace
@@ -339,108 +499,18 @@ int tree_attn_pick_splits(const ta_shape* shape, const int32_t* host_seqlens, in
 int tree_attn_decode_ex(const ta_shape* shape, const void* q, const void* k_cache,
                         const void* v_cache, const int32_t* seqlens, float* out, float* lse,
                         int num_splits, void* workspace, size_t workspace_bytes,
-                        const ta_options* options, void* stream_ptr) {
-    Strides st;
-    int rc = check_shape(shape, &st);
-    if (rc != TA_OK) return rc;
-    if (!q || !k_cache || !v_cache || !seqlens || !out) return TA_ERR_NULL;
-    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
-        !aligned(seqlens, 4) || (lse && !aligned(lse, 4)))
-        return TA_ERR_ALIGN;
-    if (options && (options->flags & ~TA_FLAG_DETERMINISTIC) != 0) return TA_ERR_SHAPE;
-    const bool deterministic = options && (options->flags & TA_FLAG_DETERMINISTIC);
-    const int kernel = resolve_kernel(shape, options ? options->kernel : TA_KERNEL_AUTO);
-    if (kernel < 0) return kernel;
-    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+                        const ta_options* options, void* stream) {
+    return decode_impl(shape, nullptr, q, k_cache, v_cache, seqlens, out, lse, num_splits,
+                       workspace, workspace_bytes, options, stream);
+}
 
-    if (num_splits > TA_MAX_SPLITS) return TA_ERR_SPLITS;
-    auto check_ws = [&](int P) {
-        if (P <= 1) return static_cast<int>(TA_OK);
-        if (!workspace || workspace_bytes < workspace_layout(shape, P).total)
-            return static_cast<int>(TA_ERR_WORKSPACE);
-        if (!aligned(workspace, 16)) return static_cast<int>(TA_ERR_ALIGN);
-        return static_cast<int>(TA_OK);
-    };
-    // With an explicit split count every argument is checked before any CUDA call.
-    if (num_splits > 0 && (rc = check_ws(num_splits)) != TA_OK) return rc;
-
-    DeviceState* ds = nullptr;
-    rc = device_state(&ds);
-    if (rc != TA_OK) return rc;
-
-    int P = num_splits;
-    if (P <= 0) {
-        P = pick_splits_impl(shape, nullptr, ds->num_sms, kernel);
-        if (P < 1 || P > TA_MAX_SPLITS) return TA_ERR_SPLITS;
-        if ((rc = check_ws(P)) != TA_OK) return rc;
-    }
-    const WsLayout ws = workspace_layout(shape, P);
-
-    const Geometry geo = geometry_of(shape, kernel);
-    CUtensorMap tk, tv;
-    rc = encode_kv_map(&tk, k_cache, shape, st, geo);
-    if (rc != TA_OK) return rc;
-    rc = encode_kv_map(&tv, v_cache, shape, st, geo);
-    if (rc != TA_OK) return rc;
-
-    ta::SplitParams p;
-    std::memset(&p, 0, sizeof p);
-    p.q = q;
-    p.q_is_bf16 = shape->q_dtype == TA_BF16;
-    p.seqlens = seqlens;
-    p.err = ds->err;
-    p.B = shape->batch;
-    p.Hq = shape->num_q_heads;
-    p.Hkv = shape->num_kv_heads;
-    p.G = shape->num_q_heads / shape->num_kv_heads;
-    p.S = shape->max_seqlen;
-    p.P = P;
-    const float scale = shape->scale > 0.f ? shape->scale
-                                           : 1.0f / std::sqrt(static_cast<float>(shape->head_dim));
-    p.scale_log2 = scale * ta::kLog2e;
-    p.chunk_tiles = std::max(1, kChunkTokens / geo.tile_tokens);
-    p.out = out;
-    p.lse = lse;
-    bool fused = false;
-    if (P > 1) {
-        char* w = static_cast<char*>(workspace);
-        p.part_o = reinterpret_cast<float*>(w + ws.o);
-        p.part_m = reinterpret_cast<float*>(w + ws.m);
-        p.part_l = reinterpret_cast<float*>(w + ws.l);
-        const unsigned rows = static_cast<unsigned>(shape->batch) * shape->num_kv_heads;
-        unsigned* slots = reserve_slots(ds, 2 * rows);
-        if (slots) {
-            // Run-time balancing pays while the grid is a few waves at most; with
-            // more waves the block scheduler balances and claims only add latency.
-            const int64_t blocks = static_cast<int64_t>(rows) * P;
-            const int64_t resident = static_cast<int64_t>(ds->num_sms) * blocks_per_sm(shape, kernel);
-            if (!deterministic && blocks <= kBalanceMaxWaves * resident) p.claim = slots;
-            fused = fuse_merge(p.G, P);
-            p.fuse = fused ? 1 : 0;
-            if (p.claim || fused) p.done = slots + rows;
-        }
-    }
-
-    if (options && options->split_start_event &&
-        cudaEventRecord(static_cast<cudaEvent_t>(options->split_start_event), stream) != cudaSuccess)
-        return TA_ERR_CUDA;
-    cudaError_t e;
-    if (kernel == TA_KERNEL_MMA)
-        e = ta::launch_split_mma(shape->head_dim, tk, tv, p, stream);
-    else if (shape->kv_dtype == TA_BF16)
-        e = ta::launch_split_fma_bf16(shape->head_dim, tk, tv, p, stream);
-    else
-        e = ta::launch_split_fma_f32(shape->head_dim, tk, tv, p, stream);
-    if (e != cudaSuccess) return TA_ERR_CUDA;
-    if (options && options->split_end_event &&
-        cudaEventRecord(static_cast<cudaEvent_t>(options->split_end_event), stream) != cudaSuccess)
-        return TA_ERR_CUDA;
-    if (P > 1 && !fused) {
-        e = ta::launch_combine(shape->head_dim, p.part_o, p.part_m, p.part_l, out, lse,
-                               shape->batch, shape->num_q_heads, P, /*dependent=*/true, stream);
-        if (e != cudaSuccess) return TA_ERR_CUDA;
-    }
-    return TA_OK;
+int tree_attn_decode_paged(const ta_shape* shape, const ta_paged_kv* paged, const void* q,
+                           const void* k_pages, const void* v_pages, const int32_t* seqlens,
+                           float* out, float* lse, int num_splits, void* workspace,
+                           size_t workspace_bytes, const ta_options* options, void* stream) {
+    if (!paged) return TA_ERR_NULL;
+    return decode_impl(shape, paged, q, k_pages, v_pages, seqlens, out, lse, num_splits, workspace,
+                       workspace_bytes, options, stream);
 }
 
 int tree_attn_launch_count(const ta_shape* shape, int num_splits, const ta_options* options) {

@@ -11,7 +11,7 @@
 namespace ta {
 
 // Error bits of the device error word.
-constexpr int kErrBadSeqlen = 1;  // a sequence length outside [0, max_seqlen]
+constexpr int kErrBadSeqlen = 1;  // a sequence length outside [0, max_seqlen], or a bad page
 constexpr int kErrTimeout = 2;    // a bounded barrier wait gave up
 
 // log2(e) and ln(2): the kernels evaluate exp(x) as 2^(x * log2 e).
@@ -35,6 +35,11 @@ struct SplitParams {
     unsigned* claim;        // [B*Hkv] chunk counters (null: static chunk assignment)
     unsigned* done;         // [B*Hkv] row tickets (null: no ticket is taken)
     int fuse;               // the row's last block merges the partial states
+    const int32_t* block_table;  // [B][max_pages] (null: dense cache, coordinate w = batch row)
+    int max_pages;          // block_table columns
+    int page_shift;         // log2(page_size)
+    int num_pages;          // pages in the pool (an out-of-range page reads zeros)
+    int box_rows;           // tokens per TMA box: the tile, or the page when it is smaller
     int B, Hq, Hkv, G, S, P;
     int chunk_tiles;        // tiles per scheduled chunk
     float scale_log2;       // logit scale * log2(e)
@@ -116,6 +121,18 @@ __device__ __forceinline__ void tma_load_4d(void* smem_dst, const CUtensorMap* m
         " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(smem_dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar)),
         "l"(policy)
+        : "memory");
+}
+
+// 5-D tiled load (x = channel within a 64-channel half, y = token, z = half,
+// w = KV head, v = batch row or physical page).
+__device__ __forceinline__ void tma_load_5d(void* smem_dst, const CUtensorMap* map, int x, int y,
+                                            int z, int w, int v, uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(v),
+        "r"(smem_u32(bar)), "l"(policy)
         : "memory");
 }
 

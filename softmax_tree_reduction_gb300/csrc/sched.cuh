@@ -35,17 +35,41 @@ struct StageMeta {
     int nvalid;  // valid tokens in the tile (1..tile); < 0: no more tiles
 };
 
-// Producer lane: stream this block's tiles into the stage ring.  `issue(s, t)`
-// enqueues the TMA copies of the tile starting at token t into stage s (the
-// full barrier is already armed with `stage_bytes`).  Returns false if a wait
-// timed out (the error word is set; the caller still drains).
+// Most TMA boxes one tile can need: a 128-token tile over 16-token pages.
+constexpr int kMaxBoxes = 8;
+
+// Box needs no page (past the row's end, or no tile).
+constexpr int kNoPage = -2147483647 - 1;
+
+// Block-table entry for box `j` of the tile at token t (paged caches), or
+// kNoPage.  The load is only started here; the entry is checked when the tile
+// is issued.
+__device__ __forceinline__ int load_box_page(const SplitParams& p, int b, int N, int t, int tile,
+                                             int j) {
+    if (t < 0 || !p.block_table) return kNoPage;
+    const int tj = t + j * p.box_rows;
+    if (j >= tile / p.box_rows || tj >= N) return kNoPage;
+    return __ldg(p.block_table + static_cast<size_t>(b) * p.max_pages + (tj >> p.page_shift));
+}
+
+// Producer warp (all 32 lanes): stream this block's tiles into the stage ring.
+// Lane 0 keeps the schedule (slices, claims, barriers, stage descriptors);
+// lane j issues the TMA copies of box j of each tile via `issue(s, t, j, page)`
+// (page = physical page for paged caches, else unused) after lane 0 has armed
+// the stage's full barrier with `stage_bytes`.  Tiles are generated one ahead
+// so each lane's block-table entry loads while the previous tile is issued.
+// Returns false if a wait timed out (the error word is set; the warp still
+// drains).
 template <int kStages, typename Issue>
-__device__ bool produce_row(const SplitParams& p, int row, int N, int split, int tile,
+__device__ bool produce_row(const SplitParams& p, int b, int row, int N, int split, int tile,
                             uint64_t* full, uint64_t* empty, volatile StageMeta* meta,
-                            volatile unsigned* sink, unsigned stage_bytes, Issue&& issue) {
+                            volatile unsigned* sink, volatile int* bad_flag, unsigned stage_bytes,
+                            Issue&& issue) {
+    const int lane = threadIdx.x & 31;
     const int P = p.P;
     const int C = tile * p.chunk_tiles;  // tokens per claimed chunk
     const bool dynamic = p.claim != nullptr;
+    const int nbox = p.block_table ? tile / p.box_rows : 1;
     long long slice;
     if (dynamic) {
         slice = (static_cast<long long>(N) * 7 / 8) / P / C * C;
@@ -60,50 +84,90 @@ __device__ bool produce_row(const SplitParams& p, int row, int N, int split, int
                              : N;
     const int npool = dynamic ? (N - base + C - 1) / C : 0;  // chunks handed out by the counter
     bool exhausted = (npool == 0);
-    unsigned pend0 = 0, pend1 = 0;  // claims in flight, oldest first
+    unsigned pend0 = 0, pend1 = 0;  // claims in flight (lane 0's registers), oldest first
     int npend = 0;
     bool claimed = false;
-    int it = 0;
-    bool ok = true;
-    while (true) {
+
+    // Next tile to stream, or -1; its token range ends at *end.  Warp-uniform:
+    // only lane 0 performs claims, and a claim's value is broadcast when used.
+    auto next_tile = [&](int* end) -> int {
         if (t >= t_end) {
-            if (exhausted) break;
+            if (exhausted) return -1;
             if (npend == 0) {
-                pend0 = atomicAdd(p.claim + row, 1u);
+                if (lane == 0) pend0 = atomicAdd(p.claim + row, 1u);
                 npend = 1;
                 claimed = true;
             }
-            const unsigned j = pend0;
+            const unsigned j = __shfl_sync(0xffffffffu, pend0, 0);
             pend0 = pend1;
             --npend;
             if (static_cast<int>(j) >= npool) {
                 exhausted = true;
-                break;
+                return -1;
             }
             t = base + static_cast<int>(j) * C;
             t_end = min(t + C, N);
         }
+        const int r = t;
+        *end = t_end;
+        t += tile;
         if (!exhausted && npend < 2 && t_end - t <= 2 * C) {
-            const unsigned v = atomicAdd(p.claim + row, 1u);
-            if (npend == 0) pend0 = v; else pend1 = v;
+            if (lane == 0) {
+                const unsigned v = atomicAdd(p.claim + row, 1u);
+                if (npend == 0) pend0 = v; else pend1 = v;
+            }
             ++npend;
             claimed = true;
         }
+        return r;
+    };
+
+    bool bad = false;
+    int it = 0;
+    bool ok = true;
+    int cur_end = 0, nxt_end = 0;
+    int cur = next_tile(&cur_end);
+    int pg_a = load_box_page(p, b, N, cur, tile, lane), pg_b = kNoPage;
+    // Issue `cur` (this lane's page in `now`) after starting the load for the tile after it.
+    auto step = [&](int& now, int& ahead) -> bool {
+        const int nxt = next_tile(&nxt_end);
+        ahead = load_box_page(p, b, N, nxt, tile, lane);
         const int s = it % kStages;
-        if (it >= kStages && !mbar_wait(&empty[s], ((it / kStages) - 1) & 1, p.err)) {
-            ok = false;
-            break;
+        if (it >= kStages) {
+            // lane 0 waits; the outcome is broadcast so the warp stays converged
+            int waited = 1;
+            if (lane == 0) waited = mbar_wait(&empty[s], ((it / kStages) - 1) & 1, p.err) ? 1 : 0;
+            if (!__shfl_sync(0xffffffffu, waited, 0)) return false;
         }
-        meta[s].tok0 = t;
-        meta[s].nvalid = min(tile, t_end - t);
-        mbar_arrive_expect_tx(&full[s], stage_bytes);
-        issue(s, t);
+        int page = p.num_pages;  // past the row's end, or out of range: the TMA unit zero-fills
+        if (now != kNoPage) {
+            if (now >= 0 && now < p.num_pages) page = now; else bad = true;
+        }
+        if (lane == 0) {
+            meta[s].tok0 = cur;
+            meta[s].nvalid = min(tile, cur_end - cur);
+            mbar_arrive_expect_tx(&full[s], stage_bytes);
+        }
+        __syncwarp();
+        if (lane < nbox) issue(s, cur, lane, page);
         ++it;
-        t += tile;
+        cur = nxt;
+        cur_end = nxt_end;
+        return true;
+    };
+    while (cur >= 0) {
+        if (!step(pg_a, pg_b)) { ok = false; break; }
+        if (cur < 0) break;
+        if (!step(pg_b, pg_a)) { ok = false; break; }
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) {
+        *bad_flag = 1;
+        atomicOr(p.err, kErrBadSeqlen);
     }
     // Every claim must have been performed before the block takes its ticket
     // (the last ticket resets the counter): consume the outstanding results.
-    if (claimed) *sink = pend0 + pend1;
+    if (claimed && lane == 0) *sink = pend0 + pend1;
+    if (lane != 0) return ok;
     int first_pending = it > kStages ? it - kStages : 0;
     if (ok) {
         // end-of-work marker in the next stage
@@ -122,12 +186,6 @@ __device__ bool produce_row(const SplitParams& p, int row, int N, int split, int
     return ok;
 }
 
-// Take the row's ticket after this block's partial state is written.  The
-// block holding the last ticket resets the row's claim counter and, when
-// `fuse` is set, merges the row's P partial states for its G query heads
-// ("The Tree Reduction Merge Operator" with the root maximum resolved first,
-// then O = o / l) and writes out / lse.
-// `scratch` holds >= 2*G*P + 2*G floats of shared memory no longer in use.
 // Ticket with acquire-release semantics at GPU scope: the block's partial
 // writes (ordered before it by the preceding block barrier) are published,
 // and the last taker sees every other block's writes.

@@ -82,6 +82,7 @@ __global__ void __launch_bounds__(FmaCfg<KV, D>::kThreads, 1)
     int* abort_flag = const_cast<int*>(reinterpret_cast<volatile int*>(meta + C::kStages));
     int* last_flag = abort_flag + 1;
     volatile unsigned* claim_sink = reinterpret_cast<volatile unsigned*>(abort_flag + 2);
+    volatile int* bad_page = reinterpret_cast<volatile int*>(abort_flag + 3);
 
     const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -92,6 +93,7 @@ __global__ void __launch_bounds__(FmaCfg<KV, D>::kThreads, 1)
             mbar_init(&empty[s], C::kWarps);
         }
         *abort_flag = 0;
+        *bad_page = 0;
         fence_barrier_init();
     }
     if (threadIdx.x == 32) {
@@ -111,14 +113,24 @@ __global__ void __launch_bounds__(FmaCfg<KV, D>::kThreads, 1)
     }
 
     if (warp == 0) {
-        if (lane == 0) {
+        {
             const uint64_t pol = l2_policy_evict_first();
-            produce_row<C::kStages>(p, b * p.Hkv + g, N, split, C::kTile, full, empty, meta,
-                                    claim_sink, C::kStageBytes, [&](int s, int y) {
-                                        uint8_t* st = stages + s * C::kStageBytes;
-                                        tma_load_4d(st, &tmK, 0, y, g, b, &full[s], pol);
-                                        tma_load_4d(st + C::kKBytes, &tmV, 0, y, g, b, &full[s], pol);
-                                    });
+            const bool paged = p.block_table != nullptr;
+            const int page_mask = (1 << p.page_shift) - 1;
+            produce_row<C::kStages>(
+                p, b, b * p.Hkv + g, N, split, C::kTile, full, empty, meta, claim_sink, bad_page,
+                C::kStageBytes, [&](int s, int y, int j, int page) {
+                    uint8_t* st = stages + s * C::kStageBytes;
+                    if (!paged) {
+                        tma_load_4d(st, &tmK, 0, y, g, b, &full[s], pol);
+                        tma_load_4d(st + C::kKBytes, &tmV, 0, y, g, b, &full[s], pol);
+                        return;
+                    }
+                    const int ty = (y + j * p.box_rows) & page_mask;
+                    const int off = j * p.box_rows * C::kRowBytes;
+                    tma_load_4d(st + off, &tmK, 0, ty, g, page, &full[s], pol);
+                    tma_load_4d(st + C::kKBytes + off, &tmV, 0, ty, g, page, &full[s], pol);
+                });
         }
         allow_dependents();
         return;
@@ -256,7 +268,7 @@ __global__ void __launch_bounds__(FmaCfg<KV, D>::kThreads, 1)
         }
     }
     consumer_sync(C::kWarps * 32);
-    const bool poison = bad || (*abort_flag != 0);
+    const bool poison = bad || (*abort_flag != 0) || (*bad_page != 0);
     const int ct = threadIdx.x - 32;
     for (int idx = ct; idx < G * D; idx += C::kWarps * 32) {
         const int h = idx / D, dd = idx - h * D;

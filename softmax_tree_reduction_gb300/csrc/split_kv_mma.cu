@@ -6,9 +6,9 @@
 // Attention pages), then merges the states of its warps with the merge
 // operator ("The Tree Reduction Merge Operator").
 //
-//  warp 0      producer: one lane streams K and V tiles (128 tokens x 128 B
-//              boxes, 128-byte swizzle) HBM -> shared memory with TMA into a
-//              ring of stages guarded by full/empty mbarriers.
+//  warp 0      producer: streams K and V tiles (128 tokens x all channels,
+//              as 128-byte-swizzled halves of 64 channels) HBM -> shared memory
+//              with TMA into a ring of stages guarded by full/empty mbarriers.
 //  warps 1..8  consumers: each owns 16 tokens of every 128-token stage (two
 //              warps per SM sub-partition hide each other's latencies).
 //     S^T[16 tok x 8 heads] = K_blk . Q^T      mma.m16n8k16 (A = K via ldmatrix,
@@ -35,8 +35,7 @@ struct MmaCfg {
     static constexpr int kWarps = 8;                 // consumer warps (two per SM sub-partition)
     static constexpr int kTile = 16 * kWarps;        // tokens per stage
     static constexpr int kHalves = D / 64;           // 128-byte column blocks per row
-    static constexpr int kBoxBytes = kTile * 128;    // one TMA box
-    static constexpr int kKBytes = kHalves * kBoxBytes;
+    static constexpr int kKBytes = kHalves * kTile * 128;
     static constexpr int kStageBytes = 2 * kKBytes;  // K and V
     static constexpr int kStages = (D == 128) ? 3 : 6;
     static constexpr int kBarBytes = 2 * kStages * 8 + kStages * 8 + 32;
@@ -107,6 +106,7 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
     int* abort_flag = const_cast<int*>(reinterpret_cast<volatile int*>(meta + C::kStages));
     int* last_flag = abort_flag + 1;
     volatile unsigned* claim_sink = reinterpret_cast<volatile unsigned*>(abort_flag + 2);
+    volatile int* bad_page = reinterpret_cast<volatile int*>(abort_flag + 3);
 
     const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -117,6 +117,7 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
             mbar_init(&empty[s], C::kWarps);
         }
         *abort_flag = 0;
+        *bad_page = 0;
         fence_barrier_init();
     }
     if (threadIdx.x == 32) {
@@ -137,19 +138,28 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------ producer
-        if (lane == 0) {
+        {
             const uint64_t pol = l2_policy_evict_first();
-            produce_row<C::kStages>(p, b * p.Hkv + g, N, split, C::kTile, full, empty, meta,
-                                    claim_sink, C::kStageBytes, [&](int s, int y) {
-                                        uint8_t* st = stages + s * C::kStageBytes;
-#pragma unroll
-                                        for (int h = 0; h < C::kHalves; ++h) {
-                                            tma_load_4d(st + h * C::kBoxBytes, &tmK, h * 64, y, g, b,
-                                                        &full[s], pol);
-                                            tma_load_4d(st + C::kKBytes + h * C::kBoxBytes, &tmV,
-                                                        h * 64, y, g, b, &full[s], pol);
-                                        }
-                                    });
+            const bool paged = p.block_table != nullptr;
+            const int page_mask = (1 << p.page_shift) - 1;
+            const int box_bytes = C::kHalves * p.box_rows * 128;
+            produce_row<C::kStages>(
+                p, b, b * p.Hkv + g, N, split, C::kTile, full, empty, meta, claim_sink, bad_page,
+                C::kStageBytes, [&](int s, int y, int j, int page) {
+                    // One box = box_rows tokens x all channels, laid out in shared
+                    // memory as [half][box_rows][128 B]; box j of a tile at j*box_bytes.
+                    uint8_t* st = stages + s * C::kStageBytes;
+                    const int off = j * box_bytes;
+                    if (!paged) {
+                        tma_load_5d(st + off, &tmK, 0, y, 0, g, b, &full[s], pol);
+                        tma_load_5d(st + C::kKBytes + off, &tmV, 0, y, 0, g, b, &full[s], pol);
+                        return;
+                    }
+                    // paged: (channel, token in page, half, KV head, physical page)
+                    const int ty = (y + j * p.box_rows) & page_mask;
+                    tma_load_5d(st + off, &tmK, 0, ty, 0, g, page, &full[s], pol);
+                    tma_load_5d(st + C::kKBytes + off, &tmV, 0, ty, 0, g, page, &full[s], pol);
+                });
         }
         allow_dependents();
         return;
@@ -181,10 +191,16 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
 #pragma unroll
     for (int mt = 0; mt < D / 16; ++mt) oacc[mt][0] = oacc[mt][1] = oacc[mt][2] = oacc[mt][3] = 0.f;
 
-    // ldmatrix row addresses (swizzled 16-byte chunk = chunk ^ (row & 7)).
-    const uint32_t k_row = (cw * 16 + r8 + 8 * ((lane >> 3) & 1)) * 128;
+    // ldmatrix row addresses (swizzled 16-byte chunk = chunk ^ (row & 7)).  A
+    // stage holds tile/R boxes of [half][R rows][128 B] (R = box_rows >= 16), so
+    // this warp's 16 rows sit in one box.
+    const int R = p.box_rows;
+    const uint32_t half_bytes = R * 128;
+    const int r0 = cw * 16;
+    const uint32_t warp_base = (r0 / R) * (C::kHalves * half_bytes) + (r0 % R) * 128;
+    const uint32_t k_row = warp_base + (r8 + 8 * ((lane >> 3) & 1)) * 128;
     const int k_chi = lane >> 4;
-    const uint32_t v_row = (cw * 16 + r8 + 8 * (lane >> 4)) * 128;
+    const uint32_t v_row = warp_base + (r8 + 8 * (lane >> 4)) * 128;
     const int v_chi = (lane >> 3) & 1;
     const float sl2 = p.scale_log2;
     bool timed_out = false;
@@ -208,7 +224,7 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
             for (int kk = 0; kk < D / 16; ++kk) {
                 const int c = 2 * (kk & 3) + k_chi;
                 uint32_t a[4];
-                ldsm_x4(a, kbase + (kk >> 2) * C::kBoxBytes + k_row + ((c ^ r8) << 4));
+                ldsm_x4(a, kbase + (kk >> 2) * half_bytes + k_row + ((c ^ r8) << 4));
                 if (kk & 1)
                     mma_bf16(sb, a, qb[kk][0], qb[kk][1]);
                 else
@@ -265,7 +281,7 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
             for (int mt = 0; mt < D / 16; ++mt) {
                 const int c = 2 * (mt & 3) + v_chi;
                 uint32_t a[4];
-                ldsm_x4_t(a, vbase + (mt >> 2) * C::kBoxBytes + v_row + ((c ^ r8) << 4));
+                ldsm_x4_t(a, vbase + (mt >> 2) * half_bytes + v_row + ((c ^ r8) << 4));
                 a[0] &= vm01;
                 a[1] &= vm01;
                 a[2] &= vm23;
@@ -301,7 +317,7 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
         mg_l[cw * 8 + 2 * tig + 1] = l1;
     }
     consumer_sync(C::kWarps * 32);
-    const bool poison = bad || (*abort_flag != 0);
+    const bool poison = bad || (*abort_flag != 0) || (*bad_page != 0);
     const int ct = threadIdx.x - 32;
     for (int idx = ct; idx < p.G * D; idx += C::kWarps * 32) {
         const int h = idx / D, dd = idx - h * D;

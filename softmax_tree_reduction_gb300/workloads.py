@@ -185,3 +185,44 @@ def seqlens_of(w: Workload, seed: Optional[int] = None):
     lo, hi = w.ragged_range
     return torch.randint(int(lo), int(hi) + 1, (w.batch,), generator=g,
                          dtype=torch.int64).numpy()
+
+
+def page_pool(k, v, seqlens, page_size, layout="NHD", extra_pages=3, seed=0):
+    """Scatter dense caches [B, Hkv, S, d] into shuffled page pools.
+
+    Returns (k_pool, v_pool, block_table): pools of shape [num_pages, page_size,
+    Hkv, d] ("NHD") or [num_pages, Hkv, page_size, d] ("HND", returned as a
+    permuted [num_pages, page_size, Hkv, d] view); unused slots, junk pages and
+    block-table entries past each row's pages are NaN / -1.  Pure data movement.
+    """
+    B, Hkv, S, d = k.shape
+    sl = [int(x) for x in seqlens]
+    pages = [(n + page_size - 1) // page_size for n in sl]
+    max_pages = max(1, (S + page_size - 1) // page_size)
+    num_pages = sum(pages) + extra_pages
+    g = torch.Generator().manual_seed(seed)
+    perm = torch.randperm(num_pages, generator=g)
+    shape = (num_pages, page_size, Hkv, d) if layout == "NHD" else (num_pages, Hkv, page_size, d)
+    kp = torch.full(shape, float("nan"), dtype=k.dtype)
+    vp = torch.full(shape, float("nan"), dtype=v.dtype)
+    bt = torch.full((B, max_pages), -1, dtype=torch.int32)
+    nxt = 0
+    for b in range(B):
+        for lp in range(pages[b]):
+            phys = int(perm[nxt])
+            nxt += 1
+            bt[b, lp] = phys
+            t0 = lp * page_size
+            n = min(page_size, sl[b] - t0)
+            src_k = k[b, :, t0:t0 + n, :]        # [Hkv, n, d]
+            src_v = v[b, :, t0:t0 + n, :]
+            if layout == "NHD":
+                kp[phys, :n] = src_k.transpose(0, 1)
+                vp[phys, :n] = src_v.transpose(0, 1)
+            else:
+                kp[phys, :, :n] = src_k
+                vp[phys, :, :n] = src_v
+    if layout == "HND":
+        kp = kp.permute(0, 2, 1, 3)
+        vp = vp.permute(0, 2, 1, 3)
+    return kp, vp, bt

@@ -188,3 +188,24 @@ def test_launch_count(ta):
         ta.tree_attn_launch_count(s, 5000)
     with pytest.raises(ta.TreeAttnError):
         ta.tree_attn_launch_count(shape(ta, head_dim=48), 4)
+
+
+def test_paged_argument_errors(ta):
+    lib = ta.load()
+    vp = ctypes.c_void_p
+    s = shape(ta, max_seqlen=4096)
+
+    def call(pg, s_=s):
+        return lib.tree_attn_decode_paged(ctypes.byref(s_), ctypes.byref(pg) if pg is not None else None,
+                                          vp(0x1000), vp(0x2000), vp(0x3000), vp(0x4000), vp(0x5000),
+                                          vp(0x6000), 1, vp(0), 0, None, vp(0))
+    ok = dict(block_table=0x8000, max_pages_per_seq=64, page_size=64, num_pages=100, reserved=0)
+    assert call(None) == -1
+    assert call(ta.TaPagedKV(**{**ok, "block_table": 0})) == -1
+    assert call(ta.TaPagedKV(**{**ok, "block_table": 0x8002})) == -2
+    assert call(ta.TaPagedKV(**{**ok, "page_size": 24})) == -3
+    assert call(ta.TaPagedKV(**{**ok, "page_size": 8})) == -3
+    assert call(ta.TaPagedKV(**{**ok, "page_size": 2048})) == -3
+    assert call(ta.TaPagedKV(**{**ok, "max_pages_per_seq": 63})) == -3   # 63*64 < 4096
+    assert call(ta.TaPagedKV(**{**ok, "num_pages": 0})) == -3
+    assert call(ta.TaPagedKV(**{**ok, "reserved": 1})) == -3
