@@ -11,6 +11,10 @@ What it restates (web pages on Tree Attention, arXiv:2408.04093):
   with the global maximum logit ("Tree Attention Guide", section "Core
   Innovation 2", the Softmax(S)_j equation), written out in C
   (``tree_attn_oracle.c``) as a two-pass double-precision loop.
+* ``attention_multi`` -- several queries per sequence (multi-query decode):
+  query i of a row of N tokens sits at position N - nq + i and, when causal,
+  attends to tokens [0, N - nq + i]; each query is the definition above over
+  its token range (a reading: the pages describe one query per step).
 * ``partials`` -- the local partial attention state (o, l, m) of one KV slice
   ("Core Innovation 1", item 2 "Local Independent Partial Attention").
 * ``merge`` -- the merge operator (+) of two states ("The Tree Reduction Merge
@@ -69,6 +73,9 @@ def _load(path: str | None = None):
     lib.oracle_partials_f64.argtypes = [i32, i32, i32, i32, i64, p, i32, p, p, i32, p, dbl,
                                         i32, p, p, p, p, p, i32]
     lib.oracle_partials_f64.restype = i32
+    lib.oracle_attention_multi_f64.argtypes = [i32, i32, i32, i32, i64, i32, i32, p, i32, p, p, i32, p,
+                                               dbl, p, p, i32]
+    lib.oracle_attention_multi_f64.restype = i32
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = i32
     return lib
@@ -138,6 +145,30 @@ def attention(q, k, v, seqlens, scale: float | None = None, threads: int = 0, li
                                 float(scale), _ptr(out), _ptr(lse), int(threads))
     if rc != 0:
         raise ValueError(f"oracle_attention_f64 failed with code {rc}")
+    return out, lse
+
+
+def attention_multi(q, k, v, seqlens, causal: bool = True, scale: float | None = None,
+                    threads: int = 0, lib_handle=None):
+    """Several queries per sequence: q [B, Hq, nq, d]; query i of row b sits at
+    position N_b - nq + i and, when causal, sees tokens [0, N_b - nq + i].
+    Returns (out [B, Hq, nq, d], lse [B, Hq, nq]) in float64."""
+    qa, qt = _as_raw(q)
+    ka, kt = _as_raw(k)
+    va, vt = _as_raw(v)
+    B, Hq, nq, d = qa.shape
+    _, Hkv, S, _ = ka.shape
+    sl = np.ascontiguousarray(np.asarray(seqlens, dtype=np.int32).reshape(B))
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    out = np.zeros((B, Hq, nq, d), dtype=np.float64)
+    lse = np.zeros((B, Hq, nq), dtype=np.float64)
+    L = lib_handle or lib()
+    rc = L.oracle_attention_multi_f64(B, Hq, Hkv, d, S, nq, int(bool(causal)), _ptr(qa), qt, _ptr(ka),
+                                      _ptr(va), kt, _ptr(sl), float(scale), _ptr(out), _ptr(lse),
+                                      int(threads))
+    if rc != 0:
+        raise ValueError(f"oracle_attention_multi_f64 failed with code {rc}")
     return out, lse
 
 
@@ -288,7 +319,7 @@ def even_bounds(seqlens, P: int):
     return starts, ends
 
 
-__all__ = ["attention", "partials", "merge", "normalize", "tree_reduce", "combine", "empty_state",
+__all__ = ["attention", "attention_multi", "partials", "merge", "normalize", "tree_reduce", "combine", "empty_state",
            "even_bounds", "build", "lib", "max_threads", "F32", "BF16"]
 
 if __name__ == "__main__":  # pragma: no cover

@@ -222,6 +222,87 @@ int oracle_partials_f64(int B, int Hq, int Hkv, int d, int64_t S,
     return bad ? -6 : 0;
 }
 
+/* Several queries per sequence (multi-query decode, e.g. verifying nq draft
+ * tokens): q is [B][Hq][nq][d] and query i of row b sits at position
+ * N_b - nq + i.  With `causal`, it attends to tokens [0, N_b - nq + i]
+ * (max(0, N_b - nq + 1 + i) tokens); without, every query attends to all N_b.
+ * For each (b, h, i) the result is the definition above over that token
+ * range; out is [B][Hq][nq][d], lse [B][Hq][nq].  A query with no tokens
+ * gives out = 0, lse = -inf. */
+int oracle_attention_multi_f64(int B, int Hq, int Hkv, int d, int64_t S, int nq, int causal,
+                               const void *q, int q_dtype,
+                               const void *k, const void *v, int kv_dtype,
+                               const int32_t *seqlens, double scale,
+                               double *out, double *lse, int nthreads)
+{
+    int rc = check_args(B, Hq, Hkv, d, S, q_dtype, kv_dtype);
+    if (rc)
+        return rc;
+    if (nq < 1)
+        return -3;
+    for (int b = 0; b < B; ++b)
+        if (seqlens[b] < 0 || seqlens[b] > S)
+            return -8;
+    const int G = Hq / Hkv;
+    const int64_t work = (int64_t)B * Hq * nq;
+    int bad = 0;
+#ifdef _OPENMP
+    if (nthreads <= 0)
+        nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads) reduction(| : bad)
+#endif
+    for (int64_t w = 0; w < work; ++w) {
+        const int i = (int)(w % nq);
+        const int64_t bh = w / nq;
+        const int b = (int)(bh / Hq);
+        const int h = (int)(bh % Hq);
+        const int g = h / G;
+        int64_t n = seqlens[b];
+        if (causal) {
+            n = n - nq + 1 + i;
+            if (n < 0)
+                n = 0;
+        }
+        const int64_t qoff = w * d;
+        const int64_t kvoff = ((int64_t)b * Hkv + g) * S * d;
+        double *o = out + w * d;
+        if (n == 0) {
+            for (int c = 0; c < d; ++c)
+                o[c] = 0.0;
+            lse[w] = -INFINITY;
+            continue;
+        }
+        double *s = (double *)malloc((size_t)n * sizeof(double));
+        if (!s) {
+            bad = 1;
+            continue;
+        }
+        double M = -INFINITY;
+        for (int64_t t = 0; t < n; ++t) {
+            double acc = 0.0;
+            for (int c = 0; c < d; ++c)
+                acc += widen(q, q_dtype, qoff + c) * widen(k, kv_dtype, kvoff + t * d + c);
+            s[t] = scale * acc;
+            if (s[t] > M)
+                M = s[t];
+        }
+        double L = 0.0;
+        for (int c = 0; c < d; ++c)
+            o[c] = 0.0;
+        for (int64_t t = 0; t < n; ++t) {
+            double e = exp(s[t] - M);
+            L += e;
+            for (int c = 0; c < d; ++c)
+                o[c] += e * widen(v, kv_dtype, kvoff + t * d + c);
+        }
+        for (int c = 0; c < d; ++c)
+            o[c] = o[c] / L;
+        lse[w] = M + log(L);
+        free(s);
+    }
+    return bad ? -6 : 0;
+}
+
 /* Number of OpenMP threads a call with nthreads <= 0 would use (1 when the
  * oracle was built without OpenMP). */
 int oracle_max_threads(void)

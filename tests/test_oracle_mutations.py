@@ -13,6 +13,7 @@ import numpy as np
 import pytest
 
 import oracle
+from tests import test_oracle_multi as multi
 from tests import test_oracle_pins as pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "tree_attn_oracle.c")
@@ -122,3 +123,47 @@ def test_merge_mutant_is_caught(mutant, monkeypatch):
             caught = check.__name__
             break
     assert caught is not None
+
+
+MULTI_MUTANTS = {
+    "causal_off_by_one": ("n = n - nq + 1 + i;", "n = n - nq + i;"),
+    "causal_reversed": ("n = n - nq + 1 + i;", "n = n - i;"),
+    "query_row_from_head": ("const int64_t qoff = w * d;", "const int64_t qoff = bh * nq * d;"),
+    "kv_head_from_query": ("const int g = h / G;\n        int64_t n = seqlens[b];",
+                           "const int g = (h + i) / G % Hkv;\n        int64_t n = seqlens[b];"),
+}
+
+
+def _multi_battery_fails(lib_handle):
+    import oracle as orc
+    real = orc.lib
+    orc_lib = lambda: lib_handle
+    try:
+        orc.lib = orc_lib
+        for check in (multi.test_single_query_equals_definition,
+                      lambda: multi.test_multi_query_brute_force(True),
+                      multi.test_multi_query_against_sdpa_with_causal_mask):
+            try:
+                with np.errstate(all="ignore"):
+                    check()
+            except (AssertionError, ValueError):
+                return True
+        return False
+    finally:
+        orc.lib = real
+
+
+@pytest.mark.parametrize("name", sorted(MULTI_MUTANTS))
+def test_multi_query_mutant_is_caught(name, tmpdir):
+    old, new = MULTI_MUTANTS[name]
+    src = open(SRC).read()
+    start = src.index("int oracle_attention_multi_f64")
+    assert src.count(old, start) >= 1, name
+    mutated = src[:start] + src[start:].replace(old, new, 1)
+    path = os.path.join(tmpdir, f"mmut_{name}.c")
+    with open(path, "w") as f:
+        f.write(mutated)
+    so = os.path.join(tmpdir, f"libmmut_{name}.so")
+    subprocess.run(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", path, "-o", so, "-lm"], check=True,
+                   capture_output=True)
+    assert _multi_battery_fails(oracle._load(so)), f"mutant {name} survived"
