@@ -73,6 +73,8 @@ def parse_args(argv=None):
     ap.add_argument("--sweep-kernels", default="mma,fma")
     ap.add_argument("--paged", type=int, default=0,
                     help="run through the paged-KV entry point with this page size (pages shuffled in a pool)")
+    ap.add_argument("--queries", type=int, default=1,
+                    help="queries per sequence (causal over the last positions, as when verifying draft tokens)")
     ap.add_argument("--paged-layout", choices=["NHD", "HND"], default="NHD",
                     help="page layout: [pages][page][heads][d] (NHD) or [pages][heads][page][d] (HND)")
     ap.add_argument("--graph", action="store_true",
@@ -271,6 +273,9 @@ def run_ours(args, rank, world, local):
     ta.load()
     w = workloads.WORKLOADS[args.workload]
     inp = workloads.make_inputs(w)
+    if args.queries > 1:
+        gq = torch.Generator().manual_seed(w.seed + 1)
+        inp["q"] = torch.randn(w.batch, w.num_q_heads, args.queries, w.head_dim, generator=gq).to(w.q_dtype)
     kv_bytes = w.kv_bytes(inp["seqlens"])
     dev = {k: inp[k].cuda() for k in ("q", "k", "v", "seqlens")}
     if args.paged:
@@ -280,25 +285,34 @@ def run_ours(args, rank, world, local):
         del kp, vp
     # two copies of the KV cache, alternated step to step (each far larger than L2)
     copies = [dev, dict(dev, k=_clone_view(dev["k"]), v=_clone_view(dev["v"]))]
-    shape = (ta.make_shape(dev["q"], inp["k"]) if not args.paged else
+    shape = (ta.make_shape(dev["q"] if args.queries == 1 else dev["q"][:, :, 0], inp["k"]) if not args.paged else
              ta.TaShape(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.max_seqlen,
                         ta.TA_BF16 if w.q_dtype == torch.bfloat16 else ta.TA_F32,
                         ta.TA_BF16 if w.kv_dtype == torch.bfloat16 else ta.TA_F32, 0.0,
                         dev["k"].stride(0), dev["k"].stride(2), dev["k"].stride(1)))
+    if args.queries > 1:  # each (head, query) pair counts as a query head
+        shape = ta.TaShape.from_buffer_copy(shape)
+        shape.num_q_heads *= args.queries
     P = args.num_splits if args.num_splits > 0 else ta.tree_attn_pick_splits(shape)
     kernel_used = args.kernel
     if kernel_used == "auto":
         kernel_used = "mma" if (w.kv_dtype == torch.bfloat16 and w.q_dtype == torch.bfloat16
-                                and w.group <= 8) else "fma"
-    B, Hq, d = dev["q"].shape
-    out = torch.empty(B, Hq, d, dtype=torch.float32, device="cuda")
-    lse = torch.empty(B, Hq, dtype=torch.float32, device="cuda")
+                                and w.group * args.queries <= 16) else "fma"
+    B, Hq, d = dev["q"].shape[0], dev["q"].shape[1], dev["q"].shape[-1]
+    out = torch.empty(dev["q"].shape, dtype=torch.float32, device="cuda")
+    lse = torch.empty(dev["q"].shape[:-1], dtype=torch.float32, device="cuda")
     nbytes = ta.tree_attn_workspace_bytes(shape, P)
     ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
 
     def step(i, events=None):
         c = copies[i & 1]
+        if args.queries > 1:
+            ta.tree_attn_decode_multi(c["q"], c["k"], c["v"], c["seqlens"], causal=True,
+                                      block_table=c.get("block_table"), out=out, lse=lse, num_splits=P,
+                                      workspace=ws, kernel=args.kernel, deterministic=args.deterministic,
+                                      max_seqlen=w.max_seqlen if args.paged else None)
+            return
         if args.paged:
             ta.tree_attn_decode_paged(c["q"], c["k"], c["v"], c["block_table"], c["seqlens"], out=out,
                                       lse=lse, num_splits=P, workspace=ws, kernel=args.kernel,
@@ -331,7 +345,7 @@ def run_ours(args, rank, world, local):
     barrier(world)
     elapsed_ms = e0.elapsed_time(e1)
     launches = ta.tree_attn_launch_count(shape, P, args.kernel, args.deterministic)
-    if launches == 1 or args.paged:
+    if launches == 1 or args.paged or args.queries > 1:
         # the step is the split-KV kernel alone: its launch duration is the step time
         split_ms = elapsed_ms / args.steps
     else:
@@ -370,7 +384,12 @@ def run_ours(args, rank, world, local):
         def e2e_step():
             for k in host:
                 dbuf[k].copy_(host[k], non_blocking=True)
-            if args.paged:
+            if args.queries > 1:
+                ta.tree_attn_decode_multi(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["seqlens"], causal=True,
+                                          block_table=dbuf.get("block_table"), out=out, lse=lse,
+                                          num_splits=P, workspace=ws, kernel=args.kernel,
+                                          max_seqlen=w.max_seqlen if args.paged else None)
+            elif args.paged:
                 ta.tree_attn_decode_paged(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["block_table"],
                                           dbuf["seqlens"], out=out, lse=lse, num_splits=P, workspace=ws,
                                           kernel=args.kernel, max_seqlen=w.max_seqlen)
@@ -417,6 +436,7 @@ def run_ours(args, rank, world, local):
                    "seq_len": int(max(inp['seqlens'])), "num_q_heads": w.num_q_heads,
                    "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "num_splits": P,
                    "kernel": kernel_used, "deterministic": args.deterministic,
+                   "queries_per_sequence": args.queries,
                    "kv_layout": f"paged ({args.paged_layout}), {args.paged}-token pages shuffled in a pool"
                    if args.paged
                    else "dense [B][Hkv][S][d]",

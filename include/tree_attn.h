@@ -83,7 +83,8 @@ typedef enum {
 typedef struct {
     int32_t batch;          /* B >= 1 */
     int32_t num_q_heads;    /* Hq >= 1 */
-    int32_t num_kv_heads;   /* Hkv >= 1, Hq % Hkv == 0, Hq/Hkv in {1,2,4,8,16} */
+    int32_t num_kv_heads;   /* Hkv >= 1, Hq % Hkv == 0, 1 <= Hq/Hkv <= 16 (a power of two
+                               unless q and the cache are BF16) */
     int32_t head_dim;       /* d: 64 or 128 */
     int32_t max_seqlen;     /* S: cache capacity per sequence, tokens (>= 1) */
     int32_t q_dtype;        /* ta_dtype */
@@ -98,7 +99,7 @@ typedef struct {
 typedef enum {
     TA_KERNEL_AUTO = 0,  /* tensor-core path when it applies, else FMA */
     TA_KERNEL_FMA = 1,   /* FP32 FMA on CUDA cores; every dtype combination */
-    TA_KERNEL_MMA = 2    /* BF16 tensor-core mma; needs q and kv in BF16, Hq/Hkv <= 8 */
+    TA_KERNEL_MMA = 2    /* BF16 tensor-core mma; needs q and kv in BF16, Hq/Hkv <= 16 */
 } ta_kernel;
 
 /* Bits of ta_options.flags. */
@@ -205,6 +206,26 @@ int tree_attn_decode_paged(const ta_shape *shape, const ta_paged_kv *paged, cons
                            const void *k_pages, const void *v_pages, const int32_t *seqlens,
                            float *out, float *lse, int num_splits, void *workspace,
                            size_t workspace_bytes, const ta_options *options, void *stream);
+
+/* Several queries per sequence (multi-query decode, e.g. verifying draft
+ * tokens): query i of batch row b sits at position seqlens[b] - num_queries + i.
+ * With `causal` != 0 it attends to tokens [0, seqlens[b] - num_queries + i];
+ * otherwise every query attends to all seqlens[b] tokens.  A query that sees
+ * no token gives out = 0, lse = -inf.
+ *  q    device [batch][num_q_heads][num_queries][head_dim], dtype q_dtype
+ *  out  device float32 [batch][num_q_heads][num_queries][head_dim]
+ *  lse  device float32 [batch][num_q_heads][num_queries], or NULL
+ *  paged  NULL for dense caches, else as for tree_attn_decode_paged
+ * Each (head, query) pair is handled as one query head of the KV group:
+ * num_q_heads * num_queries / num_kv_heads must be at most 16 (a power of two
+ * unless q and the cache are BF16), and tree_attn_workspace_bytes,
+ * tree_attn_pick_splits and tree_attn_launch_count take the shape with
+ * num_q_heads multiplied by num_queries.  num_queries in [1, 16]. */
+int tree_attn_decode_multi(const ta_shape *shape, const ta_paged_kv *paged, int num_queries,
+                           int causal, const void *q, const void *k_cache, const void *v_cache,
+                           const int32_t *seqlens, float *out, float *lse, int num_splits,
+                           void *workspace, size_t workspace_bytes, const ta_options *options,
+                           void *stream);
 
 /* The tree combine on its own ("The Tree Reduction Merge Operator" applied to
  * P states per (b, h), then the root normalisation O = o / l):

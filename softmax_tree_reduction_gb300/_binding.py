@@ -28,7 +28,8 @@ TA_NOALLOC_SCRATCH_BYTES = 8 << 20
 _EXPORTS = ["tree_attn_status_string", "tree_attn_version", "tree_attn_check_shape",
             "tree_attn_workspace_bytes", "tree_attn_pick_splits", "tree_attn_decode",
             "tree_attn_decode_ex", "tree_attn_combine", "tree_attn_get_device_error",
-            "tree_attn_decode_noalloc", "tree_attn_launch_count", "tree_attn_decode_paged"]
+            "tree_attn_decode_noalloc", "tree_attn_launch_count", "tree_attn_decode_paged",
+            "tree_attn_decode_multi"]
 
 
 class TaShape(ctypes.Structure):
@@ -94,6 +95,9 @@ def load(path: str = LIB_PATH):
         lib.tree_attn_decode_paged.argtypes = [SP, ctypes.POINTER(TaPagedKV), P, P, P, P, P, P, I32, P,
                                                SZ, ctypes.POINTER(TaOptions), P]
         lib.tree_attn_decode_paged.restype = I32
+        lib.tree_attn_decode_multi.argtypes = [SP, ctypes.POINTER(TaPagedKV), I32, I32, P, P, P, P, P, P,
+                                               I32, P, SZ, ctypes.POINTER(TaOptions), P]
+        lib.tree_attn_decode_multi.restype = I32
         lib.tree_attn_launch_count.argtypes = [SP, I32, ctypes.POINTER(TaOptions)]
         lib.tree_attn_launch_count.restype = I32
         lib.tree_attn_get_device_error.argtypes = [P]
@@ -340,4 +344,62 @@ def tree_attn_decode_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torc
                                     _ptr(workspace), ws_bytes, ctypes.byref(opts), _stream(stream))
     if rc != TA_OK:
         raise TreeAttnError(rc, "tree_attn_decode_paged")
+    return out, lse
+
+
+def tree_attn_decode_multi(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                           seqlens: torch.Tensor, causal: bool = True,
+                           block_table: Optional[torch.Tensor] = None,
+                           out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                           num_splits: int = 0, workspace: Optional[torch.Tensor] = None,
+                           kernel: str = "auto", scale: Optional[float] = None, stream=None,
+                           deterministic: bool = False, max_seqlen: Optional[int] = None):
+    """Several queries per sequence through the C ABI.
+
+    q: [B, Hq, nq, d]; query i of row b sits at position seqlens[b] - nq + i and, when
+    causal, sees tokens [0, seqlens[b] - nq + i].  k_cache/v_cache: dense [B, Hkv, S, d]
+    caches, or page pools [num_pages, page_size, Hkv, d] with ``block_table``.
+    Returns (out [B, Hq, nq, d], lse [B, Hq, nq]).
+    """
+    lib = load()
+    _check_cuda(q, k_cache, v_cache, seqlens, block_table, out, lse, workspace)
+    if q.dim() != 4 or not q.is_contiguous():
+        raise ValueError("q must be a contiguous [B, Hq, nq, d] tensor")
+    if v_cache.shape != k_cache.shape or v_cache.stride() != k_cache.stride() or k_cache.stride(3) != 1:
+        raise ValueError("k_cache and v_cache must share shape and strides, channels contiguous")
+    if seqlens.dtype != torch.int32 or not seqlens.is_contiguous():
+        raise ValueError("seqlens must be a contiguous int32 tensor")
+    B, Hq, nq, d = q.shape
+    paged = None
+    if block_table is None:
+        base = make_shape(q[:, :, 0, :], k_cache, scale)
+    else:
+        if block_table.dtype != torch.int32 or not block_table.is_contiguous():
+            raise ValueError("block_table must be a contiguous int32 tensor")
+        num_pages, page_size, Hkv, _ = k_cache.shape
+        S = int(max_seqlen) if max_seqlen is not None else block_table.shape[1] * page_size
+        sp, st, sh, _ = k_cache.stride()
+        base = TaShape(B, Hq, Hkv, d, S, _dtype_code(q.dtype), _dtype_code(k_cache.dtype),
+                       float(scale or 0.0), sp, sh, st)
+        paged = TaPagedKV(block_table.data_ptr(), block_table.shape[1], page_size, num_pages, 0)
+    eff = TaShape.from_buffer_copy(base)
+    eff.num_q_heads = Hq * nq
+    if out is None:
+        out = torch.empty(B, Hq, nq, d, dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty(B, Hq, nq, dtype=torch.float32, device=q.device)
+    P = int(num_splits)
+    if P <= 0:
+        P = tree_attn_pick_splits(eff)
+    nbytes = tree_attn_workspace_bytes(eff, P)
+    if nbytes and workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    opts = TaOptions(TA_KERNEL[kernel], TA_FLAG_DETERMINISTIC if deterministic else 0, None, None)
+    rc = lib.tree_attn_decode_multi(ctypes.byref(base), ctypes.byref(paged) if paged is not None else None,
+                                    nq, int(bool(causal)), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                    _ptr(seqlens), _ptr(out), _ptr(lse), P, _ptr(workspace), ws_bytes,
+                                    ctypes.byref(opts), _stream(stream))
+    if rc != TA_OK:
+        raise TreeAttnError(rc, "tree_attn_decode_multi")
     return out, lse

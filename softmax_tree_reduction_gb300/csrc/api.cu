@@ -119,7 +119,7 @@ int check_shape(const ta_shape* s, Strides* st, int page_size = 0) {
         return TA_ERR_SHAPE;
     if (s->num_q_heads % s->num_kv_heads != 0) return TA_ERR_SHAPE;
     const int G = s->num_q_heads / s->num_kv_heads;
-    if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return TA_ERR_SHAPE;
+    if (G < 1 || G > 16) return TA_ERR_SHAPE;
     if (s->head_dim != 64 && s->head_dim != 128) return TA_ERR_SHAPE;
     if ((s->q_dtype != TA_F32 && s->q_dtype != TA_BF16) ||
         (s->kv_dtype != TA_F32 && s->kv_dtype != TA_BF16))
@@ -153,12 +153,19 @@ int check_shape(const ta_shape* s, Strides* st, int page_size = 0) {
     return TA_OK;
 }
 
+// Kernel family for a shape (num_q_heads counts (head, query) pairs for
+// multi-query calls): the tensor-core kernel takes BF16 q and cache with up to
+// 16 columns per KV head; the FMA kernel any dtypes with a power-of-two group.
 int resolve_kernel(const ta_shape* s, int requested) {
-    const bool mma_ok = s->q_dtype == TA_BF16 && s->kv_dtype == TA_BF16 &&
-                        (s->num_q_heads / s->num_kv_heads) <= 8;
+    const int G = s->num_q_heads / s->num_kv_heads;
+    const bool bf16 = s->q_dtype == TA_BF16 && s->kv_dtype == TA_BF16;
+    const bool mma_ok = bf16 && G <= 16;
+    const bool fma_ok = (G & (G - 1)) == 0 && G <= 16;
     switch (requested) {
-        case TA_KERNEL_AUTO: return mma_ok ? TA_KERNEL_MMA : TA_KERNEL_FMA;
-        case TA_KERNEL_FMA: return TA_KERNEL_FMA;
+        case TA_KERNEL_AUTO:
+            return mma_ok ? static_cast<int>(TA_KERNEL_MMA)
+                          : (fma_ok ? static_cast<int>(TA_KERNEL_FMA) : static_cast<int>(TA_ERR_SHAPE));
+        case TA_KERNEL_FMA: return fma_ok ? static_cast<int>(TA_KERNEL_FMA) : static_cast<int>(TA_ERR_SHAPE);
         case TA_KERNEL_MMA: return mma_ok ? static_cast<int>(TA_KERNEL_MMA) : static_cast<int>(TA_ERR_DTYPE);
         default: return TA_ERR_SHAPE;
     }
@@ -329,7 +336,8 @@ int check_paged(const ta_shape* shape, const ta_paged_kv* pg) {
     return TA_OK;
 }
 
-int decode_impl(const ta_shape* shape, const ta_paged_kv* paged, const void* q,
+// `shape` counts (head, query) pairs as query heads when nq > 1.
+int decode_impl(const ta_shape* shape, const ta_paged_kv* paged, int nq, int causal, const void* q,
                 const void* k_cache, const void* v_cache, const int32_t* seqlens, float* out,
                 float* lse, int num_splits, void* workspace, size_t workspace_bytes,
                 const ta_options* options, void* stream_ptr) {
@@ -392,6 +400,8 @@ int decode_impl(const ta_shape* shape, const ta_paged_kv* paged, const void* q,
     p.G = shape->num_q_heads / shape->num_kv_heads;
     p.S = shape->max_seqlen;
     p.P = P;
+    p.nq = nq;
+    p.causal = causal ? 1 : 0;
     const float scale = shape->scale > 0.f ? shape->scale
                                            : 1.0f / std::sqrt(static_cast<float>(shape->head_dim));
     p.scale_log2 = scale * ta::kLog2e;
@@ -475,7 +485,12 @@ const char* tree_attn_status_string(int status) {
 
 int tree_attn_version(void) { return TREE_ATTN_VERSION; }
 
-int tree_attn_check_shape(const ta_shape* shape) { return check_shape(shape, nullptr); }
+int tree_attn_check_shape(const ta_shape* shape) {
+    const int rc = check_shape(shape, nullptr);
+    if (rc != TA_OK) return rc;
+    const int kernel = resolve_kernel(shape, TA_KERNEL_AUTO);
+    return kernel < 0 ? kernel : TA_OK;
+}
 
 size_t tree_attn_workspace_bytes(const ta_shape* shape, int num_splits) {
     if (check_shape(shape, nullptr) != TA_OK) return 0;
@@ -500,7 +515,7 @@ int tree_attn_decode_ex(const ta_shape* shape, const void* q, const void* k_cach
                         const void* v_cache, const int32_t* seqlens, float* out, float* lse,
                         int num_splits, void* workspace, size_t workspace_bytes,
                         const ta_options* options, void* stream) {
-    return decode_impl(shape, nullptr, q, k_cache, v_cache, seqlens, out, lse, num_splits,
+    return decode_impl(shape, nullptr, 1, 0, q, k_cache, v_cache, seqlens, out, lse, num_splits,
                        workspace, workspace_bytes, options, stream);
 }
 
@@ -509,8 +524,22 @@ int tree_attn_decode_paged(const ta_shape* shape, const ta_paged_kv* paged, cons
                            float* out, float* lse, int num_splits, void* workspace,
                            size_t workspace_bytes, const ta_options* options, void* stream) {
     if (!paged) return TA_ERR_NULL;
-    return decode_impl(shape, paged, q, k_pages, v_pages, seqlens, out, lse, num_splits, workspace,
-                       workspace_bytes, options, stream);
+    return decode_impl(shape, paged, 1, 0, q, k_pages, v_pages, seqlens, out, lse, num_splits,
+                       workspace, workspace_bytes, options, stream);
+}
+
+int tree_attn_decode_multi(const ta_shape* shape, const ta_paged_kv* paged, int num_queries,
+                           int causal, const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* seqlens, float* out, float* lse, int num_splits,
+                           void* workspace, size_t workspace_bytes, const ta_options* options,
+                           void* stream) {
+    if (!shape) return TA_ERR_NULL;
+    if (num_queries < 1 || num_queries > 16) return TA_ERR_SHAPE;
+    if (static_cast<int64_t>(shape->num_q_heads) * num_queries > (1 << 30)) return TA_ERR_SHAPE;
+    ta_shape eff = *shape;  // each (head, query) pair is a query head of the cache
+    eff.num_q_heads = shape->num_q_heads * num_queries;
+    return decode_impl(&eff, paged, num_queries, causal, q, k_cache, v_cache, seqlens, out, lse,
+                       num_splits, workspace, workspace_bytes, options, stream);
 }
 
 int tree_attn_launch_count(const ta_shape* shape, int num_splits, const ta_options* options) {

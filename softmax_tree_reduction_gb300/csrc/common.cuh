@@ -40,7 +40,9 @@ struct SplitParams {
     int page_shift;         // log2(page_size)
     int num_pages;          // pages in the pool (an out-of-range page reads zeros)
     int box_rows;           // tokens per TMA box: the tile, or the page when it is smaller
-    int B, Hq, Hkv, G, S, P;
+    int B, Hq, Hkv, G, S, P; // Hq, G count virtual heads: query heads x queries per row
+    int nq;                 // queries per row (q rows are [head][query])
+    int causal;             // query i of nq sees tokens < N - nq + 1 + i
     int chunk_tiles;        // tiles per scheduled chunk
     float scale_log2;       // logit scale * log2(e)
 };

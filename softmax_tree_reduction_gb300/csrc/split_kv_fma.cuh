@@ -164,6 +164,11 @@ __global__ void __launch_bounds__(FmaCfg<KV, D>::kThreads, 1)
                     qf[i][c * EPC + e] = qv * p.scale_log2;
                 }
     }
+    // causal limits of this warp's virtual heads (query i of nq sees tokens < N - nq + 1 + i)
+    int lim[GC];
+#pragma unroll
+    for (int i = 0; i < GC; ++i)
+        lim[i] = p.causal ? N - p.nq + 1 + (hc * GC + i) % p.nq : 0x7fffffff;
     float m[GC], l[GC], o[GC][EPL];
 #pragma unroll
     for (int i = 0; i < GC; ++i) {
@@ -182,6 +187,7 @@ __global__ void __launch_bounds__(FmaCfg<KV, D>::kThreads, 1)
         }
         const int tile_valid = meta[s].nvalid;
         if (tile_valid < 0) break;  // end of this block's work
+        const int tile_tok0 = meta[s].tok0;
         const uint8_t* kst = stages + s * C::kStageBytes;
         const uint8_t* vst = kst + C::kKBytes;
         for (int step = 0; step < steps; ++step) {
@@ -203,7 +209,8 @@ __global__ void __launch_bounds__(FmaCfg<KV, D>::kThreads, 1)
                 dot += __shfl_xor_sync(0xffffffffu, dot, 1);
                 dot += __shfl_xor_sync(0xffffffffu, dot, 2);
                 dot += __shfl_xor_sync(0xffffffffu, dot, 4);
-                const float sc = valid ? dot : -INFINITY;
+                const bool vi = valid && tile_tok0 + row < lim[i];
+                const float sc = vi ? dot : -INFINITY;
                 if (sc > m[i]) {
                     const float al = ex2(m[i] - sc);
                     m[i] = sc;
@@ -211,7 +218,7 @@ __global__ void __launch_bounds__(FmaCfg<KV, D>::kThreads, 1)
 #pragma unroll
                     for (int e = 0; e < EPL; ++e) o[i][e] *= al;
                 }
-                pv[i] = valid ? ex2(sc - m[i]) : 0.f;
+                pv[i] = vi ? ex2(sc - m[i]) : 0.f;
                 l[i] += pv[i];
             }
             if (valid) {

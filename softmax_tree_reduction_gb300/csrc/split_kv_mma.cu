@@ -19,7 +19,9 @@
 //                                              place by movmatrix.trans)
 //  P is fed to the second product as BF16 hi + lo parts (two mma), so the
 //  weights keep ~16 significant bits; every accumulation is FP32.
-//  Heads beyond G in the 8-wide n dimension are zero and never written.
+//  The n dimension holds the group's G query heads (or (head, query) pairs
+//  when several queries share the cache), 8 per n-tile, one or two n-tiles;
+//  unused columns are zero and never written.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -42,7 +44,7 @@ struct MmaCfg {
     // the warps' states are merged in the stage buffers once streaming is over
     static constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes;
     static constexpr int kThreads = 32 * (kWarps + 1);
-    static_assert(kWarps * 8 * (D + 2) * 4 <= kStages * kStageBytes, "merge buffer");
+    static_assert(kWarps * 16 * (D + 2) * 4 <= kStages * kStageBytes, "merge buffer (two n-tiles)");
     static_assert(kTile <= 256, "TMA box height");
 };
 
@@ -88,7 +90,7 @@ __device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat162 v) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-template <int D>
+template <int D, int NT>
 __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
     split_kv_mma_kernel(const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const SplitParams p) {
@@ -97,9 +99,9 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* stages = smem;
-    float* mg_o = reinterpret_cast<float*>(stages);  // [W][8][D], after streaming
-    float* mg_m = mg_o + C::kWarps * 8 * D;          // [W][8]
-    float* mg_l = mg_m + C::kWarps * 8;              // [W][8]
+    float* mg_o = reinterpret_cast<float*>(stages);  // [W][8*NT][D], after streaming
+    float* mg_m = mg_o + C::kWarps * 8 * NT * D;     // [W][8*NT]
+    float* mg_l = mg_m + C::kWarps * 8 * NT;         // [W][8*NT]
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
     uint64_t* empty = full + C::kStages;
     volatile StageMeta* meta = reinterpret_cast<volatile StageMeta*>(empty + C::kStages);
@@ -170,26 +172,46 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
     const int gid = lane >> 2, tig = lane & 3;
     const int r8 = lane & 7;
 
-    // q as the B operand of S^T = K Q^T: column n = head gid of this group.
-    uint32_t qb[D / 16][2];
-    {
-        const bool hv = gid < p.G;
-        const int hq = g * p.G + (hv ? gid : 0);
+    // q as the B operand of S^T = K Q^T.  Column n of n-tile t is virtual head
+    // c = 8t + n of this KV head's group: a query head, or a (head, query) pair
+    // when several queries share the cache (q rows are [head][query]).
+    uint32_t qb[NT][D / 16][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int c = nt * 8 + gid;
+        const bool hv = c < p.G;
+        const int hq = g * p.G + (hv ? c : 0);
         const __nv_bfloat16* qh =
             static_cast<const __nv_bfloat16*>(p.q) + (static_cast<size_t>(b) * p.Hq + hq) * D;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-            qb[kk][0] = hv ? *reinterpret_cast<const uint32_t*>(qh + 16 * kk + 2 * tig) : 0u;
-            qb[kk][1] = hv ? *reinterpret_cast<const uint32_t*>(qh + 16 * kk + 8 + 2 * tig) : 0u;
+            qb[nt][kk][0] = hv ? *reinterpret_cast<const uint32_t*>(qh + 16 * kk + 2 * tig) : 0u;
+            qb[nt][kk][1] = hv ? *reinterpret_cast<const uint32_t*>(qh + 16 * kk + 8 + 2 * tig) : 0u;
         }
     }
-
-    // Running state for heads (2*tig, 2*tig+1): maxima (log2 units, equal in
-    // all lanes of a column), per-lane partial denominators, O^T fragments.
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    float oacc[D / 16][4];
+    // Causal limits of this thread's columns (query i of nq sees tokens < N - nq + 1 + i);
+    // masking applies only to blocks reaching past N - nq + 1.
+    const int causal_from = p.causal ? N - p.nq + 1 : 0x7fffffff;
+    int lim[NT][2];
 #pragma unroll
-    for (int mt = 0; mt < D / 16; ++mt) oacc[mt][0] = oacc[mt][1] = oacc[mt][2] = oacc[mt][3] = 0.f;
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+            lim[nt][j] = p.causal ? causal_from + (nt * 8 + 2 * tig + j) % p.nq : 0x7fffffff;
+
+    // Running state for columns (2*tig, 2*tig+1) of each n-tile: maxima (log2
+    // units, equal in all lanes of a column), per-lane partial denominators,
+    // O^T fragments.
+    float m[NT][2], l[NT][2];
+    float oacc[NT][D / 16][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        m[nt][0] = m[nt][1] = -INFINITY;
+        l[nt][0] = l[nt][1] = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt)
+            oacc[nt][mt][0] = oacc[nt][mt][1] = oacc[nt][mt][2] = oacc[nt][mt][3] = 0.f;
+    }
 
     // ldmatrix row addresses (swizzled 16-byte chunk = chunk ^ (row & 7)).  A
     // stage holds tile/R boxes of [half][R rows][128 B] (R = box_rows >= 16), so
@@ -213,63 +235,85 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
         }
         const int tile_valid = meta[s].nvalid;
         if (tile_valid < 0) break;  // end of this block's work
+        const int blk0 = meta[s].tok0 + cw * 16;  // first token of this warp's block
         const uint32_t kbase = smem_u32(stages + s * C::kStageBytes);
         const uint32_t vbase = kbase + C::kKBytes;
         const int nvalid = tile_valid - cw * 16;  // valid tokens of this warp's 16-token block
 
         if (nvalid > 0) {
-            // S^T = K_blk Q^T (two accumulators to shorten the dependency chain)
-            float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+            // S^T = K_blk Q^T (two accumulators per n-tile to shorten the dependency chain)
+            float sa[NT][4], sb[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sa[nt][e] = sb[nt][e] = 0.f;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 const int c = 2 * (kk & 3) + k_chi;
                 uint32_t a[4];
                 ldsm_x4(a, kbase + (kk >> 2) * half_bytes + k_row + ((c ^ r8) << 4));
-                if (kk & 1)
-                    mma_bf16(sb, a, qb[kk][0], qb[kk][1]);
-                else
-                    mma_bf16(sa, a, qb[kk][0], qb[kk][1]);
-            }
-            float s0 = (sa[0] + sb[0]) * sl2, s1 = (sa[1] + sb[1]) * sl2;
-            float s2 = (sa[2] + sb[2]) * sl2, s3 = (sa[3] + sb[3]) * sl2;
-            if (nvalid < 16) {
-                if (gid >= nvalid) s0 = s1 = -INFINITY;
-                if (gid + 8 >= nvalid) s2 = s3 = -INFINITY;
-            }
-            // block maximum per head over the 16 tokens (lanes differing in gid)
-            float bm0 = fmaxf(s0, s2), bm1 = fmaxf(s1, s3);
 #pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
-                bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
-            }
-            const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
-            const float ms0 = (mn0 == -INFINITY) ? 0.f : mn0;
-            const float ms1 = (mn1 == -INFINITY) ? 0.f : mn1;
-            const float al0 = ex2(m0 - ms0), al1 = ex2(m1 - ms1);
-            const float p0 = ex2(s0 - ms0), p1 = ex2(s1 - ms1);
-            const float p2 = ex2(s2 - ms0), p3 = ex2(s3 - ms1);
-            l0 = l0 * al0 + (p0 + p2);
-            l1 = l1 * al1 + (p1 + p3);
-            m0 = mn0;
-            m1 = mn1;
-            if (__any_sync(0xffffffffu, (al0 != 1.f) || (al1 != 1.f))) {
-#pragma unroll
-                for (int mt = 0; mt < D / 16; ++mt) {
-                    oacc[mt][0] *= al0;
-                    oacc[mt][1] *= al1;
-                    oacc[mt][2] *= al0;
-                    oacc[mt][3] *= al1;
+                for (int nt = 0; nt < NT; ++nt) {
+                    if (kk & 1)
+                        mma_bf16(sb[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
+                    else
+                        mma_bf16(sa[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
                 }
             }
-            // P^T as B fragments (k = token, n = head), BF16 hi + lo parts.
-            const __nv_bfloat162 h01 = __floats2bfloat162_rn(p0, p1);
-            const __nv_bfloat162 h23 = __floats2bfloat162_rn(p2, p3);
-            const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
-            const __nv_bfloat162 e01 = __floats2bfloat162_rn(p0 - f01.x, p1 - f01.y);
-            const __nv_bfloat162 e23 = __floats2bfloat162_rn(p2 - f23.x, p3 - f23.y);
-            const uint32_t bh0 = movtrans(bf16x2_bits(h01)), bh1 = movtrans(bf16x2_bits(h23));
-            const uint32_t bl0 = movtrans(bf16x2_bits(e01)), bl1 = movtrans(bf16x2_bits(e23));
+            const bool causal_blk = blk0 + 16 > causal_from;
+            uint32_t bh[NT][2], bl[NT][2];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                float s0 = (sa[nt][0] + sb[nt][0]) * sl2, s1 = (sa[nt][1] + sb[nt][1]) * sl2;
+                float s2 = (sa[nt][2] + sb[nt][2]) * sl2, s3 = (sa[nt][3] + sb[nt][3]) * sl2;
+                if (nvalid < 16) {
+                    if (gid >= nvalid) s0 = s1 = -INFINITY;
+                    if (gid + 8 >= nvalid) s2 = s3 = -INFINITY;
+                }
+                if (causal_blk) {
+                    const int ta = blk0 + gid, tb = ta + 8;
+                    if (ta >= lim[nt][0]) s0 = -INFINITY;
+                    if (ta >= lim[nt][1]) s1 = -INFINITY;
+                    if (tb >= lim[nt][0]) s2 = -INFINITY;
+                    if (tb >= lim[nt][1]) s3 = -INFINITY;
+                }
+                // block maximum per column over the 16 tokens (lanes differing in gid)
+                float bm0 = fmaxf(s0, s2), bm1 = fmaxf(s1, s3);
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
+                    bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
+                }
+                const float mn0 = fmaxf(m[nt][0], bm0), mn1 = fmaxf(m[nt][1], bm1);
+                const float ms0 = (mn0 == -INFINITY) ? 0.f : mn0;
+                const float ms1 = (mn1 == -INFINITY) ? 0.f : mn1;
+                const float al0 = ex2(m[nt][0] - ms0), al1 = ex2(m[nt][1] - ms1);
+                const float p0 = ex2(s0 - ms0), p1 = ex2(s1 - ms1);
+                const float p2 = ex2(s2 - ms0), p3 = ex2(s3 - ms1);
+                l[nt][0] = l[nt][0] * al0 + (p0 + p2);
+                l[nt][1] = l[nt][1] * al1 + (p1 + p3);
+                m[nt][0] = mn0;
+                m[nt][1] = mn1;
+                if (__any_sync(0xffffffffu, (al0 != 1.f) || (al1 != 1.f))) {
+#pragma unroll
+                    for (int mt = 0; mt < D / 16; ++mt) {
+                        oacc[nt][mt][0] *= al0;
+                        oacc[nt][mt][1] *= al1;
+                        oacc[nt][mt][2] *= al0;
+                        oacc[nt][mt][3] *= al1;
+                    }
+                }
+                // P^T as B fragments (k = token, n = column), BF16 hi + lo parts.
+                const __nv_bfloat162 h01 = __floats2bfloat162_rn(p0, p1);
+                const __nv_bfloat162 h23 = __floats2bfloat162_rn(p2, p3);
+                const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+                const __nv_bfloat162 e01 = __floats2bfloat162_rn(p0 - f01.x, p1 - f01.y);
+                const __nv_bfloat162 e23 = __floats2bfloat162_rn(p2 - f23.x, p3 - f23.y);
+                bh[nt][0] = movtrans(bf16x2_bits(h01));
+                bh[nt][1] = movtrans(bf16x2_bits(h23));
+                bl[nt][0] = movtrans(bf16x2_bits(e01));
+                bl[nt][1] = movtrans(bf16x2_bits(e23));
+            }
             // V rows past the slice may hold anything (even NaN): zero them.
             uint32_t vm01 = 0xffffffffu, vm23 = 0xffffffffu;
             if (nvalid < 16) {
@@ -286,8 +330,11 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
                 a[1] &= vm01;
                 a[2] &= vm23;
                 a[3] &= vm23;
-                mma_bf16(oacc[mt], a, bh0, bh1);
-                mma_bf16(oacc[mt], a, bl0, bl1);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    mma_bf16(oacc[nt][mt], a, bh[nt][0], bh[nt][1]);
+                    mma_bf16(oacc[nt][mt], a, bl[nt][0], bl[nt][1]);
+                }
             }
         }
         __syncwarp();
@@ -296,25 +343,32 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
     if (timed_out) atomicOr(abort_flag, 1);
 
     // ------------------------------------------- merge the warps' states
+    constexpr int kCols = 8 * NT;  // columns per warp state
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-    }
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            l[nt][0] += __shfl_xor_sync(0xffffffffu, l[nt][0], off);
+            l[nt][1] += __shfl_xor_sync(0xffffffffu, l[nt][1], off);
+        }
     consumer_sync(C::kWarps * 32);  // every warp is done reading the stages
-    float* mo = mg_o + cw * 8 * D;
+    float* mo = mg_o + cw * kCols * D;
 #pragma unroll
-    for (int mt = 0; mt < D / 16; ++mt) {
-        mo[(2 * tig) * D + 16 * mt + gid] = oacc[mt][0];
-        mo[(2 * tig + 1) * D + 16 * mt + gid] = oacc[mt][1];
-        mo[(2 * tig) * D + 16 * mt + gid + 8] = oacc[mt][2];
-        mo[(2 * tig + 1) * D + 16 * mt + gid + 8] = oacc[mt][3];
-    }
-    if (gid == 0) {
-        mg_m[cw * 8 + 2 * tig] = m0;
-        mg_m[cw * 8 + 2 * tig + 1] = m1;
-        mg_l[cw * 8 + 2 * tig] = l0;
-        mg_l[cw * 8 + 2 * tig + 1] = l1;
+    for (int nt = 0; nt < NT; ++nt) {
+        const int c0 = nt * 8 + 2 * tig;
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+            mo[c0 * D + 16 * mt + gid] = oacc[nt][mt][0];
+            mo[(c0 + 1) * D + 16 * mt + gid] = oacc[nt][mt][1];
+            mo[c0 * D + 16 * mt + gid + 8] = oacc[nt][mt][2];
+            mo[(c0 + 1) * D + 16 * mt + gid + 8] = oacc[nt][mt][3];
+        }
+        if (gid == 0) {
+            mg_m[cw * kCols + c0] = m[nt][0];
+            mg_m[cw * kCols + c0 + 1] = m[nt][1];
+            mg_l[cw * kCols + c0] = l[nt][0];
+            mg_l[cw * kCols + c0 + 1] = l[nt][1];
+        }
     }
     consumer_sync(C::kWarps * 32);
     const bool poison = bad || (*abort_flag != 0) || (*bad_page != 0);
@@ -325,7 +379,7 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < C::kWarps; ++w) {
-            mw[w] = mg_m[w * 8 + h];
+            mw[w] = mg_m[w * kCols + h];
             M = fmaxf(M, mw[w]);
         }
         const float Ms = (M == -INFINITY) ? 0.f : M;
@@ -333,23 +387,23 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
 #pragma unroll
         for (int w = 0; w < C::kWarps; ++w) {
             const float wt = ex2(mw[w] - Ms);
-            ow[w] = wt * mg_o[(w * 8 + h) * D + dd];
-            lw[w] = wt * mg_l[w * 8 + h];
+            ow[w] = wt * mg_o[(w * kCols + h) * D + dd];
+            lw[w] = wt * mg_l[w * kCols + h];
         }
         // pairwise tree over the warps
         const float o = tree_sum<C::kWarps>(ow);
-        const float l = tree_sum<C::kWarps>(lw);
-        emit_state(p, b, g * p.G + h, split, D, dd, o, l, M, poison);
+        const float lsum = tree_sum<C::kWarps>(lw);
+        emit_state(p, b, g * p.G + h, split, D, dd, o, lsum, M, poison);
     }
     if (p.done) finish_row<D>(p, b, g, reinterpret_cast<float*>(stages), last_flag, ct, C::kWarps * 32);
     allow_dependents();
 }
 
-template <int D>
+template <int D, int NT>
 cudaError_t launch_impl(const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& p,
                         cudaStream_t stream) {
     using C = MmaCfg<D>;
-    cudaError_t e = cudaFuncSetAttribute(split_kv_mma_kernel<D>,
+    cudaError_t e = cudaFuncSetAttribute(split_kv_mma_kernel<D, NT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -362,7 +416,7 @@ cudaError_t launch_impl(const CUtensorMap& tk, const CUtensorMap& tv, const Spli
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<D>, tk, tv, p);
+    return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<D, NT>, tk, tv, p);
 }
 
 }  // namespace
@@ -374,9 +428,12 @@ Geometry mma_geometry(int head_dim) {
 
 cudaError_t launch_split_mma(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv,
                              const SplitParams& p, cudaStream_t stream) {
+    // one n-tile of 8 columns per KV head group, two for up to 16
+    const bool two = p.G > 8;
     switch (head_dim) {
-        case 64: return launch_impl<64>(tk, tv, p, stream);
-        case 128: return launch_impl<128>(tk, tv, p, stream);
+        case 64: return two ? launch_impl<64, 2>(tk, tv, p, stream) : launch_impl<64, 1>(tk, tv, p, stream);
+        case 128:
+            return two ? launch_impl<128, 2>(tk, tv, p, stream) : launch_impl<128, 1>(tk, tv, p, stream);
         default: return cudaErrorInvalidValue;
     }
 }
