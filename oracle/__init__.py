@@ -15,6 +15,10 @@ What it restates (web pages on Tree Attention, arXiv:2408.04093):
   query i of a row of N tokens sits at position N - nq + i and, when causal,
   attends to tokens [0, N - nq + i]; each query is the definition above over
   its token range (a reading: the pages describe one query per step).
+* ``attention_e4m3`` -- the same over an FP8 E4M3 cache with one scale per KV
+  head (an extension the pages do not describe): the cache is widened exactly
+  from the E4M3 definition and multiplied by its scale, then the definition
+  above applies.
 * ``partials`` -- the local partial attention state (o, l, m) of one KV slice
   ("Core Innovation 1", item 2 "Local Independent Partial Attention").
 * ``merge`` -- the merge operator (+) of two states ("The Tree Reduction Merge
@@ -76,6 +80,11 @@ def _load(path: str | None = None):
     lib.oracle_attention_multi_f64.argtypes = [i32, i32, i32, i32, i64, i32, i32, p, i32, p, p, i32, p,
                                                dbl, p, p, i32]
     lib.oracle_attention_multi_f64.restype = i32
+    lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_to_double.restype = dbl
+    lib.oracle_attention_e4m3_f64.argtypes = [i32, i32, i32, i32, i64, i32, i32, p, i32, p, p, p, p, p,
+                                              dbl, p, p, i32]
+    lib.oracle_attention_e4m3_f64.restype = i32
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = i32
     return lib
@@ -169,6 +178,53 @@ def attention_multi(q, k, v, seqlens, causal: bool = True, scale: float | None =
                                       int(threads))
     if rc != 0:
         raise ValueError(f"oracle_attention_multi_f64 failed with code {rc}")
+    return out, lse
+
+
+def e4m3_to_double(code: int, lib_handle=None) -> float:
+    """One FP8 E4M3 code widened from the format's definition."""
+    return float((lib_handle or lib()).oracle_e4m3_to_double(int(code) & 0xFF))
+
+
+def attention_e4m3(q, k8, v8, k_scale, v_scale, seqlens, causal: bool = True,
+                   scale: float | None = None, threads: int = 0, lib_handle=None):
+    """Decode attention over an FP8 E4M3 cache with one scale per KV head.
+
+    q: [B, Hq, d] or [B, Hq, nq, d] (float32 / bfloat16); k8, v8: uint8 codes
+    [B, Hkv, S, d] (or torch float8_e4m3fn); k_scale, v_scale: [Hkv] floats.
+    K = k_scale[g] * e4m3(k8), V likewise.  Returns float64 (out, lse) shaped like q.
+    """
+    try:
+        import torch
+        if isinstance(k8, torch.Tensor):
+            k8 = k8.detach().cpu().contiguous().view(torch.uint8).numpy()
+            v8 = v8.detach().cpu().contiguous().view(torch.uint8).numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    qa, qt = _as_raw(q)
+    single = qa.ndim == 3
+    if single:
+        qa = qa[:, :, None, :]
+    B, Hq, nq, d = qa.shape
+    ka = np.ascontiguousarray(k8, dtype=np.uint8)
+    va = np.ascontiguousarray(v8, dtype=np.uint8)
+    _, Hkv, S, _ = ka.shape
+    ks = np.ascontiguousarray(np.asarray(k_scale, dtype=np.float32).reshape(Hkv))
+    vs = np.ascontiguousarray(np.asarray(v_scale, dtype=np.float32).reshape(Hkv))
+    sl = np.ascontiguousarray(np.asarray(seqlens, dtype=np.int32).reshape(B))
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    out = np.zeros((B, Hq, nq, d), dtype=np.float64)
+    lse = np.zeros((B, Hq, nq), dtype=np.float64)
+    qa = np.ascontiguousarray(qa)
+    L = lib_handle or lib()
+    rc = L.oracle_attention_e4m3_f64(B, Hq, Hkv, d, S, nq, int(bool(causal)), _ptr(qa), qt, _ptr(ka),
+                                     _ptr(va), _ptr(ks), _ptr(vs), _ptr(sl), float(scale), _ptr(out),
+                                     _ptr(lse), int(threads))
+    if rc != 0:
+        raise ValueError(f"oracle_attention_e4m3_f64 failed with code {rc}")
+    if single:
+        return out[:, :, 0], lse[:, :, 0]
     return out, lse
 
 
@@ -319,7 +375,7 @@ def even_bounds(seqlens, P: int):
     return starts, ends
 
 
-__all__ = ["attention", "attention_multi", "partials", "merge", "normalize", "tree_reduce", "combine", "empty_state",
+__all__ = ["attention", "attention_multi", "attention_e4m3", "e4m3_to_double", "partials", "merge", "normalize", "tree_reduce", "combine", "empty_state",
            "even_bounds", "build", "lib", "max_threads", "F32", "BF16"]
 
 if __name__ == "__main__":  # pragma: no cover

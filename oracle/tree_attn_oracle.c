@@ -303,6 +303,103 @@ int oracle_attention_multi_f64(int B, int Hq, int Hkv, int d, int64_t S, int nq,
     return bad ? -6 : 0;
 }
 
+/* FP8 E4M3 (the "fn" variant: no infinities) widened to double from its
+ * definition: sign bit, 4 exponent bits with bias 7, 3 mantissa bits;
+ * exponent 0 is subnormal (m/8 * 2^-6); S.1111.111 is NaN. */
+double oracle_e4m3_to_double(uint8_t x)
+{
+    const int sign = (x >> 7) & 1;
+    const int e = (x >> 3) & 0xF;
+    const int m = x & 0x7;
+    double v;
+    if (e == 0xF && m == 0x7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m / 8.0, -6);
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* Decode attention over an FP8 E4M3 cache with one scale per KV head:
+ * K[b,g,t,i] = k_scale[g] * e4m3(k8[b,g,t,i]), V likewise with v_scale; q in
+ * FP32 or BF16.  Otherwise the definition of oracle_attention_f64, with nq
+ * queries per row as in oracle_attention_multi_f64 (nq = 1 for one). */
+int oracle_attention_e4m3_f64(int B, int Hq, int Hkv, int d, int64_t S, int nq, int causal,
+                              const void *q, int q_dtype, const uint8_t *k8, const uint8_t *v8,
+                              const float *k_scale, const float *v_scale,
+                              const int32_t *seqlens, double scale,
+                              double *out, double *lse, int nthreads)
+{
+    int rc = check_args(B, Hq, Hkv, d, S, q_dtype, ORACLE_F32);
+    if (rc)
+        return rc;
+    if (nq < 1)
+        return -3;
+    for (int b = 0; b < B; ++b)
+        if (seqlens[b] < 0 || seqlens[b] > S)
+            return -8;
+    const int G = Hq / Hkv;
+    const int64_t work = (int64_t)B * Hq * nq;
+    int bad = 0;
+#ifdef _OPENMP
+    if (nthreads <= 0)
+        nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads) reduction(| : bad)
+#endif
+    for (int64_t w = 0; w < work; ++w) {
+        const int i = (int)(w % nq);
+        const int64_t bh = w / nq;
+        const int b = (int)(bh / Hq);
+        const int h = (int)(bh % Hq);
+        const int g = h / G;
+        int64_t n = seqlens[b];
+        if (causal) {
+            n = n - nq + 1 + i;
+            if (n < 0)
+                n = 0;
+        }
+        const double ks = (double)k_scale[g], vs = (double)v_scale[g];
+        const int64_t qoff = w * d;
+        const int64_t kvoff = ((int64_t)b * Hkv + g) * S * d;
+        double *o = out + w * d;
+        if (n == 0) {
+            for (int c = 0; c < d; ++c)
+                o[c] = 0.0;
+            lse[w] = -INFINITY;
+            continue;
+        }
+        double *s = (double *)malloc((size_t)n * sizeof(double));
+        if (!s) {
+            bad = 1;
+            continue;
+        }
+        double M = -INFINITY;
+        for (int64_t t = 0; t < n; ++t) {
+            double acc = 0.0;
+            for (int c = 0; c < d; ++c)
+                acc += widen(q, q_dtype, qoff + c) * (ks * oracle_e4m3_to_double(k8[kvoff + t * d + c]));
+            s[t] = scale * acc;
+            if (s[t] > M)
+                M = s[t];
+        }
+        double L = 0.0;
+        for (int c = 0; c < d; ++c)
+            o[c] = 0.0;
+        for (int64_t t = 0; t < n; ++t) {
+            double e = exp(s[t] - M);
+            L += e;
+            for (int c = 0; c < d; ++c)
+                o[c] += e * (vs * oracle_e4m3_to_double(v8[kvoff + t * d + c]));
+        }
+        for (int c = 0; c < d; ++c)
+            o[c] = o[c] / L;
+        lse[w] = M + log(L);
+        free(s);
+    }
+    return bad ? -6 : 0;
+}
+
 /* Number of OpenMP threads a call with nthreads <= 0 would use (1 when the
  * oracle was built without OpenMP). */
 int oracle_max_threads(void)

@@ -226,3 +226,21 @@ def page_pool(k, v, seqlens, page_size, layout="NHD", extra_pages=3, seed=0):
         kp = kp.permute(0, 2, 1, 3)
         vp = vp.permute(0, 2, 1, 3)
     return kp, vp, bt
+
+
+E4M3_MAX = 448.0
+
+
+def quantize_e4m3(x, per_head_dim=1):
+    """Round a [B, Hkv, S, d] cache to FP8 E4M3 with one scale per KV head
+    (scale = max|x| over that head / 448, so the head's largest element maps
+    to the largest finite code).  NaN elements (padding) stay NaN.  Returns
+    (codes as torch.float8_e4m3fn, scales [Hkv] float32).  Data preparation only."""
+    xf = x.float()
+    finite = torch.nan_to_num(xf.abs(), nan=0.0)
+    amax = finite.amax(dim=tuple(i for i in range(xf.dim()) if i != per_head_dim))
+    scales = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax)).float()
+    shape = [1] * xf.dim()
+    shape[per_head_dim] = -1
+    codes = (xf / scales.view(shape)).to(torch.float8_e4m3fn)
+    return codes, scales

@@ -167,3 +167,44 @@ def test_multi_query_mutant_is_caught(name, tmpdir):
     subprocess.run(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", path, "-o", so, "-lm"], check=True,
                    capture_output=True)
     assert _multi_battery_fails(oracle._load(so)), f"mutant {name} survived"
+
+
+FP8_MUTANTS = {
+    "exponent_bias_8": ("v = ldexp(1.0 + (double)m / 8.0, e - 7);", "v = ldexp(1.0 + (double)m / 8.0, e - 8);"),
+    "subnormal_as_normal": ("v = ldexp((double)m / 8.0, -6);", "v = ldexp(1.0 + (double)m / 8.0, -6);"),
+    "no_nan_code": ("if (e == 0xF && m == 0x7)\n        return NAN;", "if (0)\n        return NAN;"),
+    "k_scale_dropped": ("(ks * oracle_e4m3_to_double(k8[kvoff + t * d + c]))",
+                        "(oracle_e4m3_to_double(k8[kvoff + t * d + c]))"),
+    "v_scale_from_k": ("const double ks = (double)k_scale[g], vs = (double)v_scale[g];",
+                       "const double ks = (double)k_scale[g], vs = (double)k_scale[g];"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(FP8_MUTANTS))
+def test_fp8_mutant_is_caught(name, tmpdir):
+    from tests import test_oracle_fp8 as fp8
+    old, new = FP8_MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, name
+    path = os.path.join(tmpdir, f"fmut_{name}.c")
+    with open(path, "w") as f:
+        f.write(src.replace(old, new))
+    so = os.path.join(tmpdir, f"libfmut_{name}.so")
+    subprocess.run(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", path, "-o", so, "-lm"], check=True,
+                   capture_output=True)
+    handle = oracle._load(so)
+    real = oracle.lib
+    oracle.lib = lambda: handle
+    try:
+        failed = False
+        for check in (fp8.test_e4m3_decoder_matches_torch_for_every_code,
+                      fp8.test_fp8_attention_matches_sdpa_on_dequantized_cache):
+            try:
+                with np.errstate(all="ignore"):
+                    check()
+            except (AssertionError, ValueError):
+                failed = True
+                break
+        assert failed, f"mutant {name} survived"
+    finally:
+        oracle.lib = real
