@@ -79,6 +79,8 @@ def parse_args(argv=None):
                     help="page layout: [pages][page][heads][d] (NHD) or [pages][heads][page][d] (HND)")
     ap.add_argument("--graph", action="store_true",
                     help="sweeps: capture the timed steps in one CUDA graph (removes the host's per-call cost)")
+    ap.add_argument("--fp8", action="store_true",
+                    help="FP8 E4M3 caches (the workload's K and V rounded with one scale per KV head)")
     ap.add_argument("--deterministic", action="store_true",
                     help="fixed chunk assignment (bitwise reproducible) instead of run-time balancing")
     return ap.parse_args(argv)
@@ -103,7 +105,7 @@ def load_peaks():
 
 
 def kernel_source_hash(kernel):
-    name = {"mma": "split_kv_mma.cu", "fma": "split_kv_fma.cuh"}[kernel]
+    name = {"mma": "split_kv_mma.cu", "fma": "split_kv_fma.cuh", "fp8": "split_kv_fp8.cu"}[kernel]
     h = hashlib.sha256()
     for f in (name, "common.cuh", "emit.cuh", "sched.cuh"):
         with open(os.path.join(ROOT, "softmax_tree_reduction_gb300", "csrc", f), "rb") as fh:
@@ -229,18 +231,24 @@ def l2_note(kv_bytes, copies):
 
 
 # ------------------------------------------------------------- CPU oracle
-def oracle_baseline(w, inp, target_s, max_s=30.0):
+def oracle_baseline(w, inp, target_s, max_s=30.0, kv_bytes=None):
     """Time the float64 oracle as it stands on the host's cores.
 
     Sample: the whole workload (every head, every token), repeated until
-    ``target_s`` seconds of CPU work; value = KV bytes processed / time."""
+    ``target_s`` seconds of CPU work; value = KV bytes processed / time.
+    With ``k_scale`` in ``inp`` the caches are E4M3 codes (the FP8 oracle)."""
     import oracle
     threads = oracle.max_threads()
-    kv_bytes = w.kv_bytes(inp["seqlens"])
+    if kv_bytes is None:
+        kv_bytes = w.kv_bytes(inp["seqlens"])
     reps, elapsed = 0, 0.0
     while elapsed < target_s and elapsed < max_s:
         t0 = time.perf_counter()
-        oracle.attention(inp["q"], inp["k"], inp["v"], inp["seqlens"], w.softmax_scale, threads=threads)
+        if "k_scale" in inp:
+            oracle.attention_e4m3(inp["q"], inp["k"], inp["v"], inp["k_scale"], inp["v_scale"],
+                                  inp["seqlens"], scale=w.softmax_scale, threads=threads)
+        else:
+            oracle.attention(inp["q"], inp["k"], inp["v"], inp["seqlens"], w.softmax_scale, threads=threads)
         elapsed += time.perf_counter() - t0
         reps += 1
         if reps == 1 and elapsed * 2 > max_s:
@@ -276,8 +284,16 @@ def run_ours(args, rank, world, local):
     if args.queries > 1:
         gq = torch.Generator().manual_seed(w.seed + 1)
         inp["q"] = torch.randn(w.batch, w.num_q_heads, args.queries, w.head_dim, generator=gq).to(w.q_dtype)
+    kv_names = ("q", "k", "v", "seqlens")
+    if args.fp8:
+        import dataclasses
+        inp["k"], inp["k_scale"] = workloads.quantize_e4m3(inp["k"])
+        inp["v"], inp["v_scale"] = workloads.quantize_e4m3(inp["v"])
+        w = dataclasses.replace(w, kv_dtype=torch.float8_e4m3fn)
+        kv_names = kv_names + ("k_scale", "v_scale")
     kv_bytes = w.kv_bytes(inp["seqlens"])
-    dev = {k: inp[k].cuda() for k in ("q", "k", "v", "seqlens")}
+    dev = {k: inp[k].cuda() for k in kv_names}
+    scales = dict(k_scale=dev.get("k_scale"), v_scale=dev.get("v_scale"))
     if args.paged:
         kp, vp, bt = workloads.page_pool(inp["k"], inp["v"], inp["seqlens"], args.paged, seed=w.seed,
                                          layout=args.paged_layout)
@@ -288,14 +304,17 @@ def run_ours(args, rank, world, local):
     shape = (ta.make_shape(dev["q"] if args.queries == 1 else dev["q"][:, :, 0], inp["k"]) if not args.paged else
              ta.TaShape(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.max_seqlen,
                         ta.TA_BF16 if w.q_dtype == torch.bfloat16 else ta.TA_F32,
-                        ta.TA_BF16 if w.kv_dtype == torch.bfloat16 else ta.TA_F32, 0.0,
+                        ta.TA_E4M3 if args.fp8 else ta.TA_BF16 if w.kv_dtype == torch.bfloat16
+                        else ta.TA_F32, 0.0,
                         dev["k"].stride(0), dev["k"].stride(2), dev["k"].stride(1)))
     if args.queries > 1:  # each (head, query) pair counts as a query head
         shape = ta.TaShape.from_buffer_copy(shape)
         shape.num_q_heads *= args.queries
     P = args.num_splits if args.num_splits > 0 else ta.tree_attn_pick_splits(shape)
     kernel_used = args.kernel
-    if kernel_used == "auto":
+    if args.fp8:
+        kernel_used = "fp8"
+    elif kernel_used == "auto":
         kernel_used = "mma" if (w.kv_dtype == torch.bfloat16 and w.q_dtype == torch.bfloat16
                                 and w.group * args.queries <= 16) else "fma"
     B, Hq, d = dev["q"].shape[0], dev["q"].shape[1], dev["q"].shape[-1]
@@ -311,16 +330,16 @@ def run_ours(args, rank, world, local):
             ta.tree_attn_decode_multi(c["q"], c["k"], c["v"], c["seqlens"], causal=True,
                                       block_table=c.get("block_table"), out=out, lse=lse, num_splits=P,
                                       workspace=ws, kernel=args.kernel, deterministic=args.deterministic,
-                                      max_seqlen=w.max_seqlen if args.paged else None)
+                                      max_seqlen=w.max_seqlen if args.paged else None, **scales)
             return
         if args.paged:
             ta.tree_attn_decode_paged(c["q"], c["k"], c["v"], c["block_table"], c["seqlens"], out=out,
                                       lse=lse, num_splits=P, workspace=ws, kernel=args.kernel,
-                                      deterministic=args.deterministic, max_seqlen=w.max_seqlen)
+                                      deterministic=args.deterministic, max_seqlen=w.max_seqlen, **scales)
             return
         ta.tree_attn_decode(c["q"], c["k"], c["v"], c["seqlens"], out=out, lse=lse, num_splits=P,
                             workspace=ws, kernel=args.kernel, split_events=events,
-                            deterministic=args.deterministic)
+                            deterministic=args.deterministic, **scales)
 
     for i in range(max(args.warmup, 3)):
         step(i)
@@ -374,8 +393,9 @@ def run_ours(args, rank, world, local):
     if not args.no_e2e:
         n_e2e = max(1, min(args.e2e_steps, args.steps))
         host = {k: (dev[k].cpu() if args.paged and k in ("k", "v", "block_table") else inp[k]).pin_memory()
-                for k in (("q", "k", "v", "seqlens", "block_table") if args.paged else ("q", "k", "v", "seqlens"))}
+                for k in (kv_names + ("block_table",) if args.paged else kv_names)}
         dbuf = {k: torch.empty_like(host[k], device="cuda") for k in host}
+        dscales = dict(k_scale=dbuf.get("k_scale"), v_scale=dbuf.get("v_scale"))
         h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
         h2d = sum(t.numel() * t.element_size() for t in host.values())
@@ -388,14 +408,14 @@ def run_ours(args, rank, world, local):
                 ta.tree_attn_decode_multi(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["seqlens"], causal=True,
                                           block_table=dbuf.get("block_table"), out=out, lse=lse,
                                           num_splits=P, workspace=ws, kernel=args.kernel,
-                                          max_seqlen=w.max_seqlen if args.paged else None)
+                                          max_seqlen=w.max_seqlen if args.paged else None, **dscales)
             elif args.paged:
                 ta.tree_attn_decode_paged(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["block_table"],
                                           dbuf["seqlens"], out=out, lse=lse, num_splits=P, workspace=ws,
-                                          kernel=args.kernel, max_seqlen=w.max_seqlen)
+                                          kernel=args.kernel, max_seqlen=w.max_seqlen, **dscales)
             else:
                 ta.tree_attn_decode(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["seqlens"], out=out, lse=lse,
-                                    num_splits=P, workspace=ws, kernel=args.kernel)
+                                    num_splits=P, workspace=ws, kernel=args.kernel, **dscales)
             h_out.copy_(out, non_blocking=True)
             h_lse.copy_(lse, non_blocking=True)
 
@@ -425,17 +445,20 @@ def run_ours(args, rank, world, local):
         traffic = tr["bytes_per_launch"]
     cpu = None
     if not args.no_cpu_baseline:
-        cpu = oracle_baseline(w, inp, args.cpu_seconds)
+        cpu = oracle_baseline(w, inp, args.cpu_seconds, kv_bytes=kv_bytes)
     return {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
         "us_per_step": round(ms_per_step * 1e3, 3),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded N(0,1) Llama-shaped KV cache; no weights or datasets)",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 KV, bf16 q, f16 mma / f32 accumulate" if args.fp8 else "bf16",
+        "data": "synthetic (seeded N(0,1) Llama-shaped KV cache; no weights or datasets)"
+                + ("; K and V rounded to E4M3 with one scale per KV head" if args.fp8 else ""),
         "config": {"workload": f"{w.name}: {w.description}", "batch": w.batch,
                    "seq_len": int(max(inp['seqlens'])), "num_q_heads": w.num_q_heads,
                    "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "num_splits": P,
                    "kernel": kernel_used, "deterministic": args.deterministic,
+                   "kv_dtype": "e4m3 (per-KV-head scales)" if args.fp8 else str(w.kv_dtype).replace("torch.", ""),
                    "queries_per_sequence": args.queries,
                    "kv_layout": f"paged ({args.paged_layout}), {args.paged}-token pages shuffled in a pool"
                    if args.paged

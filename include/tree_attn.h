@@ -62,7 +62,11 @@ typedef enum {
 /* Element types. */
 typedef enum {
     TA_F32 = 0,   /* IEEE binary32 */
-    TA_BF16 = 1   /* bfloat16 (upper half of a binary32) */
+    TA_BF16 = 1,  /* bfloat16 (upper half of a binary32) */
+    TA_E4M3 = 2   /* FP8 E4M3 ("fn": no infinities), KV caches only; the element
+                     value is the code times a per-KV-head scale given in
+                     ta_options (k_scale, v_scale).  Needs BF16 q, head_dim 128
+                     and at most 8 query heads (x queries) per KV head. */
 } ta_dtype;
 
 /* Largest accepted num_splits. */
@@ -99,7 +103,8 @@ typedef struct {
 typedef enum {
     TA_KERNEL_AUTO = 0,  /* tensor-core path when it applies, else FMA */
     TA_KERNEL_FMA = 1,   /* FP32 FMA on CUDA cores; every dtype combination */
-    TA_KERNEL_MMA = 2    /* BF16 tensor-core mma; needs q and kv in BF16, Hq/Hkv <= 16 */
+    TA_KERNEL_MMA = 2    /* tensor-core mma: BF16 q and kv (Hq/Hkv <= 16), or BF16 q with an
+                            E4M3 cache (Hq/Hkv <= 8, head_dim 128) */
 } ta_kernel;
 
 /* Bits of ta_options.flags. */
@@ -117,6 +122,8 @@ typedef struct {
     void *split_start_event;   /* optional cudaEvent_t recorded on `stream` just before the
                                   per-slice kernel is enqueued */
     void *split_end_event;     /* optional cudaEvent_t recorded just after it (before the combine) */
+    const float *k_scale;      /* device float [num_kv_heads]: required for TA_E4M3 caches */
+    const float *v_scale;      /* device float [num_kv_heads]: required for TA_E4M3 caches */
 } ta_options;
 
 /* Text for a status code (static storage; never NULL). */

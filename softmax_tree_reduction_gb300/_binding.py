@@ -19,7 +19,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libtreeattn.so")
 
 TA_OK = 0
-TA_F32, TA_BF16 = 0, 1
+TA_F32, TA_BF16, TA_E4M3 = 0, 1, 2
 TA_KERNEL = {"auto": 0, "fma": 1, "mma": 2}
 TA_MAX_SPLITS = 4096
 TA_FLAG_DETERMINISTIC = 1
@@ -43,7 +43,8 @@ class TaShape(ctypes.Structure):
 
 class TaOptions(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int32), ("flags", ctypes.c_int32),
-                ("split_start_event", ctypes.c_void_p), ("split_end_event", ctypes.c_void_p)]
+                ("split_start_event", ctypes.c_void_p), ("split_end_event", ctypes.c_void_p),
+                ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p)]
 
 
 class TaPagedKV(ctypes.Structure):
@@ -111,7 +112,23 @@ def _dtype_code(dt: torch.dtype) -> int:
         return TA_F32
     if dt == torch.bfloat16:
         return TA_BF16
-    raise TypeError(f"unsupported dtype {dt}; use float32 or bfloat16")
+    if dt == getattr(torch, "float8_e4m3fn", None):
+        return TA_E4M3
+    raise TypeError(f"unsupported dtype {dt}; use float32, bfloat16 or float8_e4m3fn (caches)")
+
+
+def _options(kernel, deterministic, k_scale=None, v_scale=None, events=None):
+    o = TaOptions(TA_KERNEL[kernel], TA_FLAG_DETERMINISTIC if deterministic else 0, None, None,
+                  None, None)
+    if events is not None:
+        o.split_start_event = events[0].cuda_event
+        o.split_end_event = events[1].cuda_event
+    for name, t in (("k_scale", k_scale), ("v_scale", v_scale)):
+        if t is not None:
+            if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous float32 CUDA tensor [num_kv_heads]")
+            setattr(o, name, t.data_ptr())
+    return o
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -174,7 +191,7 @@ def tree_attn_pick_splits(shape: TaShape, host_seqlens=None, num_sms: int = 0) -
 def tree_attn_launch_count(shape: TaShape, num_splits: int, kernel: str = "auto",
                            deterministic: bool = False) -> int:
     """Kernels one tree_attn_decode call enqueues (1 when the merge is fused)."""
-    opts = TaOptions(TA_KERNEL[kernel], TA_FLAG_DETERMINISTIC if deterministic else 0, None, None)
+    opts = _options(kernel, deterministic)
     r = int(load().tree_attn_launch_count(ctypes.byref(shape), int(num_splits), ctypes.byref(opts)))
     if r < 0:
         raise TreeAttnError(r, "tree_attn_launch_count")
@@ -192,7 +209,8 @@ def tree_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
                      lse: Optional[torch.Tensor] = None, num_splits: int = 0,
                      workspace: Optional[torch.Tensor] = None, kernel: str = "auto",
                      scale: Optional[float] = None, stream=None, split_events=None,
-                     want_lse: bool = True, deterministic: bool = False):
+                     want_lse: bool = True, deterministic: bool = False,
+                     k_scale: Optional[torch.Tensor] = None, v_scale: Optional[torch.Tensor] = None):
     """Decode attention through the C ABI; returns (out [B,Hq,d] fp32, lse [B,Hq] fp32 or None).
 
     ``num_splits`` <= 0 uses the library's heuristic (picked on the host so the
@@ -224,20 +242,18 @@ def tree_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     st = _stream(stream)
-    if kernel == "auto" and split_events is None and not deterministic:
+    if kernel == "auto" and split_events is None and not deterministic and k_scale is None:
         rc = lib.tree_attn_decode(ctypes.byref(shape), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                   _ptr(seqlens), _ptr(out), _ptr(lse), P, _ptr(workspace),
                                   ws_bytes, st)
     else:
-        opts = TaOptions(TA_KERNEL[kernel], TA_FLAG_DETERMINISTIC if deterministic else 0, None, None)
         if split_events is not None:
             # torch creates the CUDA event on its first record; record once so the
             # handle exists (the library's own record then replaces this one)
             torch_stream = stream if isinstance(stream, torch.cuda.Stream) else torch.cuda.current_stream()
             for ev in split_events:
                 ev.record(torch_stream)
-            opts.split_start_event = split_events[0].cuda_event
-            opts.split_end_event = split_events[1].cuda_event
+        opts = _options(kernel, deterministic, k_scale, v_scale, split_events)
         rc = lib.tree_attn_decode_ex(ctypes.byref(shape), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                      _ptr(seqlens), _ptr(out), _ptr(lse), P, _ptr(workspace),
                                      ws_bytes, ctypes.byref(opts), st)
@@ -301,7 +317,8 @@ def tree_attn_decode_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torc
                            out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
                            num_splits: int = 0, workspace: Optional[torch.Tensor] = None,
                            kernel: str = "auto", scale: Optional[float] = None, stream=None,
-                           deterministic: bool = False, max_seqlen: Optional[int] = None):
+                           deterministic: bool = False, max_seqlen: Optional[int] = None,
+                           k_scale: Optional[torch.Tensor] = None, v_scale: Optional[torch.Tensor] = None):
     """Decode attention over a paged KV cache through the C ABI.
 
     k_pages, v_pages: [num_pages, page_size, Hkv, d] views (any strides with a unit
@@ -338,7 +355,7 @@ def tree_attn_decode_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torc
     if nbytes and workspace is None:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    opts = TaOptions(TA_KERNEL[kernel], TA_FLAG_DETERMINISTIC if deterministic else 0, None, None)
+    opts = _options(kernel, deterministic, k_scale, v_scale)
     rc = lib.tree_attn_decode_paged(ctypes.byref(shape), ctypes.byref(paged), _ptr(q), _ptr(k_pages),
                                     _ptr(v_pages), _ptr(seqlens), _ptr(out), _ptr(lse), P,
                                     _ptr(workspace), ws_bytes, ctypes.byref(opts), _stream(stream))
@@ -353,7 +370,8 @@ def tree_attn_decode_multi(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
                            out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
                            num_splits: int = 0, workspace: Optional[torch.Tensor] = None,
                            kernel: str = "auto", scale: Optional[float] = None, stream=None,
-                           deterministic: bool = False, max_seqlen: Optional[int] = None):
+                           deterministic: bool = False, max_seqlen: Optional[int] = None,
+                           k_scale: Optional[torch.Tensor] = None, v_scale: Optional[torch.Tensor] = None):
     """Several queries per sequence through the C ABI.
 
     q: [B, Hq, nq, d]; query i of row b sits at position seqlens[b] - nq + i and, when
@@ -395,7 +413,7 @@ def tree_attn_decode_multi(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
     if nbytes and workspace is None:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    opts = TaOptions(TA_KERNEL[kernel], TA_FLAG_DETERMINISTIC if deterministic else 0, None, None)
+    opts = _options(kernel, deterministic, k_scale, v_scale)
     rc = lib.tree_attn_decode_multi(ctypes.byref(base), ctypes.byref(paged) if paged is not None else None,
                                     nq, int(bool(causal)), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                     _ptr(seqlens), _ptr(out), _ptr(lse), P, _ptr(workspace), ws_bytes,

@@ -104,7 +104,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-int elem_bytes(int dtype) { return dtype == TA_BF16 ? 2 : 4; }
+int elem_bytes(int dtype) { return dtype == TA_BF16 ? 2 : (dtype == TA_E4M3 ? 1 : 4); }
+
+// Internal kernel family for FP8 caches (selected by TA_KERNEL_AUTO / TA_KERNEL_MMA).
+constexpr int kKernelFp8 = 3;
 
 struct Strides {
     int64_t b, h, t;
@@ -122,7 +125,7 @@ int check_shape(const ta_shape* s, Strides* st, int page_size = 0) {
     if (G < 1 || G > 16) return TA_ERR_SHAPE;
     if (s->head_dim != 64 && s->head_dim != 128) return TA_ERR_SHAPE;
     if ((s->q_dtype != TA_F32 && s->q_dtype != TA_BF16) ||
-        (s->kv_dtype != TA_F32 && s->kv_dtype != TA_BF16))
+        (s->kv_dtype != TA_F32 && s->kv_dtype != TA_BF16 && s->kv_dtype != TA_E4M3))
         return TA_ERR_DTYPE;
     if (!(s->scale >= 0.f) || std::isinf(s->scale)) return TA_ERR_SHAPE;
     Strides r;
@@ -158,6 +161,12 @@ int check_shape(const ta_shape* s, Strides* st, int page_size = 0) {
 // 16 columns per KV head; the FMA kernel any dtypes with a power-of-two group.
 int resolve_kernel(const ta_shape* s, int requested) {
     const int G = s->num_q_heads / s->num_kv_heads;
+    if (s->kv_dtype == TA_E4M3) {
+        const bool ok = s->q_dtype == TA_BF16 && s->head_dim == 128 && G <= 8;
+        if (requested == TA_KERNEL_FMA) return TA_ERR_DTYPE;
+        if (requested != TA_KERNEL_AUTO && requested != TA_KERNEL_MMA) return TA_ERR_SHAPE;
+        return ok ? kKernelFp8 : static_cast<int>(TA_ERR_DTYPE);
+    }
     const bool bf16 = s->q_dtype == TA_BF16 && s->kv_dtype == TA_BF16;
     const bool mma_ok = bf16 && G <= 16;
     const bool fma_ok = (G & (G - 1)) == 0 && G <= 16;
@@ -172,6 +181,7 @@ int resolve_kernel(const ta_shape* s, int requested) {
 }
 
 Geometry geometry_of(const ta_shape* s, int kernel) {
+    if (kernel == kKernelFp8) return ta::fp8_geometry();
     return kernel == TA_KERNEL_MMA ? ta::mma_geometry(s->head_dim)
                                    : ta::fma_geometry(elem_bytes(s->kv_dtype), s->head_dim);
 }
@@ -297,7 +307,7 @@ int encode_kv_map(CUtensorMap* map, const void* base, const ta_shape* s, const S
                              static_cast<cuuint64_t>(st.b * es)};
     cuuint32_t box[4] = {static_cast<cuuint32_t>(geo.box_x), static_cast<cuuint32_t>(rows), 1, 1};
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-    if (geo.swizzle128) {
+    if (geo.halves5d) {
         // 5-D view (channel in half, token, half, KV head, row/page): one box
         // brings every 64-channel half of `rows` tokens, [half][rows][128 B].
         const cuuint64_t halves = static_cast<cuuint64_t>(s->head_dim / 64);
@@ -311,8 +321,9 @@ int encode_kv_map(CUtensorMap* map, const void* base, const ta_shape* s, const S
         return r5 == CUDA_SUCCESS ? TA_OK : TA_ERR_CUDA;
     }
     const CUresult r = fn(map,
-                          s->kv_dtype == TA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                                 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                          s->kv_dtype == TA_BF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                          : s->kv_dtype == TA_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                                   : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                           4, const_cast<void*>(base), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE,
                           geo.swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -355,6 +366,10 @@ int decode_impl(const ta_shape* shape, const ta_paged_kv* paged, int nq, int cau
     const bool deterministic = options && (options->flags & TA_FLAG_DETERMINISTIC);
     const int kernel = resolve_kernel(shape, options ? options->kernel : TA_KERNEL_AUTO);
     if (kernel < 0) return kernel;
+    if (shape->kv_dtype == TA_E4M3) {
+        if (!options || !options->k_scale || !options->v_scale) return TA_ERR_NULL;
+        if (!aligned(options->k_scale, 4) || !aligned(options->v_scale, 4)) return TA_ERR_ALIGN;
+    }
     cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
 
     if (num_splits > TA_MAX_SPLITS) return TA_ERR_SPLITS;
@@ -390,6 +405,10 @@ int decode_impl(const ta_shape* shape, const ta_paged_kv* paged, int nq, int cau
 
     ta::SplitParams p;
     std::memset(&p, 0, sizeof p);
+    if (options) {
+        p.k_scale = options->k_scale;
+        p.v_scale = options->v_scale;
+    }
     p.q = q;
     p.q_is_bf16 = shape->q_dtype == TA_BF16;
     p.seqlens = seqlens;
@@ -442,7 +461,9 @@ int decode_impl(const ta_shape* shape, const ta_paged_kv* paged, int nq, int cau
         cudaEventRecord(static_cast<cudaEvent_t>(options->split_start_event), stream) != cudaSuccess)
         return TA_ERR_CUDA;
     cudaError_t e;
-    if (kernel == TA_KERNEL_MMA)
+    if (kernel == kKernelFp8)
+        e = ta::launch_split_fp8(tk, tv, p, stream);
+    else if (kernel == TA_KERNEL_MMA)
         e = ta::launch_split_mma(shape->head_dim, tk, tv, p, stream);
     else if (shape->kv_dtype == TA_BF16)
         e = ta::launch_split_fma_bf16(shape->head_dim, tk, tv, p, stream);

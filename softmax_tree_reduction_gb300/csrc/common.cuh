@@ -35,6 +35,8 @@ struct SplitParams {
     unsigned* claim;        // [B*Hkv] chunk counters (null: static chunk assignment)
     unsigned* done;         // [B*Hkv] row tickets (null: no ticket is taken)
     int fuse;               // the row's last block merges the partial states
+    const float* k_scale;   // [Hkv] FP8 caches: K = k_scale[g] * e4m3 code
+    const float* v_scale;   // [Hkv] likewise for V
     const int32_t* block_table;  // [B][max_pages] (null: dense cache, coordinate w = batch row)
     int max_pages;          // block_table columns
     int page_shift;         // log2(page_size)

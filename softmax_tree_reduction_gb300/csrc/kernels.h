@@ -13,10 +13,12 @@ struct Geometry {
     int tile_tokens;   // tokens per pipeline stage (slices are cut at multiples of this)
     int box_x;         // channels per TMA box (64 with 128-byte swizzle, else head_dim)
     int swizzle128;    // 1: CU_TENSOR_MAP_SWIZZLE_128B, 0: no swizzle
+    int halves5d = 0;  // 1: 5-D view whose box brings every 64-channel half at once
 };
 
 Geometry mma_geometry(int head_dim);
 Geometry fma_geometry(int kv_elem_bytes, int head_dim);
+Geometry fp8_geometry();
 
 // Per-slice kernels.  Grid (P, Hkv, B); `tk`/`tv` are 4-D tensor maps over
 // (channel, token, KV head, batch row) with the box of the kernel's Geometry.
@@ -26,6 +28,9 @@ cudaError_t launch_split_fma_bf16(int head_dim, const CUtensorMap& tk, const CUt
                                   const SplitParams& p, cudaStream_t stream);
 cudaError_t launch_split_fma_f32(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv,
                                  const SplitParams& p, cudaStream_t stream);
+// FP8 (E4M3) caches, head_dim 128, BF16 q, up to 8 columns per KV head.
+cudaError_t launch_split_fp8(const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& p,
+                             cudaStream_t stream);
 
 // Cross-block tree combine of P partial states per (b, h) plus normalisation.
 // With `dependent` set it is launched as a programmatic dependent of the

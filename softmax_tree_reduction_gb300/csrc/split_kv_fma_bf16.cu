@@ -4,7 +4,7 @@
 namespace ta {
 
 Geometry fma_geometry(int kv_elem_bytes, int head_dim) {
-    return Geometry{32768 / (2 * head_dim * kv_elem_bytes), head_dim, 0};
+    return Geometry{32768 / (2 * head_dim * kv_elem_bytes), head_dim, 0, 0};
 }
 
 cudaError_t launch_split_fma_bf16(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -1,0 +1,414 @@
+// Split-KV partial attention over an FP8 (E4M3) KV cache with one scale per KV
+// head, on the tensor cores.  Same blocks, scheduler, warp merge and row merge
+// as the BF16 kernel; what changes is how the operands reach the mma.
+//
+// TMA brings 128-token tiles of 128-byte FP8 rows (128-byte swizzle).  There
+// is no widening pass through shared memory: each thread loads its fragment
+// bytes with 16-byte shared loads and converts E4M3 -> FP16 in registers
+// (exact), feeding FP16 mma.m16n8k16 with FP32 accumulation.
+//
+//  S^T = K Q^T   The channel order of the contraction is permuted so that
+//                thread (gid, tig) needs bytes [32 tig, 32 tig + 32) of rows
+//                gid and gid + 8: in k-step kk its k-elements (2tig, 2tig+1)
+//                and (2tig+8, 2tig+9) are channels 32tig + 4kk + {0,1} and
+//                {2,3}.  q is loaded in the same order.
+//  O^T += V^T P^T  Output channels are permuted instead: row gid (gid + 8) of
+//                m-tile mt is channel 16 gid + 2 mt (+1), so a thread reads one
+//                16-byte chunk of each of its four token rows, and byte pairs
+//                of two token rows are interleaved with prmt before the
+//                conversion.
+// q is scaled by an exact power of two into the FP16 range (folded back into
+// the logit scale with the KV head's K scale); P is scaled by 2^14 before its
+// FP16 hi + lo split so that small weights keep their precision; the V scale
+// and 2^-14 are applied to the merged numerator.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "emit.cuh"
+#include "kernels.h"
+#include "sched.cuh"
+
+namespace ta {
+namespace {
+
+struct Fp8Cfg {
+    static constexpr int D = 128;
+    static constexpr int kWarps = 8;                 // consumer warps
+    static constexpr int kTile = 16 * kWarps;        // tokens per stage
+    static constexpr int kKBytes = kTile * D;        // one byte per element
+    static constexpr int kStageBytes = 2 * kKBytes;  // K and V
+    static constexpr int kStages = 6;
+    static constexpr int kBarBytes = 2 * kStages * 8 + kStages * 8 + 32;
+    static constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes;
+    static constexpr int kThreads = 32 * (kWarps + 1);
+    static_assert(kWarps * 8 * (D + 2) * 4 <= kStages * kStageBytes, "merge buffer");
+};
+
+constexpr float kPScale = 16384.f;  // 2^14
+
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t pair16) {
+    uint32_t r;
+    const uint16_t x = static_cast<uint16_t>(pair16);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(x));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                        uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t movtrans(uint32_t x) {
+    uint32_t y;
+    asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t half2_bits(__half2 v) { return *reinterpret_cast<uint32_t*>(&v); }
+
+template <int N>
+__device__ __forceinline__ float tree_sum(const float* v) {
+    if constexpr (N == 1) {
+        return v[0];
+    } else {
+        return tree_sum<N / 2>(v) + tree_sum<N / 2>(v + N / 2);
+    }
+}
+
+__global__ void __launch_bounds__(Fp8Cfg::kThreads, 1)
+    split_kv_fp8_kernel(const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const SplitParams p) {
+    using C = Fp8Cfg;
+    constexpr int D = C::D;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* stages = smem;
+    float* mg_o = reinterpret_cast<float*>(stages);  // [W][8][D], after streaming
+    float* mg_m = mg_o + C::kWarps * 8 * D;
+    float* mg_l = mg_m + C::kWarps * 8;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
+    uint64_t* empty = full + C::kStages;
+    volatile StageMeta* meta = reinterpret_cast<volatile StageMeta*>(empty + C::kStages);
+    int* abort_flag = const_cast<int*>(reinterpret_cast<volatile int*>(meta + C::kStages));
+    int* last_flag = abort_flag + 1;
+    volatile unsigned* claim_sink = reinterpret_cast<volatile unsigned*>(abort_flag + 2);
+    volatile int* bad_page = reinterpret_cast<volatile int*>(abort_flag + 3);
+
+    const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], C::kWarps);
+        }
+        *abort_flag = 0;
+        *bad_page = 0;
+        fence_barrier_init();
+    }
+    if (threadIdx.x == 32) {
+        prefetch_tensormap(&tmK);
+        prefetch_tensormap(&tmV);
+    }
+    __syncthreads();
+    wait_primary();  // nothing an earlier kernel may write is touched before this
+
+    int N = p.seqlens[b];
+    const bool bad = (N < 0) || (N > p.S);
+    if (bad) {
+        if (threadIdx.x == 0) atomicOr(p.err, kErrBadSeqlen);
+        N = 0;
+    }
+
+    if (warp == 0) {
+        const uint64_t pol = l2_policy_evict_first();
+        const bool paged = p.block_table != nullptr;
+        const int page_mask = (1 << p.page_shift) - 1;
+        const int box_bytes = p.box_rows * D;
+        produce_row<C::kStages>(
+            p, b, b * p.Hkv + g, N, split, C::kTile, full, empty, meta, claim_sink, bad_page,
+            C::kStageBytes, [&](int s, int y, int j, int page) {
+                uint8_t* st = stages + s * C::kStageBytes;
+                const int off = j * box_bytes;
+                if (!paged) {
+                    tma_load_4d(st + off, &tmK, 0, y, g, b, &full[s], pol);
+                    tma_load_4d(st + C::kKBytes + off, &tmV, 0, y, g, b, &full[s], pol);
+                    return;
+                }
+                const int ty = (y + j * p.box_rows) & page_mask;
+                tma_load_4d(st + off, &tmK, 0, ty, g, page, &full[s], pol);
+                tma_load_4d(st + C::kKBytes + off, &tmV, 0, ty, g, page, &full[s], pol);
+            });
+        allow_dependents();
+        return;
+    }
+
+    // ---------------------------------------------------------- consumers
+    const int cw = warp - 1;
+    const int gid = lane >> 2, tig = lane & 3;
+
+    // q (BF16) of column gid, channels 32 tig .. 32 tig + 31 in the permuted order.
+    float qv[32];
+    {
+        const bool hv = gid < p.G;
+        const int hq = g * p.G + (hv ? gid : 0);
+        const __nv_bfloat16* qh =
+            static_cast<const __nv_bfloat16*>(p.q) + (static_cast<size_t>(b) * p.Hq + hq) * D + 32 * tig;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) qv[j] = hv ? __bfloat162float(qh[j]) : 0.f;
+    }
+    // exact power-of-two scale bringing max|q| into [2^14, 2^15): every q value
+    // of the group is held by some lane of this warp
+    float amax = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(qv[j]));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    int qexp = 0;
+    if (amax > 0.f) {
+        int e;
+        frexpf(amax, &e);  // amax = f * 2^e, f in [0.5, 1)
+        qexp = max(-100, min(100, 15 - e));
+    }
+    const float qs = ldexpf(1.f, qexp);
+    uint32_t qb[D / 16][2];
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        qb[kk][0] = half2_bits(__floats2half2_rn(qv[4 * kk] * qs, qv[4 * kk + 1] * qs));
+        qb[kk][1] = half2_bits(__floats2half2_rn(qv[4 * kk + 2] * qs, qv[4 * kk + 3] * qs));
+    }
+    const float ks = p.k_scale[g], vs = p.v_scale[g];
+    const float sl2 = p.scale_log2 * ks / qs;
+
+    const int causal_from = p.causal ? N - p.nq + 1 : 0x7fffffff;
+    const int lim0 = p.causal ? causal_from + (2 * tig) % p.nq : 0x7fffffff;
+    const int lim1 = p.causal ? causal_from + (2 * tig + 1) % p.nq : 0x7fffffff;
+
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float oacc[D / 16][4];
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) oacc[mt][0] = oacc[mt][1] = oacc[mt][2] = oacc[mt][3] = 0.f;
+
+    // Rows are 128 B (one swizzle row); chunk c of row r sits at chunk c ^ (r & 7).
+    const int r0 = cw * 16;
+    const int ra = r0 + gid, rb = ra + 8;                       // K rows of this thread
+    const uint32_t k_a0 = ra * 128 + (((2 * tig) ^ (ra & 7)) << 4);
+    const uint32_t k_a1 = ra * 128 + (((2 * tig + 1) ^ (ra & 7)) << 4);
+    const uint32_t k_b0 = rb * 128 + (((2 * tig) ^ (rb & 7)) << 4);
+    const uint32_t k_b1 = rb * 128 + (((2 * tig + 1) ^ (rb & 7)) << 4);
+    const int tv0 = r0 + 2 * tig;                               // V rows of this thread
+    const uint32_t v_0 = tv0 * 128 + ((gid ^ (tv0 & 7)) << 4);
+    const uint32_t v_1 = (tv0 + 1) * 128 + ((gid ^ ((tv0 + 1) & 7)) << 4);
+    const uint32_t v_2 = (tv0 + 8) * 128 + ((gid ^ ((tv0 + 8) & 7)) << 4);
+    const uint32_t v_3 = (tv0 + 9) * 128 + ((gid ^ ((tv0 + 9) & 7)) << 4);
+    bool timed_out = false;
+
+    for (int it = 0;; ++it) {
+        const int s = it % C::kStages;
+        if (!mbar_wait(&full[s], (it / C::kStages) & 1, p.err)) {
+            timed_out = true;
+            break;
+        }
+        const int tile_valid = meta[s].nvalid;
+        if (tile_valid < 0) break;
+        const int blk0 = meta[s].tok0 + r0;
+        const uint32_t kbase = smem_u32(stages + s * C::kStageBytes);
+        const uint32_t vbase = kbase + C::kKBytes;
+        const int nvalid = tile_valid - r0;
+
+        if (nvalid > 0) {
+            const uint4 ka0 = lds128(kbase + k_a0), ka1 = lds128(kbase + k_a1);
+            const uint4 kb0 = lds128(kbase + k_b0), kb1 = lds128(kbase + k_b1);
+            const uint32_t wa[8] = {ka0.x, ka0.y, ka0.z, ka0.w, ka1.x, ka1.y, ka1.z, ka1.w};
+            const uint32_t wb[8] = {kb0.x, kb0.y, kb0.z, kb0.w, kb1.x, kb1.y, kb1.z, kb1.w};
+            float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                uint32_t a[4];
+                a[0] = e4m3x2_to_f16x2(wa[kk] & 0xffffu);
+                a[1] = e4m3x2_to_f16x2(wb[kk] & 0xffffu);
+                a[2] = e4m3x2_to_f16x2(wa[kk] >> 16);
+                a[3] = e4m3x2_to_f16x2(wb[kk] >> 16);
+                if (kk & 1)
+                    mma_f16(sb, a, qb[kk][0], qb[kk][1]);
+                else
+                    mma_f16(sa, a, qb[kk][0], qb[kk][1]);
+            }
+            float s0 = (sa[0] + sb[0]) * sl2, s1 = (sa[1] + sb[1]) * sl2;
+            float s2 = (sa[2] + sb[2]) * sl2, s3 = (sa[3] + sb[3]) * sl2;
+            if (nvalid < 16) {
+                if (gid >= nvalid) s0 = s1 = -INFINITY;
+                if (gid + 8 >= nvalid) s2 = s3 = -INFINITY;
+            }
+            if (blk0 + 16 > causal_from) {
+                const int ta = blk0 + gid, tb = ta + 8;
+                if (ta >= lim0) s0 = -INFINITY;
+                if (ta >= lim1) s1 = -INFINITY;
+                if (tb >= lim0) s2 = -INFINITY;
+                if (tb >= lim1) s3 = -INFINITY;
+            }
+            float bm0 = fmaxf(s0, s2), bm1 = fmaxf(s1, s3);
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
+                bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
+            }
+            const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+            const float ms0 = (mn0 == -INFINITY) ? 0.f : mn0;
+            const float ms1 = (mn1 == -INFINITY) ? 0.f : mn1;
+            const float al0 = ex2(m0 - ms0), al1 = ex2(m1 - ms1);
+            const float p0 = ex2(s0 - ms0), p1 = ex2(s1 - ms1);
+            const float p2 = ex2(s2 - ms0), p3 = ex2(s3 - ms1);
+            l0 = l0 * al0 + (p0 + p2);
+            l1 = l1 * al1 + (p1 + p3);
+            m0 = mn0;
+            m1 = mn1;
+            if (__any_sync(0xffffffffu, (al0 != 1.f) || (al1 != 1.f))) {
+#pragma unroll
+                for (int mt = 0; mt < D / 16; ++mt) {
+                    oacc[mt][0] *= al0;
+                    oacc[mt][1] *= al1;
+                    oacc[mt][2] *= al0;
+                    oacc[mt][3] *= al1;
+                }
+            }
+            // P^T (scaled by 2^14) as FP16 hi + lo B fragments
+            const float q0 = p0 * kPScale, q1 = p1 * kPScale, q2 = p2 * kPScale, q3 = p3 * kPScale;
+            const __half2 h01 = __floats2half2_rn(q0, q1), h23 = __floats2half2_rn(q2, q3);
+            const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+            const __half2 e01 = __floats2half2_rn(q0 - f01.x, q1 - f01.y);
+            const __half2 e23 = __floats2half2_rn(q2 - f23.x, q3 - f23.y);
+            const uint32_t bh0 = movtrans(half2_bits(h01)), bh1 = movtrans(half2_bits(h23));
+            const uint32_t bl0 = movtrans(half2_bits(e01)), bl1 = movtrans(half2_bits(e23));
+            // V: tokens 2tig, 2tig+1, 2tig+8, 2tig+9 of the block, channels 16 gid .. 16 gid + 15;
+            // rows past the valid range may hold anything (even NaN codes): zero them
+            uint4 va = lds128(vbase + v_0), vb = lds128(vbase + v_1);
+            uint4 vc = lds128(vbase + v_2), vd = lds128(vbase + v_3);
+            if (nvalid < 16) {
+                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                if (2 * tig >= nvalid) va = z;
+                if (2 * tig + 1 >= nvalid) vb = z;
+                if (2 * tig + 8 >= nvalid) vc = z;
+                if (2 * tig + 9 >= nvalid) vd = z;
+            }
+            const uint32_t xa[4] = {va.x, va.y, va.z, va.w}, xb[4] = {vb.x, vb.y, vb.z, vb.w};
+            const uint32_t xc[4] = {vc.x, vc.y, vc.z, vc.w}, xd[4] = {vd.x, vd.y, vd.z, vd.w};
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const uint32_t p01 = prmt(xa[w], xb[w], 0x5140u), p23 = prmt(xa[w], xb[w], 0x7362u);
+                const uint32_t r01 = prmt(xc[w], xd[w], 0x5140u), r23 = prmt(xc[w], xd[w], 0x7362u);
+                uint32_t a[4];
+                a[0] = e4m3x2_to_f16x2(p01 & 0xffffu);
+                a[1] = e4m3x2_to_f16x2(p01 >> 16);
+                a[2] = e4m3x2_to_f16x2(r01 & 0xffffu);
+                a[3] = e4m3x2_to_f16x2(r01 >> 16);
+                mma_f16(oacc[2 * w], a, bh0, bh1);
+                mma_f16(oacc[2 * w], a, bl0, bl1);
+                a[0] = e4m3x2_to_f16x2(p23 & 0xffffu);
+                a[1] = e4m3x2_to_f16x2(p23 >> 16);
+                a[2] = e4m3x2_to_f16x2(r23 & 0xffffu);
+                a[3] = e4m3x2_to_f16x2(r23 >> 16);
+                mma_f16(oacc[2 * w + 1], a, bh0, bh1);
+                mma_f16(oacc[2 * w + 1], a, bl0, bl1);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    if (timed_out) atomicOr(abort_flag, 1);
+
+    // ------------------------------------------- merge the warps' states
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+    consumer_sync(C::kWarps * 32);  // every warp is done reading the stages
+    float* mo = mg_o + cw * 8 * D;
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+        const int ch = 16 * gid + 2 * mt;  // output channel of fragment rows gid / gid + 8
+        mo[(2 * tig) * D + ch] = oacc[mt][0];
+        mo[(2 * tig + 1) * D + ch] = oacc[mt][1];
+        mo[(2 * tig) * D + ch + 1] = oacc[mt][2];
+        mo[(2 * tig + 1) * D + ch + 1] = oacc[mt][3];
+    }
+    if (gid == 0) {
+        mg_m[cw * 8 + 2 * tig] = m0;
+        mg_m[cw * 8 + 2 * tig + 1] = m1;
+        mg_l[cw * 8 + 2 * tig] = l0;
+        mg_l[cw * 8 + 2 * tig + 1] = l1;
+    }
+    consumer_sync(C::kWarps * 32);
+    const bool poison = bad || (*abort_flag != 0) || (*bad_page != 0);
+    const float oscale = vs / kPScale;
+    const int ct = threadIdx.x - 32;
+    for (int idx = ct; idx < p.G * D; idx += C::kWarps * 32) {
+        const int h = idx / D, dd = idx - h * D;
+        float mw[C::kWarps];
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < C::kWarps; ++w) {
+            mw[w] = mg_m[w * 8 + h];
+            M = fmaxf(M, mw[w]);
+        }
+        const float Ms = (M == -INFINITY) ? 0.f : M;
+        float ow[C::kWarps], lw[C::kWarps];
+#pragma unroll
+        for (int w = 0; w < C::kWarps; ++w) {
+            const float wt = ex2(mw[w] - Ms);
+            ow[w] = wt * mg_o[(w * 8 + h) * D + dd];
+            lw[w] = wt * mg_l[w * 8 + h];
+        }
+        const float o = tree_sum<C::kWarps>(ow) * oscale;
+        const float lsum = tree_sum<C::kWarps>(lw);
+        emit_state(p, b, g * p.G + h, split, D, dd, o, lsum, M, poison);
+    }
+    if (p.done) finish_row<D>(p, b, g, reinterpret_cast<float*>(stages), last_flag, ct, C::kWarps * 32);
+    allow_dependents();
+}
+
+}  // namespace
+
+Geometry fp8_geometry() { return Geometry{Fp8Cfg::kTile, Fp8Cfg::D, 1}; }
+
+cudaError_t launch_split_fp8(const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& p,
+                             cudaStream_t stream) {
+    using C = Fp8Cfg;
+    cudaError_t e = cudaFuncSetAttribute(split_kv_fp8_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.P, p.Hkv, p.B);
+    cfg.blockDim = dim3(C::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, split_kv_fp8_kernel, tk, tv, p);
+}
+
+}  // namespace ta

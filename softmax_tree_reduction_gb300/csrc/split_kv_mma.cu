@@ -423,7 +423,7 @@ cudaError_t launch_impl(const CUtensorMap& tk, const CUtensorMap& tv, const Spli
 
 Geometry mma_geometry(int head_dim) {
     (void)head_dim;
-    return Geometry{MmaCfg<128>::kTile, 64, 1};
+    return Geometry{MmaCfg<128>::kTile, 64, 1, 1};
 }
 
 cudaError_t launch_split_mma(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv,

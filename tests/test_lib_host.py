@@ -66,6 +66,10 @@ def shape(ta, **kw):
     (dict(max_seqlen=0), -3),
     (dict(q_dtype=2), -4),
     (dict(kv_dtype=7), -4),
+    (dict(kv_dtype=2), 0),                            # FP8 cache, BF16 q, d128, G=4
+    (dict(kv_dtype=2, q_dtype=0), -4),                # FP8 needs BF16 q
+    (dict(kv_dtype=2, head_dim=64), -4),              # FP8 path is d = 128
+    (dict(kv_dtype=2, num_q_heads=128), -4),          # FP8 path takes G <= 8
     (dict(scale=-1.0), -3),
     (dict(scale=float("nan")), -3),
     (dict(kv_stride_b=131072 * 8 * 128, kv_stride_h=128, kv_stride_t=8 * 128), 0),  # token-major
@@ -148,11 +152,11 @@ def test_decode_argument_errors_before_any_cuda_call(ta):
     assert _decode_raw(ta, s, P=4, ws=0x7008, wsb=need) == -2
     assert _decode_raw(ta, shape(ta, head_dim=32)) == -3
     f32 = shape(ta, q_dtype=0, kv_dtype=0)
-    assert _decode_raw(ta, f32, opts=ta.TaOptions(2, 0, None, None)) == -4   # mma needs bf16
+    assert _decode_raw(ta, f32, opts=ta.TaOptions(2, 0, None, None, None, None)) == -4   # mma needs bf16
     assert _decode_raw(ta, shape(ta, num_q_heads=256, num_kv_heads=8),
-                       opts=ta.TaOptions(2, 0, None, None)) == -3          # G = 32 > 16
-    assert _decode_raw(ta, s, opts=ta.TaOptions(0, 2, None, None)) == -3  # unknown flag bit
-    assert _decode_raw(ta, s, opts=ta.TaOptions(9, 0, None, None)) == -3  # unknown kernel
+                       opts=ta.TaOptions(2, 0, None, None, None, None)) == -3          # G = 32 > 16
+    assert _decode_raw(ta, s, opts=ta.TaOptions(0, 2, None, None, None, None)) == -3  # unknown flag bit
+    assert _decode_raw(ta, s, opts=ta.TaOptions(9, 0, None, None, None, None)) == -3  # unknown kernel
 
 
 def test_combine_argument_errors(ta):
@@ -210,3 +214,10 @@ def test_paged_argument_errors(ta):
     assert call(ta.TaPagedKV(**{**ok, "max_pages_per_seq": 63})) == -3   # 63*64 < 4096
     assert call(ta.TaPagedKV(**{**ok, "num_pages": 0})) == -3
     assert call(ta.TaPagedKV(**{**ok, "reserved": 1})) == -3
+
+
+def test_fp8_needs_scales_before_any_cuda_call(ta):
+    s = shape(ta, kv_dtype=2)
+    assert _decode_raw(ta, s) == -1                                            # no options
+    assert _decode_raw(ta, s, opts=ta.TaOptions(0, 0, None, None, None, None)) == -1
+    assert _decode_raw(ta, s, opts=ta.TaOptions(1, 0, None, None, 0x100, 0x200)) == -4  # FMA: no FP8
