@@ -140,6 +140,31 @@ __device__ __forceinline__ void tma_load_5d(void* smem_dst, const CUtensorMap* m
         : "memory");
 }
 
+// L2 prefetch of one box of a tiled tensor (no shared memory, no barrier);
+// boxes reaching past the tensor fetch only what lies inside it.
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* map, int x, int y, int z, int w) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z), "r"(w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_5d(const CUtensorMap* map, int x, int y, int z, int w,
+                                                int v) {
+    asm volatile("cp.async.bulk.prefetch.tensor.5d.L2.global.tile [%0, {%1, %2, %3, %4, %5}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z), "r"(w), "r"(v)
+                 : "memory");
+}
+
+// Relaxed GPU-scope load: a value another grid may still be writing (used
+// only as a hint).
+__device__ __forceinline__ int ld_relaxed(const int* ptr) {
+    int v;
+    asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));

@@ -52,6 +52,54 @@ __device__ __forceinline__ int load_box_page(const SplitParams& p, int b, int N,
     return __ldg(p.block_table + static_cast<size_t>(b) * p.max_pages + (tj >> p.page_shift));
 }
 
+// The contiguous slice [*t, *t_end) that block `split` streams first, and the
+// first token of the row's claimed pool (*base; N without balancing).
+__device__ __forceinline__ void slice_bounds(const SplitParams& p, int N, int split, int tile, int* t,
+                                             int* t_end, int* base) {
+    const int P = p.P;
+    long long slice;
+    if (p.claim != nullptr) {
+        const int C = tile * p.chunk_tiles;
+        slice = (static_cast<long long>(N) * 7 / 8) / P / C * C;
+    } else {
+        slice = (static_cast<long long>(N) + P - 1) / P;
+        slice = (slice + tile - 1) / tile * tile;
+    }
+    *t = static_cast<int>(min(static_cast<long long>(split) * slice, static_cast<long long>(N)));
+    *t_end = static_cast<int>(min(static_cast<long long>(split + 1) * slice, static_cast<long long>(N)));
+    *base = p.claim != nullptr
+                ? static_cast<int>(min(static_cast<long long>(P) * slice, static_cast<long long>(N)))
+                : N;
+}
+
+// Producer warp, before the block waits for the previous grid on the stream:
+// prefetch the first `ntiles` tiles of the block's slice into L2 through
+// `pf(t, j, page)` (box j of the tile at token t).  The previous grid may
+// still be writing the lengths, block table or caches, so what is read here
+// only picks addresses (clamped to the row and the pool); the data itself is
+// loaded after the wait, from L2, which holds any newer writes.  This fills
+// the time in which the previous grid's last blocks merge and DRAM is idle.
+template <typename Prefetch>
+__device__ void prefetch_row_head(const SplitParams& p, int b, int split, int tile, int ntiles,
+                                  Prefetch&& pf) {
+    const int lane = threadIdx.x & 31;
+    const int N = max(0, min(ld_relaxed(p.seqlens + b), p.S));
+    int t, t_end, base;
+    slice_bounds(p, N, split, tile, &t, &t_end, &base);
+    const int nbox = p.block_table ? tile / p.box_rows : 1;
+    if (lane >= nbox) return;
+    for (int i = 0; i < ntiles && t < t_end; ++i, t += tile) {
+        int page = 0;
+        if (p.block_table) {
+            const int tj = t + lane * p.box_rows;
+            if (tj >= N) break;
+            page = ld_relaxed(p.block_table + static_cast<size_t>(b) * p.max_pages + (tj >> p.page_shift));
+            if (page < 0 || page >= p.num_pages) break;
+        }
+        pf(t, lane, page);
+    }
+}
+
 // Producer warp (all 32 lanes): stream this block's tiles into the stage ring.
 // Lane 0 keeps the schedule (slices, claims, barriers, stage descriptors);
 // lane j issues the TMA copies of box j of each tile via `issue(s, t, j, page)`
@@ -66,22 +114,11 @@ __device__ bool produce_row(const SplitParams& p, int b, int row, int N, int spl
                             volatile unsigned* sink, volatile int* bad_flag, unsigned stage_bytes,
                             Issue&& issue) {
     const int lane = threadIdx.x & 31;
-    const int P = p.P;
     const int C = tile * p.chunk_tiles;  // tokens per claimed chunk
     const bool dynamic = p.claim != nullptr;
     const int nbox = p.block_table ? tile / p.box_rows : 1;
-    long long slice;
-    if (dynamic) {
-        slice = (static_cast<long long>(N) * 7 / 8) / P / C * C;
-    } else {
-        slice = (static_cast<long long>(N) + P - 1) / P;
-        slice = (slice + tile - 1) / tile * tile;
-    }
-    int t = static_cast<int>(min(static_cast<long long>(split) * slice, static_cast<long long>(N)));
-    int t_end = static_cast<int>(min(static_cast<long long>(split + 1) * slice, static_cast<long long>(N)));
-    const int base = dynamic ? static_cast<int>(min(static_cast<long long>(P) * slice,
-                                                    static_cast<long long>(N)))
-                             : N;
+    int t, t_end, base;
+    slice_bounds(p, N, split, tile, &t, &t_end, &base);
     const int npool = dynamic ? (N - base + C - 1) / C : 0;  // chunks handed out by the counter
     bool exhausted = (npool == 0);
     unsigned pend0 = 0, pend1 = 0;  // claims in flight (lane 0's registers), oldest first

@@ -130,8 +130,21 @@ __global__ void __launch_bounds__(Fp8Cfg::kThreads, 1)
         prefetch_tensormap(&tmK);
         prefetch_tensormap(&tmV);
     }
+    if (warp == 0) {  // first tiles into L2 while the previous grid drains
+        const int page_mask = (1 << p.page_shift) - 1;
+        prefetch_row_head(p, b, split, C::kTile, C::kStages, [&](int y, int j, int page) {
+            if (!p.block_table) {
+                tma_prefetch_4d(&tmK, 0, y, g, b);
+                tma_prefetch_4d(&tmV, 0, y, g, b);
+                return;
+            }
+            const int ty = (y + j * p.box_rows) & page_mask;
+            tma_prefetch_4d(&tmK, 0, ty, g, page);
+            tma_prefetch_4d(&tmV, 0, ty, g, page);
+        });
+    }
     __syncthreads();
-    wait_primary();  // nothing an earlier kernel may write is touched before this
+    wait_primary();  // apart from the prefetch's address hints, nothing an earlier kernel writes is read before this
 
     int N = p.seqlens[b];
     const bool bad = (N < 0) || (N > p.S);

@@ -126,9 +126,23 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
         prefetch_tensormap(&tmK);
         prefetch_tensormap(&tmV);
     }
+    if (warp == 0) {
+        const int page_mask = (1 << p.page_shift) - 1;
+        prefetch_row_head(p, b, split, C::kTile, C::kStages, [&](int y, int j, int page) {
+            if (!p.block_table) {
+                tma_prefetch_5d(&tmK, 0, y, 0, g, b);
+                tma_prefetch_5d(&tmV, 0, y, 0, g, b);
+                return;
+            }
+            const int ty = (y + j * p.box_rows) & page_mask;
+            tma_prefetch_5d(&tmK, 0, ty, 0, g, page);
+            tma_prefetch_5d(&tmV, 0, ty, 0, g, page);
+        });
+    }
     __syncthreads();
-    // Launched as a programmatic dependent: nothing an earlier kernel may
-    // write (q, the caches, the lengths, the outputs) is touched before this.
+    // Launched as a programmatic dependent: apart from the address hints of
+    // the prefetch, nothing an earlier kernel may write (q, the caches, the
+    // lengths, the outputs) is read before this.
     wait_primary();
 
     int N = p.seqlens[b];
