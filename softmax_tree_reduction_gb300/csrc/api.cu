@@ -29,6 +29,9 @@ __device__ unsigned g_sched_ring[kRingSlots];
 
 // Tokens per run-time scheduled chunk of a row (rounded to whole tiles).
 constexpr int kChunkTokens = 128;
+// Tokens of its slice each block prefetches into L2 before waiting on the
+// previous grid (fills the DRAM time of that grid's merge tail).
+constexpr int kPrefetchTokens = 1152;
 // The row's last block merges the partial states itself when there are few
 // of them (its merge costs about one L2 round trip per 20 states, serially);
 // more splits go to the combine kernel, which spreads the merge over (h, b)
@@ -397,6 +400,7 @@ int decode_impl(const ta_shape* shape, const ta_paged_kv* paged, int nq, int cau
 
     const Geometry geo = geometry_of(shape, kernel);
     const int rows = paged ? std::min(geo.tile_tokens, paged->page_size) : geo.tile_tokens;
+    if (geo.tile_tokens / rows > 32) return TA_ERR_SHAPE;  // one producer lane per box
     CUtensorMap tk, tv;
     rc = encode_kv_map(&tk, k_cache, shape, st, geo, paged, rows);
     if (rc != TA_OK) return rc;
@@ -425,6 +429,7 @@ int decode_impl(const ta_shape* shape, const ta_paged_kv* paged, int nq, int cau
                                            : 1.0f / std::sqrt(static_cast<float>(shape->head_dim));
     p.scale_log2 = scale * ta::kLog2e;
     p.chunk_tiles = std::max(1, kChunkTokens / geo.tile_tokens);
+    p.prefetch_tiles = std::max(1, kPrefetchTokens / geo.tile_tokens);
     p.box_rows = rows;
     p.num_pages = shape->batch;
     if (paged) {

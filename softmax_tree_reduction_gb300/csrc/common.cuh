@@ -46,6 +46,7 @@ struct SplitParams {
     int nq;                 // queries per row (q rows are [head][query])
     int causal;             // query i of nq sees tokens < N - nq + 1 + i
     int chunk_tiles;        // tiles per scheduled chunk
+    int prefetch_tiles;     // tiles of its slice a block prefetches into L2 before its wait
     float scale_log2;       // logit scale * log2(e)
 };
 

@@ -35,9 +35,6 @@ struct StageMeta {
     int nvalid;  // valid tokens in the tile (1..tile); < 0: no more tiles
 };
 
-// Most TMA boxes one tile can need: a 128-token tile over 16-token pages.
-constexpr int kMaxBoxes = 8;
-
 // Box needs no page (past the row's end, or no tile).
 constexpr int kNoPage = -2147483647 - 1;
 

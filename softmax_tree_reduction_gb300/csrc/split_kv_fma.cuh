@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(FmaCfg<KV, D>::kThreads, 1)
     }
     if (warp == 0) {  // first tiles into L2 while the previous grid drains
         const int page_mask = (1 << p.page_shift) - 1;
-        prefetch_row_head(p, b, split, C::kTile, C::kStages, [&](int y, int j, int page) {
+        prefetch_row_head(p, b, split, C::kTile, p.prefetch_tiles, [&](int y, int j, int page) {
             if (!p.block_table) {
                 tma_prefetch_4d(&tmK, 0, y, g, b);
                 tma_prefetch_4d(&tmV, 0, y, g, b);

@@ -35,10 +35,11 @@ namespace {
 struct Fp8Cfg {
     static constexpr int D = 128;
     static constexpr int kWarps = 8;                 // consumer warps
-    static constexpr int kTile = 16 * kWarps;        // tokens per stage
+    static constexpr int kSub = 2;                   // 16-token slabs per warp per stage
+    static constexpr int kTile = 16 * kWarps * kSub; // tokens per stage
     static constexpr int kKBytes = kTile * D;        // one byte per element
     static constexpr int kStageBytes = 2 * kKBytes;  // K and V
-    static constexpr int kStages = 6;
+    static constexpr int kStages = 6 / kSub;
     static constexpr int kBarBytes = 2 * kStages * 8 + kStages * 8 + 32;
     static constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes;
     static constexpr int kThreads = 32 * (kWarps + 1);
@@ -132,7 +133,7 @@ __global__ void __launch_bounds__(Fp8Cfg::kThreads, 1)
     }
     if (warp == 0) {  // first tiles into L2 while the previous grid drains
         const int page_mask = (1 << p.page_shift) - 1;
-        prefetch_row_head(p, b, split, C::kTile, C::kStages, [&](int y, int j, int page) {
+        prefetch_row_head(p, b, split, C::kTile, p.prefetch_tiles, [&](int y, int j, int page) {
             if (!p.block_table) {
                 tma_prefetch_4d(&tmK, 0, y, g, b);
                 tma_prefetch_4d(&tmV, 0, y, g, b);
@@ -223,13 +224,14 @@ __global__ void __launch_bounds__(Fp8Cfg::kThreads, 1)
     for (int mt = 0; mt < D / 16; ++mt) oacc[mt][0] = oacc[mt][1] = oacc[mt][2] = oacc[mt][3] = 0.f;
 
     // Rows are 128 B (one swizzle row); chunk c of row r sits at chunk c ^ (r & 7).
-    const int r0 = cw * 16;
-    const int ra = r0 + gid, rb = ra + 8;                       // K rows of this thread
+    // Offsets within a 16-row slab (slabs start at multiples of 16 rows, so
+    // the swizzle phase of a row is the same in every slab).
+    const int ra = gid, rb = gid + 8;                           // K rows of this thread
     const uint32_t k_a0 = ra * 128 + (((2 * tig) ^ (ra & 7)) << 4);
     const uint32_t k_a1 = ra * 128 + (((2 * tig + 1) ^ (ra & 7)) << 4);
     const uint32_t k_b0 = rb * 128 + (((2 * tig) ^ (rb & 7)) << 4);
     const uint32_t k_b1 = rb * 128 + (((2 * tig + 1) ^ (rb & 7)) << 4);
-    const int tv0 = r0 + 2 * tig;                               // V rows of this thread
+    const int tv0 = 2 * tig;                                    // V rows of this thread
     const uint32_t v_0 = tv0 * 128 + ((gid ^ (tv0 & 7)) << 4);
     const uint32_t v_1 = (tv0 + 1) * 128 + ((gid ^ ((tv0 + 1) & 7)) << 4);
     const uint32_t v_2 = (tv0 + 8) * 128 + ((gid ^ ((tv0 + 8) & 7)) << 4);
@@ -244,107 +246,112 @@ __global__ void __launch_bounds__(Fp8Cfg::kThreads, 1)
         }
         const int tile_valid = meta[s].nvalid;
         if (tile_valid < 0) break;
-        const int blk0 = meta[s].tok0 + r0;
-        const uint32_t kbase = smem_u32(stages + s * C::kStageBytes);
-        const uint32_t vbase = kbase + C::kKBytes;
-        const int nvalid = tile_valid - r0;
+        const int tile_tok0 = meta[s].tok0;
+#pragma unroll 1
+        for (int sub = 0; sub < C::kSub; ++sub) {
+            const int r0 = (sub * C::kWarps + cw) * 16;  // first row of this warp's slab
+            const int blk0 = tile_tok0 + r0;
+            const uint32_t kbase = smem_u32(stages + s * C::kStageBytes) + r0 * 128;
+            const uint32_t vbase = kbase + C::kKBytes;
+            const int nvalid = tile_valid - r0;
 
-        if (nvalid > 0) {
-            const uint4 ka0 = lds128(kbase + k_a0), ka1 = lds128(kbase + k_a1);
-            const uint4 kb0 = lds128(kbase + k_b0), kb1 = lds128(kbase + k_b1);
-            const uint32_t wa[8] = {ka0.x, ka0.y, ka0.z, ka0.w, ka1.x, ka1.y, ka1.z, ka1.w};
-            const uint32_t wb[8] = {kb0.x, kb0.y, kb0.z, kb0.w, kb1.x, kb1.y, kb1.z, kb1.w};
-            float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+            if (nvalid > 0) {
+                const uint4 ka0 = lds128(kbase + k_a0), ka1 = lds128(kbase + k_a1);
+                const uint4 kb0 = lds128(kbase + k_b0), kb1 = lds128(kbase + k_b1);
+                const uint32_t wa[8] = {ka0.x, ka0.y, ka0.z, ka0.w, ka1.x, ka1.y, ka1.z, ka1.w};
+                const uint32_t wb[8] = {kb0.x, kb0.y, kb0.z, kb0.w, kb1.x, kb1.y, kb1.z, kb1.w};
+                float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                uint32_t a[4];
-                a[0] = e4m3x2_to_f16x2(wa[kk] & 0xffffu);
-                a[1] = e4m3x2_to_f16x2(wb[kk] & 0xffffu);
-                a[2] = e4m3x2_to_f16x2(wa[kk] >> 16);
-                a[3] = e4m3x2_to_f16x2(wb[kk] >> 16);
-                if (kk & 1)
-                    mma_f16(sb, a, qb[kk][0], qb[kk][1]);
-                else
-                    mma_f16(sa, a, qb[kk][0], qb[kk][1]);
-            }
-            float s0 = (sa[0] + sb[0]) * sl2, s1 = (sa[1] + sb[1]) * sl2;
-            float s2 = (sa[2] + sb[2]) * sl2, s3 = (sa[3] + sb[3]) * sl2;
-            if (nvalid < 16) {
-                if (gid >= nvalid) s0 = s1 = -INFINITY;
-                if (gid + 8 >= nvalid) s2 = s3 = -INFINITY;
-            }
-            if (blk0 + 16 > causal_from) {
-                const int ta = blk0 + gid, tb = ta + 8;
-                if (ta >= lim0) s0 = -INFINITY;
-                if (ta >= lim1) s1 = -INFINITY;
-                if (tb >= lim0) s2 = -INFINITY;
-                if (tb >= lim1) s3 = -INFINITY;
-            }
-            float bm0 = fmaxf(s0, s2), bm1 = fmaxf(s1, s3);
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    uint32_t a[4];
+                    a[0] = e4m3x2_to_f16x2(wa[kk] & 0xffffu);
+                    a[1] = e4m3x2_to_f16x2(wb[kk] & 0xffffu);
+                    a[2] = e4m3x2_to_f16x2(wa[kk] >> 16);
+                    a[3] = e4m3x2_to_f16x2(wb[kk] >> 16);
+                    if (kk & 1)
+                        mma_f16(sb, a, qb[kk][0], qb[kk][1]);
+                    else
+                        mma_f16(sa, a, qb[kk][0], qb[kk][1]);
+                }
+                float s0 = (sa[0] + sb[0]) * sl2, s1 = (sa[1] + sb[1]) * sl2;
+                float s2 = (sa[2] + sb[2]) * sl2, s3 = (sa[3] + sb[3]) * sl2;
+                if (nvalid < 16) {
+                    if (gid >= nvalid) s0 = s1 = -INFINITY;
+                    if (gid + 8 >= nvalid) s2 = s3 = -INFINITY;
+                }
+                if (blk0 + 16 > causal_from) {
+                    const int ta = blk0 + gid, tb = ta + 8;
+                    if (ta >= lim0) s0 = -INFINITY;
+                    if (ta >= lim1) s1 = -INFINITY;
+                    if (tb >= lim0) s2 = -INFINITY;
+                    if (tb >= lim1) s3 = -INFINITY;
+                }
+                float bm0 = fmaxf(s0, s2), bm1 = fmaxf(s1, s3);
 #pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
-                bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
-            }
-            const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
-            const float ms0 = (mn0 == -INFINITY) ? 0.f : mn0;
-            const float ms1 = (mn1 == -INFINITY) ? 0.f : mn1;
-            const float al0 = ex2(m0 - ms0), al1 = ex2(m1 - ms1);
-            const float p0 = ex2(s0 - ms0), p1 = ex2(s1 - ms1);
-            const float p2 = ex2(s2 - ms0), p3 = ex2(s3 - ms1);
-            l0 = l0 * al0 + (p0 + p2);
-            l1 = l1 * al1 + (p1 + p3);
-            m0 = mn0;
-            m1 = mn1;
-            if (__any_sync(0xffffffffu, (al0 != 1.f) || (al1 != 1.f))) {
+                for (int off = 4; off < 32; off <<= 1) {
+                    bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
+                    bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
+                }
+                const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+                const float ms0 = (mn0 == -INFINITY) ? 0.f : mn0;
+                const float ms1 = (mn1 == -INFINITY) ? 0.f : mn1;
+                const float al0 = ex2(m0 - ms0), al1 = ex2(m1 - ms1);
+                const float p0 = ex2(s0 - ms0), p1 = ex2(s1 - ms1);
+                const float p2 = ex2(s2 - ms0), p3 = ex2(s3 - ms1);
+                l0 = l0 * al0 + (p0 + p2);
+                l1 = l1 * al1 + (p1 + p3);
+                m0 = mn0;
+                m1 = mn1;
+                if (__any_sync(0xffffffffu, (al0 != 1.f) || (al1 != 1.f))) {
 #pragma unroll
-                for (int mt = 0; mt < D / 16; ++mt) {
-                    oacc[mt][0] *= al0;
-                    oacc[mt][1] *= al1;
-                    oacc[mt][2] *= al0;
-                    oacc[mt][3] *= al1;
+                    for (int mt = 0; mt < D / 16; ++mt) {
+                        oacc[mt][0] *= al0;
+                        oacc[mt][1] *= al1;
+                        oacc[mt][2] *= al0;
+                        oacc[mt][3] *= al1;
+                    }
+                }
+                // P^T (scaled by 2^14) as FP16 hi + lo B fragments
+                const float q0 = p0 * kPScale, q1 = p1 * kPScale, q2 = p2 * kPScale, q3 = p3 * kPScale;
+                const __half2 h01 = __floats2half2_rn(q0, q1), h23 = __floats2half2_rn(q2, q3);
+                const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+                const __half2 e01 = __floats2half2_rn(q0 - f01.x, q1 - f01.y);
+                const __half2 e23 = __floats2half2_rn(q2 - f23.x, q3 - f23.y);
+                const uint32_t bh0 = movtrans(half2_bits(h01)), bh1 = movtrans(half2_bits(h23));
+                const uint32_t bl0 = movtrans(half2_bits(e01)), bl1 = movtrans(half2_bits(e23));
+                // V: tokens 2tig, 2tig+1, 2tig+8, 2tig+9 of the block, channels 16 gid .. 16 gid + 15;
+                // rows past the valid range may hold anything (even NaN codes): zero them
+                uint4 va = lds128(vbase + v_0), vb = lds128(vbase + v_1);
+                uint4 vc = lds128(vbase + v_2), vd = lds128(vbase + v_3);
+                if (nvalid < 16) {
+                    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                    if (2 * tig >= nvalid) va = z;
+                    if (2 * tig + 1 >= nvalid) vb = z;
+                    if (2 * tig + 8 >= nvalid) vc = z;
+                    if (2 * tig + 9 >= nvalid) vd = z;
+                }
+                const uint32_t xa[4] = {va.x, va.y, va.z, va.w}, xb[4] = {vb.x, vb.y, vb.z, vb.w};
+                const uint32_t xc[4] = {vc.x, vc.y, vc.z, vc.w}, xd[4] = {vd.x, vd.y, vd.z, vd.w};
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const uint32_t p01 = prmt(xa[w], xb[w], 0x5140u), p23 = prmt(xa[w], xb[w], 0x7362u);
+                    const uint32_t r01 = prmt(xc[w], xd[w], 0x5140u), r23 = prmt(xc[w], xd[w], 0x7362u);
+                    uint32_t a[4];
+                    a[0] = e4m3x2_to_f16x2(p01 & 0xffffu);
+                    a[1] = e4m3x2_to_f16x2(p01 >> 16);
+                    a[2] = e4m3x2_to_f16x2(r01 & 0xffffu);
+                    a[3] = e4m3x2_to_f16x2(r01 >> 16);
+                    mma_f16(oacc[2 * w], a, bh0, bh1);
+                    mma_f16(oacc[2 * w], a, bl0, bl1);
+                    a[0] = e4m3x2_to_f16x2(p23 & 0xffffu);
+                    a[1] = e4m3x2_to_f16x2(p23 >> 16);
+                    a[2] = e4m3x2_to_f16x2(r23 & 0xffffu);
+                    a[3] = e4m3x2_to_f16x2(r23 >> 16);
+                    mma_f16(oacc[2 * w + 1], a, bh0, bh1);
+                    mma_f16(oacc[2 * w + 1], a, bl0, bl1);
                 }
             }
-            // P^T (scaled by 2^14) as FP16 hi + lo B fragments
-            const float q0 = p0 * kPScale, q1 = p1 * kPScale, q2 = p2 * kPScale, q3 = p3 * kPScale;
-            const __half2 h01 = __floats2half2_rn(q0, q1), h23 = __floats2half2_rn(q2, q3);
-            const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-            const __half2 e01 = __floats2half2_rn(q0 - f01.x, q1 - f01.y);
-            const __half2 e23 = __floats2half2_rn(q2 - f23.x, q3 - f23.y);
-            const uint32_t bh0 = movtrans(half2_bits(h01)), bh1 = movtrans(half2_bits(h23));
-            const uint32_t bl0 = movtrans(half2_bits(e01)), bl1 = movtrans(half2_bits(e23));
-            // V: tokens 2tig, 2tig+1, 2tig+8, 2tig+9 of the block, channels 16 gid .. 16 gid + 15;
-            // rows past the valid range may hold anything (even NaN codes): zero them
-            uint4 va = lds128(vbase + v_0), vb = lds128(vbase + v_1);
-            uint4 vc = lds128(vbase + v_2), vd = lds128(vbase + v_3);
-            if (nvalid < 16) {
-                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-                if (2 * tig >= nvalid) va = z;
-                if (2 * tig + 1 >= nvalid) vb = z;
-                if (2 * tig + 8 >= nvalid) vc = z;
-                if (2 * tig + 9 >= nvalid) vd = z;
-            }
-            const uint32_t xa[4] = {va.x, va.y, va.z, va.w}, xb[4] = {vb.x, vb.y, vb.z, vb.w};
-            const uint32_t xc[4] = {vc.x, vc.y, vc.z, vc.w}, xd[4] = {vd.x, vd.y, vd.z, vd.w};
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                const uint32_t p01 = prmt(xa[w], xb[w], 0x5140u), p23 = prmt(xa[w], xb[w], 0x7362u);
-                const uint32_t r01 = prmt(xc[w], xd[w], 0x5140u), r23 = prmt(xc[w], xd[w], 0x7362u);
-                uint32_t a[4];
-                a[0] = e4m3x2_to_f16x2(p01 & 0xffffu);
-                a[1] = e4m3x2_to_f16x2(p01 >> 16);
-                a[2] = e4m3x2_to_f16x2(r01 & 0xffffu);
-                a[3] = e4m3x2_to_f16x2(r01 >> 16);
-                mma_f16(oacc[2 * w], a, bh0, bh1);
-                mma_f16(oacc[2 * w], a, bl0, bl1);
-                a[0] = e4m3x2_to_f16x2(p23 & 0xffffu);
-                a[1] = e4m3x2_to_f16x2(p23 >> 16);
-                a[2] = e4m3x2_to_f16x2(r23 & 0xffffu);
-                a[3] = e4m3x2_to_f16x2(r23 >> 16);
-                mma_f16(oacc[2 * w + 1], a, bh0, bh1);
-                mma_f16(oacc[2 * w + 1], a, bl0, bl1);
-            }
-        }
+        }  // slabs
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
     }

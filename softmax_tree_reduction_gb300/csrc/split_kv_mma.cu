@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
     }
     if (warp == 0) {
         const int page_mask = (1 << p.page_shift) - 1;
-        prefetch_row_head(p, b, split, C::kTile, C::kStages, [&](int y, int j, int page) {
+        prefetch_row_head(p, b, split, C::kTile, p.prefetch_tiles, [&](int y, int j, int page) {
             if (!p.block_table) {
                 tma_prefetch_5d(&tmK, 0, y, 0, g, b);
                 tma_prefetch_5d(&tmV, 0, y, 0, g, b);
