@@ -493,7 +493,7 @@ def _time_steps(ta, torch, copies, P, kernel, steps, warmup, out, lse, ws, deter
         c = copies[i % len(copies)]
         ta.tree_attn_decode(c["q"], c["k"], c["v"], c["seqlens"], out=out, lse=lse, num_splits=P,
                             workspace=ws, kernel=kernel, split_events=events,
-                            deterministic=deterministic)
+                            deterministic=deterministic, k_scale=c.get("k_scale"), v_scale=c.get("v_scale"))
     for i in range(warmup):
         step(i)
     torch.cuda.synchronize()
@@ -542,6 +542,9 @@ def run_sweeps(args):
     torch.cuda.set_device(0)
     ta.load()
     w = workloads.WORKLOADS[args.workload]
+    if args.fp8:
+        import dataclasses
+        w = dataclasses.replace(w, kv_dtype=torch.float8_e4m3fn)
     gen = torch.Generator(device="cuda")
     gen.manual_seed(w.seed)
 
@@ -552,10 +555,16 @@ def run_sweeps(args):
         per_copy = 2 * B * Hkv * N * d * torch.empty((), dtype=w.kv_dtype).element_size()
         n_copies = 2 if per_copy <= (8 << 30) else 1
         for _ in range(n_copies):
-            k = (torch.randn(B, Hkv, N, d, generator=gen, device="cuda") * w.k_scale).to(w.kv_dtype)
-            v = torch.randn(B, Hkv, N, d, generator=gen, device="cuda").to(w.kv_dtype)
-            copies.append({"q": q, "k": k, "v": v,
-                           "seqlens": torch.full((B,), N, dtype=torch.int32, device="cuda")})
+            c = {"q": q, "seqlens": torch.full((B,), N, dtype=torch.int32, device="cuda")}
+            if args.fp8:  # rounded to E4M3 with one scale per KV head
+                c["k"], c["k_scale"] = workloads.quantize_e4m3(
+                    (torch.randn(B, Hkv, N, d, generator=gen, device="cuda") * w.k_scale).to(torch.bfloat16))
+                c["v"], c["v_scale"] = workloads.quantize_e4m3(
+                    torch.randn(B, Hkv, N, d, generator=gen, device="cuda").to(torch.bfloat16))
+            else:
+                c["k"] = (torch.randn(B, Hkv, N, d, generator=gen, device="cuda") * w.k_scale).to(w.kv_dtype)
+                c["v"] = torch.randn(B, Hkv, N, d, generator=gen, device="cuda").to(w.kv_dtype)
+            copies.append(c)
         return copies
 
     peak, _ = load_peaks()
@@ -568,13 +577,14 @@ def run_sweeps(args):
         out = torch.empty(B, Hq, d, device="cuda")
         lse = torch.empty(B, Hq, device="cuda")
         heur = ta.tree_attn_pick_splits(shape)
-        for kern in args.sweep_kernels.split(","):
+        for kern in (["auto"] if args.fp8 else args.sweep_kernels.split(",")):
             for P in [int(x) for x in args.sweep_splits.split(",")]:
                 ws = torch.empty(max(16, ta.tree_attn_workspace_bytes(shape, P)), dtype=torch.uint8,
                                  device="cuda")
                 ms, split = _time_steps(ta, torch, copies, P, kern, args.steps, args.warmup, out, lse, ws,
                                         args.deterministic, args.graph)
-                lines.append({"sweep": "splits", "workload": w.name, "kernel": kern, "num_splits": P,
+                lines.append({"sweep": "splits", "workload": w.name, "kernel": "fp8" if args.fp8 else kern,
+                              "num_splits": P,
                               "deterministic": args.deterministic, "graph": args.graph,
                               "heuristic": P == heur, "us_per_step": round(ms * 1e3, 3),
                               "split_kernel_us": round(split * 1e3, 3),
@@ -597,7 +607,8 @@ def run_sweeps(args):
                              device="cuda")
             ms, split = _time_steps(ta, torch, copies, P, args.kernel, args.steps, args.warmup, out, lse, ws,
                                     args.deterministic, args.graph)
-            lines.append({"sweep": "context", "workload": w.name, "context": N, "num_splits": P,
+            lines.append({"sweep": "context", "workload": w.name, "kv": "e4m3" if args.fp8 else "bf16",
+                          "context": N, "num_splits": P,
                           "graph": args.graph, "l2": "fits" if w.kv_bytes(np.full(w.batch, N)) * len(copies)
                           < L2_BYTES else "exceeds",
                           "us_per_step": round(ms * 1e3, 3), "split_kernel_us": round(split * 1e3, 3),
