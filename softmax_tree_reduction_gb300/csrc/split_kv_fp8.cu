@@ -43,7 +43,12 @@ struct Fp8Cfg {
     static constexpr int kBarBytes = 2 * kStages * 8 + kStages * 8 + 32;
     static constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes;
     static constexpr int kThreads = 32 * (kWarps + 1);
-    static_assert(kWarps * 8 * (D + 2) * 4 <= kStages * kStageBytes, "merge buffer");
+    // Merge buffer: a warp state's row holds channel c at position
+    // (c % 16) * 8 + c / 16, with 4 floats of padding per row, so the
+    // fragment stores (rows 2 tig, 2 tig + 1; channels 16 gid + 2 mt (+1))
+    // hit 32 distinct banks and the merge reads consecutive positions.
+    static constexpr int kMergeStride = D + 4;
+    static_assert(kWarps * 8 * (kMergeStride + 2) * 4 <= kStages * kStageBytes, "merge buffer");
 };
 
 constexpr float kPScale = 16384.f;  // 2^14
@@ -104,8 +109,8 @@ __global__ void __launch_bounds__(Fp8Cfg::kThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* stages = smem;
-    float* mg_o = reinterpret_cast<float*>(stages);  // [W][8][D], after streaming
-    float* mg_m = mg_o + C::kWarps * 8 * D;
+    float* mg_o = reinterpret_cast<float*>(stages);  // [W][8][D (+pad)], after streaming
+    float* mg_m = mg_o + C::kWarps * 8 * C::kMergeStride;
     float* mg_l = mg_m + C::kWarps * 8;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
     uint64_t* empty = full + C::kStages;
@@ -364,14 +369,17 @@ __global__ void __launch_bounds__(Fp8Cfg::kThreads, 1)
         l1 += __shfl_xor_sync(0xffffffffu, l1, off);
     }
     consumer_sync(C::kWarps * 32);  // every warp is done reading the stages
-    float* mo = mg_o + cw * 8 * D;
+    constexpr int MS = C::kMergeStride;
+    float* mo = mg_o + cw * 8 * MS;
 #pragma unroll
     for (int mt = 0; mt < D / 16; ++mt) {
-        const int ch = 16 * gid + 2 * mt;  // output channel of fragment rows gid / gid + 8
-        mo[(2 * tig) * D + ch] = oacc[mt][0];
-        mo[(2 * tig + 1) * D + ch] = oacc[mt][1];
-        mo[(2 * tig) * D + ch + 1] = oacc[mt][2];
-        mo[(2 * tig + 1) * D + ch + 1] = oacc[mt][3];
+        // fragment rows gid / gid + 8 are channels 16 gid + 2 mt (+1), stored at
+        // positions (2 mt) * 8 + gid and (2 mt + 1) * 8 + gid
+        const int pos = 16 * mt + gid;
+        mo[(2 * tig) * MS + pos] = oacc[mt][0];
+        mo[(2 * tig + 1) * MS + pos] = oacc[mt][1];
+        mo[(2 * tig) * MS + pos + 8] = oacc[mt][2];
+        mo[(2 * tig + 1) * MS + pos + 8] = oacc[mt][3];
     }
     if (gid == 0) {
         mg_m[cw * 8 + 2 * tig] = m0;
@@ -384,7 +392,8 @@ __global__ void __launch_bounds__(Fp8Cfg::kThreads, 1)
     const float oscale = vs / kPScale;
     const int ct = threadIdx.x - 32;
     for (int idx = ct; idx < p.G * D; idx += C::kWarps * 32) {
-        const int h = idx / D, dd = idx - h * D;
+        const int h = idx / D, pos = idx - h * D;
+        const int dd = (pos & 7) * 16 + (pos >> 3);  // channel stored at `pos`
         float mw[C::kWarps];
         float M = -INFINITY;
 #pragma unroll
@@ -397,7 +406,7 @@ __global__ void __launch_bounds__(Fp8Cfg::kThreads, 1)
 #pragma unroll
         for (int w = 0; w < C::kWarps; ++w) {
             const float wt = ex2(mw[w] - Ms);
-            ow[w] = wt * mg_o[(w * 8 + h) * D + dd];
+            ow[w] = wt * mg_o[(w * 8 + h) * MS + pos];
             lw[w] = wt * mg_l[w * 8 + h];
         }
         const float o = tree_sum<C::kWarps>(ow) * oscale;

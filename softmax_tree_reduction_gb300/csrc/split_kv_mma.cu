@@ -44,7 +44,11 @@ struct MmaCfg {
     // the warps' states are merged in the stage buffers once streaming is over
     static constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes;
     static constexpr int kThreads = 32 * (kWarps + 1);
-    static_assert(kWarps * 16 * (D + 2) * 4 <= kStages * kStageBytes, "merge buffer (two n-tiles)");
+    // Row stride of a warp state in the merge buffer: 4 floats of padding make
+    // the fragment stores (rows 2 tig, 2 tig + 1; channels 16 mt + gid) hit 32
+    // distinct banks.
+    static constexpr int kMergeStride = D + 4;
+    static_assert(kWarps * 16 * (kMergeStride + 2) * 4 <= kStages * kStageBytes, "merge buffer (two n-tiles)");
     static_assert(kTile <= 256, "TMA box height");
 };
 
@@ -99,8 +103,8 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* stages = smem;
-    float* mg_o = reinterpret_cast<float*>(stages);  // [W][8*NT][D], after streaming
-    float* mg_m = mg_o + C::kWarps * 8 * NT * D;     // [W][8*NT]
+    float* mg_o = reinterpret_cast<float*>(stages);  // [W][8*NT][D (+pad)], after streaming
+    float* mg_m = mg_o + C::kWarps * 8 * NT * C::kMergeStride;  // [W][8*NT]
     float* mg_l = mg_m + C::kWarps * 8 * NT;         // [W][8*NT]
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
     uint64_t* empty = full + C::kStages;
@@ -366,16 +370,17 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
             l[nt][1] += __shfl_xor_sync(0xffffffffu, l[nt][1], off);
         }
     consumer_sync(C::kWarps * 32);  // every warp is done reading the stages
-    float* mo = mg_o + cw * kCols * D;
+    constexpr int MS = C::kMergeStride;
+    float* mo = mg_o + cw * kCols * MS;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         const int c0 = nt * 8 + 2 * tig;
 #pragma unroll
         for (int mt = 0; mt < D / 16; ++mt) {
-            mo[c0 * D + 16 * mt + gid] = oacc[nt][mt][0];
-            mo[(c0 + 1) * D + 16 * mt + gid] = oacc[nt][mt][1];
-            mo[c0 * D + 16 * mt + gid + 8] = oacc[nt][mt][2];
-            mo[(c0 + 1) * D + 16 * mt + gid + 8] = oacc[nt][mt][3];
+            mo[c0 * MS + 16 * mt + gid] = oacc[nt][mt][0];
+            mo[(c0 + 1) * MS + 16 * mt + gid] = oacc[nt][mt][1];
+            mo[c0 * MS + 16 * mt + gid + 8] = oacc[nt][mt][2];
+            mo[(c0 + 1) * MS + 16 * mt + gid + 8] = oacc[nt][mt][3];
         }
         if (gid == 0) {
             mg_m[cw * kCols + c0] = m[nt][0];
@@ -401,7 +406,7 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
 #pragma unroll
         for (int w = 0; w < C::kWarps; ++w) {
             const float wt = ex2(mw[w] - Ms);
-            ow[w] = wt * mg_o[(w * kCols + h) * D + dd];
+            ow[w] = wt * mg_o[(w * kCols + h) * MS + dd];
             lw[w] = wt * mg_l[w * kCols + h];
         }
         // pairwise tree over the warps
