@@ -314,7 +314,7 @@ def run_ours(args, rank, world, local):
     if args.queries > 1:  # each (head, query) pair counts as a query head
         shape = ta.TaShape.from_buffer_copy(shape)
         shape.num_q_heads *= args.queries
-    P = args.num_splits if args.num_splits > 0 else ta.tree_attn_pick_splits(shape)
+    P = args.num_splits if args.num_splits > 0 else ta.tree_attn_pick_splits(shape, page_size=args.paged)
     kernel_used = args.kernel
     if args.fp8:
         kernel_used = "fp8"

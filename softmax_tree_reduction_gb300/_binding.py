@@ -29,7 +29,7 @@ _EXPORTS = ["tree_attn_status_string", "tree_attn_version", "tree_attn_check_sha
             "tree_attn_workspace_bytes", "tree_attn_pick_splits", "tree_attn_decode",
             "tree_attn_decode_ex", "tree_attn_combine", "tree_attn_get_device_error",
             "tree_attn_decode_noalloc", "tree_attn_launch_count", "tree_attn_decode_paged",
-            "tree_attn_decode_multi"]
+            "tree_attn_decode_multi", "tree_attn_pick_splits_paged"]
 
 
 class TaShape(ctypes.Structure):
@@ -84,6 +84,8 @@ def load(path: str = LIB_PATH):
         lib.tree_attn_workspace_bytes.restype = SZ
         lib.tree_attn_pick_splits.argtypes = [SP, P, I32]
         lib.tree_attn_pick_splits.restype = I32
+        lib.tree_attn_pick_splits_paged.argtypes = [SP, I32, P, I32]
+        lib.tree_attn_pick_splits_paged.restype = I32
         lib.tree_attn_decode.argtypes = [SP, P, P, P, P, P, P, I32, P, SZ, P]
         lib.tree_attn_decode.restype = I32
         lib.tree_attn_decode_ex.argtypes = [SP, P, P, P, P, P, P, I32, P, SZ,
@@ -176,13 +178,15 @@ def tree_attn_workspace_bytes(shape: TaShape, num_splits: int) -> int:
     return int(load().tree_attn_workspace_bytes(ctypes.byref(shape), int(num_splits)))
 
 
-def tree_attn_pick_splits(shape: TaShape, host_seqlens=None, num_sms: int = 0) -> int:
+def tree_attn_pick_splits(shape: TaShape, host_seqlens=None, num_sms: int = 0, page_size: int = 0) -> int:
+    """Split-count heuristic; ``page_size`` > 0 for paged caches (small pages
+    may let one block serve several KV heads, which changes the best count)."""
     arr = None
     if host_seqlens is not None:
         arr = torch.as_tensor(host_seqlens, dtype=torch.int32).cpu().contiguous()
         if arr.numel() != shape.batch:
             raise ValueError("host_seqlens must have one entry per batch row")
-    r = int(load().tree_attn_pick_splits(ctypes.byref(shape), _ptr(arr), int(num_sms)))
+    r = int(load().tree_attn_pick_splits_paged(ctypes.byref(shape), int(page_size), _ptr(arr), int(num_sms)))
     if r < 0:
         raise TreeAttnError(r, "tree_attn_pick_splits")
     return r
@@ -350,7 +354,7 @@ def tree_attn_decode_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torc
         lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
     P = int(num_splits)
     if P <= 0:
-        P = tree_attn_pick_splits(shape)
+        P = tree_attn_pick_splits(shape, page_size=page_size)
     nbytes = tree_attn_workspace_bytes(shape, P)
     if nbytes and workspace is None:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
@@ -408,7 +412,7 @@ def tree_attn_decode_multi(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
         lse = torch.empty(B, Hq, nq, dtype=torch.float32, device=q.device)
     P = int(num_splits)
     if P <= 0:
-        P = tree_attn_pick_splits(eff)
+        P = tree_attn_pick_splits(eff, page_size=paged.page_size if paged is not None else 0)
     nbytes = tree_attn_workspace_bytes(eff, P)
     if nbytes and workspace is None:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)

@@ -44,6 +44,16 @@ constexpr int kFusedMaxStates = 8192;
 bool fuse_merge(int G, int P) {
     return P <= kFusedMaxSplits && static_cast<int64_t>(G) * P <= kFusedMaxStates;
 }
+// A block serving several KV heads merges heads_per_block * G states per
+// slice; within the split limit that never changes the decision (G <= 16,
+// at most 4 heads per block), so the launch count needs no page size.
+static_assert(kFusedMaxSplits * 16 * 4 <= kFusedMaxStates, "fused-merge decision independent of heads per block");
+
+// Paged caches with small pages: one TMA box spans the same tokens of several
+// KV heads (a block serves them all), so a box is 8-16 KB instead of 2-4 KB.
+constexpr int kFp8HeadsPage16 = 4;   // FP8, 16-token pages
+constexpr int kFp8HeadsPage32 = 2;   // FP8, 32-token pages
+constexpr int kMmaHeadsPage16 = 2;   // BF16 tensor-core kernel, 16-token pages
 
 constexpr int kMaxDevices = 64;
 
@@ -183,9 +193,43 @@ int resolve_kernel(const ta_shape* s, int requested) {
     }
 }
 
-Geometry geometry_of(const ta_shape* s, int kernel) {
-    if (kernel == kKernelFp8) return ta::fp8_geometry();
-    return kernel == TA_KERNEL_MMA ? ta::mma_geometry(s->head_dim)
+Geometry geometry_hb(const ta_shape* s, int kernel, int hb) {
+    if (kernel == kKernelFp8) return ta::fp8_geometry(hb);
+    return kernel == TA_KERNEL_MMA ? ta::mma_geometry(s->head_dim, hb)
+                                   : ta::fma_geometry(elem_bytes(s->kv_dtype), s->head_dim);
+}
+
+int pick_splits_hb(const ta_shape* s, const int32_t* host_seqlens, int num_sms, int kernel, int hb);
+
+// KV heads per block for a kernel family and page size (0: dense cache).
+// Only for pools whose KV heads of a token lie closer together than the
+// tokens of a head (token-major pages, [page][token][head][d]): there a box
+// over several heads reads one contiguous run per token.  The largest
+// candidate is taken whose split count for full-length rows keeps the row
+// merge fused, when one head per block does (more splits would add a combine
+// launch).
+int heads_per_block(const ta_shape* s, int kernel, int page_size, int num_sms) {
+    if (page_size <= 0) return 1;
+    const int64_t sh = s->kv_stride_h ? s->kv_stride_h : static_cast<int64_t>(s->head_dim);
+    const int64_t st = s->kv_stride_t ? s->kv_stride_t : static_cast<int64_t>(s->num_kv_heads) * s->head_dim;
+    if (sh >= st) return 1;
+    int want = 1;
+    if (kernel == kKernelFp8)
+        want = page_size <= 16 ? kFp8HeadsPage16 : (page_size <= 32 ? kFp8HeadsPage32 : 1);
+    else if (kernel == TA_KERNEL_MMA && s->head_dim == 128)
+        want = page_size <= 16 ? kMmaHeadsPage16 : 1;
+    const bool fused1 = pick_splits_hb(s, nullptr, num_sms, kernel, 1) <= kFusedMaxSplits;
+    for (; want > 1; want /= 2) {
+        if (s->num_kv_heads % want != 0) continue;
+        if (!fused1 || pick_splits_hb(s, nullptr, num_sms, kernel, want) <= kFusedMaxSplits) break;
+    }
+    return want;
+}
+
+Geometry geometry_of(const ta_shape* s, int kernel, int page_size, int num_sms) {
+    const int hb = heads_per_block(s, kernel, page_size, num_sms);
+    if (kernel == kKernelFp8) return ta::fp8_geometry(hb);
+    return kernel == TA_KERNEL_MMA ? ta::mma_geometry(s->head_dim, hb)
                                    : ta::fma_geometry(elem_bytes(s->kv_dtype), s->head_dim);
 }
 
@@ -218,14 +262,15 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // ------------------------------------------------------------ heuristic
 // Estimated step time for P slices, in units of "one block streaming one
-// token": a block's fixed cost (pipeline fill, epilogue) is worth
-// kBlockCost tokens; a second (combine) launch kBlockCost more plus its
-// traffic (partials written and read back) spread over the whole GPU.
+// token of one KV head": a block's fixed cost (pipeline fill, epilogue) is
+// worth kBlockCost tokens; a second (combine) launch kBlockCost more plus its
+// traffic (partials written and read back) spread over the whole GPU.  A
+// block serving hb KV heads streams hb such units per token.
 constexpr double kBlockCost = 256.0;
 
 double estimate(const ta_shape* s, const std::vector<int64_t>& lens, bool uniform, int P,
-                int tile, int slots) {
-    const int Hkv = s->num_kv_heads;
+                int tile, int slots, int hb) {
+    const int Hkv = s->num_kv_heads / hb;
     const double bytes_per_token = 2.0 * s->head_dim * elem_bytes(s->kv_dtype);
     double comb = 0.0;
     if (P > 1) {
@@ -238,7 +283,7 @@ double estimate(const ta_shape* s, const std::vector<int64_t>& lens, bool unifor
         const int64_t c = ceil_div(ceil_div(N, P), tile) * tile;
         const int64_t blocks = static_cast<int64_t>(s->batch) * Hkv * P;
         const int64_t waves = ceil_div(blocks, slots);
-        return static_cast<double>(waves) * (static_cast<double>(std::min<int64_t>(c, N)) + kBlockCost) +
+        return static_cast<double>(waves) * (static_cast<double>(std::min<int64_t>(c, N)) * hb + kBlockCost) +
                comb;
     }
     // Ragged rows: list-schedule the blocks in launch order (slice fastest,
@@ -253,7 +298,7 @@ double estimate(const ta_shape* s, const std::vector<int64_t>& lens, bool unifor
             for (int p = 0; p < P; ++p) {
                 const int64_t a = c * p;
                 const int64_t len = (a >= N) ? 0 : std::min<int64_t>(c, N - a);
-                const double t = free_at.top() + static_cast<double>(len) + kBlockCost;
+                const double t = free_at.top() + static_cast<double>(len) * hb + kBlockCost;
                 free_at.pop();
                 free_at.push(t);
                 makespan = std::max(makespan, t);
@@ -263,8 +308,9 @@ double estimate(const ta_shape* s, const std::vector<int64_t>& lens, bool unifor
     return makespan + comb;
 }
 
-int pick_splits_impl(const ta_shape* s, const int32_t* host_seqlens, int num_sms, int kernel) {
-    const int tile = geometry_of(s, kernel).tile_tokens;
+int pick_splits_hb(const ta_shape* s, const int32_t* host_seqlens, int num_sms, int kernel, int hb) {
+    const Geometry geo = geometry_hb(s, kernel, hb);
+    const int tile = geo.tile_tokens;
     const int slots = std::max(1, num_sms) * blocks_per_sm(s, kernel);
     std::vector<int64_t> lens(s->batch);
     bool uniform = true;
@@ -280,18 +326,24 @@ int pick_splits_impl(const ta_shape* s, const int32_t* host_seqlens, int num_sms
     // slices of at least 256 tokens; no more than 64 waves of blocks
     int64_t pmax = std::max<int64_t>(1, ceil_div(maxN, 256));
     pmax = std::min<int64_t>(pmax, TA_MAX_SPLITS);
-    const int64_t rows = static_cast<int64_t>(s->batch) * s->num_kv_heads;
+    const int64_t rows = static_cast<int64_t>(s->batch) * (s->num_kv_heads / hb);
     pmax = std::min<int64_t>(pmax, std::max<int64_t>(1, 64 * static_cast<int64_t>(slots) / rows));
     int best = 1;
-    double best_t = estimate(s, lens, uniform, 1, tile, slots);
+    double best_t = estimate(s, lens, uniform, 1, tile, slots, hb);
     for (int P = 2; P <= pmax; ++P) {
-        const double t = estimate(s, lens, uniform, P, tile, slots);
+        const double t = estimate(s, lens, uniform, P, tile, slots, hb);
         if (t < best_t * (1.0 - 1e-9)) {
             best_t = t;
             best = P;
         }
     }
     return best;
+}
+
+int pick_splits_impl(const ta_shape* s, const int32_t* host_seqlens, int num_sms, int kernel,
+                     int page_size) {
+    return pick_splits_hb(s, host_seqlens, num_sms, kernel,
+                          heads_per_block(s, kernel, page_size, num_sms));
 }
 
 // 4-D map over (channel, token, KV head, batch row) -- or, for a page pool,
@@ -308,7 +360,8 @@ int encode_kv_map(CUtensorMap* map, const void* base, const ta_shape* s, const S
                           static_cast<cuuint64_t>(paged ? paged->num_pages : s->batch)};
     cuuint64_t strides[3] = {static_cast<cuuint64_t>(st.t * es), static_cast<cuuint64_t>(st.h * es),
                              static_cast<cuuint64_t>(st.b * es)};
-    cuuint32_t box[4] = {static_cast<cuuint32_t>(geo.box_x), static_cast<cuuint32_t>(rows), 1, 1};
+    const cuuint32_t hb = static_cast<cuuint32_t>(geo.heads_per_block);
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(geo.box_x), static_cast<cuuint32_t>(rows), hb, 1};
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     if (geo.halves5d) {
         // 5-D view (channel in half, token, half, KV head, row/page): one box
@@ -316,7 +369,7 @@ int encode_kv_map(CUtensorMap* map, const void* base, const ta_shape* s, const S
         const cuuint64_t halves = static_cast<cuuint64_t>(s->head_dim / 64);
         cuuint64_t dims5[5] = {64, dims[1], halves, dims[2], dims[3]};
         cuuint64_t strides5[4] = {strides[0], 128, strides[1], strides[2]};
-        cuuint32_t box5[5] = {64, static_cast<cuuint32_t>(rows), static_cast<cuuint32_t>(halves), 1, 1};
+        cuuint32_t box5[5] = {64, static_cast<cuuint32_t>(rows), static_cast<cuuint32_t>(halves), hb, 1};
         const CUresult r5 = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base),
                                dims5, strides5, box5, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -392,13 +445,14 @@ int decode_impl(const ta_shape* shape, const ta_paged_kv* paged, int nq, int cau
 
     int P = num_splits;
     if (P <= 0) {
-        P = pick_splits_impl(shape, nullptr, ds->num_sms, kernel);
+        P = pick_splits_impl(shape, nullptr, ds->num_sms, kernel, paged ? paged->page_size : 0);
         if (P < 1 || P > TA_MAX_SPLITS) return TA_ERR_SPLITS;
         if ((rc = check_ws(P)) != TA_OK) return rc;
     }
     const WsLayout ws = workspace_layout(shape, P);
 
-    const Geometry geo = geometry_of(shape, kernel);
+    const Geometry geo = geometry_of(shape, kernel, paged ? paged->page_size : 0, ds->num_sms);
+    const int hb = geo.heads_per_block;
     const int rows = paged ? std::min(geo.tile_tokens, paged->page_size) : geo.tile_tokens;
     if (geo.tile_tokens / rows > 32) return TA_ERR_SHAPE;  // one producer lane per box
     CUtensorMap tk, tv;
@@ -431,6 +485,7 @@ int decode_impl(const ta_shape* shape, const ta_paged_kv* paged, int nq, int cau
     p.chunk_tiles = std::max(1, kChunkTokens / geo.tile_tokens);
     p.prefetch_tiles = std::max(1, kPrefetchTokens / geo.tile_tokens);
     p.box_rows = rows;
+    p.hb = hb;
     p.num_pages = shape->batch;
     if (paged) {
         p.block_table = paged->block_table;
@@ -448,7 +503,7 @@ int decode_impl(const ta_shape* shape, const ta_paged_kv* paged, int nq, int cau
         p.part_o = reinterpret_cast<float*>(w + ws.o);
         p.part_m = reinterpret_cast<float*>(w + ws.m);
         p.part_l = reinterpret_cast<float*>(w + ws.l);
-        const unsigned rows = static_cast<unsigned>(shape->batch) * shape->num_kv_heads;
+        const unsigned rows = static_cast<unsigned>(shape->batch) * (shape->num_kv_heads / hb);
         unsigned* slots = reserve_slots(ds, 2 * rows);
         if (slots) {
             // Run-time balancing pays while the grid is a few waves at most; with
@@ -456,7 +511,7 @@ int decode_impl(const ta_shape* shape, const ta_paged_kv* paged, int nq, int cau
             const int64_t blocks = static_cast<int64_t>(rows) * P;
             const int64_t resident = static_cast<int64_t>(ds->num_sms) * blocks_per_sm(shape, kernel);
             if (!deterministic && blocks <= kBalanceMaxWaves * resident) p.claim = slots;
-            fused = fuse_merge(p.G, P);
+            fused = fuse_merge(hb * p.G, P);
             p.fuse = fused ? 1 : 0;
             if (p.claim || fused) p.done = slots + rows;
         }
@@ -524,17 +579,25 @@ size_t tree_attn_workspace_bytes(const ta_shape* shape, int num_splits) {
     return workspace_layout(shape, num_splits).total;
 }
 
-int tree_attn_pick_splits(const ta_shape* shape, const int32_t* host_seqlens, int num_sms) {
+int tree_attn_pick_splits_paged(const ta_shape* shape, int page_size, const int32_t* host_seqlens,
+                                int num_sms) {
     const int rc = check_shape(shape, nullptr);
     if (rc != TA_OK) return rc;
+    if (page_size > 0 && (page_size < 16 || page_size > 1024 || (page_size & (page_size - 1)) != 0))
+        return TA_ERR_SHAPE;
+    const int kernel = resolve_kernel(shape, TA_KERNEL_AUTO);
+    if (kernel < 0) return kernel;
     if (num_sms <= 0) {
         DeviceState* ds = nullptr;
         const int r = device_state(&ds);
         if (r != TA_OK) return r;
         num_sms = ds->num_sms;
     }
-    const int kernel = resolve_kernel(shape, TA_KERNEL_AUTO);
-    return pick_splits_impl(shape, host_seqlens, num_sms, kernel);
+    return pick_splits_impl(shape, host_seqlens, num_sms, kernel, page_size > 0 ? page_size : 0);
+}
+
+int tree_attn_pick_splits(const ta_shape* shape, const int32_t* host_seqlens, int num_sms) {
+    return tree_attn_pick_splits_paged(shape, 0, host_seqlens, num_sms);
 }
 
 int tree_attn_decode_ex(const ta_shape* shape, const void* q, const void* k_cache,
@@ -579,7 +642,7 @@ int tree_attn_launch_count(const ta_shape* shape, int num_splits, const ta_optio
     if (P <= 0) {
         DeviceState* ds = nullptr;
         if ((rc = device_state(&ds)) != TA_OK) return rc;
-        P = pick_splits_impl(shape, nullptr, ds->num_sms, kernel);
+        P = pick_splits_impl(shape, nullptr, ds->num_sms, kernel, 0);
     }
     if (P == 1) return 1;
     const int64_t G = shape->num_q_heads / shape->num_kv_heads;

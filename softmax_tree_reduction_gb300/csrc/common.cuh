@@ -32,8 +32,8 @@ struct SplitParams {
     float* part_m;          // [B][Hq][P]
     float* part_l;          // [B][Hq][P]
     int* err;               // device error word
-    unsigned* claim;        // [B*Hkv] chunk counters (null: static chunk assignment)
-    unsigned* done;         // [B*Hkv] row tickets (null: no ticket is taken)
+    unsigned* claim;        // [B*Hkv/hb] chunk counters (null: static chunk assignment)
+    unsigned* done;         // [B*Hkv/hb] row tickets (null: no ticket is taken)
     int fuse;               // the row's last block merges the partial states
     const float* k_scale;   // [Hkv] FP8 caches: K = k_scale[g] * e4m3 code
     const float* v_scale;   // [Hkv] likewise for V
@@ -42,6 +42,7 @@ struct SplitParams {
     int page_shift;         // log2(page_size)
     int num_pages;          // pages in the pool (an out-of-range page reads zeros)
     int box_rows;           // tokens per TMA box: the tile, or the page when it is smaller
+    int hb;                 // KV heads per block (a box brings box_rows tokens of each)
     int B, Hq, Hkv, G, S, P; // Hq, G count virtual heads: query heads x queries per row
     int nq;                 // queries per row (q rows are [head][query])
     int causal;             // query i of nq sees tokens < N - nq + 1 + i

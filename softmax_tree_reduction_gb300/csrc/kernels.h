@@ -14,14 +14,16 @@ struct Geometry {
     int box_x;         // channels per TMA box (64 with 128-byte swizzle, else head_dim)
     int swizzle128;    // 1: CU_TENSOR_MAP_SWIZZLE_128B, 0: no swizzle
     int halves5d = 0;  // 1: 5-D view whose box brings every 64-channel half at once
+    int heads_per_block = 1;  // KV heads a block serves; each box spans all of them
 };
 
-Geometry mma_geometry(int head_dim);
+Geometry mma_geometry(int head_dim, int heads_per_block);
 Geometry fma_geometry(int kv_elem_bytes, int head_dim);
-Geometry fp8_geometry();
+Geometry fp8_geometry(int heads_per_block);
 
-// Per-slice kernels.  Grid (P, Hkv, B); `tk`/`tv` are 4-D tensor maps over
-// (channel, token, KV head, batch row) with the box of the kernel's Geometry.
+// Per-slice kernels.  Grid (P, Hkv / hb, B); `tk`/`tv` are tensor maps over
+// (channel, token, KV head, batch row or page) with the box of the kernel's
+// Geometry (hb = p.hb KV heads per box).
 cudaError_t launch_split_mma(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv,
                              const SplitParams& p, cudaStream_t stream);
 cudaError_t launch_split_fma_bf16(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -232,12 +232,13 @@ __device__ __forceinline__ unsigned ticket_acq_rel(unsigned* p, unsigned limit) 
     return old;
 }
 
+// `row`: the block's schedule row (ticket and claim counters); the row's
+// blocks hold the states of query heads [hq0, hq0 + G) (flat b * Hq + h).
 template <int D>
-__device__ void finish_row(const SplitParams& p, int b, int g, float* scratch, int* flag, int tid,
-                           int nthr) {
+__device__ void finish_row(const SplitParams& p, int row, size_t hq0, int G, float* scratch,
+                           int* flag, int tid, int nthr) {
     consumer_sync(nthr);
     if (tid == 0) {
-        const int row = b * p.Hkv + g;
         const unsigned t = ticket_acq_rel(p.done + row, static_cast<unsigned>(p.P - 1));
         const bool last = (t == static_cast<unsigned>(p.P - 1));
         if (last && p.claim) atomicExch(p.claim + row, 0u);
@@ -245,8 +246,8 @@ __device__ void finish_row(const SplitParams& p, int b, int g, float* scratch, i
     }
     consumer_sync(nthr);
     if (!*flag || !p.fuse) return;
-    const int G = p.G, P = p.P;
-    const size_t row0 = static_cast<size_t>(b) * p.Hq + static_cast<size_t>(g) * G;
+    const int P = p.P;
+    const size_t row0 = hq0;
     float* sw = scratch;           // [G][P]  maxima, then leaf weights
     float* sl = scratch + G * P;   // [G][P]  denominators
     float* sr = sl + G * P;        // [G] root maxima, [G] root denominators

@@ -303,7 +303,9 @@ __global__ void __launch_bounds__(FmaCfg<KV, D>::kThreads, 1)
         }
         emit_state(p, b, g * G + h, split, D, dd, ov, lv, M, poison);
     }
-    if (p.done) finish_row<D>(p, b, g, reinterpret_cast<float*>(stages), last_flag, ct, C::kWarps * 32);
+    if (p.done)
+        finish_row<D>(p, b * p.Hkv + g, static_cast<size_t>(b) * p.Hq + static_cast<size_t>(g) * p.G, p.G,
+                      reinterpret_cast<float*>(stages), last_flag, ct, C::kWarps * 32);
     allow_dependents();
 }
 

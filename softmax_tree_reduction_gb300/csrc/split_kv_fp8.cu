@@ -32,12 +32,17 @@
 namespace ta {
 namespace {
 
+// HB KV heads per block: a stage holds kTile tokens of each (256 rows of
+// 128 B per operand), and kWarps / HB consumer warps serve each head.
+template <int HB>
 struct Fp8Cfg {
     static constexpr int D = 128;
     static constexpr int kWarps = 8;                 // consumer warps
     static constexpr int kSub = 2;                   // 16-token slabs per warp per stage
-    static constexpr int kTile = 16 * kWarps * kSub; // tokens per stage
-    static constexpr int kKBytes = kTile * D;        // one byte per element
+    static constexpr int kRows = 16 * kWarps * kSub; // rows per operand per stage
+    static constexpr int kTile = kRows / HB;         // tokens per stage
+    static constexpr int kWPH = kWarps / HB;         // consumer warps per KV head
+    static constexpr int kKBytes = kRows * D;        // one byte per element
     static constexpr int kStageBytes = 2 * kKBytes;  // K and V
     static constexpr int kStages = 6 / kSub;
     static constexpr int kBarBytes = 2 * kStages * 8 + kStages * 8 + 32;
@@ -100,10 +105,11 @@ __device__ __forceinline__ float tree_sum(const float* v) {
     }
 }
 
-__global__ void __launch_bounds__(Fp8Cfg::kThreads, 1)
+template <int HB>
+__global__ void __launch_bounds__(Fp8Cfg<HB>::kThreads, 1)
     split_kv_fp8_kernel(const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const SplitParams p) {
-    using C = Fp8Cfg;
+    using C = Fp8Cfg<HB>;
     constexpr int D = C::D;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -120,7 +126,9 @@ __global__ void __launch_bounds__(Fp8Cfg::kThreads, 1)
     volatile unsigned* claim_sink = reinterpret_cast<volatile unsigned*>(abort_flag + 2);
     volatile int* bad_page = reinterpret_cast<volatile int*>(abort_flag + 3);
 
-    const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    // KV heads g0 .. g0 + HB - 1 of batch row b; schedule row `row`
+    const int split = blockIdx.x, g0 = blockIdx.y * HB, b = blockIdx.z;
+    const int row = b * (p.Hkv / HB) + blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -140,13 +148,13 @@ __global__ void __launch_bounds__(Fp8Cfg::kThreads, 1)
         const int page_mask = (1 << p.page_shift) - 1;
         prefetch_row_head(p, b, split, C::kTile, p.prefetch_tiles, [&](int y, int j, int page) {
             if (!p.block_table) {
-                tma_prefetch_4d(&tmK, 0, y, g, b);
-                tma_prefetch_4d(&tmV, 0, y, g, b);
+                tma_prefetch_4d(&tmK, 0, y, g0, b);
+                tma_prefetch_4d(&tmV, 0, y, g0, b);
                 return;
             }
             const int ty = (y + j * p.box_rows) & page_mask;
-            tma_prefetch_4d(&tmK, 0, ty, g, page);
-            tma_prefetch_4d(&tmV, 0, ty, g, page);
+            tma_prefetch_4d(&tmK, 0, ty, g0, page);
+            tma_prefetch_4d(&tmV, 0, ty, g0, page);
         });
     }
     __syncthreads();
@@ -163,20 +171,21 @@ __global__ void __launch_bounds__(Fp8Cfg::kThreads, 1)
         const uint64_t pol = l2_policy_evict_first();
         const bool paged = p.block_table != nullptr;
         const int page_mask = (1 << p.page_shift) - 1;
-        const int box_bytes = p.box_rows * D;
+        // box j = box_rows tokens of the HB heads, [head][row][128 B], at j * box_bytes
+        const int box_bytes = HB * p.box_rows * D;
         produce_row<C::kStages>(
-            p, b, b * p.Hkv + g, N, split, C::kTile, full, empty, meta, claim_sink, bad_page,
+            p, b, row, N, split, C::kTile, full, empty, meta, claim_sink, bad_page,
             C::kStageBytes, [&](int s, int y, int j, int page) {
                 uint8_t* st = stages + s * C::kStageBytes;
                 const int off = j * box_bytes;
                 if (!paged) {
-                    tma_load_4d(st + off, &tmK, 0, y, g, b, &full[s], pol);
-                    tma_load_4d(st + C::kKBytes + off, &tmV, 0, y, g, b, &full[s], pol);
+                    tma_load_4d(st + off, &tmK, 0, y, g0, b, &full[s], pol);
+                    tma_load_4d(st + C::kKBytes + off, &tmV, 0, y, g0, b, &full[s], pol);
                     return;
                 }
                 const int ty = (y + j * p.box_rows) & page_mask;
-                tma_load_4d(st + off, &tmK, 0, ty, g, page, &full[s], pol);
-                tma_load_4d(st + C::kKBytes + off, &tmV, 0, ty, g, page, &full[s], pol);
+                tma_load_4d(st + off, &tmK, 0, ty, g0, page, &full[s], pol);
+                tma_load_4d(st + C::kKBytes + off, &tmV, 0, ty, g0, page, &full[s], pol);
             });
         allow_dependents();
         return;
@@ -185,6 +194,13 @@ __global__ void __launch_bounds__(Fp8Cfg::kThreads, 1)
     // ---------------------------------------------------------- consumers
     const int cw = warp - 1;
     const int gid = lane >> 2, tig = lane & 3;
+    const int hw = cw / C::kWPH, wi = cw % C::kWPH;  // this warp's head within the block
+    const int g = g0 + hw;
+    // scales first, so their loads overlap those of q
+    const float ks = p.k_scale[g];
+    float vsc[HB];  // V scales of the block's heads (applied in the merge), / 2^14
+#pragma unroll
+    for (int i = 0; i < HB; ++i) vsc[i] = p.v_scale[g0 + i] / kPScale;
 
     // q (BF16) of column gid, channels 32 tig .. 32 tig + 31 in the permuted order.
     float qv[32];
@@ -216,7 +232,6 @@ __global__ void __launch_bounds__(Fp8Cfg::kThreads, 1)
         qb[kk][0] = half2_bits(__floats2half2_rn(qv[4 * kk] * qs, qv[4 * kk + 1] * qs));
         qb[kk][1] = half2_bits(__floats2half2_rn(qv[4 * kk + 2] * qs, qv[4 * kk + 3] * qs));
     }
-    const float ks = p.k_scale[g], vs = p.v_scale[g];
     const float sl2 = p.scale_log2 * ks / qs;
 
     const int causal_from = p.causal ? N - p.nq + 1 : 0x7fffffff;
@@ -241,6 +256,14 @@ __global__ void __launch_bounds__(Fp8Cfg::kThreads, 1)
     const uint32_t v_1 = (tv0 + 1) * 128 + ((gid ^ ((tv0 + 1) & 7)) << 4);
     const uint32_t v_2 = (tv0 + 8) * 128 + ((gid ^ ((tv0 + 8) & 7)) << 4);
     const uint32_t v_3 = (tv0 + 9) * 128 + ((gid ^ ((tv0 + 9) & 7)) << 4);
+    // This warp's slabs: tokens r0 .. r0 + 15 of the tile (r0 = 16 (sub * kWPH + wi)),
+    // in box r0 / R at row r0 % R of its head's [R rows][128 B] part.
+    static_assert(C::kSub == 2, "two slabs per warp per stage");
+    const int R = p.box_rows;
+    auto slab_offset = [&](int r0) -> uint32_t {
+        return (r0 / R) * (HB * R * 128) + hw * (R * 128) + (r0 % R) * 128;
+    };
+    const uint32_t slab_off0 = slab_offset(wi * 16), slab_off1 = slab_offset((C::kWPH + wi) * 16);
     bool timed_out = false;
 
     for (int it = 0;; ++it) {
@@ -254,9 +277,13 @@ __global__ void __launch_bounds__(Fp8Cfg::kThreads, 1)
         const int tile_tok0 = meta[s].tok0;
 #pragma unroll 1
         for (int sub = 0; sub < C::kSub; ++sub) {
-            const int r0 = (sub * C::kWarps + cw) * 16;  // first row of this warp's slab
+            const int r0 = (sub * C::kWPH + wi) * 16;  // first token of this warp's slab
             const int blk0 = tile_tok0 + r0;
-            const uint32_t kbase = smem_u32(stages + s * C::kStageBytes) + r0 * 128;
+            uint32_t kbase = smem_u32(stages + s * C::kStageBytes);
+            if constexpr (HB == 1)
+                kbase += r0 * 128;  // one box of the whole tile
+            else
+                kbase += (sub == 0 ? slab_off0 : slab_off1);
             const uint32_t vbase = kbase + C::kKBytes;
             const int nvalid = tile_valid - r0;
 
@@ -389,46 +416,54 @@ __global__ void __launch_bounds__(Fp8Cfg::kThreads, 1)
     }
     consumer_sync(C::kWarps * 32);
     const bool poison = bad || (*abort_flag != 0) || (*bad_page != 0);
-    const float oscale = vs / kPScale;
     const int ct = threadIdx.x - 32;
-    for (int idx = ct; idx < p.G * D; idx += C::kWarps * 32) {
-        const int h = idx / D, pos = idx - h * D;
+    // states of the warps serving one head, merged per (head, column, channel)
+    for (int idx = ct; idx < HB * p.G * D; idx += C::kWarps * 32) {
+        int hh = 0, rem = idx;
+        if constexpr (HB > 1) {
+            hh = idx / (p.G * D);
+            rem = idx - hh * (p.G * D);
+        }
+        const int h = rem / D, pos = rem - h * D;
         const int dd = (pos & 7) * 16 + (pos >> 3);  // channel stored at `pos`
-        float mw[C::kWarps];
+        const int w0 = hh * C::kWPH;
+        float mw[C::kWPH];
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < C::kWarps; ++w) {
-            mw[w] = mg_m[w * 8 + h];
+        for (int w = 0; w < C::kWPH; ++w) {
+            mw[w] = mg_m[(w0 + w) * 8 + h];
             M = fmaxf(M, mw[w]);
         }
         const float Ms = (M == -INFINITY) ? 0.f : M;
-        float ow[C::kWarps], lw[C::kWarps];
+        float ow[C::kWPH], lw[C::kWPH];
 #pragma unroll
-        for (int w = 0; w < C::kWarps; ++w) {
+        for (int w = 0; w < C::kWPH; ++w) {
             const float wt = ex2(mw[w] - Ms);
-            ow[w] = wt * mg_o[(w * 8 + h) * MS + pos];
-            lw[w] = wt * mg_l[w * 8 + h];
+            ow[w] = wt * mg_o[((w0 + w) * 8 + h) * MS + pos];
+            lw[w] = wt * mg_l[(w0 + w) * 8 + h];
         }
-        const float o = tree_sum<C::kWarps>(ow) * oscale;
-        const float lsum = tree_sum<C::kWarps>(lw);
-        emit_state(p, b, g * p.G + h, split, D, dd, o, lsum, M, poison);
+        float osc = vsc[0];
+#pragma unroll
+        for (int i = 1; i < HB; ++i) osc = (hh == i) ? vsc[i] : osc;
+        const float o = tree_sum<C::kWPH>(ow) * osc;
+        const float lsum = tree_sum<C::kWPH>(lw);
+        emit_state(p, b, (g0 + hh) * p.G + h, split, D, dd, o, lsum, M, poison);
     }
-    if (p.done) finish_row<D>(p, b, g, reinterpret_cast<float*>(stages), last_flag, ct, C::kWarps * 32);
+    if (p.done)
+        finish_row<D>(p, row, static_cast<size_t>(b) * p.Hq + static_cast<size_t>(g0) * p.G, HB * p.G,
+                      reinterpret_cast<float*>(stages), last_flag, ct, C::kWarps * 32);
     allow_dependents();
 }
 
-}  // namespace
-
-Geometry fp8_geometry() { return Geometry{Fp8Cfg::kTile, Fp8Cfg::D, 1}; }
-
-cudaError_t launch_split_fp8(const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& p,
-                             cudaStream_t stream) {
-    using C = Fp8Cfg;
-    cudaError_t e = cudaFuncSetAttribute(split_kv_fp8_kernel,
+template <int HB>
+cudaError_t launch_hb(const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& p,
+                      cudaStream_t stream) {
+    using C = Fp8Cfg<HB>;
+    cudaError_t e = cudaFuncSetAttribute(split_kv_fp8_kernel<HB>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.P, p.Hkv, p.B);
+    cfg.gridDim = dim3(p.P, p.Hkv / HB, p.B);
     cfg.blockDim = dim3(C::kThreads, 1, 1);
     cfg.dynamicSmemBytes = C::kSmem;
     cfg.stream = stream;
@@ -437,7 +472,27 @@ cudaError_t launch_split_fp8(const CUtensorMap& tk, const CUtensorMap& tv, const
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, split_kv_fp8_kernel, tk, tv, p);
+    return cudaLaunchKernelEx(&cfg, split_kv_fp8_kernel<HB>, tk, tv, p);
+}
+
+}  // namespace
+
+Geometry fp8_geometry(int heads_per_block) {
+    switch (heads_per_block) {
+        case 2: return Geometry{Fp8Cfg<2>::kTile, Fp8Cfg<2>::D, 1, 0, 2};
+        case 4: return Geometry{Fp8Cfg<4>::kTile, Fp8Cfg<4>::D, 1, 0, 4};
+        default: return Geometry{Fp8Cfg<1>::kTile, Fp8Cfg<1>::D, 1, 0, 1};
+    }
+}
+
+cudaError_t launch_split_fp8(const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& p,
+                             cudaStream_t stream) {
+    switch (p.hb) {
+        case 1: return launch_hb<1>(tk, tv, p, stream);
+        case 2: return launch_hb<2>(tk, tv, p, stream);
+        case 4: return launch_hb<4>(tk, tv, p, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace ta

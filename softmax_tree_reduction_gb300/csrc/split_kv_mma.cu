@@ -32,12 +32,16 @@
 namespace ta {
 namespace {
 
-template <int D>
+// HB KV heads per block: a stage holds kTile tokens of each (128 rows per
+// operand), and kWarps / HB consumer warps serve each head.
+template <int D, int HB>
 struct MmaCfg {
     static constexpr int kWarps = 8;                 // consumer warps (two per SM sub-partition)
-    static constexpr int kTile = 16 * kWarps;        // tokens per stage
+    static constexpr int kRows = 16 * kWarps;        // rows per operand per stage
+    static constexpr int kTile = kRows / HB;         // tokens per stage
+    static constexpr int kWPH = kWarps / HB;         // consumer warps per KV head
     static constexpr int kHalves = D / 64;           // 128-byte column blocks per row
-    static constexpr int kKBytes = kHalves * kTile * 128;
+    static constexpr int kKBytes = kHalves * kRows * 128;
     static constexpr int kStageBytes = 2 * kKBytes;  // K and V
     static constexpr int kStages = (D == 128) ? 3 : 6;
     static constexpr int kBarBytes = 2 * kStages * 8 + kStages * 8 + 32;
@@ -94,11 +98,11 @@ __device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat162 v) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-template <int D, int NT>
-__global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
+template <int D, int NT, int HB>
+__global__ void __launch_bounds__(MmaCfg<D, HB>::kThreads, 1)
     split_kv_mma_kernel(const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const SplitParams p) {
-    using C = MmaCfg<D>;
+    using C = MmaCfg<D, HB>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -114,7 +118,9 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
     volatile unsigned* claim_sink = reinterpret_cast<volatile unsigned*>(abort_flag + 2);
     volatile int* bad_page = reinterpret_cast<volatile int*>(abort_flag + 3);
 
-    const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    // KV heads g0 .. g0 + HB - 1 of batch row b; schedule row `row`
+    const int split = blockIdx.x, g0 = blockIdx.y * HB, b = blockIdx.z;
+    const int row = b * (p.Hkv / HB) + blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -134,13 +140,13 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
         const int page_mask = (1 << p.page_shift) - 1;
         prefetch_row_head(p, b, split, C::kTile, p.prefetch_tiles, [&](int y, int j, int page) {
             if (!p.block_table) {
-                tma_prefetch_5d(&tmK, 0, y, 0, g, b);
-                tma_prefetch_5d(&tmV, 0, y, 0, g, b);
+                tma_prefetch_5d(&tmK, 0, y, 0, g0, b);
+                tma_prefetch_5d(&tmV, 0, y, 0, g0, b);
                 return;
             }
             const int ty = (y + j * p.box_rows) & page_mask;
-            tma_prefetch_5d(&tmK, 0, ty, 0, g, page);
-            tma_prefetch_5d(&tmV, 0, ty, 0, g, page);
+            tma_prefetch_5d(&tmK, 0, ty, 0, g0, page);
+            tma_prefetch_5d(&tmV, 0, ty, 0, g0, page);
         });
     }
     __syncthreads();
@@ -162,23 +168,24 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
             const uint64_t pol = l2_policy_evict_first();
             const bool paged = p.block_table != nullptr;
             const int page_mask = (1 << p.page_shift) - 1;
-            const int box_bytes = C::kHalves * p.box_rows * 128;
+            const int box_bytes = HB * C::kHalves * p.box_rows * 128;
             produce_row<C::kStages>(
-                p, b, b * p.Hkv + g, N, split, C::kTile, full, empty, meta, claim_sink, bad_page,
+                p, b, row, N, split, C::kTile, full, empty, meta, claim_sink, bad_page,
                 C::kStageBytes, [&](int s, int y, int j, int page) {
-                    // One box = box_rows tokens x all channels, laid out in shared
-                    // memory as [half][box_rows][128 B]; box j of a tile at j*box_bytes.
+                    // One box = box_rows tokens x all channels of the HB heads, laid out
+                    // in shared memory as [head][half][box_rows][128 B]; box j of a
+                    // tile at j*box_bytes.
                     uint8_t* st = stages + s * C::kStageBytes;
                     const int off = j * box_bytes;
                     if (!paged) {
-                        tma_load_5d(st + off, &tmK, 0, y, 0, g, b, &full[s], pol);
-                        tma_load_5d(st + C::kKBytes + off, &tmV, 0, y, 0, g, b, &full[s], pol);
+                        tma_load_5d(st + off, &tmK, 0, y, 0, g0, b, &full[s], pol);
+                        tma_load_5d(st + C::kKBytes + off, &tmV, 0, y, 0, g0, b, &full[s], pol);
                         return;
                     }
                     // paged: (channel, token in page, half, KV head, physical page)
                     const int ty = (y + j * p.box_rows) & page_mask;
-                    tma_load_5d(st + off, &tmK, 0, ty, 0, g, page, &full[s], pol);
-                    tma_load_5d(st + C::kKBytes + off, &tmV, 0, ty, 0, g, page, &full[s], pol);
+                    tma_load_5d(st + off, &tmK, 0, ty, 0, g0, page, &full[s], pol);
+                    tma_load_5d(st + C::kKBytes + off, &tmV, 0, ty, 0, g0, page, &full[s], pol);
                 });
         }
         allow_dependents();
@@ -189,6 +196,8 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
     const int cw = warp - 1;
     const int gid = lane >> 2, tig = lane & 3;
     const int r8 = lane & 7;
+    const int hw = cw / C::kWPH, wi = cw % C::kWPH;  // this warp's head within the block
+    const int g = g0 + hw;
 
     // q as the B operand of S^T = K Q^T.  Column n of n-tile t is virtual head
     // c = 8t + n of this KV head's group: a query head, or a (head, query) pair
@@ -232,12 +241,13 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
     }
 
     // ldmatrix row addresses (swizzled 16-byte chunk = chunk ^ (row & 7)).  A
-    // stage holds tile/R boxes of [half][R rows][128 B] (R = box_rows >= 16), so
-    // this warp's 16 rows sit in one box.
+    // stage holds tile/R boxes of [head][half][R rows][128 B] (R = box_rows >=
+    // 16), so this warp's 16 tokens (r0 .. r0 + 15 of its head) sit in one box.
     const int R = p.box_rows;
     const uint32_t half_bytes = R * 128;
-    const int r0 = cw * 16;
-    const uint32_t warp_base = (r0 / R) * (C::kHalves * half_bytes) + (r0 % R) * 128;
+    const int r0 = wi * 16;
+    const uint32_t warp_base = (r0 / R) * (HB * C::kHalves * half_bytes) + hw * (C::kHalves * half_bytes) +
+                               (r0 % R) * 128;
     const uint32_t k_row = warp_base + (r8 + 8 * ((lane >> 3) & 1)) * 128;
     const int k_chi = lane >> 4;
     const uint32_t v_row = warp_base + (r8 + 8 * (lane >> 4)) * 128;
@@ -253,10 +263,10 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
         }
         const int tile_valid = meta[s].nvalid;
         if (tile_valid < 0) break;  // end of this block's work
-        const int blk0 = meta[s].tok0 + cw * 16;  // first token of this warp's block
+        const int blk0 = meta[s].tok0 + r0;  // first token of this warp's block
         const uint32_t kbase = smem_u32(stages + s * C::kStageBytes);
         const uint32_t vbase = kbase + C::kKBytes;
-        const int nvalid = tile_valid - cw * 16;  // valid tokens of this warp's 16-token block
+        const int nvalid = tile_valid - r0;  // valid tokens of this warp's 16-token block
 
         if (nvalid > 0) {
             // S^T = K_blk Q^T (two accumulators per n-tile to shorten the dependency chain)
@@ -392,41 +402,50 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
     consumer_sync(C::kWarps * 32);
     const bool poison = bad || (*abort_flag != 0) || (*bad_page != 0);
     const int ct = threadIdx.x - 32;
-    for (int idx = ct; idx < p.G * D; idx += C::kWarps * 32) {
-        const int h = idx / D, dd = idx - h * D;
-        float mw[C::kWarps];
+    // states of the warps serving one head, merged per (head, column, channel)
+    for (int idx = ct; idx < HB * p.G * D; idx += C::kWarps * 32) {
+        int hh = 0, rem = idx;
+        if constexpr (HB > 1) {
+            hh = idx / (p.G * D);
+            rem = idx - hh * (p.G * D);
+        }
+        const int h = rem / D, dd = rem - h * D;
+        const int w0 = hh * C::kWPH;
+        float mw[C::kWPH];
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < C::kWarps; ++w) {
-            mw[w] = mg_m[w * kCols + h];
+        for (int w = 0; w < C::kWPH; ++w) {
+            mw[w] = mg_m[(w0 + w) * kCols + h];
             M = fmaxf(M, mw[w]);
         }
         const float Ms = (M == -INFINITY) ? 0.f : M;
-        float ow[C::kWarps], lw[C::kWarps];
+        float ow[C::kWPH], lw[C::kWPH];
 #pragma unroll
-        for (int w = 0; w < C::kWarps; ++w) {
+        for (int w = 0; w < C::kWPH; ++w) {
             const float wt = ex2(mw[w] - Ms);
-            ow[w] = wt * mg_o[(w * kCols + h) * MS + dd];
-            lw[w] = wt * mg_l[w * kCols + h];
+            ow[w] = wt * mg_o[((w0 + w) * kCols + h) * MS + dd];
+            lw[w] = wt * mg_l[(w0 + w) * kCols + h];
         }
         // pairwise tree over the warps
-        const float o = tree_sum<C::kWarps>(ow);
-        const float lsum = tree_sum<C::kWarps>(lw);
-        emit_state(p, b, g * p.G + h, split, D, dd, o, lsum, M, poison);
+        const float o = tree_sum<C::kWPH>(ow);
+        const float lsum = tree_sum<C::kWPH>(lw);
+        emit_state(p, b, (g0 + hh) * p.G + h, split, D, dd, o, lsum, M, poison);
     }
-    if (p.done) finish_row<D>(p, b, g, reinterpret_cast<float*>(stages), last_flag, ct, C::kWarps * 32);
+    if (p.done)
+        finish_row<D>(p, row, static_cast<size_t>(b) * p.Hq + static_cast<size_t>(g0) * p.G, HB * p.G,
+                      reinterpret_cast<float*>(stages), last_flag, ct, C::kWarps * 32);
     allow_dependents();
 }
 
-template <int D, int NT>
+template <int D, int NT, int HB>
 cudaError_t launch_impl(const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& p,
                         cudaStream_t stream) {
-    using C = MmaCfg<D>;
-    cudaError_t e = cudaFuncSetAttribute(split_kv_mma_kernel<D, NT>,
+    using C = MmaCfg<D, HB>;
+    cudaError_t e = cudaFuncSetAttribute(split_kv_mma_kernel<D, NT, HB>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.P, p.Hkv, p.B);
+    cfg.gridDim = dim3(p.P, p.Hkv / HB, p.B);
     cfg.blockDim = dim3(C::kThreads, 1, 1);
     cfg.dynamicSmemBytes = C::kSmem;
     cfg.stream = stream;
@@ -435,24 +454,29 @@ cudaError_t launch_impl(const CUtensorMap& tk, const CUtensorMap& tv, const Spli
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<D, NT>, tk, tv, p);
+    return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<D, NT, HB>, tk, tv, p);
 }
 
 }  // namespace
 
-Geometry mma_geometry(int head_dim) {
-    (void)head_dim;
-    return Geometry{MmaCfg<128>::kTile, 64, 1, 1};
+// Several KV heads per block only at head_dim 128 (small pages).
+Geometry mma_geometry(int head_dim, int heads_per_block) {
+    const int hb = (head_dim == 128 && heads_per_block == 2) ? 2 : 1;
+    return Geometry{MmaCfg<128, 1>::kRows / hb, 64, 1, 1, hb};
 }
 
 cudaError_t launch_split_mma(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv,
                              const SplitParams& p, cudaStream_t stream) {
     // one n-tile of 8 columns per KV head group, two for up to 16
     const bool two = p.G > 8;
+    if (p.hb == 2 && head_dim == 128)
+        return two ? launch_impl<128, 2, 2>(tk, tv, p, stream) : launch_impl<128, 1, 2>(tk, tv, p, stream);
+    if (p.hb != 1) return cudaErrorInvalidValue;
     switch (head_dim) {
-        case 64: return two ? launch_impl<64, 2>(tk, tv, p, stream) : launch_impl<64, 1>(tk, tv, p, stream);
+        case 64:
+            return two ? launch_impl<64, 2, 1>(tk, tv, p, stream) : launch_impl<64, 1, 1>(tk, tv, p, stream);
         case 128:
-            return two ? launch_impl<128, 2>(tk, tv, p, stream) : launch_impl<128, 1>(tk, tv, p, stream);
+            return two ? launch_impl<128, 2, 1>(tk, tv, p, stream) : launch_impl<128, 1, 1>(tk, tv, p, stream);
         default: return cudaErrorInvalidValue;
     }
 }
