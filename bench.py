@@ -44,12 +44,12 @@ FALLBACK_HBM_GBS = 6800.0
 NCU_TRAFFIC = {
     # profiles/split_kv_mma_llama31_8b_131k.md
     ("mma", "llama3.1-8b-decode-layer"): {
-        "bytes_per_launch": 537261824 + 3128576, "num_splits": 19,
-        "src_sha256": "ff7f5622f2a4d74a64cb7fdcf5f8b71992c768c04145b626fc7cad6085da0c07"},
+        "bytes_per_launch": 537206272 + 2968064, "num_splits": 19,
+        "src_sha256": "23a44a075b68e958b321fadb8d02a088685ace0d0d6f5a0fbbc9b540c2ed3536"},
     # profiles/split_kv_fp8_llama31_8b_131k.md
     ("fp8", "llama3.1-8b-decode-layer"): {
-        "bytes_per_launch": 268515328 + 2902528, "num_splits": 19,
-        "src_sha256": "93be804ef9ce693b4b57612af78cdce5e6d6aaa63ee3c522687a0aa83f8ad2a1"},
+        "bytes_per_launch": 268516352 + 2977536, "num_splits": 19,
+        "src_sha256": "9edf13779563b3ff2ad69446b2c76abe8262e9fe2d151d5d6c5df30c439e20d0"},
 }
 
 
