@@ -66,7 +66,7 @@ typedef enum {
     TA_E4M3 = 2   /* FP8 E4M3 ("fn": no infinities), KV caches only; the element
                      value is the code times a per-KV-head scale given in
                      ta_options (k_scale, v_scale).  Needs BF16 q, head_dim 128
-                     and at most 8 query heads (x queries) per KV head. */
+                     and at most 16 query heads (x queries) per KV head. */
 } ta_dtype;
 
 /* Largest accepted num_splits. */
@@ -104,7 +104,7 @@ typedef enum {
     TA_KERNEL_AUTO = 0,  /* tensor-core path when it applies, else FMA */
     TA_KERNEL_FMA = 1,   /* FP32 FMA on CUDA cores; every dtype combination */
     TA_KERNEL_MMA = 2    /* tensor-core mma: BF16 q and kv (Hq/Hkv <= 16), or BF16 q with an
-                            E4M3 cache (Hq/Hkv <= 8, head_dim 128) */
+                            E4M3 cache (Hq/Hkv <= 16, head_dim 128) */
 } ta_kernel;
 
 /* Bits of ta_options.flags. */

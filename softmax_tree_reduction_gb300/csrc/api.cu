@@ -175,7 +175,7 @@ int check_shape(const ta_shape* s, Strides* st, int page_size = 0) {
 int resolve_kernel(const ta_shape* s, int requested) {
     const int G = s->num_q_heads / s->num_kv_heads;
     if (s->kv_dtype == TA_E4M3) {
-        const bool ok = s->q_dtype == TA_BF16 && s->head_dim == 128 && G <= 8;
+        const bool ok = s->q_dtype == TA_BF16 && s->head_dim == 128 && G <= 16;
         if (requested == TA_KERNEL_FMA) return TA_ERR_DTYPE;
         if (requested != TA_KERNEL_AUTO && requested != TA_KERNEL_MMA) return TA_ERR_SHAPE;
         return ok ? kKernelFp8 : static_cast<int>(TA_ERR_DTYPE);

@@ -1,6 +1,7 @@
 // Split-KV partial attention over an FP8 (E4M3) KV cache with one scale per KV
-// head, on the tensor cores.  Same blocks, scheduler, warp merge and row merge
-// as the BF16 kernel; what changes is how the operands reach the mma.
+// head, on the tensor cores (one or two n-tiles of 8 columns per KV head).
+// Same blocks, scheduler, warp merge and row merge as the BF16 kernel; what
+// changes is how the operands reach the mma.
 //
 // TMA brings 128-token tiles of 128-byte FP8 rows (128-byte swizzle).  There
 // is no widening pass through shared memory: each thread loads its fragment
@@ -53,7 +54,7 @@ struct Fp8Cfg {
     // fragment stores (rows 2 tig, 2 tig + 1; channels 16 gid + 2 mt (+1))
     // hit 32 distinct banks and the merge reads consecutive positions.
     static constexpr int kMergeStride = D + 4;
-    static_assert(kWarps * 8 * (kMergeStride + 2) * 4 <= kStages * kStageBytes, "merge buffer");
+    static_assert(kWarps * 16 * (kMergeStride + 2) * 4 <= kStages * kStageBytes, "merge buffer (two n-tiles)");
 };
 
 constexpr float kPScale = 16384.f;  // 2^14
@@ -105,7 +106,7 @@ __device__ __forceinline__ float tree_sum(const float* v) {
     }
 }
 
-template <int HB>
+template <int HB, int NT>
 __global__ void __launch_bounds__(Fp8Cfg<HB>::kThreads, 1)
     split_kv_fp8_kernel(const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const SplitParams p) {
@@ -115,9 +116,9 @@ __global__ void __launch_bounds__(Fp8Cfg<HB>::kThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* stages = smem;
-    float* mg_o = reinterpret_cast<float*>(stages);  // [W][8][D (+pad)], after streaming
-    float* mg_m = mg_o + C::kWarps * 8 * C::kMergeStride;
-    float* mg_l = mg_m + C::kWarps * 8;
+    float* mg_o = reinterpret_cast<float*>(stages);  // [W][8*NT][D (+pad)], after streaming
+    float* mg_m = mg_o + C::kWarps * 8 * NT * C::kMergeStride;  // [W][8*NT]
+    float* mg_l = mg_m + C::kWarps * 8 * NT;                    // [W][8*NT]
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
     uint64_t* empty = full + C::kStages;
     volatile StageMeta* meta = reinterpret_cast<volatile StageMeta*>(empty + C::kStages);
@@ -202,21 +203,27 @@ __global__ void __launch_bounds__(Fp8Cfg<HB>::kThreads, 1)
 #pragma unroll
     for (int i = 0; i < HB; ++i) vsc[i] = p.v_scale[g0 + i] / kPScale;
 
-    // q (BF16) of column gid, channels 32 tig .. 32 tig + 31 in the permuted order.
-    float qv[32];
-    {
-        const bool hv = gid < p.G;
-        const int hq = g * p.G + (hv ? gid : 0);
+    // q (BF16): column c = 8 nt + gid of n-tile nt (a query head, or a (head,
+    // query) pair when several queries share the cache), channels 32 tig ..
+    // 32 tig + 31 in the permuted order.
+    float qv[NT][32];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int c = nt * 8 + gid;
+        const bool hv = c < p.G;
+        const int hq = g * p.G + (hv ? c : 0);
         const __nv_bfloat16* qh =
             static_cast<const __nv_bfloat16*>(p.q) + (static_cast<size_t>(b) * p.Hq + hq) * D + 32 * tig;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) qv[j] = hv ? __bfloat162float(qh[j]) : 0.f;
+        for (int j = 0; j < 32; ++j) qv[nt][j] = hv ? __bfloat162float(qh[j]) : 0.f;
     }
     // exact power-of-two scale bringing max|q| into [2^14, 2^15): every q value
     // of the group is held by some lane of this warp
     float amax = 0.f;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(qv[j]));
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(qv[nt][j]));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
     int qexp = 0;
@@ -226,22 +233,35 @@ __global__ void __launch_bounds__(Fp8Cfg<HB>::kThreads, 1)
         qexp = max(-100, min(100, 15 - e));
     }
     const float qs = ldexpf(1.f, qexp);
-    uint32_t qb[D / 16][2];
+    uint32_t qb[NT][D / 16][2];
 #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-        qb[kk][0] = half2_bits(__floats2half2_rn(qv[4 * kk] * qs, qv[4 * kk + 1] * qs));
-        qb[kk][1] = half2_bits(__floats2half2_rn(qv[4 * kk + 2] * qs, qv[4 * kk + 3] * qs));
-    }
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            qb[nt][kk][0] = half2_bits(__floats2half2_rn(qv[nt][4 * kk] * qs, qv[nt][4 * kk + 1] * qs));
+            qb[nt][kk][1] = half2_bits(__floats2half2_rn(qv[nt][4 * kk + 2] * qs, qv[nt][4 * kk + 3] * qs));
+        }
     const float sl2 = p.scale_log2 * ks / qs;
 
+    // causal limits of this thread's columns (2 tig, 2 tig + 1 of each n-tile)
     const int causal_from = p.causal ? N - p.nq + 1 : 0x7fffffff;
-    const int lim0 = p.causal ? causal_from + (2 * tig) % p.nq : 0x7fffffff;
-    const int lim1 = p.causal ? causal_from + (2 * tig + 1) % p.nq : 0x7fffffff;
-
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    float oacc[D / 16][4];
+    int lim[NT][2];
 #pragma unroll
-    for (int mt = 0; mt < D / 16; ++mt) oacc[mt][0] = oacc[mt][1] = oacc[mt][2] = oacc[mt][3] = 0.f;
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+            lim[nt][j] = p.causal ? causal_from + (nt * 8 + 2 * tig + j) % p.nq : 0x7fffffff;
+
+    float m[NT][2], l[NT][2];
+    float oacc[NT][D / 16][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        m[nt][0] = m[nt][1] = -INFINITY;
+        l[nt][0] = l[nt][1] = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt)
+            oacc[nt][mt][0] = oacc[nt][mt][1] = oacc[nt][mt][2] = oacc[nt][mt][3] = 0.f;
+    }
 
     // Rows are 128 B (one swizzle row); chunk c of row r sits at chunk c ^ (r & 7).
     // Offsets within a 16-row slab (slabs start at multiples of 16 rows, so
@@ -292,7 +312,11 @@ __global__ void __launch_bounds__(Fp8Cfg<HB>::kThreads, 1)
                 const uint4 kb0 = lds128(kbase + k_b0), kb1 = lds128(kbase + k_b1);
                 const uint32_t wa[8] = {ka0.x, ka0.y, ka0.z, ka0.w, ka1.x, ka1.y, ka1.z, ka1.w};
                 const uint32_t wb[8] = {kb0.x, kb0.y, kb0.z, kb0.w, kb1.x, kb1.y, kb1.z, kb1.w};
-                float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+                float sa[NT][4], sb[NT][4];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sa[nt][e] = sb[nt][e] = 0.f;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     uint32_t a[4];
@@ -300,57 +324,67 @@ __global__ void __launch_bounds__(Fp8Cfg<HB>::kThreads, 1)
                     a[1] = e4m3x2_to_f16x2(wb[kk] & 0xffffu);
                     a[2] = e4m3x2_to_f16x2(wa[kk] >> 16);
                     a[3] = e4m3x2_to_f16x2(wb[kk] >> 16);
-                    if (kk & 1)
-                        mma_f16(sb, a, qb[kk][0], qb[kk][1]);
-                    else
-                        mma_f16(sa, a, qb[kk][0], qb[kk][1]);
-                }
-                float s0 = (sa[0] + sb[0]) * sl2, s1 = (sa[1] + sb[1]) * sl2;
-                float s2 = (sa[2] + sb[2]) * sl2, s3 = (sa[3] + sb[3]) * sl2;
-                if (nvalid < 16) {
-                    if (gid >= nvalid) s0 = s1 = -INFINITY;
-                    if (gid + 8 >= nvalid) s2 = s3 = -INFINITY;
-                }
-                if (blk0 + 16 > causal_from) {
-                    const int ta = blk0 + gid, tb = ta + 8;
-                    if (ta >= lim0) s0 = -INFINITY;
-                    if (ta >= lim1) s1 = -INFINITY;
-                    if (tb >= lim0) s2 = -INFINITY;
-                    if (tb >= lim1) s3 = -INFINITY;
-                }
-                float bm0 = fmaxf(s0, s2), bm1 = fmaxf(s1, s3);
 #pragma unroll
-                for (int off = 4; off < 32; off <<= 1) {
-                    bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
-                    bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
-                }
-                const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
-                const float ms0 = (mn0 == -INFINITY) ? 0.f : mn0;
-                const float ms1 = (mn1 == -INFINITY) ? 0.f : mn1;
-                const float al0 = ex2(m0 - ms0), al1 = ex2(m1 - ms1);
-                const float p0 = ex2(s0 - ms0), p1 = ex2(s1 - ms1);
-                const float p2 = ex2(s2 - ms0), p3 = ex2(s3 - ms1);
-                l0 = l0 * al0 + (p0 + p2);
-                l1 = l1 * al1 + (p1 + p3);
-                m0 = mn0;
-                m1 = mn1;
-                if (__any_sync(0xffffffffu, (al0 != 1.f) || (al1 != 1.f))) {
-#pragma unroll
-                    for (int mt = 0; mt < D / 16; ++mt) {
-                        oacc[mt][0] *= al0;
-                        oacc[mt][1] *= al1;
-                        oacc[mt][2] *= al0;
-                        oacc[mt][3] *= al1;
+                    for (int nt = 0; nt < NT; ++nt) {
+                        if (kk & 1)
+                            mma_f16(sb[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
+                        else
+                            mma_f16(sa[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
                     }
                 }
-                // P^T (scaled by 2^14) as FP16 hi + lo B fragments
-                const float q0 = p0 * kPScale, q1 = p1 * kPScale, q2 = p2 * kPScale, q3 = p3 * kPScale;
-                const __half2 h01 = __floats2half2_rn(q0, q1), h23 = __floats2half2_rn(q2, q3);
-                const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-                const __half2 e01 = __floats2half2_rn(q0 - f01.x, q1 - f01.y);
-                const __half2 e23 = __floats2half2_rn(q2 - f23.x, q3 - f23.y);
-                const uint32_t bh0 = movtrans(half2_bits(h01)), bh1 = movtrans(half2_bits(h23));
-                const uint32_t bl0 = movtrans(half2_bits(e01)), bl1 = movtrans(half2_bits(e23));
+                const bool causal_blk = blk0 + 16 > causal_from;
+                uint32_t bh[NT][2], bl[NT][2];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    float s0 = (sa[nt][0] + sb[nt][0]) * sl2, s1 = (sa[nt][1] + sb[nt][1]) * sl2;
+                    float s2 = (sa[nt][2] + sb[nt][2]) * sl2, s3 = (sa[nt][3] + sb[nt][3]) * sl2;
+                    if (nvalid < 16) {
+                        if (gid >= nvalid) s0 = s1 = -INFINITY;
+                        if (gid + 8 >= nvalid) s2 = s3 = -INFINITY;
+                    }
+                    if (causal_blk) {
+                        const int ta = blk0 + gid, tb = ta + 8;
+                        if (ta >= lim[nt][0]) s0 = -INFINITY;
+                        if (ta >= lim[nt][1]) s1 = -INFINITY;
+                        if (tb >= lim[nt][0]) s2 = -INFINITY;
+                        if (tb >= lim[nt][1]) s3 = -INFINITY;
+                    }
+                    float bm0 = fmaxf(s0, s2), bm1 = fmaxf(s1, s3);
+#pragma unroll
+                    for (int off = 4; off < 32; off <<= 1) {
+                        bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
+                        bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
+                    }
+                    const float mn0 = fmaxf(m[nt][0], bm0), mn1 = fmaxf(m[nt][1], bm1);
+                    const float ms0 = (mn0 == -INFINITY) ? 0.f : mn0;
+                    const float ms1 = (mn1 == -INFINITY) ? 0.f : mn1;
+                    const float al0 = ex2(m[nt][0] - ms0), al1 = ex2(m[nt][1] - ms1);
+                    const float p0 = ex2(s0 - ms0), p1 = ex2(s1 - ms1);
+                    const float p2 = ex2(s2 - ms0), p3 = ex2(s3 - ms1);
+                    l[nt][0] = l[nt][0] * al0 + (p0 + p2);
+                    l[nt][1] = l[nt][1] * al1 + (p1 + p3);
+                    m[nt][0] = mn0;
+                    m[nt][1] = mn1;
+                    if (__any_sync(0xffffffffu, (al0 != 1.f) || (al1 != 1.f))) {
+#pragma unroll
+                        for (int mt = 0; mt < D / 16; ++mt) {
+                            oacc[nt][mt][0] *= al0;
+                            oacc[nt][mt][1] *= al1;
+                            oacc[nt][mt][2] *= al0;
+                            oacc[nt][mt][3] *= al1;
+                        }
+                    }
+                    // P^T (scaled by 2^14) as FP16 hi + lo B fragments
+                    const float q0 = p0 * kPScale, q1 = p1 * kPScale, q2 = p2 * kPScale, q3 = p3 * kPScale;
+                    const __half2 h01 = __floats2half2_rn(q0, q1), h23 = __floats2half2_rn(q2, q3);
+                    const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+                    const __half2 e01 = __floats2half2_rn(q0 - f01.x, q1 - f01.y);
+                    const __half2 e23 = __floats2half2_rn(q2 - f23.x, q3 - f23.y);
+                    bh[nt][0] = movtrans(half2_bits(h01));
+                    bh[nt][1] = movtrans(half2_bits(h23));
+                    bl[nt][0] = movtrans(half2_bits(e01));
+                    bl[nt][1] = movtrans(half2_bits(e23));
+                }
                 // V: tokens 2tig, 2tig+1, 2tig+8, 2tig+9 of the block, channels 16 gid .. 16 gid + 15;
                 // rows past the valid range may hold anything (even NaN codes): zero them
                 uint4 va = lds128(vbase + v_0), vb = lds128(vbase + v_1);
@@ -373,14 +407,20 @@ __global__ void __launch_bounds__(Fp8Cfg<HB>::kThreads, 1)
                     a[1] = e4m3x2_to_f16x2(p01 >> 16);
                     a[2] = e4m3x2_to_f16x2(r01 & 0xffffu);
                     a[3] = e4m3x2_to_f16x2(r01 >> 16);
-                    mma_f16(oacc[2 * w], a, bh0, bh1);
-                    mma_f16(oacc[2 * w], a, bl0, bl1);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        mma_f16(oacc[nt][2 * w], a, bh[nt][0], bh[nt][1]);
+                        mma_f16(oacc[nt][2 * w], a, bl[nt][0], bl[nt][1]);
+                    }
                     a[0] = e4m3x2_to_f16x2(p23 & 0xffffu);
                     a[1] = e4m3x2_to_f16x2(p23 >> 16);
                     a[2] = e4m3x2_to_f16x2(r23 & 0xffffu);
                     a[3] = e4m3x2_to_f16x2(r23 >> 16);
-                    mma_f16(oacc[2 * w + 1], a, bh0, bh1);
-                    mma_f16(oacc[2 * w + 1], a, bl0, bl1);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        mma_f16(oacc[nt][2 * w + 1], a, bh[nt][0], bh[nt][1]);
+                        mma_f16(oacc[nt][2 * w + 1], a, bl[nt][0], bl[nt][1]);
+                    }
                 }
             }
         }  // slabs
@@ -391,28 +431,35 @@ __global__ void __launch_bounds__(Fp8Cfg<HB>::kThreads, 1)
 
     // ------------------------------------------- merge the warps' states
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-    }
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            l[nt][0] += __shfl_xor_sync(0xffffffffu, l[nt][0], off);
+            l[nt][1] += __shfl_xor_sync(0xffffffffu, l[nt][1], off);
+        }
     consumer_sync(C::kWarps * 32);  // every warp is done reading the stages
     constexpr int MS = C::kMergeStride;
-    float* mo = mg_o + cw * 8 * MS;
+    constexpr int kCols = 8 * NT;  // columns per warp state
+    float* mo = mg_o + cw * kCols * MS;
 #pragma unroll
-    for (int mt = 0; mt < D / 16; ++mt) {
-        // fragment rows gid / gid + 8 are channels 16 gid + 2 mt (+1), stored at
-        // positions (2 mt) * 8 + gid and (2 mt + 1) * 8 + gid
-        const int pos = 16 * mt + gid;
-        mo[(2 * tig) * MS + pos] = oacc[mt][0];
-        mo[(2 * tig + 1) * MS + pos] = oacc[mt][1];
-        mo[(2 * tig) * MS + pos + 8] = oacc[mt][2];
-        mo[(2 * tig + 1) * MS + pos + 8] = oacc[mt][3];
-    }
-    if (gid == 0) {
-        mg_m[cw * 8 + 2 * tig] = m0;
-        mg_m[cw * 8 + 2 * tig + 1] = m1;
-        mg_l[cw * 8 + 2 * tig] = l0;
-        mg_l[cw * 8 + 2 * tig + 1] = l1;
+    for (int nt = 0; nt < NT; ++nt) {
+        const int c0 = nt * 8 + 2 * tig;
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+            // fragment rows gid / gid + 8 are channels 16 gid + 2 mt (+1), stored at
+            // positions (2 mt) * 8 + gid and (2 mt + 1) * 8 + gid
+            const int pos = 16 * mt + gid;
+            mo[c0 * MS + pos] = oacc[nt][mt][0];
+            mo[(c0 + 1) * MS + pos] = oacc[nt][mt][1];
+            mo[c0 * MS + pos + 8] = oacc[nt][mt][2];
+            mo[(c0 + 1) * MS + pos + 8] = oacc[nt][mt][3];
+        }
+        if (gid == 0) {
+            mg_m[cw * kCols + c0] = m[nt][0];
+            mg_m[cw * kCols + c0 + 1] = m[nt][1];
+            mg_l[cw * kCols + c0] = l[nt][0];
+            mg_l[cw * kCols + c0 + 1] = l[nt][1];
+        }
     }
     consumer_sync(C::kWarps * 32);
     const bool poison = bad || (*abort_flag != 0) || (*bad_page != 0);
@@ -431,7 +478,7 @@ __global__ void __launch_bounds__(Fp8Cfg<HB>::kThreads, 1)
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < C::kWPH; ++w) {
-            mw[w] = mg_m[(w0 + w) * 8 + h];
+            mw[w] = mg_m[(w0 + w) * kCols + h];
             M = fmaxf(M, mw[w]);
         }
         const float Ms = (M == -INFINITY) ? 0.f : M;
@@ -439,8 +486,8 @@ __global__ void __launch_bounds__(Fp8Cfg<HB>::kThreads, 1)
 #pragma unroll
         for (int w = 0; w < C::kWPH; ++w) {
             const float wt = ex2(mw[w] - Ms);
-            ow[w] = wt * mg_o[((w0 + w) * 8 + h) * MS + pos];
-            lw[w] = wt * mg_l[(w0 + w) * 8 + h];
+            ow[w] = wt * mg_o[((w0 + w) * kCols + h) * MS + pos];
+            lw[w] = wt * mg_l[(w0 + w) * kCols + h];
         }
         float osc = vsc[0];
 #pragma unroll
@@ -455,11 +502,11 @@ __global__ void __launch_bounds__(Fp8Cfg<HB>::kThreads, 1)
     allow_dependents();
 }
 
-template <int HB>
+template <int HB, int NT>
 cudaError_t launch_hb(const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& p,
                       cudaStream_t stream) {
     using C = Fp8Cfg<HB>;
-    cudaError_t e = cudaFuncSetAttribute(split_kv_fp8_kernel<HB>,
+    cudaError_t e = cudaFuncSetAttribute(split_kv_fp8_kernel<HB, NT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -472,7 +519,7 @@ cudaError_t launch_hb(const CUtensorMap& tk, const CUtensorMap& tv, const SplitP
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, split_kv_fp8_kernel<HB>, tk, tv, p);
+    return cudaLaunchKernelEx(&cfg, split_kv_fp8_kernel<HB, NT>, tk, tv, p);
 }
 
 }  // namespace
@@ -487,10 +534,12 @@ Geometry fp8_geometry(int heads_per_block) {
 
 cudaError_t launch_split_fp8(const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& p,
                              cudaStream_t stream) {
+    // one n-tile of 8 columns per KV head group, two for up to 16
+    const bool two = p.G > 8;
     switch (p.hb) {
-        case 1: return launch_hb<1>(tk, tv, p, stream);
-        case 2: return launch_hb<2>(tk, tv, p, stream);
-        case 4: return launch_hb<4>(tk, tv, p, stream);
+        case 1: return two ? launch_hb<1, 2>(tk, tv, p, stream) : launch_hb<1, 1>(tk, tv, p, stream);
+        case 2: return two ? launch_hb<2, 2>(tk, tv, p, stream) : launch_hb<2, 1>(tk, tv, p, stream);
+        case 4: return two ? launch_hb<4, 2>(tk, tv, p, stream) : launch_hb<4, 1>(tk, tv, p, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -1,7 +1,8 @@
 """FP8 (E4M3) KV caches with one scale per KV head, on the GPU, against the
 float64 oracle over the same codes and scales: ragged rows with NaN padding,
-several split counts, strided and paged caches, several queries per sequence,
-skewed logits, and the fixed (bitwise reproducible) chunk assignment."""
+several split counts, strided and paged caches, several queries per sequence
+(one or two n-tiles of columns), skewed logits, and the fixed (bitwise
+reproducible) chunk assignment."""
 import numpy as np
 import pytest
 import torch
@@ -51,7 +52,7 @@ def _check(out, lse, ref_o, ref_l, what):
         assert np.max(np.abs(l[fin] - ref_l[fin])) <= TOL_LSE, what
 
 
-@pytest.mark.parametrize("G", [1, 2, 4, 8])
+@pytest.mark.parametrize("G", [1, 2, 4, 8, 12, 16])
 def test_fp8_dense_ragged(G):
     lens = [0, 1, 15, 16, 127, 128, 129, 1000, 3001]
     inp = _inputs(lens, 3072, G=G, seed=G)
@@ -120,7 +121,7 @@ def test_fp8_paged(page_size, layout):
         _check(out, lse, ref_o, ref_l, f"paged {page_size} {layout} P={P}")
 
 
-@pytest.mark.parametrize("G,nq", [(1, 2), (4, 2), (2, 4), (1, 8), (8, 1)])
+@pytest.mark.parametrize("G,nq", [(1, 2), (4, 2), (2, 4), (1, 8), (8, 1), (8, 2), (4, 4), (3, 5), (1, 16)])
 @pytest.mark.parametrize("causal", [True, False])
 def test_fp8_multi_query(G, nq, causal):
     inp = _inputs([0, 3, 300, 1700], 1792, G=G, seed=10 * G + nq, nq=nq)
@@ -153,4 +154,27 @@ def test_fp8_argument_errors():
         ta.tree_attn_decode(q, k8, v8, sl, num_splits=1, kernel="fma", k_scale=ks, v_scale=vs)
     with pytest.raises(ValueError):
         ta.tree_attn_decode(q, k8, v8, sl, num_splits=1, k_scale=ks.double(), v_scale=vs)
+    assert ta.tree_attn_get_device_error() == 0
+
+
+@pytest.mark.parametrize("page_size", [16, 32])
+def test_fp8_paged_multi_query_eight_kv_heads(page_size):
+    """16 columns per KV head (two n-tiles) with blocks serving several KV heads
+    of 16/32-token pages, causal over the last 4 positions."""
+    lens = [2000, 5, 700]
+    w = workloads.Workload("fp8mq", len(lens), 32, 8, 128, 2048, torch.bfloat16, torch.bfloat16, seed=page_size,
+                           seqlen=None, ragged_range=(0, 1), pad_nan=True, k_scale=0.5)
+    inp = workloads.make_inputs(w, seqlens=lens)
+    g = torch.Generator().manual_seed(5)
+    q = torch.randn(len(lens), 32, 4, 128, generator=g).to(torch.bfloat16)
+    k8, ks = workloads.quantize_e4m3(inp["k"])
+    v8, vs = workloads.quantize_e4m3(inp["v"])
+    ref_o, ref_l = oracle.attention_e4m3(q, k8, v8, ks, vs, inp["seqlens"], causal=True)
+    kp, vp, bt = workloads.page_pool(k8, v8, inp["seqlens"], page_size, seed=4)
+    for P in (0, 3, 40):
+        out, lse = ta.tree_attn_decode_multi(q.cuda(), kp.cuda(), vp.cuda(), inp["seqlens"].cuda(), causal=True,
+                                             block_table=bt.cuda(), num_splits=P, max_seqlen=2048,
+                                             k_scale=ks.cuda(), v_scale=vs.cuda())
+        torch.cuda.synchronize()
+        _check(out, lse, ref_o, ref_l, f"paged {page_size} P={P}")
     assert ta.tree_attn_get_device_error() == 0

@@ -69,7 +69,7 @@ def shape(ta, **kw):
     (dict(kv_dtype=2), 0),                            # FP8 cache, BF16 q, d128, G=4
     (dict(kv_dtype=2, q_dtype=0), -4),                # FP8 needs BF16 q
     (dict(kv_dtype=2, head_dim=64), -4),              # FP8 path is d = 128
-    (dict(kv_dtype=2, num_q_heads=128), -4),          # FP8 path takes G <= 8
+    (dict(kv_dtype=2, num_q_heads=128), 0),           # FP8 path: G = 16 (two n-tiles)
     (dict(scale=-1.0), -3),
     (dict(scale=float("nan")), -3),
     (dict(kv_stride_b=131072 * 8 * 128, kv_stride_h=128, kv_stride_t=8 * 128), 0),  # token-major
