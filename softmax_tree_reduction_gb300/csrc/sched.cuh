@@ -248,11 +248,56 @@ __device__ void finish_row(const SplitParams& p, int row, size_t hq0, int G, flo
     if (!*flag || !p.fuse) return;
     const int P = p.P;
     const size_t row0 = hq0;
+    constexpr int D4 = D / 4;
+    constexpr int kBatch = 20;     // leaf numerators in flight per thread
+    if (P <= kBatch) {
+        // Few leaves: each thread loads its channel's numerators together with
+        // its head's maxima and denominators (one round trip to L2) and merges
+        // them on its own: no block barrier on the way to the outputs.
+        for (int idx = tid; idx < G * D4; idx += nthr) {
+            const int h = idx / D4, d4 = idx - h * D4;
+            const float4* o = reinterpret_cast<const float4*>(p.part_o + (row0 + h) * P * D) + d4;
+            const float* mrow = p.part_m + (row0 + h) * P;
+            const float* lrow = p.part_l + (row0 + h) * P;
+            float4 v[kBatch];
+            float mq[kBatch], lq[kBatch];
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                v[k] = k < P ? __ldcg(o + static_cast<size_t>(k) * D4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                mq[k] = k < P ? __ldcg(mrow + k) : -INFINITY;
+                lq[k] = k < P ? __ldcg(lrow + k) : 0.f;
+            }
+            float M = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) M = fmaxf(M, mq[k]);
+            const float Ms = (M == -INFINITY) ? 0.f : M;
+            float L = 0.f;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                const float w = (mq[k] == -INFINITY) ? 0.f : ex2((mq[k] - Ms) * kLog2e);
+                L = fmaf(w, lq[k], L);
+                acc.x = fmaf(w, v[k].x, acc.x);
+                acc.y = fmaf(w, v[k].y, acc.y);
+                acc.z = fmaf(w, v[k].z, acc.z);
+                acc.w = fmaf(w, v[k].w, acc.w);
+            }
+            if (L == 0.f) {
+                acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            } else {  // NaN inputs propagate
+                acc.x /= L;
+                acc.y /= L;
+                acc.z /= L;
+                acc.w /= L;
+            }
+            reinterpret_cast<float4*>(p.out + (row0 + h) * D)[d4] = acc;
+            if (d4 == 0 && p.lse) p.lse[row0 + h] = (L > 0.f) ? M + logf(L) : (L == 0.f ? -INFINITY : L);
+        }
+        return;
+    }
     float* sw = scratch;           // [G][P]  maxima, then leaf weights
     float* sl = scratch + G * P;   // [G][P]  denominators
     float* sr = sl + G * P;        // [G] root maxima, [G] root denominators
-    constexpr int D4 = D / 4;
-    constexpr int kBatch = 20;     // leaf numerators in flight per thread
     // The first batch of each thread's numerators is loaded together with the
     // maxima and denominators, so the merge costs one round trip to L2.
     const int idx0 = tid;
