@@ -22,8 +22,9 @@ using ta::Geometry;
 __device__ int g_error_word;  // bits ta::kErrBadSeqlen | ta::kErrTimeout
 
 // Scheduling counters (chunk claims and row tickets) of the split kernels.
-// Zero at load; each call reserves 2*B*Hkv consecutive slots and leaves them
-// at zero when it completes, so slots are reused as the cursor wraps.
+// Zero at load; each call reserves two consecutive slots per schedule row
+// (B * Hkv / heads_per_block rows) and leaves them at zero when it
+// completes, so slots are reused as the cursor wraps.
 constexpr unsigned kRingSlots = 1u << 20;
 __device__ unsigned g_sched_ring[kRingSlots];
 

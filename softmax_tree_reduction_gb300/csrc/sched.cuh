@@ -1,4 +1,5 @@
-// Work distribution inside a (batch row, KV head) sequence and the row's
+// Work distribution inside a schedule row -- one batch row and the KV head
+// (or the hb KV heads sharing each copy) its blocks serve -- and the row's
 // final merge, shared by the split-KV kernels.
 //
 // Scheduling.  With run-time balancing (the default) each of a row's P blocks
@@ -11,6 +12,10 @@
 // is commutative, so this changes nothing in the result.  Without balancing
 // (P == 1, or the deterministic flag) block p streams the contiguous slice
 // [p*c, (p+1)*c), c = ceil(N/P) rounded up to a tile.
+//
+// The row merge: for up to 20 splits each thread merges one channel of one
+// head from a single round trip of loads; beyond that the maxima and
+// denominators are reduced per head in shared memory first.
 //
 // Counters start at zero.  Claims are atomicAdds issued up to two ahead, when
 // the block has at most two chunks of work left in hand, so their latency
