@@ -224,8 +224,8 @@ def test_fp8_needs_scales_before_any_cuda_call(ta):
 
 
 def test_pick_splits_paged_small_pages_share_blocks(ta):
-    """Pages of <= 32 tokens let one block serve several KV heads (one copy per
-    page brings all of them), so the heuristic spreads the row over more slices."""
+    """16-token pages let one block serve several KV heads (one copy per page
+    brings all of them), so the heuristic spreads the row over more slices."""
     bf16 = shape(ta)                      # B1, 32/8 heads, d128, 131072 tokens
     fp8 = shape(ta, kv_dtype=2)
     for s in (bf16, fp8):
@@ -235,13 +235,15 @@ def test_pick_splits_paged_small_pages_share_blocks(ta):
     assert ta.tree_attn_pick_splits(bf16, None, 152, page_size=32) == 19
     # 4 heads per block would need 76 splits (a combine launch): 2 heads, 38 splits
     assert ta.tree_attn_pick_splits(fp8, None, 152, page_size=16) == 38
-    assert ta.tree_attn_pick_splits(fp8, None, 152, page_size=32) == 38    # 2 heads per block
+    assert ta.tree_attn_pick_splits(fp8, None, 152, page_size=32) == 19    # one head per block
     # B4, 64/8 heads: 4 heads per block keeps 19 splits (152 blocks)
     big = shape(ta, kv_dtype=2, batch=4, num_q_heads=64, max_seqlen=262144)
     assert ta.tree_attn_pick_splits(big, None, 152, page_size=16) == 19
-    # a head-major pool ([page][head][token][d]) keeps one head per block
-    hnd = shape(ta, kv_dtype=2, kv_stride_b=8 * 16 * 128, kv_stride_h=16 * 128, kv_stride_t=128)
-    assert ta.tree_attn_pick_splits(hnd, None, 152, page_size=16) == 19
+    # head-major pools ([page][head][token][d]): FP8 still shares blocks, BF16 does not
+    hnd8 = shape(ta, kv_dtype=2, kv_stride_b=8 * 16 * 128, kv_stride_h=16 * 128, kv_stride_t=128)
+    assert ta.tree_attn_pick_splits(hnd8, None, 152, page_size=16) == 38
+    hnd16 = shape(ta, kv_stride_b=8 * 16 * 128, kv_stride_h=16 * 128, kv_stride_t=128)
+    assert ta.tree_attn_pick_splits(hnd16, None, 152, page_size=16) == 19
     # heads per block must divide the KV heads: 2 KV heads cap it at 2
     two = shape(ta, kv_dtype=2, num_q_heads=8, num_kv_heads=2)
     assert ta.tree_attn_pick_splits(two, None, 152, page_size=16) > ta.tree_attn_pick_splits(two, None, 152)
