@@ -178,3 +178,59 @@ def test_fp8_paged_multi_query_eight_kv_heads(page_size):
         torch.cuda.synchronize()
         _check(out, lse, ref_o, ref_l, f"paged {page_size} P={P}")
     assert ta.tree_attn_get_device_error() == 0
+
+
+def _full_groups(w, count, seed):
+    rng = np.random.default_rng(seed)
+    picks = {(0, 0), (w.batch - 1, w.num_kv_heads - 1)}
+    while len(picks) < count:
+        picks.add((int(rng.integers(w.batch)), int(rng.integers(w.num_kv_heads))))
+    return sorted(picks)
+
+
+def _full_fp8(w, sweep, page_size=0, n_groups=3):
+    """Full-size workload with its caches rounded to E4M3 (the bench's --fp8
+    configuration), sampled (row, KV head) groups against the oracle."""
+    inp = workloads.make_inputs(w)
+    k8, ks = workloads.quantize_e4m3(inp["k"])
+    v8, vs = workloads.quantize_e4m3(inp["v"])
+    G = w.group
+    refs = {}
+    for (b, g) in _full_groups(w, n_groups, seed=2):
+        ro, rl = oracle.attention_e4m3(inp["q"][b:b + 1, g * G:(g + 1) * G], k8[b:b + 1, g:g + 1],
+                                       v8[b:b + 1, g:g + 1], ks[g:g + 1], vs[g:g + 1], inp["seqlens"][b:b + 1],
+                                       scale=w.softmax_scale)
+        refs[(b, g)] = (ro[0], rl[0])
+    q, sl = inp["q"].cuda(), inp["seqlens"].cuda()
+    kw = dict(k_scale=ks.cuda(), v_scale=vs.cuda())
+    if page_size:
+        kp, vp, bt = workloads.page_pool(k8, v8, inp["seqlens"], page_size, seed=1)
+        args = (q, kp.cuda(), vp.cuda(), bt.cuda(), sl)
+        call = lambda P: ta.tree_attn_decode_paged(*args, num_splits=P, max_seqlen=w.max_seqlen, **kw)
+    else:
+        k8d, v8d = k8.cuda(), v8.cuda()
+        call = lambda P: ta.tree_attn_decode(q, k8d, v8d, sl, num_splits=P, **kw)
+    for P in [0] + list(sweep):
+        out, lse = call(P)
+        torch.cuda.synchronize()
+        o, l = out.double().cpu().numpy(), lse.double().cpu().numpy()
+        assert np.isfinite(o).all() and np.isfinite(l).all(), P
+        for (b, g), (ro, rl) in refs.items():
+            assert np.max(np.abs(o[b, g * G:(g + 1) * G] - ro)) <= TOL_OUT, (w.name, P, b, g)
+            assert np.max(np.abs(l[b, g * G:(g + 1) * G] - rl)) <= TOL_LSE, (w.name, P, b, g)
+    assert ta.tree_attn_get_device_error() == 0
+
+
+@pytest.mark.slow
+def test_full_llama31_8b_fp8():
+    _full_fp8(workloads.LLAMA31_8B, [8, 19, 64])
+
+
+@pytest.mark.slow
+def test_full_llama31_8b_fp8_paged16():
+    _full_fp8(workloads.LLAMA31_8B, [19, 38], page_size=16)
+
+
+@pytest.mark.slow
+def test_full_llama3_70b_fp8():
+    _full_fp8(workloads.LLAMA3_70B, [19, 64], n_groups=2)
