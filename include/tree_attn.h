@@ -114,6 +114,12 @@ typedef enum {
                                     bitwise reproducible for a given num_splits (balancing,
                                     used by default when the grid is at most four waves of
                                     blocks, changes the rounding order from run to run) */
+#define TA_FLAG_DIAG_STALL 2     /* diagnostic, for testing the failure path: the copy warps
+                                    publish no tile, so every compute warp's bounded wait
+                                    gives up (after about two seconds); the call completes,
+                                    its outputs are NaN and tree_attn_get_device_error
+                                    returns TA_ERR_DEVICE_TIMEOUT.  Nothing faults or hangs,
+                                    and the device stays usable. */
 
 /* Optional per-call settings (pass NULL for defaults). */
 typedef struct {

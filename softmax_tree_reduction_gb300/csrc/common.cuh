@@ -43,6 +43,7 @@ struct SplitParams {
     int num_pages;          // pages in the pool (an out-of-range page reads zeros)
     int box_rows;           // tokens per TMA box: the tile, or the page when it is smaller
     int hb;                 // KV heads per block (a box brings box_rows tokens of each)
+    int stall;              // diagnostic: the producer publishes nothing (waits give up)
     int B, Hq, Hkv, G, S, P; // Hq, G count virtual heads: query heads x queries per row
     int nq;                 // queries per row (q rows are [head][query])
     int causal;             // query i of nq sees tokens < N - nq + 1 + i

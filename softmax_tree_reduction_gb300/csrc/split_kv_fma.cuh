@@ -126,6 +126,10 @@ __global__ void __launch_bounds__(FmaCfg<KV, D>::kThreads, 1)
     }
 
     if (warp == 0) {
+        if (p.stall) {  // diagnostic: publish nothing, so the consumers' waits give up
+            allow_dependents();
+            return;
+        }
         {
             const uint64_t pol = l2_policy_evict_first();
             const bool paged = p.block_table != nullptr;

@@ -169,6 +169,10 @@ __global__ void __launch_bounds__(Fp8Cfg<HB>::kThreads, 1)
     }
 
     if (warp == 0) {
+        if (p.stall) {  // diagnostic: publish nothing, so the consumers' waits give up
+            allow_dependents();
+            return;
+        }
         const uint64_t pol = l2_policy_evict_first();
         const bool paged = p.block_table != nullptr;
         const int page_mask = (1 << p.page_shift) - 1;

@@ -163,6 +163,10 @@ __global__ void __launch_bounds__(MmaCfg<D, HB>::kThreads, 1)
     }
 
     if (warp == 0) {
+        if (p.stall) {  // diagnostic: publish nothing, so the consumers' waits give up
+            allow_dependents();
+            return;
+        }
         // ------------------------------------------------------ producer
         {
             const uint64_t pol = l2_policy_evict_first();

@@ -1,0 +1,51 @@
+"""The failure path of the bounded on-chip waits, exercised without a fault:
+with the diagnostic flag the copy warps publish no tile, every compute warp's
+wait gives up after its time limit, the call still completes, its outputs are
+NaN, tree_attn_get_device_error reports the timeout, and the next call on the
+same context is correct again."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import softmax_tree_reduction_gb300 as ta
+from softmax_tree_reduction_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+def _inputs(kv, d, fp8=False):
+    w = workloads.Workload("stall", 2, 8, 2, d, 1024, kv, kv, seed=3, seqlen=None, ragged_range=(0, 1),
+                           pad_nan=True, k_scale=0.5)
+    inp = workloads.make_inputs(w, seqlens=[1000, 333])
+    if fp8:
+        inp["k"], inp["ks"] = workloads.quantize_e4m3(inp["k"])
+        inp["v"], inp["vs"] = workloads.quantize_e4m3(inp["v"])
+    return inp
+
+
+@pytest.mark.parametrize("family", ["mma", "fma", "fp8"])
+@pytest.mark.parametrize("P", [1, 5])
+def test_stalled_waits_report_timeout_and_leave_the_device_usable(family, P):
+    fp8 = family == "fp8"
+    kv = torch.float32 if family == "fma" else torch.bfloat16
+    inp = _inputs(kv, 128 if family != "fma" else 64, fp8=fp8)
+    q, k, v, sl = (inp[x].cuda() for x in ("q", "k", "v", "seqlens"))
+    kw = dict(k_scale=inp["ks"].cuda(), v_scale=inp["vs"].cuda()) if fp8 else {}
+    kern = "auto" if fp8 else family
+    assert ta.tree_attn_get_device_error() == 0
+    out, lse = ta.tree_attn_decode(q, k, v, sl, num_splits=P, kernel=kern, diag_stall=True, **kw)
+    assert ta.tree_attn_get_device_error() == ta.TA_ERR_DEVICE_TIMEOUT
+    assert torch.isnan(out).all() and torch.isnan(lse).all()
+    assert ta.tree_attn_get_device_error() == 0          # the word was read and cleared
+    # the context and the scheduling counters are usable again
+    out, lse = ta.tree_attn_decode(q, k, v, sl, num_splits=P, kernel=kern, **kw)
+    torch.cuda.synchronize()
+    assert ta.tree_attn_get_device_error() == 0
+    if fp8:
+        ref_o, ref_l = oracle.attention_e4m3(inp["q"], inp["k"], inp["v"], inp["ks"], inp["vs"], inp["seqlens"])
+    else:
+        ref_o, ref_l = oracle.attention(inp["q"], inp["k"], inp["v"], inp["seqlens"])
+    tol = 1e-4 if kv == torch.float32 else 2e-3
+    assert np.max(np.abs(out.double().cpu().numpy() - ref_o)) <= tol
+    assert np.max(np.abs(lse.double().cpu().numpy() - ref_l)) <= max(tol, 1e-3)
