@@ -120,6 +120,11 @@ typedef enum {
                                     its outputs are NaN and tree_attn_get_device_error
                                     returns TA_ERR_DEVICE_TIMEOUT.  Nothing faults or hangs,
                                     and the device stays usable. */
+#define TA_FLAG_DIAG_MISHINT 4   /* diagnostic, for testing: the copy warps' length hint
+                                    (used to start the first copies before the row length
+                                    is read) is made wrong, so those copies are discarded
+                                    and the step streams its real tiles after them; results
+                                    are unchanged */
 
 /* Optional per-call settings (pass NULL for defaults). */
 typedef struct {

@@ -26,6 +26,7 @@ TA_KERNEL = {"auto": 0, "fma": 1, "mma": 2}
 TA_MAX_SPLITS = 4096
 TA_FLAG_DETERMINISTIC = 1
 TA_FLAG_DIAG_STALL = 2
+TA_FLAG_DIAG_MISHINT = 4
 TA_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 _EXPORTS = ["tree_attn_status_string", "tree_attn_version", "tree_attn_check_shape",
@@ -122,8 +123,10 @@ def _dtype_code(dt: torch.dtype) -> int:
     raise TypeError(f"unsupported dtype {dt}; use float32, bfloat16 or float8_e4m3fn (caches)")
 
 
-def _options(kernel, deterministic, k_scale=None, v_scale=None, events=None, diag_stall=False):
-    flags = (TA_FLAG_DETERMINISTIC if deterministic else 0) | (TA_FLAG_DIAG_STALL if diag_stall else 0)
+def _options(kernel, deterministic, k_scale=None, v_scale=None, events=None, diag_stall=False,
+             diag_mishint=False):
+    flags = ((TA_FLAG_DETERMINISTIC if deterministic else 0) | (TA_FLAG_DIAG_STALL if diag_stall else 0)
+             | (TA_FLAG_DIAG_MISHINT if diag_mishint else 0))
     o = TaOptions(TA_KERNEL[kernel], flags, None, None, None, None)
     if events is not None:
         o.split_start_event = events[0].cuda_event
@@ -218,7 +221,7 @@ def tree_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
                      scale: Optional[float] = None, stream=None, split_events=None,
                      want_lse: bool = True, deterministic: bool = False,
                      k_scale: Optional[torch.Tensor] = None, v_scale: Optional[torch.Tensor] = None,
-                     diag_stall: bool = False):
+                     diag_stall: bool = False, diag_mishint: bool = False):
     """Decode attention through the C ABI; returns (out [B,Hq,d] fp32, lse [B,Hq] fp32 or None).
 
     ``num_splits`` <= 0 uses the library's heuristic (picked on the host so the
@@ -227,6 +230,8 @@ def tree_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
     fixed chunk assignment (bitwise reproducible results for a given split count).
     ``diag_stall`` (testing only) makes every on-chip wait give up: NaN outputs and
     TA_ERR_DEVICE_TIMEOUT from tree_attn_get_device_error, after about two seconds.
+    ``diag_mishint`` (testing only) makes the copy warps' length hint wrong, so their
+    first copies are discarded; the results must not change.
     """
     lib = load()
     _check_cuda(q, k_cache, v_cache, seqlens, out, lse, workspace)
@@ -252,7 +257,8 @@ def tree_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     st = _stream(stream)
-    if kernel == "auto" and split_events is None and not deterministic and k_scale is None and not diag_stall:
+    if (kernel == "auto" and split_events is None and not deterministic and k_scale is None and not diag_stall
+            and not diag_mishint):
         rc = lib.tree_attn_decode(ctypes.byref(shape), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                   _ptr(seqlens), _ptr(out), _ptr(lse), P, _ptr(workspace),
                                   ws_bytes, st)
@@ -263,7 +269,7 @@ def tree_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
             torch_stream = stream if isinstance(stream, torch.cuda.Stream) else torch.cuda.current_stream()
             for ev in split_events:
                 ev.record(torch_stream)
-        opts = _options(kernel, deterministic, k_scale, v_scale, split_events, diag_stall)
+        opts = _options(kernel, deterministic, k_scale, v_scale, split_events, diag_stall, diag_mishint)
         rc = lib.tree_attn_decode_ex(ctypes.byref(shape), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                      _ptr(seqlens), _ptr(out), _ptr(lse), P, _ptr(workspace),
                                      ws_bytes, ctypes.byref(opts), st)

@@ -419,7 +419,7 @@ int decode_impl(const ta_shape* shape, const ta_paged_kv* paged, int nq, int cau
     if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
         !aligned(seqlens, 4) || (lse && !aligned(lse, 4)))
         return TA_ERR_ALIGN;
-    if (options && (options->flags & ~(TA_FLAG_DETERMINISTIC | TA_FLAG_DIAG_STALL)) != 0) return TA_ERR_SHAPE;
+    if (options && (options->flags & ~(TA_FLAG_DETERMINISTIC | TA_FLAG_DIAG_STALL | TA_FLAG_DIAG_MISHINT)) != 0) return TA_ERR_SHAPE;
     const bool deterministic = options && (options->flags & TA_FLAG_DETERMINISTIC);
     const int kernel = resolve_kernel(shape, options ? options->kernel : TA_KERNEL_AUTO);
     if (kernel < 0) return kernel;
@@ -488,6 +488,7 @@ int decode_impl(const ta_shape* shape, const ta_paged_kv* paged, int nq, int cau
     p.box_rows = rows;
     p.hb = hb;
     p.stall = (options && (options->flags & TA_FLAG_DIAG_STALL)) ? 1 : 0;
+    p.mishint = (options && (options->flags & TA_FLAG_DIAG_MISHINT)) ? 1 : 0;
     p.num_pages = shape->batch;
     if (paged) {
         p.block_table = paged->block_table;
@@ -636,7 +637,7 @@ int tree_attn_decode_multi(const ta_shape* shape, const ta_paged_kv* paged, int 
 int tree_attn_launch_count(const ta_shape* shape, int num_splits, const ta_options* options) {
     int rc = check_shape(shape, nullptr);
     if (rc != TA_OK) return rc;
-    if (options && (options->flags & ~(TA_FLAG_DETERMINISTIC | TA_FLAG_DIAG_STALL)) != 0) return TA_ERR_SHAPE;
+    if (options && (options->flags & ~(TA_FLAG_DETERMINISTIC | TA_FLAG_DIAG_STALL | TA_FLAG_DIAG_MISHINT)) != 0) return TA_ERR_SHAPE;
     const int kernel = resolve_kernel(shape, options ? options->kernel : TA_KERNEL_AUTO);
     if (kernel < 0) return kernel;
     int P = num_splits;

@@ -44,6 +44,7 @@ struct SplitParams {
     int box_rows;           // tokens per TMA box: the tile, or the page when it is smaller
     int hb;                 // KV heads per block (a box brings box_rows tokens of each)
     int stall;              // diagnostic: the producer publishes nothing (waits give up)
+    int mishint;            // diagnostic: the producer's length hint is made wrong
     int B, Hq, Hkv, G, S, P; // Hq, G count virtual heads: query heads x queries per row
     int nq;                 // queries per row (q rows are [head][query])
     int causal;             // query i of nq sees tokens < N - nq + 1 + i
@@ -90,6 +91,13 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, unsigned by
         "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
         "r"(bytes)
         : "memory");
+}
+
+// Adds `bytes` to the transaction count of the current phase without
+// arriving: the phase cannot complete before a later arrive.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, unsigned bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {

@@ -81,15 +81,16 @@ __device__ __forceinline__ void slice_bounds(const SplitParams& p, int N, int sp
 // only picks addresses (clamped to the row and the pool); the data itself is
 // loaded after the wait, from L2, which holds any newer writes.  This fills
 // the time in which the previous grid's last blocks merge and DRAM is idle.
+// Returns the row length it read (the hint), in [0, S].
 template <typename Prefetch>
-__device__ void prefetch_row_head(const SplitParams& p, int b, int split, int tile, int ntiles,
-                                  Prefetch&& pf) {
+__device__ int prefetch_row_head(const SplitParams& p, int b, int split, int tile, int ntiles,
+                                 Prefetch&& pf) {
     const int lane = threadIdx.x & 31;
     const int N = max(0, min(ld_relaxed(p.seqlens + b), p.S));
     int t, t_end, base;
     slice_bounds(p, N, split, tile, &t, &t_end, &base);
     const int nbox = p.block_table ? tile / p.box_rows : 1;
-    if (lane >= nbox) return;
+    if (lane >= nbox) return N;
     for (int i = 0; i < ntiles && t < t_end; ++i, t += tile) {
         int page = 0;
         if (p.block_table) {
@@ -100,6 +101,7 @@ __device__ void prefetch_row_head(const SplitParams& p, int b, int split, int ti
         }
         pf(t, lane, page);
     }
+    return N;
 }
 
 // Producer warp (all 32 lanes): stream this block's tiles into the stage ring.
@@ -110,17 +112,58 @@ __device__ void prefetch_row_head(const SplitParams& p, int b, int split, int ti
 // so each lane's block-table entry loads while the previous tile is issued.
 // Returns false if a wait timed out (the error word is set; the warp still
 // drains).
+//
+// Dense caches: the first ring of tiles is issued from `N_hint` (the length
+// read before the dependency wait, or -1) while the real length N is still
+// in flight.  Those stages get their transaction bytes but not the arrive
+// that completes them; once N is known they are released as they are (same
+// tiles) or with nvalid = 0 (the consumers skip them), and the schedule
+// continues after them.
 template <int kStages, typename Issue>
-__device__ bool produce_row(const SplitParams& p, int b, int row, int N, int split, int tile,
-                            uint64_t* full, uint64_t* empty, volatile StageMeta* meta,
+__device__ bool produce_row(const SplitParams& p, int b, int row, const int& N_ref, int N_hint, int split,
+                            int tile, uint64_t* full, uint64_t* empty, volatile StageMeta* meta,
                             volatile unsigned* sink, volatile int* bad_flag, unsigned stage_bytes,
                             Issue&& issue) {
     const int lane = threadIdx.x & 31;
     const int C = tile * p.chunk_tiles;  // tokens per claimed chunk
     const bool dynamic = p.claim != nullptr;
     const int nbox = p.block_table ? tile / p.box_rows : 1;
+    int spec = 0, spec_t = 0, spec_end = 0;
+    if (p.mishint && N_hint > 0) N_hint = N_hint / 2 + 1;  // diagnostic: a stale hint
+    if (!p.block_table && N_hint > 0) {
+        int hb_;
+        slice_bounds(p, N_hint, split, tile, &spec_t, &spec_end, &hb_);
+        spec = min(kStages, (spec_end - spec_t + tile - 1) / tile);
+        for (int i = 0; i < spec; ++i) {
+            const int t0 = spec_t + i * tile;
+            if (lane == 0) {
+                meta[i].tok0 = t0;
+                meta[i].nvalid = min(tile, spec_end - t0);
+                mbar_expect_tx(&full[i], stage_bytes);
+            }
+            __syncwarp();
+            if (lane < nbox) issue(i, t0, lane, 0);
+        }
+    }
+    // the real length (its load was issued before the copies above); a length
+    // outside [0, S] streams nothing (the consumers report it)
+    const int N = (N_ref < 0 || N_ref > p.S) ? 0 : N_ref;
     int t, t_end, base;
     slice_bounds(p, N, split, tile, &t, &t_end, &base);
+    int it = 0;
+    if (spec > 0) {
+        // same tiles iff the slice starts at the same token and the covered
+        // ranges end at the same place
+        const bool same = (spec_t == t) && (min(spec_end, spec_t + spec * tile) == min(t_end, t + spec * tile));
+        if (lane == 0) {
+            for (int i = 0; i < spec; ++i) {
+                if (!same) meta[i].nvalid = 0;
+                mbar_arrive(&full[i]);
+            }
+        }
+        if (same) t += spec * tile;
+        it = spec;
+    }
     const int npool = dynamic ? (N - base + C - 1) / C : 0;  // chunks handed out by the counter
     bool exhausted = (npool == 0);
     unsigned pend0 = 0, pend1 = 0;  // claims in flight (lane 0's registers), oldest first
@@ -162,7 +205,6 @@ __device__ bool produce_row(const SplitParams& p, int b, int row, int N, int spl
     };
 
     bool bad = false;
-    int it = 0;
     bool ok = true;
     int cur_end = 0, nxt_end = 0;
     int cur = next_tile(&cur_end);

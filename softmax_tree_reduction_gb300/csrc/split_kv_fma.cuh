@@ -100,9 +100,10 @@ __global__ void __launch_bounds__(FmaCfg<KV, D>::kThreads, 1)
         prefetch_tensormap(&tmK);
         prefetch_tensormap(&tmV);
     }
+    int n_hint = -1;  // row length read before the dependency wait (a hint)
     if (warp == 0) {  // first tiles into L2 while the previous grid drains
         const int page_mask = (1 << p.page_shift) - 1;
-        prefetch_row_head(p, b, split, C::kTile, p.prefetch_tiles, [&](int y, int j, int page) {
+        n_hint = prefetch_row_head(p, b, split, C::kTile, p.prefetch_tiles, [&](int y, int j, int page) {
             if (!p.block_table) {
                 tma_prefetch_4d(&tmK, 0, y, g, b);
                 tma_prefetch_4d(&tmV, 0, y, g, b);
@@ -118,12 +119,7 @@ __global__ void __launch_bounds__(FmaCfg<KV, D>::kThreads, 1)
     // the prefetch, nothing an earlier kernel may write is read before this.
     wait_primary();
 
-    int N = p.seqlens[b];
-    const bool bad = (N < 0) || (N > p.S);
-    if (bad) {
-        if (threadIdx.x == 0) atomicOr(p.err, kErrBadSeqlen);
-        N = 0;
-    }
+    const int n_raw = p.seqlens[b];  // validated by each side where it is used
 
     if (warp == 0) {
         if (p.stall) {  // diagnostic: publish nothing, so the consumers' waits give up
@@ -135,7 +131,7 @@ __global__ void __launch_bounds__(FmaCfg<KV, D>::kThreads, 1)
             const bool paged = p.block_table != nullptr;
             const int page_mask = (1 << p.page_shift) - 1;
             produce_row<C::kStages>(
-                p, b, b * p.Hkv + g, N, split, C::kTile, full, empty, meta, claim_sink, bad_page,
+                p, b, b * p.Hkv + g, n_raw, n_hint, split, C::kTile, full, empty, meta, claim_sink, bad_page,
                 C::kStageBytes, [&](int s, int y, int j, int page) {
                     uint8_t* st = stages + s * C::kStageBytes;
                     if (!paged) {
@@ -154,6 +150,12 @@ __global__ void __launch_bounds__(FmaCfg<KV, D>::kThreads, 1)
     }
 
     // ---------------------------------------------------------- consumers
+    int N = n_raw;
+    const bool bad = (N < 0) || (N > p.S);
+    if (bad) {
+        if (threadIdx.x == 32) atomicOr(p.err, kErrBadSeqlen);
+        N = 0;
+    }
     const int G = p.G;
     const int NHC = G / GC;                  // head chunks (1, 2 or 4)
     const int NTS = C::kWarps / NHC;         // token slices of a stage

@@ -145,9 +145,10 @@ __global__ void __launch_bounds__(Fp8Cfg<HB>::kThreads, 1)
         prefetch_tensormap(&tmK);
         prefetch_tensormap(&tmV);
     }
+    int n_hint = -1;  // row length read before the dependency wait (a hint)
     if (warp == 0) {  // first tiles into L2 while the previous grid drains
         const int page_mask = (1 << p.page_shift) - 1;
-        prefetch_row_head(p, b, split, C::kTile, p.prefetch_tiles, [&](int y, int j, int page) {
+        n_hint = prefetch_row_head(p, b, split, C::kTile, p.prefetch_tiles, [&](int y, int j, int page) {
             if (!p.block_table) {
                 tma_prefetch_4d(&tmK, 0, y, g0, b);
                 tma_prefetch_4d(&tmV, 0, y, g0, b);
@@ -161,12 +162,7 @@ __global__ void __launch_bounds__(Fp8Cfg<HB>::kThreads, 1)
     __syncthreads();
     wait_primary();  // apart from the prefetch's address hints, nothing an earlier kernel writes is read before this
 
-    int N = p.seqlens[b];
-    const bool bad = (N < 0) || (N > p.S);
-    if (bad) {
-        if (threadIdx.x == 0) atomicOr(p.err, kErrBadSeqlen);
-        N = 0;
-    }
+    const int n_raw = p.seqlens[b];  // validated by each side where it is used
 
     if (warp == 0) {
         if (p.stall) {  // diagnostic: publish nothing, so the consumers' waits give up
@@ -179,7 +175,7 @@ __global__ void __launch_bounds__(Fp8Cfg<HB>::kThreads, 1)
         // box j = box_rows tokens of the HB heads, [head][row][128 B], at j * box_bytes
         const int box_bytes = HB * p.box_rows * D;
         produce_row<C::kStages>(
-            p, b, row, N, split, C::kTile, full, empty, meta, claim_sink, bad_page,
+            p, b, row, n_raw, n_hint, split, C::kTile, full, empty, meta, claim_sink, bad_page,
             C::kStageBytes, [&](int s, int y, int j, int page) {
                 uint8_t* st = stages + s * C::kStageBytes;
                 const int off = j * box_bytes;
@@ -197,6 +193,12 @@ __global__ void __launch_bounds__(Fp8Cfg<HB>::kThreads, 1)
     }
 
     // ---------------------------------------------------------- consumers
+    int N = n_raw;
+    const bool bad = (N < 0) || (N > p.S);
+    if (bad) {
+        if (threadIdx.x == 32) atomicOr(p.err, kErrBadSeqlen);
+        N = 0;
+    }
     const int cw = warp - 1;
     const int gid = lane >> 2, tig = lane & 3;
     const int hw = cw / C::kWPH, wi = cw % C::kWPH;  // this warp's head within the block

@@ -136,9 +136,10 @@ __global__ void __launch_bounds__(MmaCfg<D, HB>::kThreads, 1)
         prefetch_tensormap(&tmK);
         prefetch_tensormap(&tmV);
     }
+    int n_hint = -1;  // row length read before the dependency wait (a hint)
     if (warp == 0) {
         const int page_mask = (1 << p.page_shift) - 1;
-        prefetch_row_head(p, b, split, C::kTile, p.prefetch_tiles, [&](int y, int j, int page) {
+        n_hint = prefetch_row_head(p, b, split, C::kTile, p.prefetch_tiles, [&](int y, int j, int page) {
             if (!p.block_table) {
                 tma_prefetch_5d(&tmK, 0, y, 0, g0, b);
                 tma_prefetch_5d(&tmV, 0, y, 0, g0, b);
@@ -155,12 +156,7 @@ __global__ void __launch_bounds__(MmaCfg<D, HB>::kThreads, 1)
     // lengths, the outputs) is read before this.
     wait_primary();
 
-    int N = p.seqlens[b];
-    const bool bad = (N < 0) || (N > p.S);
-    if (bad) {
-        if (threadIdx.x == 0) atomicOr(p.err, kErrBadSeqlen);
-        N = 0;
-    }
+    const int n_raw = p.seqlens[b];  // validated by each side where it is used
 
     if (warp == 0) {
         if (p.stall) {  // diagnostic: publish nothing, so the consumers' waits give up
@@ -174,7 +170,7 @@ __global__ void __launch_bounds__(MmaCfg<D, HB>::kThreads, 1)
             const int page_mask = (1 << p.page_shift) - 1;
             const int box_bytes = HB * C::kHalves * p.box_rows * 128;
             produce_row<C::kStages>(
-                p, b, row, N, split, C::kTile, full, empty, meta, claim_sink, bad_page,
+                p, b, row, n_raw, n_hint, split, C::kTile, full, empty, meta, claim_sink, bad_page,
                 C::kStageBytes, [&](int s, int y, int j, int page) {
                     // One box = box_rows tokens x all channels of the HB heads, laid out
                     // in shared memory as [head][half][box_rows][128 B]; box j of a
@@ -197,6 +193,12 @@ __global__ void __launch_bounds__(MmaCfg<D, HB>::kThreads, 1)
     }
 
     // ---------------------------------------------------------- consumers
+    int N = n_raw;
+    const bool bad = (N < 0) || (N > p.S);
+    if (bad) {
+        if (threadIdx.x == 32) atomicOr(p.err, kErrBadSeqlen);
+        N = 0;
+    }
     const int cw = warp - 1;
     const int gid = lane >> 2, tig = lane & 3;
     const int r8 = lane & 7;

@@ -1,8 +1,13 @@
-"""The failure path of the bounded on-chip waits, exercised without a fault:
-with the diagnostic flag the copy warps publish no tile, every compute warp's
-wait gives up after its time limit, the call still completes, its outputs are
-NaN, tree_attn_get_device_error reports the timeout, and the next call on the
-same context is correct again."""
+"""Paths that normal inputs rarely take, forced by diagnostic flags (no fault,
+no hang):
+
+* the failure path of the bounded on-chip waits: the copy warps publish no
+  tile, every compute warp's wait gives up after its time limit, the call still
+  completes, its outputs are NaN, tree_attn_get_device_error reports the
+  timeout, and the next call on the same context is correct again;
+* a wrong length hint: the first copies, issued before the row length is read,
+  are discarded and the real tiles streamed after them; results are unchanged
+  (bitwise, with the deterministic flag)."""
 import numpy as np
 import pytest
 import torch
@@ -49,3 +54,27 @@ def test_stalled_waits_report_timeout_and_leave_the_device_usable(family, P):
     tol = 1e-4 if kv == torch.float32 else 2e-3
     assert np.max(np.abs(out.double().cpu().numpy() - ref_o)) <= tol
     assert np.max(np.abs(lse.double().cpu().numpy() - ref_l)) <= max(tol, 1e-3)
+
+
+@pytest.mark.parametrize("family", ["mma", "fma", "fp8"])
+@pytest.mark.parametrize("P", [1, 5, 19])
+def test_wrong_length_hint_changes_nothing(family, P):
+    fp8 = family == "fp8"
+    kv = torch.float32 if family == "fma" else torch.bfloat16
+    inp = _inputs(kv, 128 if family != "fma" else 64, fp8=fp8)
+    q, k, v, sl = (inp[x].cuda() for x in ("q", "k", "v", "seqlens"))
+    kw = dict(k_scale=inp["ks"].cuda(), v_scale=inp["vs"].cuda()) if fp8 else {}
+    kern = "auto" if fp8 else family
+    o1, l1 = ta.tree_attn_decode(q, k, v, sl, num_splits=P, kernel=kern, deterministic=True, **kw)
+    o2, l2 = ta.tree_attn_decode(q, k, v, sl, num_splits=P, kernel=kern, deterministic=True, diag_mishint=True, **kw)
+    o3, l3 = ta.tree_attn_decode(q, k, v, sl, num_splits=P, kernel=kern, diag_mishint=True, **kw)
+    torch.cuda.synchronize()
+    assert ta.tree_attn_get_device_error() == 0
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    if fp8:
+        ref_o, ref_l = oracle.attention_e4m3(inp["q"], inp["k"], inp["v"], inp["ks"], inp["vs"], inp["seqlens"])
+    else:
+        ref_o, ref_l = oracle.attention(inp["q"], inp["k"], inp["v"], inp["seqlens"])
+    tol = 1e-4 if kv == torch.float32 else 2e-3
+    assert np.max(np.abs(o3.double().cpu().numpy() - ref_o)) <= tol
+    assert np.max(np.abs(l3.double().cpu().numpy() - ref_l)) <= max(tol, 1e-3)

@@ -155,7 +155,7 @@ def test_decode_argument_errors_before_any_cuda_call(ta):
     assert _decode_raw(ta, f32, opts=ta.TaOptions(2, 0, None, None, None, None)) == -4   # mma needs bf16
     assert _decode_raw(ta, shape(ta, num_q_heads=256, num_kv_heads=8),
                        opts=ta.TaOptions(2, 0, None, None, None, None)) == -3          # G = 32 > 16
-    assert _decode_raw(ta, s, opts=ta.TaOptions(0, 4, None, None, None, None)) == -3  # unknown flag bit
+    assert _decode_raw(ta, s, opts=ta.TaOptions(0, 8, None, None, None, None)) == -3  # unknown flag bit
     assert _decode_raw(ta, s, opts=ta.TaOptions(9, 0, None, None, None, None)) == -3  # unknown kernel
 
 
