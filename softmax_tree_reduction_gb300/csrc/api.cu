@@ -8,7 +8,9 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <memory>
 #include <mutex>
+#include <new>
 #include <queue>
 #include <vector>
 
@@ -66,6 +68,7 @@ struct DeviceState {
     int* err = nullptr;        // device address of g_error_word on this device
     unsigned* ring = nullptr;  // device address of g_sched_ring on this device
     unsigned cursor = 0;       // next free ring slot
+    int device = 0;            // this entry's CUDA device
 };
 
 std::mutex g_mu;
@@ -86,6 +89,7 @@ int device_state(DeviceState** out) {
         void* r = nullptr;
         if (cudaGetSymbolAddress(&r, g_sched_ring) != cudaSuccess) return TA_ERR_CUDA;
         s.num_sms = sms;
+        s.device = dev;
         s.err = static_cast<int*>(p);
         s.ring = static_cast<unsigned*>(r);
         s.ready = true;
@@ -350,8 +354,8 @@ int pick_splits_impl(const ta_shape* s, const int32_t* host_seqlens, int num_sms
 // 4-D map over (channel, token, KV head, batch row) -- or, for a page pool,
 // (channel, token in page, KV head, physical page).  Box: box_x channels x
 // `rows` tokens.
-int encode_kv_map(CUtensorMap* map, const void* base, const ta_shape* s, const Strides& st,
-                  const Geometry& geo, const ta_paged_kv* paged, int rows) {
+int encode_kv_map_uncached(CUtensorMap* map, const void* base, const ta_shape* s, const Strides& st,
+                           const Geometry& geo, const ta_paged_kv* paged, int rows) {
     auto fn = encode_fn();
     if (!fn) return TA_ERR_CUDA;
     const int64_t es = elem_bytes(s->kv_dtype);
@@ -386,6 +390,70 @@ int encode_kv_map(CUtensorMap* map, const void* base, const ta_shape* s, const S
                           geo.swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? TA_OK : TA_ERR_CUDA;
+}
+
+// Every input of a tensor-map encode: a map is a pure function of these, so a
+// cached map stays valid for as long as the same inputs come back (decode
+// steps reuse the same cache buffers and sizes).
+struct MapKey {
+    const void* base;
+    int64_t dims[4], strides[3];
+    int32_t dtype, rows, box_x, swizzle128, halves5d, hb;
+};
+
+struct MapSlot {
+    MapKey key;
+    CUtensorMap map;
+    bool valid;
+};
+
+constexpr int kMapSlots = 1024;  // direct-mapped, per device (allocated on first use)
+
+std::unique_ptr<MapSlot[]> g_maps[kMaxDevices];
+
+uint64_t hash_key(const MapKey& k) {
+    const unsigned char* b = reinterpret_cast<const unsigned char*>(&k);
+    uint64_t h = 1469598103934665603ull;  // FNV-1a
+    for (size_t i = 0; i < sizeof k; ++i) h = (h ^ b[i]) * 1099511628211ull;
+    return h;
+}
+
+int encode_kv_map(int dev, CUtensorMap* map, const void* base, const ta_shape* s, const Strides& st,
+                  const Geometry& geo, const ta_paged_kv* paged, int rows) {
+    MapKey k;
+    std::memset(&k, 0, sizeof k);  // padding bytes take part in the hash and the compare
+    k.base = base;
+    k.dims[0] = s->head_dim;
+    k.dims[1] = paged ? paged->page_size : s->max_seqlen;
+    k.dims[2] = s->num_kv_heads;
+    k.dims[3] = paged ? paged->num_pages : s->batch;
+    k.strides[0] = st.t;
+    k.strides[1] = st.h;
+    k.strides[2] = st.b;
+    k.dtype = s->kv_dtype;
+    k.rows = rows;
+    k.box_x = geo.box_x;
+    k.swizzle128 = geo.swizzle128;
+    k.halves5d = geo.halves5d;
+    k.hb = geo.heads_per_block;
+    const size_t i = hash_key(k) % kMapSlots;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (!g_maps[dev]) g_maps[dev].reset(new (std::nothrow) MapSlot[kMapSlots]());
+        if (g_maps[dev] && g_maps[dev][i].valid && std::memcmp(&g_maps[dev][i].key, &k, sizeof k) == 0) {
+            *map = g_maps[dev][i].map;
+            return TA_OK;
+        }
+    }
+    const int rc = encode_kv_map_uncached(map, base, s, st, geo, paged, rows);
+    if (rc != TA_OK) return rc;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_maps[dev]) {
+        g_maps[dev][i].key = k;
+        g_maps[dev][i].map = *map;
+        g_maps[dev][i].valid = true;
+    }
+    return TA_OK;
 }
 
 }  // namespace
@@ -457,9 +525,9 @@ int decode_impl(const ta_shape* shape, const ta_paged_kv* paged, int nq, int cau
     const int rows = paged ? std::min(geo.tile_tokens, paged->page_size) : geo.tile_tokens;
     if (geo.tile_tokens / rows > 32) return TA_ERR_SHAPE;  // one producer lane per box
     CUtensorMap tk, tv;
-    rc = encode_kv_map(&tk, k_cache, shape, st, geo, paged, rows);
+    rc = encode_kv_map(ds->device, &tk, k_cache, shape, st, geo, paged, rows);
     if (rc != TA_OK) return rc;
-    rc = encode_kv_map(&tv, v_cache, shape, st, geo, paged, rows);
+    rc = encode_kv_map(ds->device, &tv, v_cache, shape, st, geo, paged, rows);
     if (rc != TA_OK) return rc;
 
     ta::SplitParams p;

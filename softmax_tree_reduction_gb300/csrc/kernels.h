@@ -4,9 +4,26 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "common.cuh"
 
 namespace ta {
+
+// Raises a kernel's dynamic shared-memory limit once per device (the setting
+// persists), instead of on every launch.  `done` is the kernel's own bit set
+// of devices already configured.
+template <typename Kernel>
+cudaError_t set_smem_once(Kernel kernel, int bytes, std::atomic<unsigned long long>& done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
 
 // How a split-KV kernel wants its K/V tiles delivered by TMA.
 struct Geometry {

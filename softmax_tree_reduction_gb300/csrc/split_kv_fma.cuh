@@ -319,8 +319,8 @@ template <typename KV, int D, int GC>
 cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& p,
                        cudaStream_t stream) {
     using C = FmaCfg<KV, D>;
-    cudaError_t e = cudaFuncSetAttribute(split_kv_fma_kernel<KV, D, GC>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    static std::atomic<unsigned long long> configured{0};
+    cudaError_t e = set_smem_once(split_kv_fma_kernel<KV, D, GC>, C::kSmem, configured);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.P, p.Hkv, p.B);

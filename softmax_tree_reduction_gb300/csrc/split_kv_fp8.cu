@@ -512,8 +512,8 @@ template <int HB, int NT>
 cudaError_t launch_hb(const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& p,
                       cudaStream_t stream) {
     using C = Fp8Cfg<HB>;
-    cudaError_t e = cudaFuncSetAttribute(split_kv_fp8_kernel<HB, NT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    static std::atomic<unsigned long long> configured{0};
+    cudaError_t e = set_smem_once(split_kv_fp8_kernel<HB, NT>, C::kSmem, configured);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.P, p.Hkv / HB, p.B);

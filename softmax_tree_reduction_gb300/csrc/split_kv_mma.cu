@@ -447,8 +447,8 @@ template <int D, int NT, int HB>
 cudaError_t launch_impl(const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& p,
                         cudaStream_t stream) {
     using C = MmaCfg<D, HB>;
-    cudaError_t e = cudaFuncSetAttribute(split_kv_mma_kernel<D, NT, HB>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    static std::atomic<unsigned long long> configured{0};
+    cudaError_t e = set_smem_once(split_kv_mma_kernel<D, NT, HB>, C::kSmem, configured);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.P, p.Hkv / HB, p.B);
