@@ -85,6 +85,8 @@ def parse_args(argv=None):
                     help="sweeps: capture the timed steps in one CUDA graph (removes the host's per-call cost)")
     ap.add_argument("--fp8", action="store_true",
                     help="FP8 E4M3 caches (the workload's K and V rounded with one scale per KV head)")
+    ap.add_argument("--cluster-merge", action="store_true",
+                    help="each row's (2..8) blocks merge through a thread-block cluster's shared memory")
     ap.add_argument("--deterministic", action="store_true",
                     help="fixed chunk assignment (bitwise reproducible) instead of run-time balancing")
     return ap.parse_args(argv)
@@ -297,7 +299,7 @@ def run_ours(args, rank, world, local):
         kv_names = kv_names + ("k_scale", "v_scale")
     kv_bytes = w.kv_bytes(inp["seqlens"])
     dev = {k: inp[k].cuda() for k in kv_names}
-    scales = dict(k_scale=dev.get("k_scale"), v_scale=dev.get("v_scale"))
+    scales = dict(k_scale=dev.get("k_scale"), v_scale=dev.get("v_scale"), cluster_merge=args.cluster_merge)
     if args.paged:
         kp, vp, bt = workloads.page_pool(inp["k"], inp["v"], inp["seqlens"], args.paged, seed=w.seed,
                                          layout=args.paged_layout)
@@ -315,6 +317,8 @@ def run_ours(args, rank, world, local):
         shape = ta.TaShape.from_buffer_copy(shape)
         shape.num_q_heads *= args.queries
     P = args.num_splits if args.num_splits > 0 else ta.tree_attn_pick_splits(shape, page_size=args.paged)
+    if args.cluster_merge and args.num_splits <= 0:
+        P = min(P, 8)  # one cluster per row: at most 8 blocks
     kernel_used = args.kernel
     if args.fp8:
         kernel_used = "fp8"
@@ -399,7 +403,7 @@ def run_ours(args, rank, world, local):
         host = {k: (dev[k].cpu() if args.paged and k in ("k", "v", "block_table") else inp[k]).pin_memory()
                 for k in (kv_names + ("block_table",) if args.paged else kv_names)}
         dbuf = {k: torch.empty_like(host[k], device="cuda") for k in host}
-        dscales = dict(k_scale=dbuf.get("k_scale"), v_scale=dbuf.get("v_scale"))
+        dscales = dict(k_scale=dbuf.get("k_scale"), v_scale=dbuf.get("v_scale"), cluster_merge=args.cluster_merge)
         h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
         h2d = sum(t.numel() * t.element_size() for t in host.values())
@@ -463,6 +467,7 @@ def run_ours(args, rank, world, local):
                    "seq_len": int(max(inp['seqlens'])), "num_q_heads": w.num_q_heads,
                    "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "num_splits": P,
                    "kernel": kernel_used, "deterministic": args.deterministic,
+                   "cluster_merge": args.cluster_merge,
                    "kv_dtype": "e4m3 (per-KV-head scales)" if args.fp8 else str(w.kv_dtype).replace("torch.", ""),
                    "queries_per_sequence": args.queries,
                    "kv_layout": f"paged ({args.paged_layout}), {args.paged}-token pages shuffled in a pool"
@@ -485,7 +490,7 @@ def run_ours(args, rank, world, local):
 
 # ----------------------------------------------------------------- sweeps
 def _time_steps(ta, torch, copies, P, kernel, steps, warmup, out, lse, ws, deterministic=False,
-                graph=False):
+                graph=False, cluster_merge=False):
     """(ms per step, split-kernel ms) over ``steps`` decode calls; when the step
     is a single kernel the two are the same number.  With ``graph`` the steps
     are captured once in a CUDA graph and the replay is timed."""
@@ -493,7 +498,8 @@ def _time_steps(ta, torch, copies, P, kernel, steps, warmup, out, lse, ws, deter
         c = copies[i % len(copies)]
         ta.tree_attn_decode(c["q"], c["k"], c["v"], c["seqlens"], out=out, lse=lse, num_splits=P,
                             workspace=ws, kernel=kernel, split_events=events,
-                            deterministic=deterministic, k_scale=c.get("k_scale"), v_scale=c.get("v_scale"))
+                            deterministic=deterministic, k_scale=c.get("k_scale"), v_scale=c.get("v_scale"),
+                            cluster_merge=cluster_merge)
     for i in range(warmup):
         step(i)
     torch.cuda.synchronize()
@@ -599,6 +605,8 @@ def run_sweeps(args):
             copies = draw(N)
             shape = ta.make_shape(copies[0]["q"], copies[0]["k"])
             P = ta.tree_attn_pick_splits(shape)
+            if args.cluster_merge:
+                P = min(P, 8)  # one cluster per row: at most 8 blocks
             kv_bytes = w.kv_bytes(np.full(w.batch, N))
             B, Hq, d = copies[0]["q"].shape
             out = torch.empty(B, Hq, d, device="cuda")
@@ -606,8 +614,9 @@ def run_sweeps(args):
             ws = torch.empty(max(16, ta.tree_attn_workspace_bytes(shape, P)), dtype=torch.uint8,
                              device="cuda")
             ms, split = _time_steps(ta, torch, copies, P, args.kernel, args.steps, args.warmup, out, lse, ws,
-                                    args.deterministic, args.graph)
+                                    args.deterministic, args.graph, args.cluster_merge)
             lines.append({"sweep": "context", "workload": w.name, "kv": "e4m3" if args.fp8 else "bf16",
+                          "cluster_merge": args.cluster_merge,
                           "context": N, "num_splits": P,
                           "graph": args.graph, "l2": "fits" if w.kv_bytes(np.full(w.batch, N)) * len(copies)
                           < L2_BYTES else "exceeds",

@@ -120,6 +120,12 @@ typedef enum {
                                     its outputs are NaN and tree_attn_get_device_error
                                     returns TA_ERR_DEVICE_TIMEOUT.  Nothing faults or hangs,
                                     and the device stays usable. */
+#define TA_FLAG_CLUSTER_MERGE 8  /* the row's num_splits (2..8) thread blocks run as one
+                                    thread-block cluster and merge their partial states
+                                    through the cluster's distributed shared memory instead
+                                    of the last-arriving block reading them back from L2:
+                                    a shorter step end for short contexts.  Tensor-core and
+                                    FP8 kernels; a heuristic split count is capped at 8 */
 #define TA_FLAG_DIAG_MISHINT 4   /* diagnostic, for testing: the copy warps' length hint
                                     (used to start the first copies before the row length
                                     is read) is made wrong, so those copies are discarded

@@ -27,6 +27,8 @@ TA_MAX_SPLITS = 4096
 TA_FLAG_DETERMINISTIC = 1
 TA_FLAG_DIAG_STALL = 2
 TA_FLAG_DIAG_MISHINT = 4
+TA_FLAG_CLUSTER_MERGE = 8
+TA_CLUSTER_MAX_SPLITS = 8
 TA_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 _EXPORTS = ["tree_attn_status_string", "tree_attn_version", "tree_attn_check_shape",
@@ -124,9 +126,9 @@ def _dtype_code(dt: torch.dtype) -> int:
 
 
 def _options(kernel, deterministic, k_scale=None, v_scale=None, events=None, diag_stall=False,
-             diag_mishint=False):
+             diag_mishint=False, cluster_merge=False):
     flags = ((TA_FLAG_DETERMINISTIC if deterministic else 0) | (TA_FLAG_DIAG_STALL if diag_stall else 0)
-             | (TA_FLAG_DIAG_MISHINT if diag_mishint else 0))
+             | (TA_FLAG_DIAG_MISHINT if diag_mishint else 0) | (TA_FLAG_CLUSTER_MERGE if cluster_merge else 0))
     o = TaOptions(TA_KERNEL[kernel], flags, None, None, None, None)
     if events is not None:
         o.split_start_event = events[0].cuda_event
@@ -221,7 +223,7 @@ def tree_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
                      scale: Optional[float] = None, stream=None, split_events=None,
                      want_lse: bool = True, deterministic: bool = False,
                      k_scale: Optional[torch.Tensor] = None, v_scale: Optional[torch.Tensor] = None,
-                     diag_stall: bool = False, diag_mishint: bool = False):
+                     diag_stall: bool = False, diag_mishint: bool = False, cluster_merge: bool = False):
     """Decode attention through the C ABI; returns (out [B,Hq,d] fp32, lse [B,Hq] fp32 or None).
 
     ``num_splits`` <= 0 uses the library's heuristic (picked on the host so the
@@ -231,7 +233,9 @@ def tree_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
     ``diag_stall`` (testing only) makes every on-chip wait give up: NaN outputs and
     TA_ERR_DEVICE_TIMEOUT from tree_attn_get_device_error, after about two seconds.
     ``diag_mishint`` (testing only) makes the copy warps' length hint wrong, so their
-    first copies are discarded; the results must not change.
+    first copies are discarded; the results must not change.  ``cluster_merge`` runs
+    each row's 2..8 blocks as a thread-block cluster merging through distributed
+    shared memory (a heuristic split count is capped at 8).
     """
     lib = load()
     _check_cuda(q, k_cache, v_cache, seqlens, out, lse, workspace)
@@ -252,13 +256,15 @@ def tree_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
     P = int(num_splits)
     if P <= 0:
         P = tree_attn_pick_splits(shape)
+        if cluster_merge:
+            P = min(P, TA_CLUSTER_MAX_SPLITS)  # one cluster per row
     nbytes = tree_attn_workspace_bytes(shape, P)
     if nbytes and workspace is None:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     st = _stream(stream)
     if (kernel == "auto" and split_events is None and not deterministic and k_scale is None and not diag_stall
-            and not diag_mishint):
+            and not diag_mishint and not cluster_merge):
         rc = lib.tree_attn_decode(ctypes.byref(shape), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                   _ptr(seqlens), _ptr(out), _ptr(lse), P, _ptr(workspace),
                                   ws_bytes, st)
@@ -269,7 +275,8 @@ def tree_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
             torch_stream = stream if isinstance(stream, torch.cuda.Stream) else torch.cuda.current_stream()
             for ev in split_events:
                 ev.record(torch_stream)
-        opts = _options(kernel, deterministic, k_scale, v_scale, split_events, diag_stall, diag_mishint)
+        opts = _options(kernel, deterministic, k_scale, v_scale, split_events, diag_stall, diag_mishint,
+                        cluster_merge)
         rc = lib.tree_attn_decode_ex(ctypes.byref(shape), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                      _ptr(seqlens), _ptr(out), _ptr(lse), P, _ptr(workspace),
                                      ws_bytes, ctypes.byref(opts), st)
@@ -334,7 +341,8 @@ def tree_attn_decode_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torc
                            num_splits: int = 0, workspace: Optional[torch.Tensor] = None,
                            kernel: str = "auto", scale: Optional[float] = None, stream=None,
                            deterministic: bool = False, max_seqlen: Optional[int] = None,
-                           k_scale: Optional[torch.Tensor] = None, v_scale: Optional[torch.Tensor] = None):
+                           k_scale: Optional[torch.Tensor] = None, v_scale: Optional[torch.Tensor] = None,
+                           cluster_merge: bool = False):
     """Decode attention over a paged KV cache through the C ABI.
 
     k_pages, v_pages: [num_pages, page_size, Hkv, d] views (any strides with a unit
@@ -367,11 +375,13 @@ def tree_attn_decode_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torc
     P = int(num_splits)
     if P <= 0:
         P = tree_attn_pick_splits(shape, page_size=page_size)
+        if cluster_merge:
+            P = min(P, TA_CLUSTER_MAX_SPLITS)  # one cluster per row
     nbytes = tree_attn_workspace_bytes(shape, P)
     if nbytes and workspace is None:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    opts = _options(kernel, deterministic, k_scale, v_scale)
+    opts = _options(kernel, deterministic, k_scale, v_scale, cluster_merge=cluster_merge)
     rc = lib.tree_attn_decode_paged(ctypes.byref(shape), ctypes.byref(paged), _ptr(q), _ptr(k_pages),
                                     _ptr(v_pages), _ptr(seqlens), _ptr(out), _ptr(lse), P,
                                     _ptr(workspace), ws_bytes, ctypes.byref(opts), _stream(stream))
@@ -387,7 +397,8 @@ def tree_attn_decode_multi(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
                            num_splits: int = 0, workspace: Optional[torch.Tensor] = None,
                            kernel: str = "auto", scale: Optional[float] = None, stream=None,
                            deterministic: bool = False, max_seqlen: Optional[int] = None,
-                           k_scale: Optional[torch.Tensor] = None, v_scale: Optional[torch.Tensor] = None):
+                           k_scale: Optional[torch.Tensor] = None, v_scale: Optional[torch.Tensor] = None,
+                           cluster_merge: bool = False):
     """Several queries per sequence through the C ABI.
 
     q: [B, Hq, nq, d]; query i of row b sits at position seqlens[b] - nq + i and, when
@@ -425,11 +436,13 @@ def tree_attn_decode_multi(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
     P = int(num_splits)
     if P <= 0:
         P = tree_attn_pick_splits(eff, page_size=paged.page_size if paged is not None else 0)
+        if cluster_merge:
+            P = min(P, TA_CLUSTER_MAX_SPLITS)  # one cluster per row
     nbytes = tree_attn_workspace_bytes(eff, P)
     if nbytes and workspace is None:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    opts = _options(kernel, deterministic, k_scale, v_scale)
+    opts = _options(kernel, deterministic, k_scale, v_scale, cluster_merge=cluster_merge)
     rc = lib.tree_attn_decode_multi(ctypes.byref(base), ctypes.byref(paged) if paged is not None else None,
                                     nq, int(bool(causal)), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                     _ptr(seqlens), _ptr(out), _ptr(lse), P, _ptr(workspace), ws_bytes,

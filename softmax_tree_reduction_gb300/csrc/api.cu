@@ -60,6 +60,10 @@ static_assert(kFusedMaxSplits * 16 * 4 <= kFusedMaxStates, "fused-merge decision
 constexpr int kFp8HeadsPage16 = 4;   // FP8 cache
 constexpr int kMmaHeadsPage16 = 2;   // BF16 tensor-core kernel, token-major pools
 
+constexpr int kKnownFlags =
+    TA_FLAG_DETERMINISTIC | TA_FLAG_DIAG_STALL | TA_FLAG_DIAG_MISHINT | TA_FLAG_CLUSTER_MERGE;
+constexpr int kClusterMaxSplits = 8;  // portable cluster size
+
 constexpr int kMaxDevices = 64;
 
 struct DeviceState {
@@ -487,10 +491,13 @@ int decode_impl(const ta_shape* shape, const ta_paged_kv* paged, int nq, int cau
     if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
         !aligned(seqlens, 4) || (lse && !aligned(lse, 4)))
         return TA_ERR_ALIGN;
-    if (options && (options->flags & ~(TA_FLAG_DETERMINISTIC | TA_FLAG_DIAG_STALL | TA_FLAG_DIAG_MISHINT)) != 0) return TA_ERR_SHAPE;
+    if (options && (options->flags & ~kKnownFlags) != 0) return TA_ERR_SHAPE;
     const bool deterministic = options && (options->flags & TA_FLAG_DETERMINISTIC);
+    const bool cluster = options && (options->flags & TA_FLAG_CLUSTER_MERGE);
     const int kernel = resolve_kernel(shape, options ? options->kernel : TA_KERNEL_AUTO);
     if (kernel < 0) return kernel;
+    if (cluster && kernel != TA_KERNEL_MMA && kernel != kKernelFp8) return TA_ERR_SHAPE;
+    if (cluster && num_splits > kClusterMaxSplits) return TA_ERR_SPLITS;
     if (shape->kv_dtype == TA_E4M3) {
         if (!options || !options->k_scale || !options->v_scale) return TA_ERR_NULL;
         if (!aligned(options->k_scale, 4) || !aligned(options->v_scale, 4)) return TA_ERR_ALIGN;
@@ -515,6 +522,7 @@ int decode_impl(const ta_shape* shape, const ta_paged_kv* paged, int nq, int cau
     int P = num_splits;
     if (P <= 0) {
         P = pick_splits_impl(shape, nullptr, ds->num_sms, kernel, paged ? paged->page_size : 0);
+        if (cluster) P = std::min(P, kClusterMaxSplits);
         if (P < 1 || P > TA_MAX_SPLITS) return TA_ERR_SPLITS;
         if ((rc = check_ws(P)) != TA_OK) return rc;
     }
@@ -582,9 +590,15 @@ int decode_impl(const ta_shape* shape, const ta_paged_kv* paged, int nq, int cau
             const int64_t blocks = static_cast<int64_t>(rows) * P;
             const int64_t resident = static_cast<int64_t>(ds->num_sms) * blocks_per_sm(shape, kernel);
             if (!deterministic && blocks <= kBalanceMaxWaves * resident) p.claim = slots;
-            fused = fuse_merge(hb * p.G, P);
-            p.fuse = fused ? 1 : 0;
-            if (p.claim || fused) p.done = slots + rows;
+            if (!cluster) {
+                fused = fuse_merge(hb * p.G, P);
+                p.fuse = fused ? 1 : 0;
+                if (p.claim || fused) p.done = slots + rows;
+            }
+        }
+        if (cluster) {  // the row's blocks merge through the cluster: no ticket, no combine
+            p.cluster = 1;
+            fused = true;
         }
     }
 
@@ -705,7 +719,7 @@ int tree_attn_decode_multi(const ta_shape* shape, const ta_paged_kv* paged, int 
 int tree_attn_launch_count(const ta_shape* shape, int num_splits, const ta_options* options) {
     int rc = check_shape(shape, nullptr);
     if (rc != TA_OK) return rc;
-    if (options && (options->flags & ~(TA_FLAG_DETERMINISTIC | TA_FLAG_DIAG_STALL | TA_FLAG_DIAG_MISHINT)) != 0) return TA_ERR_SHAPE;
+    if (options && (options->flags & ~kKnownFlags) != 0) return TA_ERR_SHAPE;
     const int kernel = resolve_kernel(shape, options ? options->kernel : TA_KERNEL_AUTO);
     if (kernel < 0) return kernel;
     int P = num_splits;
@@ -716,6 +730,7 @@ int tree_attn_launch_count(const ta_shape* shape, int num_splits, const ta_optio
         P = pick_splits_impl(shape, nullptr, ds->num_sms, kernel, 0);
     }
     if (P == 1) return 1;
+    if (options && (options->flags & TA_FLAG_CLUSTER_MERGE)) return 1;
     const int64_t G = shape->num_q_heads / shape->num_kv_heads;
     const unsigned rows = static_cast<unsigned>(shape->batch) * shape->num_kv_heads;
     const bool have_slots = 2 * static_cast<uint64_t>(rows) <= kRingSlots;

@@ -45,6 +45,7 @@ struct SplitParams {
     int hb;                 // KV heads per block (a box brings box_rows tokens of each)
     int stall;              // diagnostic: the producer publishes nothing (waits give up)
     int mishint;            // diagnostic: the producer's length hint is made wrong
+    int cluster;            // a row's P blocks form a cluster and merge through its shared memory
     int B, Hq, Hkv, G, S, P; // Hq, G count virtual heads: query heads x queries per row
     int nq;                 // queries per row (q rows are [head][query])
     int causal;             // query i of nq sees tokens < N - nq + 1 + i
@@ -192,6 +193,32 @@ __device__ __forceinline__ void consumer_sync(int nthreads) {
 }
 
 // Programmatic dependent launch: let the combine grid start its launch early.
+// ------------------------------------------------------------ clusters
+// Barrier over every thread of the thread-block cluster (writes to shared
+// memory before it are visible to loads from any block of the cluster after).
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+__device__ __forceinline__ unsigned cluster_rank() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Address of this block's shared-memory word `local` in block `rank` of the cluster.
+__device__ __forceinline__ uint32_t dsmem_addr(const void* local, unsigned rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ float ld_dsmem(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void allow_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }

@@ -279,6 +279,54 @@ __device__ __forceinline__ unsigned ticket_acq_rel(unsigned* p, unsigned limit) 
     return old;
 }
 
+// Row merge through the cluster's distributed shared memory (a row's P
+// blocks form one thread-block cluster; block rank = slice).  Every block has
+// written its merged state -- numerators cs_o [nh][D], maxima cs_m (log2
+// units) and denominators cs_l [nh] -- to its own shared memory and passed a
+// cluster barrier; each block then merges a share of the row's (head,
+// channel) outputs from all P states, normalises and writes them.  The
+// caller ends with a second cluster barrier, so no block's state goes away
+// while a peer still reads it.
+template <int D, int kMaxP>
+__device__ void cluster_merge_row(const SplitParams& p, size_t hq0, int nh, const float* cs_o,
+                                  const float* cs_m, const float* cs_l, int tid, int nthr) {
+    const int P = p.P;
+    const int rank = static_cast<int>(cluster_rank());
+    const int items = nh * D;
+    const int per = (items + P - 1) / P;
+    const int i0 = rank * per, i1 = min(items, i0 + per);
+    for (int idx = i0 + tid; idx < i1; idx += nthr) {
+        const int h = idx / D, dd = idx - h * D;
+        float mq[kMaxP], lq[kMaxP], oq[kMaxP];
+#pragma unroll
+        for (int q = 0; q < kMaxP; ++q) {
+            if (q < P) {
+                mq[q] = ld_dsmem(dsmem_addr(cs_m + h, q));
+                lq[q] = ld_dsmem(dsmem_addr(cs_l + h, q));
+                oq[q] = ld_dsmem(dsmem_addr(cs_o + idx, q));
+            } else {
+                mq[q] = -INFINITY;
+                lq[q] = 0.f;
+                oq[q] = 0.f;
+            }
+        }
+        float M = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < kMaxP; ++q) M = fmaxf(M, mq[q]);
+        const float Ms = (M == -INFINITY) ? 0.f : M;
+        float L = 0.f, O = 0.f;
+#pragma unroll
+        for (int q = 0; q < kMaxP; ++q) {
+            const float w = (mq[q] == -INFINITY) ? 0.f : ex2(mq[q] - Ms);
+            L = fmaf(w, lq[q], L);
+            O = fmaf(w, oq[q], O);
+        }
+        const size_t r = hq0 + h;
+        p.out[r * D + dd] = (L == 0.f) ? 0.f : O / L;  // NaN inputs propagate
+        if (dd == 0 && p.lse) p.lse[r] = (L > 0.f) ? (M + log2f(L)) * kLn2 : (L == 0.f ? -INFINITY : L);
+    }
+}
+
 // `row`: the block's schedule row (ticket and claim counters); the row's
 // blocks hold the states of query heads [hq0, hq0 + G) (flat b * Hq + h).
 template <int D>

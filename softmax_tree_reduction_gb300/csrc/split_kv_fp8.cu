@@ -55,6 +55,9 @@ struct Fp8Cfg {
     // hit 32 distinct banks and the merge reads consecutive positions.
     static constexpr int kMergeStride = D + 4;
     static_assert(kWarps * 16 * (kMergeStride + 2) * 4 <= kStages * kStageBytes, "merge buffer (two n-tiles)");
+    // cluster row merge: the block's merged state, [HB*16 heads][D] + 2 x [HB*16]
+    static_assert((kWarps * 16 * (kMergeStride + 2) + HB * 16 * (D + 2)) * 4 <= kStages * kStageBytes,
+                  "cluster state buffer");
 };
 
 constexpr float kPScale = 16384.f;  // 2^14
@@ -119,6 +122,9 @@ __global__ void __launch_bounds__(Fp8Cfg<HB>::kThreads, 1)
     float* mg_o = reinterpret_cast<float*>(stages);  // [W][8*NT][D (+pad)], after streaming
     float* mg_m = mg_o + C::kWarps * 8 * NT * C::kMergeStride;  // [W][8*NT]
     float* mg_l = mg_m + C::kWarps * 8 * NT;                    // [W][8*NT]
+    float* cs_o = mg_l + C::kWarps * 8 * NT;  // cluster merge: [HB*G][D], m, l [HB*G]
+    float* cs_m = cs_o + HB * 16 * D;
+    float* cs_l = cs_m + HB * 16;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
     uint64_t* empty = full + C::kStages;
     volatile StageMeta* meta = reinterpret_cast<volatile StageMeta*>(empty + C::kStages);
@@ -167,6 +173,10 @@ __global__ void __launch_bounds__(Fp8Cfg<HB>::kThreads, 1)
     if (warp == 0) {
         if (p.stall) {  // diagnostic: publish nothing, so the consumers' waits give up
             allow_dependents();
+            if (p.cluster) {  // the cluster barriers of the row merge
+                cluster_sync_all();
+                cluster_sync_all();
+            }
             return;
         }
         const uint64_t pol = l2_policy_evict_first();
@@ -189,6 +199,10 @@ __global__ void __launch_bounds__(Fp8Cfg<HB>::kThreads, 1)
                 tma_load_4d(st + C::kKBytes + off, &tmV, 0, ty, g0, page, &full[s], pol);
             });
         allow_dependents();
+        if (p.cluster) {  // the cluster barriers of the row merge
+            cluster_sync_all();
+            cluster_sync_all();
+        }
         return;
     }
 
@@ -500,11 +514,27 @@ __global__ void __launch_bounds__(Fp8Cfg<HB>::kThreads, 1)
         for (int i = 1; i < HB; ++i) osc = (hh == i) ? vsc[i] : osc;
         const float o = tree_sum<C::kWPH>(ow) * osc;
         const float lsum = tree_sum<C::kWPH>(lw);
-        emit_state(p, b, (g0 + hh) * p.G + h, split, D, dd, o, lsum, M, poison);
+        if (p.cluster) {  // kept for the cluster row merge
+            const float nan = __int_as_float(0x7fc00000);
+            const int hb_h = hh * p.G + h;
+            cs_o[hb_h * D + dd] = poison ? nan : o;
+            if (dd == 0) {
+                cs_m[hb_h] = poison ? nan : M;
+                cs_l[hb_h] = poison ? nan : lsum;
+            }
+        } else {
+            emit_state(p, b, (g0 + hh) * p.G + h, split, D, dd, o, lsum, M, poison);
+        }
     }
-    if (p.done)
-        finish_row<D>(p, row, static_cast<size_t>(b) * p.Hq + static_cast<size_t>(g0) * p.G, HB * p.G,
-                      reinterpret_cast<float*>(stages), last_flag, ct, C::kWarps * 32);
+    const size_t hq0 = static_cast<size_t>(b) * p.Hq + static_cast<size_t>(g0) * p.G;
+    if (p.cluster) {
+        cluster_sync_all();  // every block's state is in its shared memory; every claim is made
+        if (p.claim && ct == 0 && cluster_rank() == 0) atomicExch(p.claim + row, 0u);
+        cluster_merge_row<D, 8>(p, hq0, HB * p.G, cs_o, cs_m, cs_l, ct, C::kWarps * 32);
+        cluster_sync_all();  // no block's state goes away while a peer reads it
+    } else if (p.done) {
+        finish_row<D>(p, row, hq0, HB * p.G, reinterpret_cast<float*>(stages), last_flag, ct, C::kWarps * 32);
+    }
     allow_dependents();
 }
 
@@ -520,11 +550,15 @@ cudaError_t launch_hb(const CUtensorMap& tk, const CUtensorMap& tv, const SplitP
     cfg.blockDim = dim3(C::kThreads, 1, 1);
     cfg.dynamicSmemBytes = C::kSmem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;  // a row's P blocks form one cluster
+    attr[1].val.clusterDim.x = static_cast<unsigned>(p.P);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = p.cluster ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, split_kv_fp8_kernel<HB, NT>, tk, tv, p);
 }
 

@@ -155,7 +155,7 @@ def test_decode_argument_errors_before_any_cuda_call(ta):
     assert _decode_raw(ta, f32, opts=ta.TaOptions(2, 0, None, None, None, None)) == -4   # mma needs bf16
     assert _decode_raw(ta, shape(ta, num_q_heads=256, num_kv_heads=8),
                        opts=ta.TaOptions(2, 0, None, None, None, None)) == -3          # G = 32 > 16
-    assert _decode_raw(ta, s, opts=ta.TaOptions(0, 8, None, None, None, None)) == -3  # unknown flag bit
+    assert _decode_raw(ta, s, opts=ta.TaOptions(0, 16, None, None, None, None)) == -3  # unknown flag bit
     assert _decode_raw(ta, s, opts=ta.TaOptions(9, 0, None, None, None, None)) == -3  # unknown kernel
 
 
@@ -250,3 +250,12 @@ def test_pick_splits_paged_small_pages_share_blocks(ta):
     for bad in (8, 24, 2048):
         with pytest.raises(ta.TreeAttnError):
             ta.tree_attn_pick_splits(fp8, None, 152, page_size=bad)
+
+
+def test_cluster_merge_arguments(ta):
+    s = shape(ta)
+    f32 = shape(ta, q_dtype=0, kv_dtype=0)
+    cl = ta.TA_FLAG_CLUSTER_MERGE
+    assert _decode_raw(ta, s, P=9, ws=0x7000, wsb=1 << 30, opts=ta.TaOptions(0, cl, None, None, None, None)) == -5
+    assert _decode_raw(ta, f32, P=4, ws=0x7000, wsb=1 << 30, opts=ta.TaOptions(1, cl, None, None, None, None)) == -3
+    assert ta.tree_attn_launch_count(s, 8) == 1
