@@ -44,12 +44,12 @@ FALLBACK_HBM_GBS = 6800.0
 NCU_TRAFFIC = {
     # profiles/split_kv_mma_llama31_8b_131k.md
     ("mma", "llama3.1-8b-decode-layer"): {
-        "bytes_per_launch": 537206272 + 2968064, "num_splits": 19,
-        "src_sha256": "23a44a075b68e958b321fadb8d02a088685ace0d0d6f5a0fbbc9b540c2ed3536"},
+        "bytes_per_launch": 537336320 + 3180032, "num_splits": 19,
+        "src_sha256": "6ee28ccf5f8de4a7280c4e49fe742baaa571464a88947abcc77ec22cf319f172"},
     # profiles/split_kv_fp8_llama31_8b_131k.md
     ("fp8", "llama3.1-8b-decode-layer"): {
-        "bytes_per_launch": 268516352 + 2977536, "num_splits": 19,
-        "src_sha256": "9edf13779563b3ff2ad69446b2c76abe8262e9fe2d151d5d6c5df30c439e20d0"},
+        "bytes_per_launch": 268540416 + 3370496, "num_splits": 19,
+        "src_sha256": "467c49cb2c8a7f07bd440048bc42e92e9a62db9fc2aa3f180e936441efa4a4ee"},
 }
 
 
