@@ -113,7 +113,7 @@ def load_peaks():
 def kernel_source_hash(kernel):
     name = {"mma": "split_kv_mma.cu", "fma": "split_kv_fma.cuh", "fp8": "split_kv_fp8.cu"}[kernel]
     h = hashlib.sha256()
-    for f in (name, "common.cuh", "emit.cuh", "sched.cuh", "api.cu"):
+    for f in (name, "common.cuh", "emit.cuh", "sched.cuh", "warp_mma.cuh", "api.cu"):
         with open(os.path.join(ROOT, "softmax_tree_reduction_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()

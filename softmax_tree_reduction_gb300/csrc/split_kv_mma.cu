@@ -28,6 +28,7 @@
 #include "emit.cuh"
 #include "kernels.h"
 #include "sched.cuh"
+#include "warp_mma.cuh"
 
 namespace ta {
 namespace {
@@ -58,48 +59,6 @@ struct MmaCfg {
                   "cluster state buffer");
     static_assert(kTile <= 256, "TMA box height");
 };
-
-// Pairwise tree sum of N values (N a power of two).
-template <int N>
-__device__ __forceinline__ float tree_sum(const float* v) {
-    if constexpr (N == 1) {
-        return v[0];
-    } else {
-        return tree_sum<N / 2>(v) + tree_sum<N / 2>(v + N / 2);
-    }
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr)
-                 : "memory");
-}
-
-__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint32_t movtrans(uint32_t x) {
-    uint32_t y;
-    asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
-    return y;
-}
-
-__device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat162 v) {
-    return *reinterpret_cast<uint32_t*>(&v);
-}
 
 template <int D, int NT, int HB>
 __global__ void __launch_bounds__(MmaCfg<D, HB>::kThreads, 1)
