@@ -316,7 +316,9 @@ def run_ours(args, rank, world, local):
     if args.queries > 1:  # each (head, query) pair counts as a query head
         shape = ta.TaShape.from_buffer_copy(shape)
         shape.num_q_heads *= args.queries
-    P = args.num_splits if args.num_splits > 0 else ta.tree_attn_pick_splits(shape, page_size=args.paged)
+    # the workload's row lengths are known on the host, as a serving engine knows its sequences'
+    P = (args.num_splits if args.num_splits > 0
+         else ta.tree_attn_pick_splits(shape, inp["seqlens"], page_size=args.paged))
     if args.cluster_merge and args.num_splits <= 0:
         P = min(P, 8)  # one cluster per row: at most 8 blocks
     kernel_used = args.kernel

@@ -274,8 +274,11 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // token of one KV head": a block's fixed cost (pipeline fill, epilogue) is
 // worth kBlockCost tokens; a second (combine) launch kBlockCost more plus its
 // traffic (partials written and read back) spread over the whole GPU.  A
-// block serving hb KV heads streams hb such units per token.
-constexpr double kBlockCost = 256.0;
+// block serving hb KV heads streams hb such units per token.  512 matches the
+// measured split sweeps on GB300: it keeps the best counts of the uniform
+// layers (19 on 152 SMs) and picks the best one of the ragged batch (5; 256
+// picked 16, measured 7 % slower).
+constexpr double kBlockCost = 512.0;
 
 double estimate(const ta_shape* s, const std::vector<int64_t>& lens, bool uniform, int P,
                 int tile, int slots, int hb) {

@@ -115,7 +115,7 @@ def test_pick_splits_ragged_uses_lengths(ta):
     sl = workloads.seqlens_of(workloads.BATCHED_RAGGED)
     s = shape(ta, batch=16, max_seqlen=65536)
     P = ta.tree_attn_pick_splits(s, sl, 152)
-    assert 1 <= P <= 256
+    assert P == 5   # the best of a measured sweep on GB300 (3..19)
     # all rows at the shortest length: the uniform model applies
     P2 = ta.tree_attn_pick_splits(s, np.full(16, 8192), 152)
     assert 1 <= P2 <= 32
