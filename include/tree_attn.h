@@ -88,7 +88,8 @@ typedef struct {
     int32_t batch;          /* B >= 1 */
     int32_t num_q_heads;    /* Hq >= 1 */
     int32_t num_kv_heads;   /* Hkv >= 1, Hq % Hkv == 0, 1 <= Hq/Hkv <= 16 (a power of two
-                               unless q and the cache are BF16) */
+                               unless q and the cache are BF16); up to 64 with BF16 q
+                               and cache at head_dim 128 */
     int32_t head_dim;       /* d: 64 or 128 */
     int32_t max_seqlen;     /* S: cache capacity per sequence, tokens (>= 1) */
     int32_t q_dtype;        /* ta_dtype */
@@ -103,8 +104,9 @@ typedef struct {
 typedef enum {
     TA_KERNEL_AUTO = 0,  /* tensor-core path when it applies, else FMA */
     TA_KERNEL_FMA = 1,   /* FP32 FMA on CUDA cores; every dtype combination */
-    TA_KERNEL_MMA = 2    /* tensor-core mma: BF16 q and kv (Hq/Hkv <= 16), or BF16 q with an
-                            E4M3 cache (Hq/Hkv <= 16, head_dim 128) */
+    TA_KERNEL_MMA = 2    /* tensor-core mma: BF16 q and kv (Hq/Hkv <= 16, or <= 64 at
+                            head_dim 128), or BF16 q with an E4M3 cache (Hq/Hkv <= 16,
+                            head_dim 128) */
 } ta_kernel;
 
 /* Bits of ta_options.flags. */
@@ -252,7 +254,8 @@ int tree_attn_decode_paged(const ta_shape *shape, const ta_paged_kv *paged, cons
  *  paged  NULL for dense caches, else as for tree_attn_decode_paged
  * Each (head, query) pair is handled as one query head of the KV group:
  * num_q_heads * num_queries / num_kv_heads must be at most 16 (a power of two
- * unless q and the cache are BF16), and tree_attn_workspace_bytes,
+ * unless q and the cache are BF16; up to 64 with BF16 q and cache at head_dim
+ * 128), and tree_attn_workspace_bytes,
  * tree_attn_pick_splits and tree_attn_launch_count take the shape with
  * num_q_heads multiplied by num_queries.  num_queries in [1, 16]. */
 int tree_attn_decode_multi(const ta_shape *shape, const ta_paged_kv *paged, int num_queries,

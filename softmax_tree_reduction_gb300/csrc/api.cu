@@ -146,7 +146,7 @@ int check_shape(const ta_shape* s, Strides* st, int page_size = 0) {
         return TA_ERR_SHAPE;
     if (s->num_q_heads % s->num_kv_heads != 0) return TA_ERR_SHAPE;
     const int G = s->num_q_heads / s->num_kv_heads;
-    if (G < 1 || G > 16) return TA_ERR_SHAPE;
+    if (G < 1 || G > 64) return TA_ERR_SHAPE;
     if (s->head_dim != 64 && s->head_dim != 128) return TA_ERR_SHAPE;
     if ((s->q_dtype != TA_F32 && s->q_dtype != TA_BF16) ||
         (s->kv_dtype != TA_F32 && s->kv_dtype != TA_BF16 && s->kv_dtype != TA_E4M3))
@@ -182,7 +182,8 @@ int check_shape(const ta_shape* s, Strides* st, int page_size = 0) {
 
 // Kernel family for a shape (num_q_heads counts (head, query) pairs for
 // multi-query calls): the tensor-core kernel takes BF16 q and cache with up to
-// 16 columns per KV head; the FMA kernel any dtypes with a power-of-two group.
+// 16 columns per KV head (64 at head_dim 128, in column groups of 16); the
+// FMA kernel any dtypes with a power-of-two group up to 16.
 int resolve_kernel(const ta_shape* s, int requested) {
     const int G = s->num_q_heads / s->num_kv_heads;
     if (s->kv_dtype == TA_E4M3) {
@@ -192,7 +193,7 @@ int resolve_kernel(const ta_shape* s, int requested) {
         return ok ? kKernelFp8 : static_cast<int>(TA_ERR_DTYPE);
     }
     const bool bf16 = s->q_dtype == TA_BF16 && s->kv_dtype == TA_BF16;
-    const bool mma_ok = bf16 && G <= 16;
+    const bool mma_ok = bf16 && (G <= 16 || (G <= 64 && s->head_dim == 128));
     const bool fma_ok = (G & (G - 1)) == 0 && G <= 16;
     switch (requested) {
         case TA_KERNEL_AUTO:
@@ -225,7 +226,7 @@ int heads_per_block(const ta_shape* s, int kernel, int page_size, int num_sms) {
     int want = 1;
     if (kernel == kKernelFp8)
         want = kFp8HeadsPage16;
-    else if (kernel == TA_KERNEL_MMA && s->head_dim == 128 && sh < st)
+    else if (kernel == TA_KERNEL_MMA && s->head_dim == 128 && sh < st && s->num_q_heads <= 16 * s->num_kv_heads)
         want = kMmaHeadsPage16;
     const bool fused1 = pick_splits_hb(s, nullptr, num_sms, kernel, 1) <= kFusedMaxSplits;
     for (; want > 1; want /= 2) {

@@ -33,14 +33,21 @@
 namespace ta {
 namespace {
 
-// HB KV heads per block: a stage holds kTile tokens of each (128 rows per
-// operand), and kWarps / HB consumer warps serve each head.
-template <int D, int HB>
+// Consumer warps are split into groups.  HB KV heads per block: a stage
+// holds kTile tokens of each (128 rows per operand) and each head has its
+// group of warps, one 16-token slab per warp.  CG column groups (more than 16
+// columns per KV head, HB = 1): each group of warps owns 16 columns and every
+// warp takes CG slabs of each 128-token stage.
+template <int D, int HB, int CG = 1>
 struct MmaCfg {
+    static_assert(HB == 1 || CG == 1, "heads per block or column groups");
     static constexpr int kWarps = 8;                 // consumer warps (two per SM sub-partition)
     static constexpr int kRows = 16 * kWarps;        // rows per operand per stage
     static constexpr int kTile = kRows / HB;         // tokens per stage
-    static constexpr int kWPH = kWarps / HB;         // consumer warps per KV head
+    static constexpr int kGroups = HB * CG;          // warp groups (heads or column groups)
+    static constexpr int kWPG = kWarps / kGroups;    // consumer warps per group
+    static constexpr int kSub = CG;                  // 16-token slabs per warp per stage
+    static constexpr int kLocalHeads = 16 * HB * CG; // most (head, column) states a block holds
     static constexpr int kHalves = D / 64;           // 128-byte column blocks per row
     static constexpr int kKBytes = kHalves * kRows * 128;
     static constexpr int kStageBytes = 2 * kKBytes;  // K and V
@@ -54,17 +61,17 @@ struct MmaCfg {
     // distinct banks.
     static constexpr int kMergeStride = D + 4;
     static_assert(kWarps * 16 * (kMergeStride + 2) * 4 <= kStages * kStageBytes, "merge buffer (two n-tiles)");
-    // cluster row merge: the block's merged state, [HB*16 heads][D] + 2 x [HB*16]
-    static_assert((kWarps * 16 * (kMergeStride + 2) + HB * 16 * (D + 2)) * 4 <= kStages * kStageBytes,
+    // cluster row merge: the block's merged state, [kLocalHeads][D] + 2 x [kLocalHeads]
+    static_assert((kWarps * 16 * (kMergeStride + 2) + kLocalHeads * (D + 2)) * 4 <= kStages * kStageBytes,
                   "cluster state buffer");
     static_assert(kTile <= 256, "TMA box height");
 };
 
-template <int D, int NT, int HB>
-__global__ void __launch_bounds__(MmaCfg<D, HB>::kThreads, 1)
+template <int D, int NT, int HB, int CG>
+__global__ void __launch_bounds__(MmaCfg<D, HB, CG>::kThreads, 1)
     split_kv_mma_kernel(const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const SplitParams p) {
-    using C = MmaCfg<D, HB>;
+    using C = MmaCfg<D, HB, CG>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -73,8 +80,8 @@ __global__ void __launch_bounds__(MmaCfg<D, HB>::kThreads, 1)
     float* mg_m = mg_o + C::kWarps * 8 * NT * C::kMergeStride;  // [W][8*NT]
     float* mg_l = mg_m + C::kWarps * 8 * NT;         // [W][8*NT]
     float* cs_o = mg_l + C::kWarps * 8 * NT;         // cluster merge: [HB*G][D], m, l [HB*G]
-    float* cs_m = cs_o + HB * 16 * D;
-    float* cs_l = cs_m + HB * 16;
+    float* cs_m = cs_o + C::kLocalHeads * D;
+    float* cs_l = cs_m + C::kLocalHeads;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
     uint64_t* empty = full + C::kStages;
     volatile StageMeta* meta = reinterpret_cast<volatile StageMeta*>(empty + C::kStages);
@@ -175,7 +182,9 @@ __global__ void __launch_bounds__(MmaCfg<D, HB>::kThreads, 1)
     const int cw = warp - 1;
     const int gid = lane >> 2, tig = lane & 3;
     const int r8 = lane & 7;
-    const int hw = cw / C::kWPH, wi = cw % C::kWPH;  // this warp's head within the block
+    const int grp = cw / C::kWPG, wi = cw % C::kWPG;  // this warp's group, rank in the group
+    const int hw = (CG > 1) ? 0 : grp;                 // its head within the block
+    const int cbase = (CG > 1) ? grp * 16 : 0;         // its first column of the head's group
     const int g = g0 + hw;
 
     // q as the B operand of S^T = K Q^T.  Column n of n-tile t is virtual head
@@ -184,7 +193,7 @@ __global__ void __launch_bounds__(MmaCfg<D, HB>::kThreads, 1)
     uint32_t qb[NT][D / 16][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-        const int c = nt * 8 + gid;
+        const int c = cbase + nt * 8 + gid;
         const bool hv = c < p.G;
         const int hq = g * p.G + (hv ? c : 0);
         const __nv_bfloat16* qh =
@@ -203,7 +212,7 @@ __global__ void __launch_bounds__(MmaCfg<D, HB>::kThreads, 1)
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int j = 0; j < 2; ++j)
-            lim[nt][j] = p.causal ? causal_from + (nt * 8 + 2 * tig + j) % p.nq : 0x7fffffff;
+            lim[nt][j] = p.causal ? causal_from + (cbase + nt * 8 + 2 * tig + j) % p.nq : 0x7fffffff;
 
     // Running state for columns (2*tig, 2*tig+1) of each n-tile: maxima (log2
     // units, equal in all lanes of a column), per-lane partial denominators,
@@ -221,15 +230,15 @@ __global__ void __launch_bounds__(MmaCfg<D, HB>::kThreads, 1)
 
     // ldmatrix row addresses (swizzled 16-byte chunk = chunk ^ (row & 7)).  A
     // stage holds tile/R boxes of [head][half][R rows][128 B] (R = box_rows >=
-    // 16), so this warp's 16 tokens (r0 .. r0 + 15 of its head) sit in one box.
+    // 16), so each 16-token slab of a head (r0 .. r0 + 15) sits in one box.
     const int R = p.box_rows;
     const uint32_t half_bytes = R * 128;
-    const int r0 = wi * 16;
-    const uint32_t warp_base = (r0 / R) * (HB * C::kHalves * half_bytes) + hw * (C::kHalves * half_bytes) +
-                               (r0 % R) * 128;
-    const uint32_t k_row = warp_base + (r8 + 8 * ((lane >> 3) & 1)) * 128;
+    auto slab_base = [&](int r0) -> uint32_t {
+        return (r0 / R) * (HB * C::kHalves * half_bytes) + hw * (C::kHalves * half_bytes) + (r0 % R) * 128;
+    };
+    const uint32_t k_lane = (r8 + 8 * ((lane >> 3) & 1)) * 128;
     const int k_chi = lane >> 4;
-    const uint32_t v_row = warp_base + (r8 + 8 * (lane >> 4)) * 128;
+    const uint32_t v_lane = (r8 + 8 * (lane >> 4)) * 128;
     const int v_chi = (lane >> 3) & 1;
     const float sl2 = p.scale_log2;
     bool timed_out = false;
@@ -242,108 +251,114 @@ __global__ void __launch_bounds__(MmaCfg<D, HB>::kThreads, 1)
         }
         const int tile_valid = meta[s].nvalid;
         if (tile_valid < 0) break;  // end of this block's work
-        const int blk0 = meta[s].tok0 + r0;  // first token of this warp's block
         const uint32_t kbase = smem_u32(stages + s * C::kStageBytes);
         const uint32_t vbase = kbase + C::kKBytes;
-        const int nvalid = tile_valid - r0;  // valid tokens of this warp's 16-token block
+#pragma unroll 1
+        for (int sub = 0; sub < C::kSub; ++sub) {
+            const int r0 = (sub * C::kWPG + wi) * 16;  // this warp's slab of the stage
+            const int blk0 = meta[s].tok0 + r0;       // its first token
+            const int nvalid = tile_valid - r0;       // valid tokens of the slab
+            const uint32_t k_row = slab_base(r0) + k_lane;
+            const uint32_t v_row = slab_base(r0) + v_lane;
 
-        if (nvalid > 0) {
-            // S^T = K_blk Q^T (two accumulators per n-tile to shorten the dependency chain)
-            float sa[NT][4], sb[NT][4];
+            if (nvalid > 0) {
+                // S^T = K_blk Q^T (two accumulators per n-tile to shorten the dependency chain)
+                float sa[NT][4], sb[NT][4];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
+                for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) sa[nt][e] = sb[nt][e] = 0.f;
+                    for (int e = 0; e < 4; ++e) sa[nt][e] = sb[nt][e] = 0.f;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const int c = 2 * (kk & 3) + k_chi;
-                uint32_t a[4];
-                ldsm_x4(a, kbase + (kk >> 2) * half_bytes + k_row + ((c ^ r8) << 4));
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const int c = 2 * (kk & 3) + k_chi;
+                    uint32_t a[4];
+                    ldsm_x4(a, kbase + (kk >> 2) * half_bytes + k_row + ((c ^ r8) << 4));
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    if (kk & 1)
-                        mma_bf16(sb[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
-                    else
-                        mma_bf16(sa[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
-                }
-            }
-            const bool causal_blk = blk0 + 16 > causal_from;
-            uint32_t bh[NT][2], bl[NT][2];
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                float s0 = (sa[nt][0] + sb[nt][0]) * sl2, s1 = (sa[nt][1] + sb[nt][1]) * sl2;
-                float s2 = (sa[nt][2] + sb[nt][2]) * sl2, s3 = (sa[nt][3] + sb[nt][3]) * sl2;
-                if (nvalid < 16) {
-                    if (gid >= nvalid) s0 = s1 = -INFINITY;
-                    if (gid + 8 >= nvalid) s2 = s3 = -INFINITY;
-                }
-                if (causal_blk) {
-                    const int ta = blk0 + gid, tb = ta + 8;
-                    if (ta >= lim[nt][0]) s0 = -INFINITY;
-                    if (ta >= lim[nt][1]) s1 = -INFINITY;
-                    if (tb >= lim[nt][0]) s2 = -INFINITY;
-                    if (tb >= lim[nt][1]) s3 = -INFINITY;
-                }
-                // block maximum per column over the 16 tokens (lanes differing in gid)
-                float bm0 = fmaxf(s0, s2), bm1 = fmaxf(s1, s3);
-#pragma unroll
-                for (int off = 4; off < 32; off <<= 1) {
-                    bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
-                    bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
-                }
-                const float mn0 = fmaxf(m[nt][0], bm0), mn1 = fmaxf(m[nt][1], bm1);
-                const float ms0 = (mn0 == -INFINITY) ? 0.f : mn0;
-                const float ms1 = (mn1 == -INFINITY) ? 0.f : mn1;
-                const float al0 = ex2(m[nt][0] - ms0), al1 = ex2(m[nt][1] - ms1);
-                const float p0 = ex2(s0 - ms0), p1 = ex2(s1 - ms1);
-                const float p2 = ex2(s2 - ms0), p3 = ex2(s3 - ms1);
-                l[nt][0] = l[nt][0] * al0 + (p0 + p2);
-                l[nt][1] = l[nt][1] * al1 + (p1 + p3);
-                m[nt][0] = mn0;
-                m[nt][1] = mn1;
-                if (__any_sync(0xffffffffu, (al0 != 1.f) || (al1 != 1.f))) {
-#pragma unroll
-                    for (int mt = 0; mt < D / 16; ++mt) {
-                        oacc[nt][mt][0] *= al0;
-                        oacc[nt][mt][1] *= al1;
-                        oacc[nt][mt][2] *= al0;
-                        oacc[nt][mt][3] *= al1;
+                    for (int nt = 0; nt < NT; ++nt) {
+                        if (kk & 1)
+                            mma_bf16(sb[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
+                        else
+                            mma_bf16(sa[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
                     }
                 }
-                // P^T as B fragments (k = token, n = column), BF16 hi + lo parts.
-                const __nv_bfloat162 h01 = __floats2bfloat162_rn(p0, p1);
-                const __nv_bfloat162 h23 = __floats2bfloat162_rn(p2, p3);
-                const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
-                const __nv_bfloat162 e01 = __floats2bfloat162_rn(p0 - f01.x, p1 - f01.y);
-                const __nv_bfloat162 e23 = __floats2bfloat162_rn(p2 - f23.x, p3 - f23.y);
-                bh[nt][0] = movtrans(bf16x2_bits(h01));
-                bh[nt][1] = movtrans(bf16x2_bits(h23));
-                bl[nt][0] = movtrans(bf16x2_bits(e01));
-                bl[nt][1] = movtrans(bf16x2_bits(e23));
-            }
-            // V rows past the slice may hold anything (even NaN): zero them.
-            uint32_t vm01 = 0xffffffffu, vm23 = 0xffffffffu;
-            if (nvalid < 16) {
-                const int ta = 2 * tig, tb = 8 + 2 * tig;
-                vm01 = (ta < nvalid ? 0x0000ffffu : 0u) | (ta + 1 < nvalid ? 0xffff0000u : 0u);
-                vm23 = (tb < nvalid ? 0x0000ffffu : 0u) | (tb + 1 < nvalid ? 0xffff0000u : 0u);
-            }
-#pragma unroll
-            for (int mt = 0; mt < D / 16; ++mt) {
-                const int c = 2 * (mt & 3) + v_chi;
-                uint32_t a[4];
-                ldsm_x4_t(a, vbase + (mt >> 2) * half_bytes + v_row + ((c ^ r8) << 4));
-                a[0] &= vm01;
-                a[1] &= vm01;
-                a[2] &= vm23;
-                a[3] &= vm23;
+                const bool causal_blk = blk0 + 16 > causal_from;
+                uint32_t bh[NT][2], bl[NT][2];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    mma_bf16(oacc[nt][mt], a, bh[nt][0], bh[nt][1]);
-                    mma_bf16(oacc[nt][mt], a, bl[nt][0], bl[nt][1]);
+                    float s0 = (sa[nt][0] + sb[nt][0]) * sl2, s1 = (sa[nt][1] + sb[nt][1]) * sl2;
+                    float s2 = (sa[nt][2] + sb[nt][2]) * sl2, s3 = (sa[nt][3] + sb[nt][3]) * sl2;
+                    if (nvalid < 16) {
+                        if (gid >= nvalid) s0 = s1 = -INFINITY;
+                        if (gid + 8 >= nvalid) s2 = s3 = -INFINITY;
+                    }
+                    if (causal_blk) {
+                        const int ta = blk0 + gid, tb = ta + 8;
+                        if (ta >= lim[nt][0]) s0 = -INFINITY;
+                        if (ta >= lim[nt][1]) s1 = -INFINITY;
+                        if (tb >= lim[nt][0]) s2 = -INFINITY;
+                        if (tb >= lim[nt][1]) s3 = -INFINITY;
+                    }
+                    // block maximum per column over the 16 tokens (lanes differing in gid)
+                    float bm0 = fmaxf(s0, s2), bm1 = fmaxf(s1, s3);
+#pragma unroll
+                    for (int off = 4; off < 32; off <<= 1) {
+                        bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
+                        bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
+                    }
+                    const float mn0 = fmaxf(m[nt][0], bm0), mn1 = fmaxf(m[nt][1], bm1);
+                    const float ms0 = (mn0 == -INFINITY) ? 0.f : mn0;
+                    const float ms1 = (mn1 == -INFINITY) ? 0.f : mn1;
+                    const float al0 = ex2(m[nt][0] - ms0), al1 = ex2(m[nt][1] - ms1);
+                    const float p0 = ex2(s0 - ms0), p1 = ex2(s1 - ms1);
+                    const float p2 = ex2(s2 - ms0), p3 = ex2(s3 - ms1);
+                    l[nt][0] = l[nt][0] * al0 + (p0 + p2);
+                    l[nt][1] = l[nt][1] * al1 + (p1 + p3);
+                    m[nt][0] = mn0;
+                    m[nt][1] = mn1;
+                    if (__any_sync(0xffffffffu, (al0 != 1.f) || (al1 != 1.f))) {
+#pragma unroll
+                        for (int mt = 0; mt < D / 16; ++mt) {
+                            oacc[nt][mt][0] *= al0;
+                            oacc[nt][mt][1] *= al1;
+                            oacc[nt][mt][2] *= al0;
+                            oacc[nt][mt][3] *= al1;
+                        }
+                    }
+                    // P^T as B fragments (k = token, n = column), BF16 hi + lo parts.
+                    const __nv_bfloat162 h01 = __floats2bfloat162_rn(p0, p1);
+                    const __nv_bfloat162 h23 = __floats2bfloat162_rn(p2, p3);
+                    const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+                    const __nv_bfloat162 e01 = __floats2bfloat162_rn(p0 - f01.x, p1 - f01.y);
+                    const __nv_bfloat162 e23 = __floats2bfloat162_rn(p2 - f23.x, p3 - f23.y);
+                    bh[nt][0] = movtrans(bf16x2_bits(h01));
+                    bh[nt][1] = movtrans(bf16x2_bits(h23));
+                    bl[nt][0] = movtrans(bf16x2_bits(e01));
+                    bl[nt][1] = movtrans(bf16x2_bits(e23));
+                }
+                // V rows past the slice may hold anything (even NaN): zero them.
+                uint32_t vm01 = 0xffffffffu, vm23 = 0xffffffffu;
+                if (nvalid < 16) {
+                    const int ta = 2 * tig, tb = 8 + 2 * tig;
+                    vm01 = (ta < nvalid ? 0x0000ffffu : 0u) | (ta + 1 < nvalid ? 0xffff0000u : 0u);
+                    vm23 = (tb < nvalid ? 0x0000ffffu : 0u) | (tb + 1 < nvalid ? 0xffff0000u : 0u);
+                }
+#pragma unroll
+                for (int mt = 0; mt < D / 16; ++mt) {
+                    const int c = 2 * (mt & 3) + v_chi;
+                    uint32_t a[4];
+                    ldsm_x4_t(a, vbase + (mt >> 2) * half_bytes + v_row + ((c ^ r8) << 4));
+                    a[0] &= vm01;
+                    a[1] &= vm01;
+                    a[2] &= vm23;
+                    a[3] &= vm23;
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        mma_bf16(oacc[nt][mt], a, bh[nt][0], bh[nt][1]);
+                        mma_bf16(oacc[nt][mt], a, bl[nt][0], bl[nt][1]);
+                    }
                 }
             }
-        }
+        }  // slabs
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
     }
@@ -382,42 +397,46 @@ __global__ void __launch_bounds__(MmaCfg<D, HB>::kThreads, 1)
     const bool poison = bad || (*abort_flag != 0) || (*bad_page != 0);
     const int ct = threadIdx.x - 32;
     // states of the warps serving one head, merged per (head, column, channel)
-    for (int idx = ct; idx < HB * p.G * D; idx += C::kWarps * 32) {
+    // states of the warps of one group, merged per (group, column, channel);
+    // lh = the column's query head within the block's g0 * G ..
+    const int cpg = (CG > 1) ? 16 : p.G;  // columns per group
+    for (int idx = ct; idx < C::kGroups * cpg * D; idx += C::kWarps * 32) {
         int hh = 0, rem = idx;
-        if constexpr (HB > 1) {
-            hh = idx / (p.G * D);
-            rem = idx - hh * (p.G * D);
+        if constexpr (C::kGroups > 1) {
+            hh = idx / (cpg * D);
+            rem = idx - hh * (cpg * D);
         }
         const int h = rem / D, dd = rem - h * D;
-        const int w0 = hh * C::kWPH;
-        float mw[C::kWPH];
+        const int lh = (CG > 1) ? hh * 16 + h : hh * p.G + h;
+        if (CG > 1 && lh >= p.G) continue;  // padding columns of the last group
+        const int w0 = hh * C::kWPG;
+        float mw[C::kWPG];
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < C::kWPH; ++w) {
+        for (int w = 0; w < C::kWPG; ++w) {
             mw[w] = mg_m[(w0 + w) * kCols + h];
             M = fmaxf(M, mw[w]);
         }
         const float Ms = (M == -INFINITY) ? 0.f : M;
-        float ow[C::kWPH], lw[C::kWPH];
+        float ow[C::kWPG], lw[C::kWPG];
 #pragma unroll
-        for (int w = 0; w < C::kWPH; ++w) {
+        for (int w = 0; w < C::kWPG; ++w) {
             const float wt = ex2(mw[w] - Ms);
             ow[w] = wt * mg_o[((w0 + w) * kCols + h) * MS + dd];
             lw[w] = wt * mg_l[(w0 + w) * kCols + h];
         }
         // pairwise tree over the warps
-        const float o = tree_sum<C::kWPH>(ow);
-        const float lsum = tree_sum<C::kWPH>(lw);
+        const float o = tree_sum<C::kWPG>(ow);
+        const float lsum = tree_sum<C::kWPG>(lw);
         if (p.cluster) {  // kept for the cluster row merge
             const float nan = __int_as_float(0x7fc00000);
-            const int hb_h = hh * p.G + h;
-            cs_o[hb_h * D + dd] = poison ? nan : o;
+            cs_o[lh * D + dd] = poison ? nan : o;
             if (dd == 0) {
-                cs_m[hb_h] = poison ? nan : M;
-                cs_l[hb_h] = poison ? nan : lsum;
+                cs_m[lh] = poison ? nan : M;
+                cs_l[lh] = poison ? nan : lsum;
             }
         } else {
-            emit_state(p, b, (g0 + hh) * p.G + h, split, D, dd, o, lsum, M, poison);
+            emit_state(p, b, g0 * p.G + lh, split, D, dd, o, lsum, M, poison);
         }
     }
     const size_t hq0 = static_cast<size_t>(b) * p.Hq + static_cast<size_t>(g0) * p.G;
@@ -432,12 +451,12 @@ __global__ void __launch_bounds__(MmaCfg<D, HB>::kThreads, 1)
     allow_dependents();
 }
 
-template <int D, int NT, int HB>
+template <int D, int NT, int HB, int CG = 1>
 cudaError_t launch_impl(const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& p,
                         cudaStream_t stream) {
-    using C = MmaCfg<D, HB>;
+    using C = MmaCfg<D, HB, CG>;
     static std::atomic<unsigned long long> configured{0};
-    cudaError_t e = set_smem_once(split_kv_mma_kernel<D, NT, HB>, C::kSmem, configured);
+    cudaError_t e = set_smem_once(split_kv_mma_kernel<D, NT, HB, CG>, C::kSmem, configured);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.P, p.Hkv / HB, p.B);
@@ -453,7 +472,7 @@ cudaError_t launch_impl(const CUtensorMap& tk, const CUtensorMap& tv, const Spli
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = p.cluster ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<D, NT, HB>, tk, tv, p);
+    return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<D, NT, HB, CG>, tk, tv, p);
 }
 
 }  // namespace
@@ -466,7 +485,12 @@ Geometry mma_geometry(int head_dim, int heads_per_block) {
 
 cudaError_t launch_split_mma(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv,
                              const SplitParams& p, cudaStream_t stream) {
-    // one n-tile of 8 columns per KV head group, two for up to 16
+    // one n-tile of 8 columns per KV head group, two for up to 16; beyond, 2 or
+    // 4 column groups of 16 (head_dim 128, one KV head per block)
+    if (p.G > 16) {
+        if (head_dim != 128 || p.hb != 1 || p.G > 64) return cudaErrorInvalidValue;
+        return p.G > 32 ? launch_impl<128, 2, 1, 4>(tk, tv, p, stream) : launch_impl<128, 2, 1, 2>(tk, tv, p, stream);
+    }
     const bool two = p.G > 8;
     if (p.hb == 2 && head_dim == 128)
         return two ? launch_impl<128, 2, 2>(tk, tv, p, stream) : launch_impl<128, 1, 2>(tk, tv, p, stream);

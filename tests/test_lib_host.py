@@ -60,7 +60,10 @@ def shape(ta, **kw):
     (dict(num_q_heads=12, num_kv_heads=8), -3),      # Hq % Hkv != 0
     (dict(num_q_heads=24, num_kv_heads=8), 0),       # G = 3: tensor-core kernel (BF16)
     (dict(num_q_heads=24, num_kv_heads=8, q_dtype=0, kv_dtype=0), -3),   # G = 3 without BF16: no kernel
-    (dict(num_q_heads=128, num_kv_heads=4), -3),     # G = 32 unsupported
+    (dict(num_q_heads=128, num_kv_heads=4), 0),      # G = 32: BF16 column groups
+    (dict(num_q_heads=256, num_kv_heads=2), -3),     # G = 128 unsupported
+    (dict(num_q_heads=128, num_kv_heads=4, head_dim=64), -3),  # G > 16 needs head_dim 128
+    (dict(num_q_heads=128, num_kv_heads=4, q_dtype=0, kv_dtype=0), -3),  # FMA: G <= 16
     (dict(head_dim=96), -3),
     (dict(batch=0), -3),
     (dict(max_seqlen=0), -3),
@@ -153,8 +156,8 @@ def test_decode_argument_errors_before_any_cuda_call(ta):
     assert _decode_raw(ta, shape(ta, head_dim=32)) == -3
     f32 = shape(ta, q_dtype=0, kv_dtype=0)
     assert _decode_raw(ta, f32, opts=ta.TaOptions(2, 0, None, None, None, None)) == -4   # mma needs bf16
-    assert _decode_raw(ta, shape(ta, num_q_heads=256, num_kv_heads=8),
-                       opts=ta.TaOptions(2, 0, None, None, None, None)) == -3          # G = 32 > 16
+    assert _decode_raw(ta, shape(ta, num_q_heads=256, num_kv_heads=2),
+                       opts=ta.TaOptions(2, 0, None, None, None, None)) == -3          # G = 128 > 64
     assert _decode_raw(ta, s, opts=ta.TaOptions(0, 16, None, None, None, None)) == -3  # unknown flag bit
     assert _decode_raw(ta, s, opts=ta.TaOptions(9, 0, None, None, None, None)) == -3  # unknown kernel
 

@@ -84,7 +84,7 @@ def test_multi_query_paged(page_size):
 
 
 def test_multi_query_argument_errors():
-    inp = _inputs(torch.bfloat16, 128, 2, 8, 4, [100], 128, seed=1)   # G*nq = 32 > 16
+    inp = _inputs(torch.bfloat16, 128, 2, 8, 16, [100], 128, seed=1)   # G*nq = 128 > 64
     with pytest.raises(ta.TreeAttnError):
         ta.tree_attn_decode_multi(inp["qm"].cuda(), inp["k"].cuda(), inp["v"].cuda(),
                                   inp["seqlens"].cuda())
