@@ -240,6 +240,9 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, CG>::kThreads, 1)
     const int k_chi = lane >> 4;
     const uint32_t v_lane = (r8 + 8 * (lane >> 4)) * 128;
     const int v_chi = (lane >> 3) & 1;
+    uint32_t sbase[C::kSub];  // this warp's slab offsets within a stage (fixed for the whole loop)
+#pragma unroll
+    for (int sub = 0; sub < C::kSub; ++sub) sbase[sub] = slab_base((sub * C::kWPG + wi) * 16);
     const float sl2 = p.scale_log2;
     bool timed_out = false;
 
@@ -253,13 +256,13 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, CG>::kThreads, 1)
         if (tile_valid < 0) break;  // end of this block's work
         const uint32_t kbase = smem_u32(stages + s * C::kStageBytes);
         const uint32_t vbase = kbase + C::kKBytes;
-#pragma unroll 1
+#pragma unroll
         for (int sub = 0; sub < C::kSub; ++sub) {
             const int r0 = (sub * C::kWPG + wi) * 16;  // this warp's slab of the stage
             const int blk0 = meta[s].tok0 + r0;       // its first token
             const int nvalid = tile_valid - r0;       // valid tokens of the slab
-            const uint32_t k_row = slab_base(r0) + k_lane;
-            const uint32_t v_row = slab_base(r0) + v_lane;
+            const uint32_t k_row = sbase[sub] + k_lane;
+            const uint32_t v_row = sbase[sub] + v_lane;
 
             if (nvalid > 0) {
                 // S^T = K_blk Q^T (two accumulators per n-tile to shorten the dependency chain)
