@@ -388,6 +388,20 @@ def run_ours(args, rank, world, local):
         torch.cuda.synchronize()
         barrier(world)
         split_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    # ---- per-step spread: each step bracketed by its own events (outside the timed regions)
+    n_dist = min(args.steps, 1000)
+    dev_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n_dist)]
+    torch.cuda.synchronize()
+    for i in range(n_dist):
+        dev_evs[i][0].record(stream)
+        step(i)
+        dev_evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    per_step = sorted(a.elapsed_time(b) * 1e3 for a, b in dev_evs)
+    dist = {"p10": round(per_step[n_dist // 10], 3), "p50": round(statistics.median(per_step), 3),
+            "p90": round(per_step[min(n_dist - 1, (9 * n_dist) // 10)], 3), "steps": n_dist,
+            "unit": "us", "how": "one event pair per step, after the timed region"}
     if rank == 0:
         time.sleep(0.1)
         sampler.stop()
@@ -461,6 +475,7 @@ def run_ours(args, rank, world, local):
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
         "us_per_step": round(ms_per_step * 1e3, 3),
+        "us_per_step_dist": dist,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3 KV, bf16 q, f16 mma / f32 accumulate" if args.fp8 else "bf16",
         "data": "synthetic (seeded N(0,1) Llama-shaped KV cache; no weights or datasets)"
