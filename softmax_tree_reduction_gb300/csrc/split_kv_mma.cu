@@ -207,12 +207,8 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, CG>::kThreads, 1)
     // Causal limits of this thread's columns (query i of nq sees tokens < N - nq + 1 + i);
     // masking applies only to blocks reaching past N - nq + 1.
     const int causal_from = p.causal ? N - p.nq + 1 : 0x7fffffff;
-    int lim[NT][2];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int j = 0; j < 2; ++j)
-            lim[nt][j] = p.causal ? causal_from + (cbase + nt * 8 + 2 * tig + j) % p.nq : 0x7fffffff;
+    // (recomputed where used: only blocks that reach the causal edge need them)
+    auto lim = [&](int nt, int j) { return causal_from + (cbase + nt * 8 + 2 * tig + j) % p.nq; };
 
     // Running state for columns (2*tig, 2*tig+1) of each n-tile: maxima (log2
     // units, equal in all lanes of a column), per-lane partial denominators,
@@ -244,6 +240,7 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, CG>::kThreads, 1)
 #pragma unroll
     for (int sub = 0; sub < C::kSub; ++sub) sbase[sub] = slab_base((sub * C::kWPG + wi) * 16);
     const float sl2 = p.scale_log2;
+    constexpr int J = (C::kSub >= 2) ? 2 : 1;  // slabs taken together
     bool timed_out = false;
 
     for (int it = 0;; ++it) {
@@ -256,53 +253,74 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, CG>::kThreads, 1)
         if (tile_valid < 0) break;  // end of this block's work
         const uint32_t kbase = smem_u32(stages + s * C::kStageBytes);
         const uint32_t vbase = kbase + C::kKBytes;
+        // A warp's slabs of the stage are taken J at a time as one block of
+        // 16 J tokens: the J score products are independent chains, and the
+        // block maximum, the rescale and the denominator update happen once.
 #pragma unroll
-        for (int sub = 0; sub < C::kSub; ++sub) {
-            const int r0 = (sub * C::kWPG + wi) * 16;  // this warp's slab of the stage
-            const int blk0 = meta[s].tok0 + r0;       // its first token
-            const int nvalid = tile_valid - r0;       // valid tokens of the slab
-            const uint32_t k_row = sbase[sub] + k_lane;
-            const uint32_t v_row = sbase[sub] + v_lane;
+        for (int sp = 0; sp < C::kSub; sp += J) {
+            int blk0[J], nvalid[J];  // first token, valid tokens of each slab
+            uint32_t k_row[J], v_row[J];
+#pragma unroll
+            for (int j = 0; j < J; ++j) {
+                const int r0 = ((sp + j) * C::kWPG + wi) * 16;  // this warp's slab of the stage
+                blk0[j] = meta[s].tok0 + r0;
+                nvalid[j] = tile_valid - r0;
+                k_row[j] = sbase[sp + j] + k_lane;
+                v_row[j] = sbase[sp + j] + v_lane;
+            }
 
-            if (nvalid > 0) {
-                // S^T = K_blk Q^T (two accumulators per n-tile to shorten the dependency chain)
-                float sa[NT][4], sb[NT][4];
+            if (nvalid[0] > 0) {  // later slabs of the block hold later tokens
+                // S^T = K_blk Q^T.  One slab: two accumulators per n-tile to
+                // shorten the chains; two slabs are independent chains already.
+                constexpr int kAcc = (J == 1) ? 2 : 1;
+                float sacc[kAcc][J][NT][4];
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
+                for (int u = 0; u < kAcc; ++u)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) sa[nt][e] = sb[nt][e] = 0.f;
+                    for (int j = 0; j < J; ++j)
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) sacc[u][j][nt][e] = 0.f;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const int c = 2 * (kk & 3) + k_chi;
-                    uint32_t a[4];
-                    ldsm_x4(a, kbase + (kk >> 2) * half_bytes + k_row + ((c ^ r8) << 4));
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        if (kk & 1)
-                            mma_bf16(sb[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
-                        else
-                            mma_bf16(sa[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
+                    for (int j = 0; j < J; ++j) {
+                        uint32_t a[4];
+                        ldsm_x4(a, kbase + (kk >> 2) * half_bytes + k_row[j] + ((c ^ r8) << 4));
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+                            mma_bf16(sacc[(kAcc == 2) ? (kk & 1) : 0][j][nt], a, qb[nt][kk][0], qb[nt][kk][1]);
                     }
                 }
-                const bool causal_blk = blk0 + 16 > causal_from;
-                uint32_t bh[NT][2], bl[NT][2];
+                uint32_t bh[J][NT][2], bl[J][NT][2];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    float s0 = (sa[nt][0] + sb[nt][0]) * sl2, s1 = (sa[nt][1] + sb[nt][1]) * sl2;
-                    float s2 = (sa[nt][2] + sb[nt][2]) * sl2, s3 = (sa[nt][3] + sb[nt][3]) * sl2;
-                    if (nvalid < 16) {
-                        if (gid >= nvalid) s0 = s1 = -INFINITY;
-                        if (gid + 8 >= nvalid) s2 = s3 = -INFINITY;
+                    float sc[J][4];
+                    float bm0 = -INFINITY, bm1 = -INFINITY;
+#pragma unroll
+                    for (int j = 0; j < J; ++j) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            sc[j][e] = ((kAcc == 2) ? sacc[0][j][nt][e] + sacc[kAcc - 1][j][nt][e]
+                                                    : sacc[0][j][nt][e]) * sl2;
+                        if (nvalid[j] < 16) {
+                            if (gid >= nvalid[j]) sc[j][0] = sc[j][1] = -INFINITY;
+                            if (gid + 8 >= nvalid[j]) sc[j][2] = sc[j][3] = -INFINITY;
+                        }
+                        if (blk0[j] + 16 > causal_from) {
+                            const int ta = blk0[j] + gid, tb = ta + 8;
+                            const int l0 = lim(nt, 0), l1 = lim(nt, 1);
+                            if (ta >= l0) sc[j][0] = -INFINITY;
+                            if (ta >= l1) sc[j][1] = -INFINITY;
+                            if (tb >= l0) sc[j][2] = -INFINITY;
+                            if (tb >= l1) sc[j][3] = -INFINITY;
+                        }
+                        bm0 = fmaxf(bm0, fmaxf(sc[j][0], sc[j][2]));
+                        bm1 = fmaxf(bm1, fmaxf(sc[j][1], sc[j][3]));
                     }
-                    if (causal_blk) {
-                        const int ta = blk0 + gid, tb = ta + 8;
-                        if (ta >= lim[nt][0]) s0 = -INFINITY;
-                        if (ta >= lim[nt][1]) s1 = -INFINITY;
-                        if (tb >= lim[nt][0]) s2 = -INFINITY;
-                        if (tb >= lim[nt][1]) s3 = -INFINITY;
-                    }
-                    // block maximum per column over the 16 tokens (lanes differing in gid)
-                    float bm0 = fmaxf(s0, s2), bm1 = fmaxf(s1, s3);
+                    // block maximum per column over its 16 J tokens (lanes differing in gid)
 #pragma unroll
                     for (int off = 4; off < 32; off <<= 1) {
                         bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
@@ -312,10 +330,26 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, CG>::kThreads, 1)
                     const float ms0 = (mn0 == -INFINITY) ? 0.f : mn0;
                     const float ms1 = (mn1 == -INFINITY) ? 0.f : mn1;
                     const float al0 = ex2(m[nt][0] - ms0), al1 = ex2(m[nt][1] - ms1);
-                    const float p0 = ex2(s0 - ms0), p1 = ex2(s1 - ms1);
-                    const float p2 = ex2(s2 - ms0), p3 = ex2(s3 - ms1);
-                    l[nt][0] = l[nt][0] * al0 + (p0 + p2);
-                    l[nt][1] = l[nt][1] * al1 + (p1 + p3);
+                    float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+                    for (int j = 0; j < J; ++j) {
+                        const float p0 = ex2(sc[j][0] - ms0), p1 = ex2(sc[j][1] - ms1);
+                        const float p2 = ex2(sc[j][2] - ms0), p3 = ex2(sc[j][3] - ms1);
+                        ps0 += p0 + p2;
+                        ps1 += p1 + p3;
+                        // P^T as B fragments (k = token, n = column), BF16 hi + lo parts.
+                        const __nv_bfloat162 h01 = __floats2bfloat162_rn(p0, p1);
+                        const __nv_bfloat162 h23 = __floats2bfloat162_rn(p2, p3);
+                        const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+                        const __nv_bfloat162 e01 = __floats2bfloat162_rn(p0 - f01.x, p1 - f01.y);
+                        const __nv_bfloat162 e23 = __floats2bfloat162_rn(p2 - f23.x, p3 - f23.y);
+                        bh[j][nt][0] = movtrans(bf16x2_bits(h01));
+                        bh[j][nt][1] = movtrans(bf16x2_bits(h23));
+                        bl[j][nt][0] = movtrans(bf16x2_bits(e01));
+                        bl[j][nt][1] = movtrans(bf16x2_bits(e23));
+                    }
+                    l[nt][0] = l[nt][0] * al0 + ps0;
+                    l[nt][1] = l[nt][1] * al1 + ps1;
                     m[nt][0] = mn0;
                     m[nt][1] = mn1;
                     if (__any_sync(0xffffffffu, (al0 != 1.f) || (al1 != 1.f))) {
@@ -327,37 +361,30 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, CG>::kThreads, 1)
                             oacc[nt][mt][3] *= al1;
                         }
                     }
-                    // P^T as B fragments (k = token, n = column), BF16 hi + lo parts.
-                    const __nv_bfloat162 h01 = __floats2bfloat162_rn(p0, p1);
-                    const __nv_bfloat162 h23 = __floats2bfloat162_rn(p2, p3);
-                    const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
-                    const __nv_bfloat162 e01 = __floats2bfloat162_rn(p0 - f01.x, p1 - f01.y);
-                    const __nv_bfloat162 e23 = __floats2bfloat162_rn(p2 - f23.x, p3 - f23.y);
-                    bh[nt][0] = movtrans(bf16x2_bits(h01));
-                    bh[nt][1] = movtrans(bf16x2_bits(h23));
-                    bl[nt][0] = movtrans(bf16x2_bits(e01));
-                    bl[nt][1] = movtrans(bf16x2_bits(e23));
-                }
-                // V rows past the slice may hold anything (even NaN): zero them.
-                uint32_t vm01 = 0xffffffffu, vm23 = 0xffffffffu;
-                if (nvalid < 16) {
-                    const int ta = 2 * tig, tb = 8 + 2 * tig;
-                    vm01 = (ta < nvalid ? 0x0000ffffu : 0u) | (ta + 1 < nvalid ? 0xffff0000u : 0u);
-                    vm23 = (tb < nvalid ? 0x0000ffffu : 0u) | (tb + 1 < nvalid ? 0xffff0000u : 0u);
                 }
 #pragma unroll
-                for (int mt = 0; mt < D / 16; ++mt) {
-                    const int c = 2 * (mt & 3) + v_chi;
-                    uint32_t a[4];
-                    ldsm_x4_t(a, vbase + (mt >> 2) * half_bytes + v_row + ((c ^ r8) << 4));
-                    a[0] &= vm01;
-                    a[1] &= vm01;
-                    a[2] &= vm23;
-                    a[3] &= vm23;
+                for (int j = 0; j < J; ++j) {
+                    // V rows past the slice may hold anything (even NaN): zero them.
+                    uint32_t vm01 = 0xffffffffu, vm23 = 0xffffffffu;
+                    if (nvalid[j] < 16) {
+                        const int ta = 2 * tig, tb = 8 + 2 * tig;
+                        vm01 = (ta < nvalid[j] ? 0x0000ffffu : 0u) | (ta + 1 < nvalid[j] ? 0xffff0000u : 0u);
+                        vm23 = (tb < nvalid[j] ? 0x0000ffffu : 0u) | (tb + 1 < nvalid[j] ? 0xffff0000u : 0u);
+                    }
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        mma_bf16(oacc[nt][mt], a, bh[nt][0], bh[nt][1]);
-                        mma_bf16(oacc[nt][mt], a, bl[nt][0], bl[nt][1]);
+                    for (int mt = 0; mt < D / 16; ++mt) {
+                        const int c = 2 * (mt & 3) + v_chi;
+                        uint32_t a[4];
+                        ldsm_x4_t(a, vbase + (mt >> 2) * half_bytes + v_row[j] + ((c ^ r8) << 4));
+                        a[0] &= vm01;
+                        a[1] &= vm01;
+                        a[2] &= vm23;
+                        a[3] &= vm23;
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            mma_bf16(oacc[nt][mt], a, bh[j][nt][0], bh[j][nt][1]);
+                            mma_bf16(oacc[nt][mt], a, bl[j][nt][0], bl[j][nt][1]);
+                        }
                     }
                 }
             }
