@@ -228,10 +228,17 @@ int heads_per_block(const ta_shape* s, int kernel, int page_size, int num_sms) {
         want = kFp8HeadsPage16;
     else if (kernel == TA_KERNEL_MMA && s->head_dim == 128 && sh < st && s->num_q_heads <= 16 * s->num_kv_heads)
         want = kMmaHeadsPage16;
-    const bool fused1 = pick_splits_hb(s, nullptr, num_sms, kernel, 1) <= kFusedMaxSplits;
+    const int splits1 = pick_splits_hb(s, nullptr, num_sms, kernel, 1);
+    const bool fused1 = splits1 <= kFusedMaxSplits;
+    // With two n-tiles (9..16 columns) the consumers carry twice the work per
+    // token: sharing a block between heads pays only when it does not also
+    // shorten every block's slice (more splits).
+    const bool wide = s->num_q_heads > 8 * s->num_kv_heads;
     for (; want > 1; want /= 2) {
         if (s->num_kv_heads % want != 0) continue;
-        if (!fused1 || pick_splits_hb(s, nullptr, num_sms, kernel, want) <= kFusedMaxSplits) break;
+        const int splits = pick_splits_hb(s, nullptr, num_sms, kernel, want);
+        if (wide && splits > splits1) continue;
+        if (!fused1 || splits <= kFusedMaxSplits) break;
     }
     return want;
 }

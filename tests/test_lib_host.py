@@ -255,6 +255,22 @@ def test_pick_splits_paged_small_pages_share_blocks(ta):
             ta.tree_attn_pick_splits(fp8, None, 152, page_size=bad)
 
 
+def test_pick_splits_paged_wide_groups(ta):
+    """With 9..16 columns per KV head (two n-tiles) a block serves several KV
+    heads only where that needs no more splits than one head per block."""
+    # 8B-shaped, 4 queries per row: 16 columns per KV head; sharing would need 38 splits
+    for kv in (1, 2):
+        nq4 = shape(ta, kv_dtype=kv, num_q_heads=32 * 4)
+        assert ta.tree_attn_pick_splits(nq4, None, 152, page_size=16) == 19
+    # 70B-shaped B4, 2 queries: shared blocks keep 19 splits, so they stay
+    for kv in (1, 2):
+        big = shape(ta, kv_dtype=kv, batch=4, num_q_heads=64 * 2, max_seqlen=262144)
+        assert ta.tree_attn_pick_splits(big, None, 152, page_size=16) == 19
+    # 8 columns (one n-tile) still shares: 2 heads per block, 38 splits
+    nq2 = shape(ta, num_q_heads=32 * 2)
+    assert ta.tree_attn_pick_splits(nq2, None, 152, page_size=16) == 38
+
+
 def test_cluster_merge_arguments(ta):
     s = shape(ta)
     f32 = shape(ta, q_dtype=0, kv_dtype=0)
