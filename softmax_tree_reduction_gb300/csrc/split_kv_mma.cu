@@ -53,8 +53,16 @@ struct MmaCfg {
     static constexpr int kStageBytes = 2 * kKBytes;  // K and V
     static constexpr int kStages = (D == 128) ? 3 : 6;
     static constexpr int kBarBytes = 2 * kStages * 8 + kStages * 8 + 32;
+    // Column groups keep q in shared memory ([column][d] rows padded by 16
+    // bytes, so the 8 rows an ldmatrix reads fall in distinct banks) and load
+    // its fragments per k-step, which leaves the registers to the running state.
+    static constexpr bool kQSmem = CG > 1;
+    static constexpr int kQRowBytes = (D + 8) * 2;
+    static constexpr int kQOff = (kStages * kStageBytes + kBarBytes + 127) / 128 * 128;
+    static constexpr int kQBytes = kQSmem ? 16 * CG * kQRowBytes : 0;
     // the warps' states are merged in the stage buffers once streaming is over
-    static constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes;
+    static constexpr int kSmem = 1024 + (kQSmem ? kQOff + kQBytes : kStages * kStageBytes + kBarBytes);
+    static_assert(kSmem <= 227 * 1024, "shared memory per block");
     static constexpr int kThreads = 32 * (kWarps + 1);
     // Row stride of a warp state in the merge buffer: 4 floats of padding make
     // the fragment stores (rows 2 tig, 2 tig + 1; channels 16 mt + gid) hit 32
@@ -191,8 +199,23 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, CG>::kThreads, 1)
     // c = 8t + n of this KV head's group: a query head, or a (head, query) pair
     // when several queries share the cache (q rows are [head][query]).
     uint32_t qb[NT][D / 16][2];
+    uint32_t q_lane = 0;  // kQSmem: this lane's ldmatrix row address (k-step 0)
+    if constexpr (C::kQSmem) {
+        // all groups' columns, [column][d] bf16 pairs; padding columns are zero
+        uint8_t* qs = smem + C::kQOff;
+        const uint32_t* q32 = static_cast<const uint32_t*>(p.q);
+        for (int idx = threadIdx.x - 32; idx < 16 * CG * (D / 2); idx += C::kWarps * 32) {
+            const int c = idx / (D / 2), w = idx - c * (D / 2);
+            const uint32_t v =
+                (c < p.G) ? q32[(static_cast<size_t>(b) * p.Hq + g0 * p.G + c) * (D / 2) + w] : 0u;
+            *reinterpret_cast<uint32_t*>(qs + c * C::kQRowBytes + 4 * w) = v;
+        }
+        consumer_sync(C::kWarps * 32);
+        // matrices of an x4 load: (n-tile 0, k 0..7), (0, 8..15), (1, 0..7), (1, 8..15)
+        q_lane = smem_u32(qs) + (cbase + 8 * (lane >> 4) + r8) * C::kQRowBytes + 16 * ((lane >> 3) & 1);
+    }
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
+    for (int nt = 0; nt < NT && !C::kQSmem; ++nt) {
         const int c = cbase + nt * 8 + gid;
         const bool hv = c < p.G;
         const int hq = g * p.G + (hv ? c : 0);
@@ -285,13 +308,19 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, CG>::kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const int c = 2 * (kk & 3) + k_chi;
+                    uint32_t qf[4];  // kQSmem: B fragments of both n-tiles for this k-step
+                    if constexpr (C::kQSmem) ldsm_x4(qf, q_lane + 32 * kk);
 #pragma unroll
                     for (int j = 0; j < J; ++j) {
                         uint32_t a[4];
                         ldsm_x4(a, kbase + (kk >> 2) * half_bytes + k_row[j] + ((c ^ r8) << 4));
 #pragma unroll
-                        for (int nt = 0; nt < NT; ++nt)
-                            mma_bf16(sacc[(kAcc == 2) ? (kk & 1) : 0][j][nt], a, qb[nt][kk][0], qb[nt][kk][1]);
+                        for (int nt = 0; nt < NT; ++nt) {
+                            if constexpr (C::kQSmem)
+                                mma_bf16(sacc[(kAcc == 2) ? (kk & 1) : 0][j][nt], a, qf[2 * nt], qf[2 * nt + 1]);
+                            else
+                                mma_bf16(sacc[(kAcc == 2) ? (kk & 1) : 0][j][nt], a, qb[nt][kk][0], qb[nt][kk][1]);
+                        }
                     }
                 }
                 uint32_t bh[J][NT][2], bl[J][NT][2];
