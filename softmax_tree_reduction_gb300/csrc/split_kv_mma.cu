@@ -293,9 +293,10 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, CG>::kThreads, 1)
             }
 
             if (nvalid[0] > 0) {  // later slabs of the block hold later tokens
-                // S^T = K_blk Q^T.  One slab: two accumulators per n-tile to
-                // shorten the chains; two slabs are independent chains already.
-                constexpr int kAcc = (J == 1) ? 2 : 1;
+                // S^T = K_blk Q^T, two accumulators per slab and n-tile to
+                // shorten the chains (one with four slabs a stage, where the
+                // registers are short: measured slower with two).
+                constexpr int kAcc = (C::kSub <= 2) ? 2 : 1;
                 float sacc[kAcc][J][NT][4];
 #pragma unroll
                 for (int u = 0; u < kAcc; ++u)
