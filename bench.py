@@ -75,6 +75,8 @@ def parse_args(argv=None):
                     help="comma list of context lengths for the workload's head shape (heuristic splits): "
                          "print one JSON line per length, then exit")
     ap.add_argument("--sweep-kernels", default="mma,fma")
+    ap.add_argument("--sweep-len", type=int, default=0,
+                    help="split sweep: context length per row instead of the workload's (0: the workload's)")
     ap.add_argument("--paged", type=int, default=0,
                     help="run through the paged-KV entry point with this page size (pages shuffled in a pool)")
     ap.add_argument("--queries", type=int, default=1,
@@ -597,9 +599,10 @@ def run_sweeps(args):
     peak, _ = load_peaks()
     lines = []
     if args.sweep_splits:
-        copies = draw(w.max_seqlen)
+        n_tok = args.sweep_len if args.sweep_len > 0 else w.max_seqlen
+        copies = draw(n_tok)
         shape = ta.make_shape(copies[0]["q"], copies[0]["k"])
-        kv_bytes = w.kv_bytes(np.full(w.batch, w.max_seqlen))
+        kv_bytes = w.kv_bytes(np.full(w.batch, n_tok))
         B, Hq, d = copies[0]["q"].shape
         out = torch.empty(B, Hq, d, device="cuda")
         lse = torch.empty(B, Hq, device="cuda")
@@ -611,7 +614,7 @@ def run_sweeps(args):
                 ms, split = _time_steps(ta, torch, copies, P, kern, args.steps, args.warmup, out, lse, ws,
                                         args.deterministic, args.graph)
                 lines.append({"sweep": "splits", "workload": w.name, "kernel": "fp8" if args.fp8 else kern,
-                              "num_splits": P,
+                              "context": n_tok, "num_splits": P,
                               "deterministic": args.deterministic, "graph": args.graph,
                               "heuristic": P == heur, "us_per_step": round(ms * 1e3, 3),
                               "split_kernel_us": round(split * 1e3, 3),
