@@ -193,24 +193,33 @@ __global__ void __launch_bounds__(Fp8Cfg<HB>::kThreads, 1)
     // q (BF16): column c = 8 nt + gid of n-tile nt (a query head, or a (head,
     // query) pair when several queries share the cache), channels 32 tig ..
     // 32 tig + 31 in the permuted order.
-    float qv[NT][32];
+    // (kept as BF16 pairs: element 2 i of the chunk in the low half of word i)
+    uint32_t qw[NT][16];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         const int c = nt * 8 + gid;
         const bool hv = c < p.G;
         const int hq = g * p.G + (hv ? c : 0);
-        const __nv_bfloat16* qh =
-            static_cast<const __nv_bfloat16*>(p.q) + (static_cast<size_t>(b) * p.Hq + hq) * D + 32 * tig;
+        const uint4* qh = reinterpret_cast<const uint4*>(
+            static_cast<const __nv_bfloat16*>(p.q) + (static_cast<size_t>(b) * p.Hq + hq) * D + 32 * tig);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) qv[nt][j] = hv ? __bfloat162float(qh[j]) : 0.f;
+        for (int i = 0; i < 4; ++i) {
+            const uint4 v = hv ? qh[i] : make_uint4(0u, 0u, 0u, 0u);
+            qw[nt][4 * i] = v.x;
+            qw[nt][4 * i + 1] = v.y;
+            qw[nt][4 * i + 2] = v.z;
+            qw[nt][4 * i + 3] = v.w;
+        }
     }
+    auto lo = [](uint32_t w) { return __uint_as_float(w << 16); };
+    auto hi = [](uint32_t w) { return __uint_as_float(w & 0xffff0000u); };
     // exact power-of-two scale bringing max|q| into [2^14, 2^15): every q value
     // of the group is held by some lane of this warp
     float amax = 0.f;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(qv[nt][j]));
+        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fmaxf(fabsf(lo(qw[nt][i])), fabsf(hi(qw[nt][i]))));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
     int qexp = 0;
@@ -225,8 +234,9 @@ __global__ void __launch_bounds__(Fp8Cfg<HB>::kThreads, 1)
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-            qb[nt][kk][0] = half2_bits(__floats2half2_rn(qv[nt][4 * kk] * qs, qv[nt][4 * kk + 1] * qs));
-            qb[nt][kk][1] = half2_bits(__floats2half2_rn(qv[nt][4 * kk + 2] * qs, qv[nt][4 * kk + 3] * qs));
+            qb[nt][kk][0] = half2_bits(__floats2half2_rn(lo(qw[nt][2 * kk]) * qs, hi(qw[nt][2 * kk]) * qs));
+            qb[nt][kk][1] =
+                half2_bits(__floats2half2_rn(lo(qw[nt][2 * kk + 1]) * qs, hi(qw[nt][2 * kk + 1]) * qs));
         }
     const float sl2 = p.scale_log2 * ks / qs;
 
