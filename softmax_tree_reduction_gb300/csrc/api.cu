@@ -33,8 +33,11 @@ __device__ unsigned g_sched_ring[kRingSlots];
 // Tokens per run-time scheduled chunk of a row (rounded to whole tiles).
 constexpr int kChunkTokens = 128;
 // Tokens of its slice each block prefetches into L2 before waiting on the
-// previous grid (fills the DRAM time of that grid's merge tail).
+// previous grid (fills the DRAM time of that grid's merge tail).  Measured
+// optima: 1152 for BF16 caches (576 KB per KV head), 768 for FP8 (192 KB;
+// 512 / 1152 / 1792 / 2304 were slower on the 8B-shaped layer).
 constexpr int kPrefetchTokens = 1152;
+constexpr int kPrefetchTokensFp8 = 768;
 // The row's last block merges the partial states itself when there are few
 // of them (its merge costs about one L2 round trip per 20 states, serially);
 // more splits go to the combine kernel, which spreads the merge over (h, b)
@@ -571,7 +574,8 @@ int decode_impl(const ta_shape* shape, const ta_paged_kv* paged, int nq, int cau
                                            : 1.0f / std::sqrt(static_cast<float>(shape->head_dim));
     p.scale_log2 = scale * ta::kLog2e;
     p.chunk_tiles = std::max(1, kChunkTokens / geo.tile_tokens);
-    p.prefetch_tiles = std::max(1, kPrefetchTokens / geo.tile_tokens);
+    p.prefetch_tiles =
+        std::max(1, (kernel == kKernelFp8 ? kPrefetchTokensFp8 : kPrefetchTokens) / geo.tile_tokens);
     p.box_rows = rows;
     p.hb = hb;
     p.stall = (options && (options->flags & TA_FLAG_DIAG_STALL)) ? 1 : 0;
