@@ -44,12 +44,12 @@ FALLBACK_HBM_GBS = 6800.0
 NCU_TRAFFIC = {
     # profiles/split_kv_mma_llama31_8b_131k.md
     ("mma", "llama3.1-8b-decode-layer"): {
-        "bytes_per_launch": 537336320 + 3180032, "num_splits": 19,
-        "src_sha256": "6ee28ccf5f8de4a7280c4e49fe742baaa571464a88947abcc77ec22cf319f172"},
+        "bytes_per_launch": 537324800 + 2997504, "num_splits": 19,
+        "src_sha256": "696e23f05d8bd1508358c5982ea2f3223cce80b325e630299f2717986676f60b"},
     # profiles/split_kv_fp8_llama31_8b_131k.md
     ("fp8", "llama3.1-8b-decode-layer"): {
-        "bytes_per_launch": 268540416 + 3370496, "num_splits": 19,
-        "src_sha256": "467c49cb2c8a7f07bd440048bc42e92e9a62db9fc2aa3f180e936441efa4a4ee"},
+        "bytes_per_launch": 268520960 + 2965248, "num_splits": 19,
+        "src_sha256": "5f8dbf729267369e5bfa9ce20bfb4e3f67c003f9c734ae4f114ddee1765daa73"},
 }
 
 
