@@ -278,3 +278,29 @@ def test_cluster_merge_arguments(ta):
     assert _decode_raw(ta, s, P=9, ws=0x7000, wsb=1 << 30, opts=ta.TaOptions(0, cl, None, None, None, None)) == -5
     assert _decode_raw(ta, f32, P=4, ws=0x7000, wsb=1 << 30, opts=ta.TaOptions(1, cl, None, None, None, None)) == -3
     assert ta.tree_attn_launch_count(s, 8) == 1
+
+
+def test_binding_shape_cache_validates_every_new_layout(ta):
+    """The binding caches a validated descriptor per (shapes, strides, dtypes,
+    scale); a call whose layout differs in any of them is validated afresh."""
+    import torch
+    from softmax_tree_reduction_gb300 import _binding as b
+    q = torch.zeros(2, 8, 128, dtype=torch.bfloat16)
+    k = torch.zeros(2, 2, 64, 128, dtype=torch.bfloat16)
+    sl = torch.zeros(2, dtype=torch.int32)
+    first = b._dense_shape(q, k, k.clone(), sl, None)
+    assert b._dense_shape(q, k, k.clone(), sl, None) is first      # same layout: cached
+    assert first[0].num_q_heads == 8 and first[0].num_kv_heads == 2 and first[0].max_seqlen == 64
+    assert b._dense_shape(q, k, k.clone(), sl, 0.5) is not first   # the scale is part of the key
+    with pytest.raises(ValueError):                                # V strided differently from K
+        b._dense_shape(q, k, k.transpose(1, 2).contiguous().transpose(1, 2), sl, None)
+    with pytest.raises(ValueError):                                # V of another dtype
+        b._dense_shape(q, k, k.float(), sl, None)
+    with pytest.raises(ValueError):                                # q with the same shape, not contiguous
+        b._dense_shape(torch.zeros(2, 128, 8, dtype=torch.bfloat16).transpose(1, 2), k, k, sl, None)
+    with pytest.raises(ValueError):                                # lengths must be int32
+        b._dense_shape(q, k, k, sl.long(), None)
+    # a token-major view is a new key with its strides in the descriptor
+    kt = torch.zeros(2, 64, 2, 128, dtype=torch.bfloat16).transpose(1, 2)
+    d = b._dense_shape(q, kt, kt, sl, None)[0]
+    assert (d.kv_stride_b, d.kv_stride_h, d.kv_stride_t) == (64 * 2 * 128, 128, 2 * 128)
