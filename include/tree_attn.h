@@ -174,7 +174,8 @@ int tree_attn_pick_splits(const ta_shape *shape, const int32_t *host_seqlens, in
  * tree_attn_decode_paged and tree_attn_decode_multi use when called with
  * num_splits <= 0).  With 16-token pages one thread block may serve several
  * KV heads of a row (each copy then brings the same tokens of all of them:
- * FP8 caches, and BF16 caches in token-major pools), which changes the block
+ * FP8 caches, and BF16 caches in token-major pools; with more than 8 columns
+ * per KV head only where that needs no more slices), which changes the block
  * count and so the best P.  page_size <= 0 is the dense heuristic.  Returns P
  * or a negative ta_status. */
 int tree_attn_pick_splits_paged(const ta_shape *shape, int page_size, const int32_t *host_seqlens,
