@@ -57,3 +57,20 @@ def test_bench_argument_defaults():
     a = bench.parse_args([])
     assert a.gpus == 1 and a.impl == "ours" and a.warmup >= 3
     assert a.workload == "llama3.1-8b-decode-layer"
+
+
+def test_reference_arm_line_on_cpu(capsys, monkeypatch):
+    """The reference arm (the oracle on host cores) prints one JSON line with
+    the contract's keys on the small exact workload; it needs no GPU."""
+    import json
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    assert bench.main(["--impl", "reference", "--workload", "tiny_exact", "--steps", "2", "--warmup", "3",
+                       "--ref-tokens", "1024"]) == 0
+    lines = [l for l in capsys.readouterr().out.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["n_gpus"] == 1 and d["higher_is_better"]
+    assert d["value"] > 0 and d["steps"] == 2 and d["config"]["seq_len"] == 1024
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
