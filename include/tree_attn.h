@@ -30,6 +30,12 @@
  *    [0, max_seqlen]) never traps: the affected rows become NaN and an error
  *    word is set, reported by tree_attn_get_device_error.
  *  - Outputs `out` and `lse` are fully overwritten; inputs are never written.
+ *  - The library sets itself up once per device and process, the first time
+ *    it is called with that device current: it looks up the device addresses
+ *    of its own fixed buffers (error word, scheduling counters, the
+ *    no-allocation scratch) and raises its kernels' shared-memory limits.
+ *    That set-up does not survive cudaDeviceReset: after resetting a device,
+ *    a process must not call the library on that device again.
  */
 #ifndef TREE_ATTN_H
 #define TREE_ATTN_H
@@ -315,7 +321,17 @@ int tree_attn_decode_noalloc(const ta_shape *shape, const void *q, const void *k
 
 /* Synchronise `stream`, then read and clear the current device's error word.
  * Returns TA_OK, TA_ERR_DEVICE_DATA or TA_ERR_DEVICE_TIMEOUT (or TA_ERR_CUDA
- * when the synchronisation itself fails). */
+ * when the synchronisation itself fails).
+ *
+ * The error word is one per device, shared by every call and stream: it
+ * reports what any call since the last read found.  The library's scheduling
+ * counters (a fixed per-device ring; each call uses its own slots) are back at
+ * zero when a call ends, also after a wait gave up, so a timeout needs no
+ * clean-up and calls running on other streams are not disturbed.  Only if a
+ * block's copy warp did not end within its own bounded wait either (a second
+ * timeout inside the same block) does this function synchronise the whole
+ * device and clear the ring; no call may be enqueued from another host thread
+ * while it does. */
 int tree_attn_get_device_error(void *stream);
 
 #ifdef __cplusplus

@@ -21,12 +21,14 @@ namespace {
 
 using ta::Geometry;
 
-__device__ int g_error_word;  // bits ta::kErrBadSeqlen | ta::kErrTimeout
+__device__ int g_error_word;  // bits ta::kErrBadSeqlen | ta::kErrTimeout | ta::kErrCounters
 
 // Scheduling counters (chunk claims and row tickets) of the split kernels.
 // Zero at load; each call reserves two consecutive slots per schedule row
 // (B * Hkv / heads_per_block rows) and leaves them at zero when it
-// completes, so slots are reused as the cursor wraps.
+// completes -- also when one of its waits gave up, because a row's ticket is
+// taken only after the block's copy warp has made its last claim -- so slots
+// are reused as the cursor wraps.
 constexpr unsigned kRingSlots = 1u << 20;
 __device__ unsigned g_sched_ring[kRingSlots];
 
@@ -788,12 +790,16 @@ int tree_attn_get_device_error(void* stream) {
     const int zero = 0;
     if (cudaMemcpy(ds->err, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
         return TA_ERR_CUDA;
-    if (h & ta::kErrTimeout) {
-        // a block that gave up may have left scheduling counters mid-count
+    if (h & ta::kErrCounters) {
+        // A copy warp outlived its bounded hand-over to the row's ticket, so
+        // some counters may be off zero.  Only then is the ring cleared, after
+        // every stream of the device has drained (no call may be enqueued
+        // from another host thread meanwhile).
+        if (cudaDeviceSynchronize() != cudaSuccess) return TA_ERR_CUDA;
         if (cudaMemset(ds->ring, 0, sizeof(unsigned) * kRingSlots) != cudaSuccess) return TA_ERR_CUDA;
         if (cudaDeviceSynchronize() != cudaSuccess) return TA_ERR_CUDA;
-        return TA_ERR_DEVICE_TIMEOUT;
     }
+    if (h & (ta::kErrTimeout | ta::kErrCounters)) return TA_ERR_DEVICE_TIMEOUT;
     return TA_ERR_DEVICE_DATA;
 }
 

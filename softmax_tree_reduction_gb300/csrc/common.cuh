@@ -13,6 +13,8 @@ namespace ta {
 // Error bits of the device error word.
 constexpr int kErrBadSeqlen = 1;  // a sequence length outside [0, max_seqlen], or a bad page
 constexpr int kErrTimeout = 2;    // a bounded barrier wait gave up
+constexpr int kErrCounters = 4;   // a row's copy warp outlived its bounded hand-over, so the
+                                  // row's scheduling counters may not be back at zero
 
 // log2(e) and ln(2): the kernels evaluate exp(x) as 2^(x * log2 e).
 constexpr float kLog2e = 1.4426950408889634f;

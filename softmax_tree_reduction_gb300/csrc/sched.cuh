@@ -329,11 +329,17 @@ __device__ void cluster_merge_row(const SplitParams& p, size_t hq0, int nh, cons
 
 // `row`: the block's schedule row (ticket and claim counters); the row's
 // blocks hold the states of query heads [hq0, hq0 + G) (flat b * Hq + h).
+// `prod_done`: the mbarrier the block's copy warp arrives on once it has made
+// its last claim.  The ticket is taken only after that arrival, so when the
+// last ticket resets the claim counter every claim of the row has landed --
+// also when the compute warps left the stage ring early after a timed-out
+// wait -- and a finished call leaves both counters at zero.
 template <int D>
 __device__ void finish_row(const SplitParams& p, int row, size_t hq0, int G, float* scratch,
-                           int* flag, int tid, int nthr) {
+                           int* flag, uint64_t* prod_done, int tid, int nthr) {
     consumer_sync(nthr);
     if (tid == 0) {
+        if (!mbar_wait(prod_done, 0, p.err)) atomicOr(p.err, kErrCounters);
         const unsigned t = ticket_acq_rel(p.done + row, static_cast<unsigned>(p.P - 1));
         const bool last = (t == static_cast<unsigned>(p.P - 1));
         if (last && p.claim) atomicExch(p.claim + row, 0u);

@@ -83,6 +83,7 @@ __global__ void __launch_bounds__(FmaCfg<KV, D>::kThreads, 1)
     int* last_flag = abort_flag + 1;
     volatile unsigned* claim_sink = reinterpret_cast<volatile unsigned*>(abort_flag + 2);
     volatile int* bad_page = reinterpret_cast<volatile int*>(abort_flag + 3);
+    uint64_t* prod_done = reinterpret_cast<uint64_t*>(abort_flag + 4);  // the copy warp's last claim is made
 
     const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -92,6 +93,7 @@ __global__ void __launch_bounds__(FmaCfg<KV, D>::kThreads, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], C::kWarps);
         }
+        mbar_init(prod_done, 1);
         *abort_flag = 0;
         *bad_page = 0;
         fence_barrier_init();
@@ -123,6 +125,7 @@ __global__ void __launch_bounds__(FmaCfg<KV, D>::kThreads, 1)
 
     if (warp == 0) {
         if (p.stall) {  // diagnostic: publish nothing, so the consumers' waits give up
+            if (lane == 0) mbar_arrive(prod_done);
             allow_dependents();
             return;
         }
@@ -145,6 +148,7 @@ __global__ void __launch_bounds__(FmaCfg<KV, D>::kThreads, 1)
                     tma_load_4d(st + C::kKBytes + off, &tmV, 0, ty, g, page, &full[s], pol);
                 });
         }
+        if (lane == 0) mbar_arrive(prod_done);  // after its last claim (lane 0 makes them)
         allow_dependents();
         return;
     }
@@ -311,7 +315,7 @@ __global__ void __launch_bounds__(FmaCfg<KV, D>::kThreads, 1)
     }
     if (p.done)
         finish_row<D>(p, b * p.Hkv + g, static_cast<size_t>(b) * p.Hq + static_cast<size_t>(g) * p.G, p.G,
-                      reinterpret_cast<float*>(stages), last_flag, ct, C::kWarps * 32);
+                      reinterpret_cast<float*>(stages), last_flag, prod_done, ct, C::kWarps * 32);
     allow_dependents();
 }
 

@@ -97,6 +97,7 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, CG>::kThreads, 1)
     int* last_flag = abort_flag + 1;
     volatile unsigned* claim_sink = reinterpret_cast<volatile unsigned*>(abort_flag + 2);
     volatile int* bad_page = reinterpret_cast<volatile int*>(abort_flag + 3);
+    uint64_t* prod_done = reinterpret_cast<uint64_t*>(abort_flag + 4);  // the copy warp's last claim is made
 
     // KV heads g0 .. g0 + HB - 1 of batch row b; schedule row `row`
     const int split = blockIdx.x, g0 = blockIdx.y * HB, b = blockIdx.z;
@@ -108,6 +109,7 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, CG>::kThreads, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], C::kWarps);
         }
+        mbar_init(prod_done, 1);
         *abort_flag = 0;
         *bad_page = 0;
         fence_barrier_init();
@@ -140,6 +142,7 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, CG>::kThreads, 1)
 
     if (warp == 0) {
         if (p.stall) {  // diagnostic: publish nothing, so the consumers' waits give up
+            if (lane == 0) mbar_arrive(prod_done);
             allow_dependents();
             if (p.cluster) {  // the cluster barriers of the row merge
                 cluster_sync_all();
@@ -172,6 +175,7 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, CG>::kThreads, 1)
                     tma_load_5d(st + C::kKBytes + off, &tmV, 0, ty, 0, g0, page, &full[s], pol);
                 });
         }
+        if (lane == 0) mbar_arrive(prod_done);  // after its last claim (lane 0 makes them)
         allow_dependents();
         if (p.cluster) {  // the cluster barriers of the row merge
             cluster_sync_all();
@@ -506,7 +510,7 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, CG>::kThreads, 1)
         cluster_merge_row<D, 8>(p, hq0, HB * p.G, cs_o, cs_m, cs_l, ct, C::kWarps * 32);
         cluster_sync_all();  // no block's state goes away while a peer reads it
     } else if (p.done) {
-        finish_row<D>(p, row, hq0, HB * p.G, reinterpret_cast<float*>(stages), last_flag, ct, C::kWarps * 32);
+        finish_row<D>(p, row, hq0, HB * p.G, reinterpret_cast<float*>(stages), last_flag, prod_done, ct, C::kWarps * 32);
     }
     allow_dependents();
 }

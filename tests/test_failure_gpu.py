@@ -78,3 +78,56 @@ def test_wrong_length_hint_changes_nothing(family, P):
     tol = 1e-4 if kv == torch.float32 else 2e-3
     assert np.max(np.abs(o3.double().cpu().numpy() - ref_o)) <= tol
     assert np.max(np.abs(l3.double().cpu().numpy() - ref_l)) <= max(tol, 1e-3)
+
+
+def test_timeout_on_one_stream_leaves_calls_on_another_stream_intact():
+    """A call on stream A gives up its waits (diagnostic stall, about two
+    seconds) while calls on a second non-blocking stream B run back to back.
+    Reading the timeout from A must not disturb B: every B call's output, each
+    in a buffer of its own, matches the oracle, also the ones in flight while
+    A's error is read and cleared.  (Clearing the library's scheduling counters
+    at that moment would break the B call whose row tickets are mid-count.)"""
+    import threading
+
+    w = workloads.Workload("busy", 1, 32, 8, 128, 131072, torch.bfloat16, torch.bfloat16, seed=21,
+                           seqlen=131072, k_scale=0.5)
+    inp = workloads.make_inputs(w)
+    ref_o, ref_l = oracle.attention(inp["q"], inp["k"], inp["v"], inp["seqlens"])
+    q, k, v, sl = (inp[x].cuda() for x in ("q", "k", "v", "seqlens"))
+    stall = _inputs(torch.bfloat16, 128)
+    sq, sk, sv, ssl = (stall[x].cuda() for x in ("q", "k", "v", "seqlens"))
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    n = 64
+    outs = torch.empty(n, 1, 32, 128, device="cuda")
+    lses = torch.empty(n, 1, 32, device="cuda")
+    shape = ta.make_shape(q, k)
+    ws = torch.empty(ta.tree_attn_workspace_bytes(shape, 19), dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+    assert ta.tree_attn_get_device_error() == 0
+
+    ta.tree_attn_decode(sq, sk, sv, ssl, num_splits=5, kernel="mma", diag_stall=True, stream=sa)
+    result = {}
+    reader = threading.Thread(target=lambda: result.update(rc=ta.tree_attn_get_device_error(sa)))
+    reader.start()
+    rounds, after = 0, 0
+    while True:
+        with torch.cuda.stream(sb):
+            outs.fill_(float("nan"))
+            lses.fill_(float("nan"))
+        for i in range(n):
+            ta.tree_attn_decode(q, k, v, sl, out=outs[i], lse=lses[i], num_splits=19, workspace=ws, stream=sb)
+        sb.synchronize()
+        o = outs.double().cpu().numpy()
+        l = lses.double().cpu().numpy()
+        assert np.isfinite(o).all() and np.isfinite(l).all(), f"round {rounds}"
+        assert np.max(np.abs(o - ref_o[None])) <= 2e-3, f"round {rounds}"
+        assert np.max(np.abs(l - ref_l[None])) <= 1e-3, f"round {rounds}"
+        rounds += 1
+        if not reader.is_alive():
+            after += 1
+            if after >= 2:
+                break
+    reader.join()
+    assert result["rc"] == ta.TA_ERR_DEVICE_TIMEOUT
+    assert rounds >= 4
+    assert ta.tree_attn_get_device_error() == 0

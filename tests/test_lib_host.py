@@ -304,3 +304,28 @@ def test_binding_shape_cache_validates_every_new_layout(ta):
     kt = torch.zeros(2, 64, 2, 128, dtype=torch.bfloat16).transpose(1, 2)
     d = b._dense_shape(q, kt, kt, sl, None)[0]
     assert (d.kv_stride_b, d.kv_stride_h, d.kv_stride_t) == (64 * 2 * 128, 128, 2 * 128)
+
+
+def _header_constants():
+    """#define'd integer constants and enum values of the header, evaluated."""
+    text = open(HEADER).read()
+    consts = {}
+    for name, expr in re.findall(r"^#define\s+(TA_\w+)\s+(.+?)\s*(?:/\*.*)?$", text, flags=re.M):
+        expr = re.sub(r"(\d+)[uU]\b", r"\1", expr)
+        if re.fullmatch(r"[\d\s()<>+\-*x]+", expr):
+            consts[name] = int(eval(expr))
+    for name, val in re.findall(r"^\s*(TA_\w+)\s*=\s*(-?\d+)", text, flags=re.M):
+        consts[name] = int(val)
+    return consts
+
+
+def test_binding_constants_match_the_header(ta):
+    """The Python binding's copies of the header's constants (scratch size,
+    split limit, flag bits, status codes, dtype codes) equal the header's."""
+    h = _header_constants()
+    for name in ("TA_NOALLOC_SCRATCH_BYTES", "TA_MAX_SPLITS", "TA_FLAG_DETERMINISTIC", "TA_FLAG_DIAG_STALL",
+                 "TA_FLAG_DIAG_MISHINT", "TA_FLAG_CLUSTER_MERGE", "TA_OK", "TA_ERR_DEVICE_DATA",
+                 "TA_ERR_DEVICE_TIMEOUT", "TA_F32", "TA_BF16", "TA_E4M3"):
+        assert name in h, name
+        assert getattr(ta, name) == h[name], (name, getattr(ta, name), h[name])
+    assert h["TA_NOALLOC_SCRATCH_BYTES"] == 8 << 20

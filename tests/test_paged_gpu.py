@@ -134,20 +134,19 @@ def test_paged_eight_kv_heads(fp8, page_size):
 @pytest.mark.parametrize("page_size", [16, 256])
 def test_full_llama31_8b_paged(page_size):
     """The 131072-token 8B-shaped layer from a shuffled page pool (the bench's
-    --paged configuration): sampled KV-head groups against the oracle."""
+    --paged configuration): every output row against the oracle over the whole
+    input."""
     w = workloads.LLAMA31_8B
     inp = workloads.make_inputs(w)
     kp, vp, bt = workloads.page_pool(inp["k"], inp["v"], inp["seqlens"], page_size, seed=w.seed)
-    G = w.group
     args = (inp["q"].cuda(), kp.cuda(), vp.cuda(), bt.cuda(), inp["seqlens"].cuda())
-    for g in (0, 5, 7):
-        ro, rl = oracle.attention(inp["q"][:, g * G:(g + 1) * G], inp["k"][:, g:g + 1], inp["v"][:, g:g + 1],
-                                  inp["seqlens"], w.softmax_scale)
-        for P in (0, 19, 38):
-            o, l = ta.tree_attn_decode_paged(*args, num_splits=P, max_seqlen=w.max_seqlen)
-            torch.cuda.synchronize()
-            o64 = o[:, g * G:(g + 1) * G].double().cpu().numpy()
-            l64 = l[:, g * G:(g + 1) * G].double().cpu().numpy()
-            assert np.max(np.abs(o64 - ro)) <= 2e-3, (page_size, g, P)
-            assert np.max(np.abs(l64 - rl)) <= 1e-3, (page_size, g, P)
+    ro, rl = oracle.attention(inp["q"], inp["k"], inp["v"], inp["seqlens"], w.softmax_scale)
+    for P in (0, 19, 38):
+        o, l = ta.tree_attn_decode_paged(*args, num_splits=P, max_seqlen=w.max_seqlen)
+        torch.cuda.synchronize()
+        o64 = o.double().cpu().numpy()
+        l64 = l.double().cpu().numpy()
+        assert np.isfinite(o64).all() and np.isfinite(l64).all(), (page_size, P)
+        assert np.max(np.abs(o64 - ro)) <= 2e-3, (page_size, P)
+        assert np.max(np.abs(l64 - rl)) <= 1e-3, (page_size, P)
     assert ta.tree_attn_get_device_error() == 0
