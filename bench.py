@@ -61,7 +61,7 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama3.1-8b-decode-layer")
     ap.add_argument("--num-splits", type=int, default=0, help="<= 0: the library's heuristic")
-    ap.add_argument("--kernel", choices=["auto", "mma", "fma"], default="auto")
+    ap.add_argument("--kernel", choices=["auto", "mma", "fma", "tc05"], default="auto")
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle baseline sample")
@@ -113,9 +113,10 @@ def load_peaks():
 
 
 def kernel_source_hash(kernel):
-    name = {"mma": "split_kv_mma.cu", "fma": "split_kv_fma.cuh", "fp8": "split_kv_fp8.cu"}[kernel]
+    name = {"mma": "split_kv_mma.cu", "fma": "split_kv_fma.cuh", "fp8": "split_kv_fp8.cu",
+            "tc05": "split_kv_tc05.cu"}[kernel]
     h = hashlib.sha256()
-    for f in (name, "common.cuh", "emit.cuh", "sched.cuh", "warp_mma.cuh", "api.cu"):
+    for f in (name, "common.cuh", "emit.cuh", "sched.cuh", "warp_mma.cuh", "tc05.cuh", "api.cu"):
         with open(os.path.join(ROOT, "softmax_tree_reduction_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
@@ -327,11 +328,15 @@ def run_ours(args, rank, world, local):
     if args.fp8:
         kernel_used = "fp8"
     elif kernel_used == "auto":
-        # the library's choice: tensor cores for BF16 with up to 16 columns per KV
-        # head, or up to 64 in column groups of 16 when head_dim is 128
+        # the library's choice: warp-level tensor cores for BF16 with up to 16
+        # columns per KV head; tcgen05 for 17..64 columns at head_dim 128 (the
+        # warp-level kernel when the cluster merge is asked for)
         cols = w.group * args.queries
-        kernel_used = "mma" if (w.kv_dtype == torch.bfloat16 and w.q_dtype == torch.bfloat16
-                                and (cols <= 16 or (cols <= 64 and w.head_dim == 128))) else "fma"
+        bf16 = w.kv_dtype == torch.bfloat16 and w.q_dtype == torch.bfloat16
+        if bf16 and 16 < cols <= 64 and w.head_dim == 128:
+            kernel_used = "mma" if args.cluster_merge else "tc05"
+        else:
+            kernel_used = "mma" if (bf16 and cols <= 16) else "fma"
     B, Hq, d = dev["q"].shape[0], dev["q"].shape[1], dev["q"].shape[-1]
     out = torch.empty(dev["q"].shape, dtype=torch.float32, device="cuda")
     lse = torch.empty(dev["q"].shape[:-1], dtype=torch.float32, device="cuda")

@@ -22,7 +22,7 @@ TA_OK = 0
 TA_ERR_DEVICE_DATA = -8      # a length or page-table entry outside its range (rows are NaN)
 TA_ERR_DEVICE_TIMEOUT = -9   # a bounded on-chip wait gave up (outputs are NaN)
 TA_F32, TA_BF16, TA_E4M3 = 0, 1, 2
-TA_KERNEL = {"auto": 0, "fma": 1, "mma": 2}
+TA_KERNEL = {"auto": 0, "fma": 1, "mma": 2, "tc05": 3}
 TA_MAX_SPLITS = 4096
 TA_FLAG_DETERMINISTIC = 1
 TA_FLAG_DIAG_STALL = 2

@@ -136,7 +136,10 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 int elem_bytes(int dtype) { return dtype == TA_BF16 ? 2 : (dtype == TA_E4M3 ? 1 : 4); }
 
 // Internal kernel family for FP8 caches (selected by TA_KERNEL_AUTO / TA_KERNEL_MMA).
-constexpr int kKernelFp8 = 3;
+constexpr int kKernelFp8 = 4;
+static_assert(kKernelFp8 != TA_KERNEL_AUTO && kKernelFp8 != TA_KERNEL_FMA && kKernelFp8 != TA_KERNEL_MMA &&
+                  kKernelFp8 != TA_KERNEL_TC05,
+              "internal kernel id");
 
 struct Strides {
     int64_t b, h, t;
@@ -186,32 +189,41 @@ int check_shape(const ta_shape* s, Strides* st, int page_size = 0) {
 }
 
 // Kernel family for a shape (num_q_heads counts (head, query) pairs for
-// multi-query calls): the tensor-core kernel takes BF16 q and cache with up to
-// 16 columns per KV head (64 at head_dim 128, in column groups of 16); the
-// FMA kernel any dtypes with a power-of-two group up to 16.
-int resolve_kernel(const ta_shape* s, int requested) {
+// multi-query calls): the warp-level tensor-core kernel takes BF16 q and cache
+// with up to 16 columns per KV head (64 at head_dim 128, in column groups of
+// 16); the tcgen05 kernel BF16 q and cache at head_dim 128 with up to 64
+// columns, and is the automatic choice above 16 columns (the cluster merge
+// is built into the warp-level kernels only); the FMA kernel any dtypes with
+// a power-of-two group up to 16.
+int resolve_kernel(const ta_shape* s, int requested, bool cluster = false) {
     const int G = s->num_q_heads / s->num_kv_heads;
     if (s->kv_dtype == TA_E4M3) {
         const bool ok = s->q_dtype == TA_BF16 && s->head_dim == 128 && G <= 16;
-        if (requested == TA_KERNEL_FMA) return TA_ERR_DTYPE;
+        if (requested == TA_KERNEL_FMA || requested == TA_KERNEL_TC05) return TA_ERR_DTYPE;
         if (requested != TA_KERNEL_AUTO && requested != TA_KERNEL_MMA) return TA_ERR_SHAPE;
         return ok ? kKernelFp8 : static_cast<int>(TA_ERR_DTYPE);
     }
     const bool bf16 = s->q_dtype == TA_BF16 && s->kv_dtype == TA_BF16;
     const bool mma_ok = bf16 && (G <= 16 || (G <= 64 && s->head_dim == 128));
+    const bool tc05_ok = bf16 && G <= 64 && s->head_dim == 128;
     const bool fma_ok = (G & (G - 1)) == 0 && G <= 16;
     switch (requested) {
         case TA_KERNEL_AUTO:
+            if (tc05_ok && G > 16 && !cluster) return TA_KERNEL_TC05;
             return mma_ok ? static_cast<int>(TA_KERNEL_MMA)
                           : (fma_ok ? static_cast<int>(TA_KERNEL_FMA) : static_cast<int>(TA_ERR_SHAPE));
         case TA_KERNEL_FMA: return fma_ok ? static_cast<int>(TA_KERNEL_FMA) : static_cast<int>(TA_ERR_SHAPE);
         case TA_KERNEL_MMA: return mma_ok ? static_cast<int>(TA_KERNEL_MMA) : static_cast<int>(TA_ERR_DTYPE);
+        case TA_KERNEL_TC05:
+            if (!tc05_ok) return bf16 ? static_cast<int>(TA_ERR_SHAPE) : static_cast<int>(TA_ERR_DTYPE);
+            return cluster ? static_cast<int>(TA_ERR_SHAPE) : static_cast<int>(TA_KERNEL_TC05);
         default: return TA_ERR_SHAPE;
     }
 }
 
 Geometry geometry_hb(const ta_shape* s, int kernel, int hb) {
     if (kernel == kKernelFp8) return ta::fp8_geometry(hb);
+    if (kernel == TA_KERNEL_TC05) return ta::mma_geometry(s->head_dim, 1);  // same tiles, one KV head per block
     return kernel == TA_KERNEL_MMA ? ta::mma_geometry(s->head_dim, hb)
                                    : ta::fma_geometry(elem_bytes(s->kv_dtype), s->head_dim);
 }
@@ -249,10 +261,7 @@ int heads_per_block(const ta_shape* s, int kernel, int page_size, int num_sms) {
 }
 
 Geometry geometry_of(const ta_shape* s, int kernel, int page_size, int num_sms) {
-    const int hb = heads_per_block(s, kernel, page_size, num_sms);
-    if (kernel == kKernelFp8) return ta::fp8_geometry(hb);
-    return kernel == TA_KERNEL_MMA ? ta::mma_geometry(s->head_dim, hb)
-                                   : ta::fma_geometry(elem_bytes(s->kv_dtype), s->head_dim);
+    return geometry_hb(s, kernel, heads_per_block(s, kernel, page_size, num_sms));
 }
 
 // Resident thread blocks per SM of each kernel family (shared memory bound:
@@ -510,7 +519,7 @@ int decode_impl(const ta_shape* shape, const ta_paged_kv* paged, int nq, int cau
     if (options && (options->flags & ~kKnownFlags) != 0) return TA_ERR_SHAPE;
     const bool deterministic = options && (options->flags & TA_FLAG_DETERMINISTIC);
     const bool cluster = options && (options->flags & TA_FLAG_CLUSTER_MERGE);
-    const int kernel = resolve_kernel(shape, options ? options->kernel : TA_KERNEL_AUTO);
+    const int kernel = resolve_kernel(shape, options ? options->kernel : TA_KERNEL_AUTO, cluster);
     if (kernel < 0) return kernel;
     if (cluster && kernel != TA_KERNEL_MMA && kernel != kKernelFp8) return TA_ERR_SHAPE;
     if (cluster && num_splits > kClusterMaxSplits) return TA_ERR_SPLITS;
@@ -625,6 +634,8 @@ int decode_impl(const ta_shape* shape, const ta_paged_kv* paged, int nq, int cau
     cudaError_t e;
     if (kernel == kKernelFp8)
         e = ta::launch_split_fp8(tk, tv, p, stream);
+    else if (kernel == TA_KERNEL_TC05)
+        e = ta::launch_split_tc05(tk, tv, p, stream);
     else if (kernel == TA_KERNEL_MMA)
         e = ta::launch_split_mma(shape->head_dim, tk, tv, p, stream);
     else if (shape->kv_dtype == TA_BF16)
@@ -737,7 +748,8 @@ int tree_attn_launch_count(const ta_shape* shape, int num_splits, const ta_optio
     int rc = check_shape(shape, nullptr);
     if (rc != TA_OK) return rc;
     if (options && (options->flags & ~kKnownFlags) != 0) return TA_ERR_SHAPE;
-    const int kernel = resolve_kernel(shape, options ? options->kernel : TA_KERNEL_AUTO);
+    const int kernel = resolve_kernel(shape, options ? options->kernel : TA_KERNEL_AUTO,
+                                      options && (options->flags & TA_FLAG_CLUSTER_MERGE));
     if (kernel < 0) return kernel;
     int P = num_splits;
     if (P > TA_MAX_SPLITS) return TA_ERR_SPLITS;

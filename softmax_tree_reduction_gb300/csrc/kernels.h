@@ -47,6 +47,10 @@ cudaError_t launch_split_fma_bf16(int head_dim, const CUtensorMap& tk, const CUt
                                   const SplitParams& p, cudaStream_t stream);
 cudaError_t launch_split_fma_f32(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv,
                                  const SplitParams& p, cudaStream_t stream);
+// Fifth-generation tensor cores (tcgen05, accumulators in TMEM): BF16 q and
+// cache, head_dim 128, up to 64 columns per KV head, one KV head per block.
+cudaError_t launch_split_tc05(const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& p,
+                              cudaStream_t stream);
 // FP8 (E4M3) caches, head_dim 128, BF16 q, up to 16 columns per KV head.
 cudaError_t launch_split_fp8(const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& p,
                              cudaStream_t stream);

@@ -86,7 +86,10 @@ def test_timeout_on_one_stream_leaves_calls_on_another_stream_intact():
     Reading the timeout from A must not disturb B: every B call's output, each
     in a buffer of its own, matches the oracle, also the ones in flight while
     A's error is read and cleared.  (Clearing the library's scheduling counters
-    at that moment would break the B call whose row tickets are mid-count.)"""
+    at that moment would break the B call whose row tickets are mid-count.)
+    B's first round is enqueued while A stalls, so its calls are in flight
+    when A's error word is read and cleared, whether the GPU runs them beside
+    A's blocks or after them."""
     import threading
 
     w = workloads.Workload("busy", 1, 32, 8, 128, 131072, torch.bfloat16, torch.bfloat16, seed=21,
@@ -101,7 +104,7 @@ def test_timeout_on_one_stream_leaves_calls_on_another_stream_intact():
     outs = torch.empty(n, 1, 32, 128, device="cuda")
     lses = torch.empty(n, 1, 32, device="cuda")
     shape = ta.make_shape(q, k)
-    ws = torch.empty(ta.tree_attn_workspace_bytes(shape, 19), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(ta.tree_attn_workspace_bytes(shape, 8), dtype=torch.uint8, device="cuda")
     torch.cuda.synchronize()
     assert ta.tree_attn_get_device_error() == 0
 
@@ -110,12 +113,13 @@ def test_timeout_on_one_stream_leaves_calls_on_another_stream_intact():
     reader = threading.Thread(target=lambda: result.update(rc=ta.tree_attn_get_device_error(sa)))
     reader.start()
     rounds, after = 0, 0
+    started_during = reader.is_alive()
     while True:
         with torch.cuda.stream(sb):
             outs.fill_(float("nan"))
             lses.fill_(float("nan"))
         for i in range(n):
-            ta.tree_attn_decode(q, k, v, sl, out=outs[i], lse=lses[i], num_splits=19, workspace=ws, stream=sb)
+            ta.tree_attn_decode(q, k, v, sl, out=outs[i], lse=lses[i], num_splits=8, workspace=ws, stream=sb)
         sb.synchronize()
         o = outs.double().cpu().numpy()
         l = lses.double().cpu().numpy()
@@ -129,5 +133,5 @@ def test_timeout_on_one_stream_leaves_calls_on_another_stream_intact():
                 break
     reader.join()
     assert result["rc"] == ta.TA_ERR_DEVICE_TIMEOUT
-    assert rounds >= 4
+    assert started_during   # the first round was enqueued before A's error was read
     assert ta.tree_attn_get_device_error() == 0

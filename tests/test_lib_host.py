@@ -329,3 +329,24 @@ def test_binding_constants_match_the_header(ta):
         assert name in h, name
         assert getattr(ta, name) == h[name], (name, getattr(ta, name), h[name])
     assert h["TA_NOALLOC_SCRATCH_BYTES"] == 8 << 20
+
+
+def test_tc05_kernel_choice_and_limits(ta):
+    """The tcgen05 kernel takes BF16 q and cache at head_dim 128 with up to 64
+    columns per KV head; it is the automatic choice above 16 columns, and
+    refused (before any CUDA call) for other dtypes, head_dim 64, an E4M3
+    cache, or together with the cluster merge."""
+    wide = shape(ta, num_q_heads=256, num_kv_heads=8)       # 32 columns per KV head
+    assert ta.tree_attn_launch_count(wide, 19, kernel="tc05") == 1
+    assert ta.tree_attn_launch_count(wide, 64, kernel="tc05") == 2
+    assert ta.tree_attn_launch_count(shape(ta), 19, kernel="tc05") == 1   # 4 columns, asked for
+    for bad, code in ((shape(ta, q_dtype=ta.TA_F32), -4), (shape(ta, head_dim=64), -3),
+                      (shape(ta, kv_dtype=ta.TA_E4M3), -4)):
+        with pytest.raises(ta.TreeAttnError) as ei:
+            ta.tree_attn_launch_count(bad, 8, kernel="tc05")
+        assert ei.value.status == code
+    lib = ta.load()
+    opts = ta.TaOptions(ta.TA_KERNEL["tc05"], ta.TA_FLAG_CLUSTER_MERGE, None, None, None, None)
+    assert lib.tree_attn_launch_count(ctypes.byref(wide), 4, ctypes.byref(opts)) == -3
+    opts = ta.TaOptions(ta.TA_KERNEL["auto"], ta.TA_FLAG_CLUSTER_MERGE, None, None, None, None)
+    assert lib.tree_attn_launch_count(ctypes.byref(wide), 4, ctypes.byref(opts)) == 1   # warp-level kernel

@@ -1,8 +1,11 @@
-"""More than 16 columns per KV head on the BF16 tensor-core path (column
-groups of 16): multi-query-attention layouts (many query heads on one KV
-head) and GQA with many draft tokens, against the float64 oracle: ragged rows
-with NaN padding, fused and launched merges, paged caches, causal multi-query,
-the cluster merge and the deterministic flag."""
+"""More than 16 columns per KV head on BF16 caches, on both tensor-core
+kernels: the tcgen05 kernel (the automatic choice; accumulators in tensor
+memory) and the warp-level mma kernel (column groups of 16).  Multi-query-
+attention layouts (many query heads on one KV head) and GQA with many draft
+tokens, against the float64 oracle: ragged rows with NaN padding, fused and
+launched merges, paged caches, causal multi-query, the cluster merge (mma
+kernel) and the deterministic flag.  The tcgen05 kernel is also run on small
+groups (1-16 columns) and through the failure-path diagnostics."""
 import numpy as np
 import pytest
 import torch
@@ -34,17 +37,18 @@ def _check(out, lse, ref_o, ref_l, what):
         assert np.max(np.abs(l[fin] - ref_l[fin])) <= 1e-3, what
 
 
+@pytest.mark.parametrize("kern", ["auto", "mma"])
 @pytest.mark.parametrize("G,Hkv", [(24, 2), (32, 1), (48, 1), (64, 2)])
-def test_wide_groups_dense(G, Hkv):
+def test_wide_groups_dense(G, Hkv, kern):
     inp = _inputs(G, Hkv, [0, 5, 129, 1000, 2900], 3072, seed=G)
     ref_o, ref_l = oracle.attention(inp["q"], inp["k"], inp["v"], inp["seqlens"])
     q, k, v, sl = (inp[x].cuda() for x in ("q", "k", "v", "seqlens"))
     for P in (0, 1, 5, 19, 41):
-        out, lse = ta.tree_attn_decode(q, k, v, sl, num_splits=P)
+        out, lse = ta.tree_attn_decode(q, k, v, sl, num_splits=P, kernel=kern)
         torch.cuda.synchronize()
-        _check(out, lse, ref_o, ref_l, f"G={G} P={P}")
-    o1, l1 = ta.tree_attn_decode(q, k, v, sl, num_splits=7, deterministic=True)
-    o2, l2 = ta.tree_attn_decode(q, k, v, sl, num_splits=7, deterministic=True)
+        _check(out, lse, ref_o, ref_l, f"G={G} P={P} {kern}")
+    o1, l1 = ta.tree_attn_decode(q, k, v, sl, num_splits=7, deterministic=True, kernel=kern)
+    o2, l2 = ta.tree_attn_decode(q, k, v, sl, num_splits=7, deterministic=True, kernel=kern)
     out, lse = ta.tree_attn_decode(q, k, v, sl, num_splits=6, cluster_merge=True)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
@@ -52,25 +56,88 @@ def test_wide_groups_dense(G, Hkv):
     assert ta.tree_attn_get_device_error() == 0
 
 
-@pytest.mark.parametrize("page_size", [16, 128])
-def test_wide_groups_paged(page_size):
+@pytest.mark.parametrize("kern", ["auto", "mma"])
+@pytest.mark.parametrize("page_size", [16, 32, 128, 256])
+def test_wide_groups_paged(page_size, kern):
     inp = _inputs(32, 2, [2000, 33, 700], 2048, seed=page_size)
     ref_o, ref_l = oracle.attention(inp["q"], inp["k"], inp["v"], inp["seqlens"])
     kp, vp, bt = workloads.page_pool(inp["k"], inp["v"], inp["seqlens"], page_size, seed=5)
     for P in (0, 9):
         out, lse = ta.tree_attn_decode_paged(inp["q"].cuda(), kp.cuda(), vp.cuda(), bt.cuda(), inp["seqlens"].cuda(),
-                                             num_splits=P, max_seqlen=2048)
+                                             num_splits=P, max_seqlen=2048, kernel=kern)
         torch.cuda.synchronize()
-        _check(out, lse, ref_o, ref_l, f"paged {page_size} P={P}")
+        _check(out, lse, ref_o, ref_l, f"paged {page_size} P={P} {kern}")
 
 
-@pytest.mark.parametrize("G,nq", [(8, 4), (16, 4), (4, 16)])
+@pytest.mark.parametrize("kern", ["auto", "mma"])
+@pytest.mark.parametrize("G,nq", [(8, 4), (16, 4), (4, 16), (6, 3)])
 @pytest.mark.parametrize("causal", [True, False])
-def test_wide_multi_query(G, nq, causal):
+def test_wide_multi_query(G, nq, causal, kern):
     inp = _inputs(G, 2, [1500, 4, 300], 1536, seed=G + nq, nq=nq)
     ref_o, ref_l = oracle.attention_multi(inp["q"], inp["k"], inp["v"], inp["seqlens"], causal=causal)
     q, k, v, sl = (inp[x].cuda() for x in ("q", "k", "v", "seqlens"))
     for P in (1, 11):
-        out, lse = ta.tree_attn_decode_multi(q, k, v, sl, causal=causal, num_splits=P)
+        out, lse = ta.tree_attn_decode_multi(q, k, v, sl, causal=causal, num_splits=P, kernel=kern)
         torch.cuda.synchronize()
-        _check(out, lse, ref_o, ref_l, f"G={G} nq={nq} causal={causal} P={P}")
+        _check(out, lse, ref_o, ref_l, f"G={G} nq={nq} causal={causal} P={P} {kern}")
+
+
+@pytest.mark.parametrize("G", [1, 4, 8, 13, 16, 40])
+def test_tc05_any_group_size(G):
+    """The tcgen05 kernel asked for explicitly, on groups of 1 to 64 columns:
+    ragged rows with NaN padding, planted spikes, one and several splits."""
+    inp = _inputs(G, 2, [0, 1, 17, 128, 129, 2900], 3072, seed=100 + G)
+    ref_o, ref_l = oracle.attention(inp["q"], inp["k"], inp["v"], inp["seqlens"])
+    q, k, v, sl = (inp[x].cuda() for x in ("q", "k", "v", "seqlens"))
+    for P in (1, 3, 8, 64):
+        out, lse = ta.tree_attn_decode(q, k, v, sl, num_splits=P, kernel="tc05")
+        torch.cuda.synchronize()
+        _check(out, lse, ref_o, ref_l, f"tc05 G={G} P={P}")
+    o = out.cpu()
+    assert torch.all(o[0] == 0) and torch.all(torch.isneginf(lse.cpu()[0]))
+    assert ta.tree_attn_get_device_error() == 0
+
+
+def test_tc05_rescale_on_growing_logits():
+    """Logits that grow along the sequence make the lazy reference maximum move
+    many times (each move rescales O in tensor memory)."""
+    G, N = 32, 4096
+    w = workloads.Workload("grow", 1, G, 1, 128, N, torch.bfloat16, torch.bfloat16, seed=7, seqlen=N)
+    inp = workloads.make_inputs(w)
+    ramp = torch.linspace(0.0, 6.0, N).view(1, 1, N, 1)
+    inp["k"] = (inp["k"].float() * (0.25 + ramp)).to(torch.bfloat16)
+    ref_o, ref_l = oracle.attention(inp["q"], inp["k"], inp["v"], inp["seqlens"])
+    q, k, v, sl = (inp[x].cuda() for x in ("q", "k", "v", "seqlens"))
+    for P in (1, 2, 5):
+        out, lse = ta.tree_attn_decode(q, k, v, sl, num_splits=P, kernel="tc05", deterministic=True)
+        torch.cuda.synchronize()
+        _check(out, lse, ref_o, ref_l, f"growing logits P={P}")
+
+
+@pytest.mark.parametrize("P", [1, 5])
+def test_tc05_stalled_waits_report_timeout(P):
+    """Failure path of the tcgen05 kernel: no tile is published, every wait
+    gives up, outputs are NaN, the timeout is reported, the TMEM is freed and
+    the next call is correct."""
+    inp = _inputs(32, 2, [1000, 333], 1024, seed=3)
+    q, k, v, sl = (inp[x].cuda() for x in ("q", "k", "v", "seqlens"))
+    assert ta.tree_attn_get_device_error() == 0
+    out, lse = ta.tree_attn_decode(q, k, v, sl, num_splits=P, kernel="tc05", diag_stall=True)
+    assert ta.tree_attn_get_device_error() == ta.TA_ERR_DEVICE_TIMEOUT
+    assert torch.isnan(out).all() and torch.isnan(lse).all()
+    ref_o, ref_l = oracle.attention(inp["q"], inp["k"], inp["v"], inp["seqlens"])
+    out, lse = ta.tree_attn_decode(q, k, v, sl, num_splits=P, kernel="tc05")
+    torch.cuda.synchronize()
+    assert ta.tree_attn_get_device_error() == 0
+    _check(out, lse, ref_o, ref_l, "after the stall")
+
+
+@pytest.mark.parametrize("P", [1, 5, 19])
+def test_tc05_wrong_length_hint_changes_nothing(P):
+    inp = _inputs(48, 2, [1000, 333], 1024, seed=4)
+    q, k, v, sl = (inp[x].cuda() for x in ("q", "k", "v", "seqlens"))
+    o1, l1 = ta.tree_attn_decode(q, k, v, sl, num_splits=P, kernel="tc05", deterministic=True)
+    o2, l2 = ta.tree_attn_decode(q, k, v, sl, num_splits=P, kernel="tc05", deterministic=True, diag_mishint=True)
+    torch.cuda.synchronize()
+    assert ta.tree_attn_get_device_error() == 0
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
