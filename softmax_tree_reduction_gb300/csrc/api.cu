@@ -223,7 +223,7 @@ int resolve_kernel(const ta_shape* s, int requested, bool cluster = false) {
 
 Geometry geometry_hb(const ta_shape* s, int kernel, int hb) {
     if (kernel == kKernelFp8) return ta::fp8_geometry(hb);
-    if (kernel == TA_KERNEL_TC05) return ta::mma_geometry(s->head_dim, 1);  // same tiles, one KV head per block
+    if (kernel == TA_KERNEL_TC05) return ta::tc05_geometry(0);  // one KV head per block
     return kernel == TA_KERNEL_MMA ? ta::mma_geometry(s->head_dim, hb)
                                    : ta::fma_geometry(elem_bytes(s->kv_dtype), s->head_dim);
 }
@@ -261,6 +261,7 @@ int heads_per_block(const ta_shape* s, int kernel, int page_size, int num_sms) {
 }
 
 Geometry geometry_of(const ta_shape* s, int kernel, int page_size, int num_sms) {
+    if (kernel == TA_KERNEL_TC05) return ta::tc05_geometry(page_size);
     return geometry_hb(s, kernel, heads_per_block(s, kernel, page_size, num_sms));
 }
 
@@ -403,7 +404,8 @@ int encode_kv_map_uncached(CUtensorMap* map, const void* base, const ta_shape* s
         const cuuint64_t halves = static_cast<cuuint64_t>(s->head_dim / 64);
         cuuint64_t dims5[5] = {64, dims[1], halves, dims[2], dims[3]};
         cuuint64_t strides5[4] = {strides[0], 128, strides[1], strides[2]};
-        cuuint32_t box5[5] = {64, static_cast<cuuint32_t>(rows), static_cast<cuuint32_t>(halves), hb, 1};
+        cuuint32_t box5[5] = {64, static_cast<cuuint32_t>(rows),
+                              geo.split_halves ? 1u : static_cast<cuuint32_t>(halves), hb, 1};
         const CUresult r5 = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base),
                                dims5, strides5, box5, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -427,7 +429,7 @@ int encode_kv_map_uncached(CUtensorMap* map, const void* base, const ta_shape* s
 struct MapKey {
     const void* base;
     int64_t dims[4], strides[3];
-    int32_t dtype, rows, box_x, swizzle128, halves5d, hb;
+    int32_t dtype, rows, box_x, swizzle128, halves5d, hb, split_halves;
 };
 
 struct MapSlot {
@@ -464,6 +466,7 @@ int encode_kv_map(int dev, CUtensorMap* map, const void* base, const ta_shape* s
     k.box_x = geo.box_x;
     k.swizzle128 = geo.swizzle128;
     k.halves5d = geo.halves5d;
+    k.split_halves = geo.split_halves;
     k.hb = geo.heads_per_block;
     const size_t i = hash_key(k) % kMapSlots;
     {

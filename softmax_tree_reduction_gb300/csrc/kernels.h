@@ -32,6 +32,7 @@ struct Geometry {
     int swizzle128;    // 1: CU_TENSOR_MAP_SWIZZLE_128B, 0: no swizzle
     int halves5d = 0;  // 1: 5-D view whose box brings every 64-channel half at once
     int heads_per_block = 1;  // KV heads a block serves; each box spans all of them
+    int split_halves = 0;  // 1 (with halves5d): the box brings one 64-channel half; one copy per half
 };
 
 Geometry mma_geometry(int head_dim, int heads_per_block);
@@ -49,6 +50,7 @@ cudaError_t launch_split_fma_f32(int head_dim, const CUtensorMap& tk, const CUte
                                  const SplitParams& p, cudaStream_t stream);
 // Fifth-generation tensor cores (tcgen05, accumulators in TMEM): BF16 q and
 // cache, head_dim 128, up to 64 columns per KV head, one KV head per block.
+Geometry tc05_geometry(int page_size);
 cudaError_t launch_split_tc05(const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& p,
                               cudaStream_t stream);
 // FP8 (E4M3) caches, head_dim 128, BF16 q, up to 16 columns per KV head.

@@ -6,34 +6,38 @@
 // One thread block per (slice p, KV head g, batch row b) computes the partial
 // state (o, l, m) of its slice for every column of the group ("Local
 // Independent Partial Attention" on the Tree Attention pages) and writes it
-// for the row merge ("The Tree Reduction Merge Operator").  The columns are
-// the M dimension of both products, so each column's scores sit in one TMEM
-// lane, read by a pair of softmax threads (half of the tokens each): its
-// running maximum and denominator need one shuffle per stage:
+// for the row merge ("The Tree Reduction Merge Operator").  Both products put
+// 128 rows in the M dimension, so they run at the tensor cores' full rate:
 //
-//   S  [64 columns x 128 tokens]  = Q . K^T   tcgen05.mma, FP32 in TMEM
-//   P  = 2^(S scale log2e - m)                 softmax warps, FP32
-//   O  [64 columns x 128 channels] += P . V   tcgen05.mma, FP32 in TMEM,
-//                                              P as BF16 hi + lo parts
+//   S^T [128 tokens x NC columns]     = K . Q^T          tcgen05.mma, FP32 in TMEM
+//   P^T = 2^(S^T scale log2e - m_c)                        softmax warps, one token each
+//   O^T [128 channels x 2 NC] += V^T . [P_hi | P_lo]^T   tcgen05.mma, FP32 in TMEM
 //
-//  warp 0     copies: K and V tiles of 128 tokens (128-byte swizzled halves
-//             of 64 channels) HBM -> shared memory by TMA, 3-stage ring
-//  warp 1     allocates 512 TMEM columns (two S buffers, O) and issues every
-//             MMA from one thread; each MMA group is committed to an mbarrier
-//  warps 2-5  softmax: read S from TMEM, online softmax with a lazy rescale
-//             (the reference maximum moves only when a column's maximum grows
-//             by more than 2^8, so O in TMEM is rarely touched), write P into
-//             the stage's K half (free once S is computed) as the A operand
-//             of the second product, and finally read O and emit the state.
+// (NC = the group's columns rounded up to 32 or 64.)  P's BF16 hi and lo
+// parts are two halves of the second product's N dimension, so one MMA per K
+// step carries both, and O = O_hi + O_lo at the end.
+//
+//  warp 0     copies: K and V tiles of 128 tokens, [half][128 tokens][128 B]
+//             (128-byte swizzle), HBM -> shared memory by TMA, 3-stage ring
+//  warp 1     allocates TMEM (two S^T buffers, O^T) and issues every MMA
+//             from one thread; each MMA group is committed to an mbarrier
+//  warps 2-5  softmax (warps 2-9 with more than 32 columns, two threads per
+//  (2-9)      token taking 32 columns each), one token of the stage per
+//             thread: exponentials against one reference maximum per column,
+//             shared by all threads in shared memory.  The reference moves only when a column's
+//             logits exceed it by more than 2^8 (one barrier reduction per
+//             stage tells), and then O^T in TMEM is rescaled.  Each thread
+//             keeps per-column partial denominators, summed once at the end;
+//             P^T goes into the stage's K half (free once S^T is computed).
 //
 // Operands in shared memory (128-byte swizzle, 1024-byte atoms of 8 rows):
-//   Q   [half][64 rows][128 B]        A of S = Q K^T, K-major
-//   K   [half][128 tokens][128 B]     B of S = Q K^T, K-major (as TMA left it)
-//   P   [half][64 rows][128 B] x2     A of O += P V, K-major (hi, then lo)
-//   V   [half][128 tokens][128 B]     B of O += P V, MN-major (as TMA left it)
-// With a paged cache whose pages hold fewer than 128 tokens a stage is
-// [page][half][R tokens][128 B]: S is computed per page (N = R) and each
-// 16-token K step of P V addresses its page.
+//   K    [half][128 tokens][128 B]    A of S^T, K-major (as TMA left it)
+//   Q    [half][64 rows][128 B]       B of S^T, K-major
+//   V    [half][128 tokens][128 B]    A of O^T, MN-major (as TMA left it)
+//   P^T  [block][128 tokens][128 B]   B of O^T, MN-major: N = [hi | lo] columns,
+//                                     64 per block
+// Paged caches with pages of fewer than 128 tokens land each page's two
+// channel halves with one copy each, so a stage has the same layout.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -44,29 +48,32 @@
 namespace ta {
 namespace {
 
+template <int NCP>
 struct Tc05Cfg {
+    static_assert(NCP == 32 || NCP == 64, "columns per MMA");
     static constexpr int D = 128;
-    static constexpr int kTile = 128;                   // tokens per stage
+    static constexpr int kTile = 128;                   // tokens per stage (M of S^T)
     static constexpr int kStages = 3;
-    static constexpr int kKBytes = 2 * kTile * 128;     // K (or V) of a stage
+    static constexpr int kKBytes = 2 * kTile * 128;     // K (or V) of a stage: [half][tile][128 B]
     static constexpr int kStageBytes = 2 * kKBytes;
-    static constexpr int kRows = 64;                    // M of both products (columns of the group)
+    static constexpr int kPBlocks = 2 * NCP / 64;       // 64-column blocks of [hi | lo]
+    static_assert(kPBlocks * kTile * 128 <= kKBytes, "P^T fits the stage's K half");
     static constexpr int kQOff = kStages * kStageBytes;
-    static constexpr int kQBytes = 2 * kRows * 128;
+    static constexpr int kQBytes = 2 * 64 * 128;
     static constexpr int kCtlOff = kQOff + kQBytes;
     static constexpr int kCtlBytes = 256;
-    static constexpr int kSmem = 1024 + kCtlOff + kCtlBytes;
+    static constexpr int kRedOff = kCtlOff + kCtlBytes;  // m_ref, alpha, shift [64]; partials [4][64];
+    static constexpr int kRedBytes = (3 * 64 + 4 * 64 + 2 * 16) * 4;  // causal column masks [2][16]
+    static constexpr int kSmem = 1024 + kRedOff + kRedBytes;
     static_assert(kSmem <= 227 * 1024, "shared memory per block");
     static_assert(kSmem > 114 * 1024, "one block per SM: the block's TMEM allocation never waits");
-    static constexpr int kThreads = 192;
-    static constexpr uint32_t kTmemCols = 512;
-    static constexpr uint32_t kColS = 128;              // S buffer x at columns x * 128 (x = 0, 1)
-    static constexpr uint32_t kColO = 256;              // O
+    static constexpr int kSoftmaxWarps = NCP / 8;       // 4 or 8: each thread takes 32 columns of a token
+    static constexpr int kThreads = 64 + 32 * kSoftmaxWarps;
+    static constexpr uint32_t kColS = NCP;              // S^T buffer x at columns x * NCP (x = 0, 1)
+    static constexpr uint32_t kColO = 2 * NCP;          // O^T: [hi | lo], 2 NCP columns
+    static constexpr uint32_t kTmemCols = 4 * NCP;      // 128 or 256
     static constexpr float kRescaleLog2 = 8.f;          // lazy-rescale margin (log2 units)
 };
-
-// Row r of an M = 64 accumulator is TMEM lane 32 (r / 16) + r % 16: the warp
-// reading lane quarter q reaches rows 16 q .. 16 q + 15.
 
 // Bounded wait that also gives up when another role of the block has aborted.
 __device__ bool wait_or_abort(uint64_t* bar, unsigned parity, int* err, const volatile int* abort_flag) {
@@ -110,65 +117,100 @@ __device__ __forceinline__ bool warp_wait_count(int* count, int target, int* err
     return ok != 0;
 }
 
+// OR of `pred` over the NT softmax threads (named barrier 1), which also
+// synchronises them.
+template <int NT>
+__device__ __forceinline__ bool softmax_any(bool pred) {
+    uint32_t out;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.or.pred po, 1, %2, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(out)
+        : "r"(pred ? 1u : 0u), "n"(NT)
+        : "memory");
+    return out != 0;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-__global__ void __launch_bounds__(Tc05Cfg::kThreads, 1)
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
+}
+
+template <int NCP>
+__global__ void __launch_bounds__(Tc05Cfg<NCP>::kThreads, 1)
     split_kv_tc05_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                          const SplitParams p) {
-    using C = Tc05Cfg;
+    using C = Tc05Cfg<NCP>;
     constexpr int D = C::D;
+    constexpr int kS = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* stages = smem;
     uint8_t* qs = smem + C::kQOff;
     uint8_t* ctl = smem + C::kCtlOff;
-    uint64_t* full = reinterpret_cast<uint64_t*>(ctl);           // [3] copies landed
-    uint64_t* empty = full + C::kStages;                          // [3] stage released (after O += P V)
-    volatile StageMeta* meta = reinterpret_cast<volatile StageMeta*>(ctl + 48);
-    int* abort_flag = reinterpret_cast<int*>(ctl + 72);
+    uint64_t* full = reinterpret_cast<uint64_t*>(ctl);            // [kS] copies landed
+    uint64_t* empty = full + kS;                                   // [kS] stage released (after O^T += ...)
+    volatile StageMeta* meta = reinterpret_cast<volatile StageMeta*>(empty + kS);
+    int* abort_flag = const_cast<int*>(reinterpret_cast<volatile int*>(meta + kS));
     int* last_flag = abort_flag + 1;
     volatile unsigned* claim_sink = reinterpret_cast<volatile unsigned*>(abort_flag + 2);
     volatile int* bad_page = reinterpret_cast<volatile int*>(abort_flag + 3);
-    uint64_t* prod_done = reinterpret_cast<uint64_t*>(ctl + 88);  // the copy warp's last claim is made
-    uint64_t* s_full = reinterpret_cast<uint64_t*>(ctl + 96);     // [2] S of an event computed
-    uint64_t* s_free = s_full + 2;                                // [2] S read by the softmax warps
-    uint64_t* p_full = s_full + 4;                                // [2] P of an event written
-    uint64_t* o_done = s_full + 6;                                // [2] O += P V of an event done
-    uint64_t* tmem_free = s_full + 8;                             // softmax warps are done with TMEM
-    uint64_t* final_bar = s_full + 9;                             // every MMA has completed
-    uint64_t* q_full = s_full + 10;                               // Q is in shared memory
-    volatile int* smeta = reinterpret_cast<volatile int*>(ctl + 192);  // [2][4]: tok0, nvalid, stage
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctl + 224);
-    // Number of events whose O += P V has completed, published by the issuer
-    // (it alone waits on o_done, in order); the softmax warps read it when they
-    // must touch O, instead of waiting on a barrier phase that may have moved on.
-    int* o_count = reinterpret_cast<int*>(ctl + 228);
-    static_assert(228 + 4 <= C::kCtlBytes, "control block");
+    uint64_t* prod_done = reinterpret_cast<uint64_t*>(abort_flag + 4);  // the copy warp's last claim is made
+    uint64_t* s_full = prod_done + 1;                              // [2] S^T of an event computed
+    uint64_t* s_free = s_full + 2;                                 // [2] S^T read by the softmax warps
+    uint64_t* p_full = s_full + 4;                                 // [2] P^T of an event written
+    uint64_t* o_done = s_full + 6;                                 // [2] O^T += ... of an event done
+    uint64_t* tmem_free = s_full + 8;                              // softmax warps are done with TMEM
+    uint64_t* final_bar = s_full + 9;                              // every MMA has completed
+    uint64_t* q_full = s_full + 10;                                // Q is in shared memory
+    volatile int* smeta = reinterpret_cast<volatile int*>(s_full + 11);  // [2][4]: tok0, nvalid, stage
+    uint32_t* tmem_slot = const_cast<uint32_t*>(reinterpret_cast<volatile uint32_t*>(smeta + 8));
+    // Number of events whose O^T product has completed, published by the
+    // issuer (it alone waits on o_done, in order); the softmax warps read it
+    // when they must touch O^T, instead of waiting on a barrier phase that may
+    // have moved on.
+    int* o_count = reinterpret_cast<int*>(tmem_slot + 1);
+    static_assert(3 * kS * 8 + 16 + 8 + 11 * 8 + 32 + 8 <= C::kCtlBytes, "control block");
+    float* m_ref = reinterpret_cast<float*>(smem + C::kRedOff);   // [64] reference maxima (log2 units)
+    float* alpha_s = m_ref + 64;                                   // [64] scale of a moved reference
+    float* shift_s = alpha_s + 64;                                 // [64] offset change of a moved reference
+    float* wred = shift_s + 64;                                    // [4][64] per-warp partials
+    // cmask[slice][d]: bit i set iff column 32 slice + i of the group sees a
+    // token d positions into the causal diagonal, i.e. (32 slice + i) % nq >= d
+    uint32_t* cmask = reinterpret_cast<uint32_t*>(wred + 4 * 64);
 
     const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int row = b * p.Hkv + g;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool split_halves = p.block_table != nullptr && p.box_rows < C::kTile;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::kStages; ++s) {
+        for (int s = 0; s < kS; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
         mbar_init(prod_done, 1);
         for (int x = 0; x < 2; ++x) {
             mbar_init(&s_full[x], 2);  // the issuer's release of the event, and the MMA commit
-            mbar_init(&s_free[x], 4);
-            mbar_init(&p_full[x], 4);
+            mbar_init(&s_free[x], C::kSoftmaxWarps);
+            mbar_init(&p_full[x], C::kSoftmaxWarps);
+            mbar_init(&o_done[x], 1);
         }
-        mbar_init(&o_done[0], 1);
-        mbar_init(&o_done[1], 1);
-        mbar_init(tmem_free, 4);
+        mbar_init(tmem_free, C::kSoftmaxWarps);
         mbar_init(final_bar, 1);
-        mbar_init(q_full, 4);
+        mbar_init(q_full, C::kSoftmaxWarps);
         *o_count = 0;
         *abort_flag = 0;
         *bad_page = 0;
@@ -189,8 +231,10 @@ __global__ void __launch_bounds__(Tc05Cfg::kThreads, 1)
                 return;
             }
             const int ty = (y + j * p.box_rows) & page_mask;
-            tma_prefetch_5d(&tmK, 0, ty, 0, g, page);
-            tma_prefetch_5d(&tmV, 0, ty, 0, g, page);
+            for (int hf = 0; hf < (split_halves ? 2 : 1); ++hf) {
+                tma_prefetch_5d(&tmK, 0, ty, hf, g, page);
+                tma_prefetch_5d(&tmV, 0, ty, hf, g, page);
+            }
         });
     }
     tc_fence_before();
@@ -208,21 +252,29 @@ __global__ void __launch_bounds__(Tc05Cfg::kThreads, 1)
             const uint64_t pol = l2_policy_evict_first();
             const bool paged = p.block_table != nullptr;
             const int page_mask = (1 << p.page_shift) - 1;
-            const int box_bytes = 2 * p.box_rows * 128;
-            produce_row<C::kStages>(
+            const int R = p.box_rows;
+            produce_row<kS>(
                 p, b, row, n_raw, n_hint, split, C::kTile, full, empty, meta, claim_sink, bad_page,
                 C::kStageBytes, [&](int s, int y, int j, int page) {
-                    // box j = box_rows tokens x both channel halves, [half][box_rows][128 B]
+                    // every stage is [half][128 tokens][128 B] for K, then for V
                     uint8_t* st = stages + s * C::kStageBytes;
-                    const int off = j * box_bytes;
                     if (!paged) {
-                        tma_load_5d(st + off, &tmK, 0, y, 0, g, b, &full[s], pol);
-                        tma_load_5d(st + C::kKBytes + off, &tmV, 0, y, 0, g, b, &full[s], pol);
+                        tma_load_5d(st, &tmK, 0, y, 0, g, b, &full[s], pol);
+                        tma_load_5d(st + C::kKBytes, &tmV, 0, y, 0, g, b, &full[s], pol);
                         return;
                     }
-                    const int ty = (y + j * p.box_rows) & page_mask;
-                    tma_load_5d(st + off, &tmK, 0, ty, 0, g, page, &full[s], pol);
-                    tma_load_5d(st + C::kKBytes + off, &tmV, 0, ty, 0, g, page, &full[s], pol);
+                    const int ty = (y + j * R) & page_mask;
+                    if (!split_halves) {  // one box: both halves of the 128 tokens
+                        tma_load_5d(st, &tmK, 0, ty, 0, g, page, &full[s], pol);
+                        tma_load_5d(st + C::kKBytes, &tmV, 0, ty, 0, g, page, &full[s], pol);
+                        return;
+                    }
+                    // box j: tokens [j R, j R + R) of one half per copy
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const int off = hf * (C::kTile * 128) + j * R * 128;
+                        tma_load_5d(st + off, &tmK, 0, ty, hf, g, page, &full[s], pol);
+                        tma_load_5d(st + C::kKBytes + off, &tmV, 0, ty, hf, g, page, &full[s], pol);
+                    }
                 });
         }
         if (lane == 0) mbar_arrive(prod_done);  // after its last claim (lane 0 makes them)
@@ -230,58 +282,36 @@ __global__ void __launch_bounds__(Tc05Cfg::kThreads, 1)
         return;
     }
 
-    const int R = p.box_rows;        // tokens per box: 128, or the page size when smaller
-    const int nbox = C::kTile / R;
-
     // ---------------------------------------------------------- MMA issuer
     if (warp == 1) {
         if (lane == 0) {
             bool ok = wait_or_abort(q_full, 0, p.err, abort_flag);
-            const uint32_t id_s = idesc_bf16(64, R, 0, 0);    // S = Q K^T: both K-major
-            const uint32_t id_o = idesc_bf16(64, 128, 0, 1);  // O += P V: V MN-major
+            constexpr uint32_t id_s = idesc_bf16(128, NCP, 0, 0);      // S^T = K Q^T: both K-major
+            constexpr uint32_t id_o = idesc_bf16(128, 2 * NCP, 1, 1);  // O^T += V^T P^T: both MN-major
             const uint32_t q_addr = smem_u32(qs), st_addr = smem_u32(stages);
             int it = 0;          // copy stage sequence
-            int j1 = 0, j2 = 0;  // next event for S = Q K^T; next event for O += P V
-            int o_seen = 0;      // events whose O += P V completion was observed and published
-            int ev_stage[4];     // stage of each event whose O += P V is outstanding
+            int j1 = 0, j2 = 0;  // next event for S^T; next event for O^T
+            int o_seen = 0;      // events whose O^T completion was observed and published
+            int ev_stage[4];     // stage of each event whose O^T product is outstanding (<= kS)
             bool end = false;
             unsigned long long idle_since = 0;
             // Every barrier is polled without blocking, so that whichever becomes
             // ready first is served.  No barrier can run two phases ahead of its
-            // poll: o_done[x] because at most two O += P V are in flight, p_full
-            // because a softmax warp arrives on P of event j only after event j - 2's
-            // O += P V has completed (o_count), s_full / s_free as the events alternate.
+            // poll: o_done[x] because at most two O^T products are in flight,
+            // p_full because the softmax warps arrive on P^T of event j only after
+            // event j - 2's O^T product has completed (o_count), s_full / s_free
+            // as the events alternate.
             while (ok) {
                 bool progress = false;
-                // publish completed O += P V, in order
+                // publish completed O^T products, in order
                 if (o_seen < j2 && mbar_test_wait(&o_done[o_seen & 1], (o_seen >> 1) & 1)) {
                     ++o_seen;
                     st_release_smem(o_count, o_seen);
                     progress = true;
                 }
-                // O += P V for the oldest event whose P is written
-                if (j2 < j1 && o_seen >= j2 - 1 && mbar_test_wait(&p_full[j2 & 1], (j2 >> 1) & 1)) {
-                    tc_fence_after();
-                    const int s = ev_stage[j2 & 3];
-                    const uint32_t kb = st_addr + s * C::kStageBytes, vb = kb + C::kKBytes;
-#pragma unroll 1
-                    for (int kk = 0; kk < C::kTile / 16; ++kk) {
-                        const uint32_t aoff = (kk >> 2) * 8192 + (kk & 3) * 32;
-                        const int t0 = 16 * kk;
-                        const uint64_t vdesc =
-                            smem_desc_sw128(vb + (t0 / R) * (256 * R) + (t0 % R) * 128, R * 128, 1024);
-                        umma_bf16(tmem + C::kColO, smem_desc_sw128(kb + aoff, 16, 1024), vdesc, id_o,
-                                  (j2 > 0 || kk > 0) ? 1u : 0u);
-                        umma_bf16(tmem + C::kColO, smem_desc_sw128(kb + 16384 + aoff, 16, 1024), vdesc, id_o, 1u);
-                    }
-                    umma_commit(&empty[s]);
-                    umma_commit(&o_done[j2 & 1]);
-                    ++j2;
-                    progress = true;
-                }
-                // S = Q K^T for the next stage once its copies landed and its S buffer is free
-                if (!end && mbar_test_wait(&full[it % C::kStages], (it / C::kStages) & 1)) {
-                    const int s = it % C::kStages;
+                // S^T = K Q^T for the next stage once its copies landed and its buffer is free
+                if (!end && mbar_test_wait(&full[it % kS], (it / kS) & 1)) {
+                    const int s = it % kS;
                     const int nv = meta[s].nvalid;
                     if (nv < 0) {
                         end = true;
@@ -298,16 +328,12 @@ __global__ void __launch_bounds__(Tc05Cfg::kThreads, 1)
                         smeta[4 * x + 2] = s;
                         mbar_arrive(&s_full[x]);
                         const uint32_t kb = st_addr + s * C::kStageBytes;
-#pragma unroll 1
-                        for (int bx = 0; bx < nbox; ++bx) {
 #pragma unroll
-                            for (int kk = 0; kk < D / 16; ++kk) {
-                                const uint64_t qdesc =
-                                    smem_desc_sw128(q_addr + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
-                                const uint64_t kdesc = smem_desc_sw128(
-                                    kb + bx * (256 * R) + (kk >> 2) * (R * 128) + (kk & 3) * 32, 16, 1024);
-                                umma_bf16(tmem + C::kColS * x + bx * R, qdesc, kdesc, id_s, kk > 0 ? 1u : 0u);
-                            }
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t koff = (kk >> 2) * (C::kTile * 128) + (kk & 3) * 32;
+                            const uint32_t qoff = (kk >> 2) * 8192 + (kk & 3) * 32;
+                            umma_bf16(tmem + C::kColS * x, smem_desc_sw128(kb + koff, 16, 1024),
+                                      smem_desc_sw128(q_addr + qoff, 16, 1024), id_s, kk > 0 ? 1u : 0u);
                         }
                         umma_commit(&s_full[x]);
                         ev_stage[j1 & 3] = s;
@@ -316,14 +342,38 @@ __global__ void __launch_bounds__(Tc05Cfg::kThreads, 1)
                         progress = true;
                     }
                 }
+                // O^T += V^T P^T for the oldest event whose P^T is written (at most two in flight)
+                if (j2 < j1 && o_seen >= j2 - 1 && mbar_test_wait(&p_full[j2 & 1], (j2 >> 1) & 1)) {
+                    tc_fence_after();
+                    const int s = ev_stage[j2 & 3];
+                    const uint32_t pb = st_addr + s * C::kStageBytes, vb = pb + C::kKBytes;
+#pragma unroll
+                    for (int kk = 0; kk < C::kTile / 16; ++kk) {
+                        // 16 tokens: two groups of 8 rows; V's channel halves and
+                        // P^T's 64-column blocks are 16 KB apart
+                        umma_bf16(tmem + C::kColO, smem_desc_sw128(vb + kk * 2048, C::kTile * 128, 1024),
+                                  smem_desc_sw128(pb + kk * 2048, C::kTile * 128, 1024), id_o,
+                                  (j2 > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    umma_commit(&empty[s]);
+                    umma_commit(&o_done[j2 & 1]);
+                    ++j2;
+                    progress = true;
+                }
                 if (end && j2 == j1 && o_seen == j2) break;
                 if (progress) {
                     idle_since = 0;
-                } else if (idle_since == 0) {
-                    idle_since = globaltimer();
-                } else if (globaltimer() - idle_since > kWaitLimitNs) {
-                    atomicOr(p.err, kErrTimeout);
-                    ok = false;
+                } else {
+                    // leave the issue slots of this sub-partition to the softmax warp
+                    __nanosleep(20);
+                    if (*const_cast<volatile int*>(abort_flag)) {
+                        ok = false;
+                    } else if (idle_since == 0) {
+                        idle_since = globaltimer();
+                    } else if (globaltimer() - idle_since > kWaitLimitNs) {
+                        atomicOr(p.err, kErrTimeout);
+                        ok = false;
+                    }
                 }
             }
             if (ok) {  // the end-of-work event for the softmax warps
@@ -350,30 +400,45 @@ __global__ void __launch_bounds__(Tc05Cfg::kThreads, 1)
     }
 
     // ---------------------------------------------------------- softmax
-    // Row r = 16 quarter + (lane % 16) of S and O belongs to a pair of threads
-    // of the warp reading lane quarter `quarter`: half h = lane / 16 takes the
-    // row's tokens [64 h, 64 h + 64) of each stage and its channels
-    // [64 h, 64 h + 64) of O (the TMEM loads split the row at column 64).
+    // Softmax warp sw (of SW) reads TMEM lane quarter `quarter` = warp % 4 and
+    // owns the 32 columns [32 cs, 32 cs + 32), cs = sw / 4: its thread t =
+    // 32 quarter + lane handles token t of each stage and, at the end,
+    // channel t of O^T for those columns.
+    constexpr int SW = C::kSoftmaxWarps;
+    constexpr int NT = 32 * SW;       // softmax threads
     const int quarter = warp & 3;
     const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
-    const int ct = threadIdx.x - 64;              // 0..127
-    const int r = 16 * quarter + (lane & 15);     // accumulator row = column of the group
-    const int h = lane >> 4;
-    const bool act = r < p.G;
+    const int ct = threadIdx.x - 64;  // 0 .. NT - 1
+    const int cs = (warp - 2) >> 2;   // column slice
+    const int c_base = 32 * cs;
+    const int t = 32 * quarter + lane;
+    const int G = p.G;
 
-    // Q rows (columns of the group; rows past G are zero), 16-byte chunks, swizzled
+    // Q rows (columns of the group; rows past G are zero), 16-byte chunks,
+    // swizzled; reference maxima start empty
     {
         const uint4* q16 = static_cast<const uint4*>(p.q);
-        for (int idx = ct; idx < C::kRows * 16; idx += 128) {
+        for (int idx = ct; idx < 64 * 16; idx += NT) {
             const int rr = idx >> 4, ch = idx & 15;
             uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (rr < p.G) v = __ldg(q16 + (static_cast<size_t>(b) * p.Hq + static_cast<size_t>(g) * p.G + rr) * 16 + ch);
+            if (rr < G) v = __ldg(q16 + (static_cast<size_t>(b) * p.Hq + static_cast<size_t>(g) * G + rr) * 16 + ch);
             *reinterpret_cast<uint4*>(qs + (ch >> 3) * 8192 + rr * 128 + (((ch & 7) ^ (rr & 7)) << 4)) = v;
+        }
+        if (ct < 64) m_ref[ct] = -INFINITY;
+        if (ct < 32) {
+            const int sl = ct >> 4, d = ct & 15;
+            uint32_t m = 0;
+            for (int i = 0; i < 32; ++i) m |= static_cast<uint32_t>((32 * sl + i) % p.nq >= d) << i;
+            cmask[ct] = m;
         }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(q_full);
     }
+    consumer_sync(NT);  // m_ref and cmask initialised
+    // bit i of gmask: column c_base + i exists in the group
+    const uint32_t gmask = G >= c_base + 32 ? 0xffffffffu : (G <= c_base ? 0u : (1u << (G - c_base)) - 1u);
+    const uint32_t* cm = cmask + 16 * cs;
 
     int N = n_raw;
     const bool bad = (N < 0) || (N > p.S);
@@ -382,191 +447,211 @@ __global__ void __launch_bounds__(Tc05Cfg::kThreads, 1)
         N = 0;
     }
     // causal: query i of nq sees tokens < N - nq + 1 + i
-    const int lim = !act ? 0 : (p.causal ? N - p.nq + 1 + r % p.nq : 0x7fffffff);
+    const int causal_from = p.causal ? N - p.nq + 1 : 0x7fffffff;
     const float sl2 = p.scale_log2;
-    float m_ref = -INFINITY;  // reference maximum (log2 units of the scaled logits), same in both halves
-    float lsum = 0.f;         // this half's denominator relative to m_ref
+    float lp[32];  // this thread's partial denominators of its columns, relative to m_ref
+#pragma unroll
+    for (int c = 0; c < 32; ++c) lp[c] = 0.f;
+    // Every exit from this loop is decided together by the softmax warps at a
+    // barrier reduction (a warp leaving alone would strand the others at the
+    // next named barrier); a failed wait only sets `failed`.
     bool failed = false;
     int j = 0;
     for (;; ++j) {
         const int x = j & 1;
-        if (!warp_wait(&s_full[x], (j >> 1) & 1, p.err, abort_flag)) {
+        failed |= !warp_wait(&s_full[x], (j >> 1) & 1, p.err, abort_flag);
+        if (softmax_any<NT>(failed)) {
             failed = true;
             break;
         }
         const int tok0 = smeta[4 * x + 0], nv = smeta[4 * x + 1], s = smeta[4 * x + 2];
-        if (nv < 0) break;
+        if (nv < 0) break;  // every warp saw the same end-of-work event
         tc_fence_after();
-        float sv[2][32];  // scores of tokens 64 h + 32 k + i
-#pragma unroll
-        for (int k = 0; k < 2; ++k) tmem_ld16x2_32(tmem + lane_base + C::kColS * x + 32 * k, sv[k]);
+        float xs[32];  // this token's logits of the warp's columns, then their offsets from the references
+        tmem_ld32(tmem + lane_base + C::kColS * x + c_base, xs);
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s_free[x]);
 
-        // this half's valid tokens of the stage, relative to its first: [0, nvc)
-        const int nvc = max(0, min(min(nv, lim - tok0) - 64 * h, 64));
-        float tmax = -INFINITY;
-        if (nvc == 64) {
-#pragma unroll
-            for (int k = 0; k < 2; ++k)
-#pragma unroll
-                for (int i = 0; i < 32; ++i) tmax = fmaxf(tmax, sv[k][i]);
-        } else {
-#pragma unroll
-            for (int k = 0; k < 2; ++k)
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (32 * k + i < nvc) tmax = fmaxf(tmax, sv[k][i]);
-        }
-        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
-        const float tm = tmax * sl2;
-        float alpha = 1.f;
-        bool resc = false;
-        if (tm != -INFINITY) {
-            if (m_ref == -INFINITY) {
-                m_ref = tm;
-            } else if (tm > m_ref + C::kRescaleLog2) {
-                alpha = ex2(m_ref - tm);
-                m_ref = tm;
-                lsum *= alpha;
-                resc = true;
-            }
-        }
-        if (__any_sync(0xffffffffu, resc)) {
-            // O += P V of every earlier event must be complete before O is rescaled
-            if (!warp_wait_count(o_count, j, p.err, abort_flag)) {
-                failed = true;
-                break;
-            }
-            tc_fence_after();
-#pragma unroll 1
-            for (int k = 0; k < 2; ++k) {
-                float ov[32];
-                tmem_ld16x2_32(tmem + lane_base + C::kColO + 32 * k, ov);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) ov[i] *= alpha;
-                tmem_st16x2_32(tmem + lane_base + C::kColO + 32 * k, ov);
-            }
-            tmem_wait_st();
-        }
-        // P = 2^(s sl2 - m_ref) into row r of the A operand (the stage's K half):
-        // this half's 64 tokens are the K half h of the operand; hi parts, then
-        // lo parts 16 KB further; masked tokens are 0
-        uint8_t* pb = stages + s * C::kStageBytes;
+        // column c counts this token iff c < G, t < nv and (causal) tok0 + t <
+        // causal_from + c % nq, i.e. c % nq >= d for the token's depth d into the diagonal
+        const bool tok_ok = t < nv;
+        uint32_t vmask = tok_ok ? gmask : 0u;  // bit i: column c_base + i counts this token
         {
-            const float ms = (m_ref == -INFINITY) ? 0.f : m_ref;
-            float ps = 0.f;
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                float pv[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int t = 8 * ch + e;
-                    pv[e] = (t < nvc) ? ex2(fmaf(sv[t >> 5][t & 31], sl2, -ms)) : 0.f;
-                    ps += pv[e];
-                }
-                uint4 hi, lo;
-                uint32_t* hw = reinterpret_cast<uint32_t*>(&hi);
-                uint32_t* lw = reinterpret_cast<uint32_t*>(&lo);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    hw[e] = pack_bf16(pv[2 * e], pv[2 * e + 1]);
-                    const float h0 = __uint_as_float(hw[e] << 16), h1 = __uint_as_float(hw[e] & 0xffff0000u);
-                    lw[e] = pack_bf16(pv[2 * e] - h0, pv[2 * e + 1] - h1);
-                }
-                const uint32_t off = h * 8192 + r * 128 + ((ch ^ (r & 7)) << 4);
-                *reinterpret_cast<uint4*>(pb + off) = hi;
-                *reinterpret_cast<uint4*>(pb + 16384 + off) = lo;
-            }
-            lsum += ps;
+            const int d = tok0 + t - causal_from + 1;  // <= 0 before the diagonal (and without causality)
+            if (d > 0) vmask &= cm[min(d, 15)];
         }
-        // V rows past the stage's valid tokens may hold anything (even NaN): zero them
-        if (nv < C::kTile) {
-            uint8_t* vb = pb + C::kKBytes;
-            for (int idx = ct; idx < (C::kTile - nv) * 16; idx += 128) {
-                const int t = nv + (idx >> 4), ch = idx & 15;
-                const int off = (t / R) * (256 * R) + (ch >> 3) * (R * 128) + (t % R) * 128 + (ch & 7) * 16;
-                *reinterpret_cast<uint4*>(vb + off) = make_uint4(0u, 0u, 0u, 0u);
+        // offsets from the references; a logit past its reference by more than
+        // the margin, or a column's first logits, move the reference (rare)
+        bool over = false;
+#pragma unroll
+        for (int i4 = 0; i4 < 8; ++i4) {
+            const float4 m4 = *reinterpret_cast<const float4*>(m_ref + c_base + 4 * i4);
+            const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int i = 4 * i4 + e;
+                const bool v = (vmask >> i) & 1;
+                xs[i] = fmaf(xs[i], sl2, (mv[e] == -INFINITY) ? 0.f : -mv[e]);
+                over |= v && (mv[e] == -INFINITY || xs[i] > C::kRescaleLog2);
+            }
+        }
+        bool rescale_o = false;  // O^T needs the moved references' scales (after P^T is written)
+        if (softmax_any<NT>(over)) {
+            // new references: per column, the maximum over the stage's counted tokens
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float wm = warp_max(((vmask >> i) & 1) ? xs[i] : -INFINITY);
+                if (lane == 0) wred[quarter * 64 + c_base + i] = wm;
+            }
+            consumer_sync(NT);
+            float alpha = 1.f;
+            if (ct < NCP) {  // one thread per column decides its new reference
+                const int c = ct;
+                const float tx = fmaxf(fmaxf(wred[c], wred[64 + c]), fmaxf(wred[128 + c], wred[192 + c]));
+                const float m_old = m_ref[c];
+                const float base = (m_old == -INFINITY) ? 0.f : m_old;  // xs = logit - base
+                float m_new = m_old;
+                if (tx != -INFINITY && (m_old == -INFINITY || tx > C::kRescaleLog2)) m_new = tx + base;
+                alpha = (m_old == -INFINITY || m_new == m_old) ? 1.f : ex2(m_old - m_new);
+                alpha_s[c] = alpha;
+                shift_s[c] = (m_new == -INFINITY) ? 0.f : base - m_new;
+                m_ref[c] = m_new;
+            }
+            const bool resc = softmax_any<NT>(alpha != 1.f);  // also publishes alpha_s, shift_s, m_ref
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                lp[i] *= alpha_s[c_base + i];
+                xs[i] += shift_s[c_base + i];
+            }
+            rescale_o = resc && j > 0;  // the same decision in every thread
+        }
+        // P^T row t of the B operand in the stage's K half: element n of
+        // [hi | lo] at block n / 64, 16-byte chunk (n % 64) / 8 (swizzled)
+        uint8_t* pb = stages + s * C::kStageBytes;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {  // hi columns c_base + 8k .. + 7, lo columns NCP + the same
+            uint32_t hw[4], lw[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int i = 8 * k + 2 * e;
+                const float p0 = ((vmask >> i) & 1) ? ex2(xs[i]) : 0.f;
+                const float p1 = ((vmask >> (i + 1)) & 1) ? ex2(xs[i + 1]) : 0.f;
+                lp[i] += p0;
+                lp[i + 1] += p1;
+                hw[e] = pack_bf16(p0, p1);
+                lw[e] = pack_bf16(p0 - __uint_as_float(hw[e] << 16), p1 - __uint_as_float(hw[e] & 0xffff0000u));
+            }
+            const int nh = c_base + 8 * k, nl = NCP + c_base + 8 * k;
+            const uint32_t oh = (nh / 64) * (C::kTile * 128) + t * 128 + ((((nh % 64) / 8) ^ (t & 7)) << 4);
+            const uint32_t ol = (nl / 64) * (C::kTile * 128) + t * 128 + ((((nl % 64) / 8) ^ (t & 7)) << 4);
+            *reinterpret_cast<uint4*>(pb + oh) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4*>(pb + ol) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
+        // V rows past the stage's valid tokens may hold anything (even NaN): zero
+        // them (with two column slices each zeroes one channel half)
+        if (!tok_ok) {
+            uint4* vr = reinterpret_cast<uint4*>(pb + C::kKBytes + t * 128);
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                if (SW == 8 && hf != cs) continue;
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) vr[hf * C::kTile * 8 + ch] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        if (rescale_o) {
+            // every earlier O^T product must be complete before O^T is rescaled:
+            // this warp's columns, hi and lo
+            failed |= !warp_wait_count(o_count, j, p.err, abort_flag);
+            if (!failed) {
+                tc_fence_after();
+#pragma unroll 1
+                for (int k = 0; k < 2; ++k) {
+                    float ov[32];
+                    const uint32_t col = C::kColO + k * NCP + c_base;
+                    tmem_ld32(tmem + lane_base + col, ov);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) ov[i] *= alpha_s[c_base + i];
+                    tmem_st32(tmem + lane_base + col, ov);
+                }
+                tmem_wait_st();
             }
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        // event j - 2's P must have been taken (its O += P V completed) before
-        // p_full[x] gets event j's arrivals
-        if (j >= 2 && !warp_wait_count(o_count, j - 1, p.err, abort_flag)) {
-            failed = true;
-            break;
-        }
+        // event j - 2's P^T must have been taken (its O^T product completed)
+        // before p_full[x] gets event j's arrivals
+        if (j >= 2 && !failed) failed = !warp_wait_count(o_count, j - 1, p.err, abort_flag);
         __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full[x]);
+        if (lane == 0 && !failed) mbar_arrive(&p_full[x]);
     }
+    if (failed && lane == 0) atomicOr(abort_flag, 1);  // the issuer stops polling too
 
-    // the block's state: O (relative to m_ref) from TMEM once the last O += P V is done
-    float o[2][32];  // channels 64 h + 32 k + i
+    // the block's state: the denominators summed over the threads, then O^T
+    // (relative to m_ref) from TMEM once the last product is done
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const float ws = warp_sum(lp[i]);
+        if (lane == 0) wred[quarter * 64 + c_base + i] = ws;
+    }
     if (!failed && j > 0) failed = !warp_wait_count(o_count, j, p.err, abort_flag);
+    float o[32];  // channel t of the warp's columns
     if (!failed && j > 0) {
         tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < 2; ++k) tmem_ld16x2_32(tmem + lane_base + C::kColO + 32 * k, o[k]);
+        float lo[32];
+        tmem_ld32(tmem + lane_base + C::kColO + c_base, o);
+        tmem_ld32(tmem + lane_base + C::kColO + NCP + c_base, lo);
         tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] += lo[i];
     } else {
 #pragma unroll
-        for (int k = 0; k < 2; ++k)
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[k][i] = 0.f;
+        for (int i = 0; i < 32; ++i) o[i] = 0.f;
     }
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(tmem_free);
-    lsum += __shfl_xor_sync(0xffffffffu, lsum, 16);  // the row's denominator
+    const bool any_failed = softmax_any<NT>(failed);  // also publishes the partial sums
 
-    const bool poison = bad || failed || (*const_cast<volatile int*>(abort_flag) != 0) || (*bad_page != 0);
-    if (act) {
-        const size_t hrow = static_cast<size_t>(b) * p.Hq + static_cast<size_t>(g) * p.G + r;
-        const float nan = __int_as_float(0x7fc00000);
-        if (p.P == 1) {
-            const float inv = (lsum > 0.f) ? 1.f / lsum : 0.f;
-            float4* dst = reinterpret_cast<float4*>(p.out + hrow * D + 64 * h);
+    const bool poison = bad || any_failed || (*const_cast<volatile int*>(abort_flag) != 0) || (*bad_page != 0);
+    const float nan = __int_as_float(0x7fc00000);
+    const size_t hrow0 = static_cast<size_t>(b) * p.Hq + static_cast<size_t>(g) * G;
 #pragma unroll
-            for (int c4 = 0; c4 < 16; ++c4) {
-                const int k = c4 >> 3, i = (c4 & 7) * 4;
-                dst[c4] = poison ? make_float4(nan, nan, nan, nan)
-                                 : make_float4(o[k][i] * inv, o[k][i + 1] * inv, o[k][i + 2] * inv, o[k][i + 3] * inv);
-            }
-            if (p.lse && h == 0) p.lse[hrow] = poison ? nan : (lsum > 0.f ? (m_ref + log2f(lsum)) * kLn2 : -INFINITY);
+    for (int i = 0; i < 32; ++i) {
+        const int c = c_base + i;
+        if (c >= G) break;
+        const float L = (wred[c] + wred[64 + c]) + (wred[128 + c] + wred[192 + c]);
+        const size_t hrow = hrow0 + c;
+        if (p.P == 1) {
+            p.out[hrow * D + t] = poison ? nan : (L > 0.f ? o[i] / L : 0.f);
+        } else {
+            p.part_o[(hrow * p.P + split) * D + t] = poison ? nan : o[i];
+        }
+    }
+    if (ct < G) {  // one thread per column: maximum and denominator
+        const float L = (wred[ct] + wred[64 + ct]) + (wred[128 + ct] + wred[192 + ct]);
+        const float m = m_ref[ct];
+        const size_t hrow = hrow0 + ct;
+        if (p.P == 1) {
+            if (p.lse) p.lse[hrow] = poison ? nan : (L > 0.f ? (m + log2f(L)) * kLn2 : -INFINITY);
         } else {
             const size_t pr = hrow * p.P + split;
-            float4* dst = reinterpret_cast<float4*>(p.part_o + pr * D + 64 * h);
-#pragma unroll
-            for (int c4 = 0; c4 < 16; ++c4) {
-                const int k = c4 >> 3, i = (c4 & 7) * 4;
-                dst[c4] = poison ? make_float4(nan, nan, nan, nan)
-                                 : make_float4(o[k][i], o[k][i + 1], o[k][i + 2], o[k][i + 3]);
-            }
-            if (h == 0) {
-                p.part_m[pr] = poison ? nan : (m_ref == -INFINITY || lsum == 0.f ? -INFINITY : m_ref * kLn2);
-                p.part_l[pr] = poison ? nan : lsum;
-            }
+            p.part_m[pr] = poison ? nan : (m == -INFINITY || L == 0.f ? -INFINITY : m * kLn2);
+            p.part_l[pr] = poison ? nan : L;
         }
     }
     if (p.done)
-        finish_row<D>(p, row, static_cast<size_t>(b) * p.Hq + static_cast<size_t>(g) * p.G, p.G,
-                      reinterpret_cast<float*>(stages), last_flag, prod_done, ct, 128);
+        finish_row<D>(p, row, hrow0, G, reinterpret_cast<float*>(stages), last_flag, prod_done, ct, NT);
     allow_dependents();
 }
 
-}  // namespace
-
-cudaError_t launch_split_tc05(const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& p,
-                              cudaStream_t stream) {
-    using C = Tc05Cfg;
-    if (p.G < 1 || p.G > C::kRows || p.hb != 1 || p.cluster || p.box_rows < 16 || p.box_rows > C::kTile)
-        return cudaErrorInvalidValue;
+template <int NCP>
+cudaError_t launch_ncp(const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& p, cudaStream_t stream) {
+    using C = Tc05Cfg<NCP>;
     static std::atomic<unsigned long long> configured{0};
-    cudaError_t e = set_smem_once(split_kv_tc05_kernel, C::kSmem, configured);
+    cudaError_t e = set_smem_once(split_kv_tc05_kernel<NCP>, C::kSmem, configured);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.P, p.Hkv, p.B);
@@ -578,7 +663,24 @@ cudaError_t launch_split_tc05(const CUtensorMap& tk, const CUtensorMap& tv, cons
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, split_kv_tc05_kernel, tk, tv, p);
+    return cudaLaunchKernelEx(&cfg, split_kv_tc05_kernel<NCP>, tk, tv, p);
+}
+
+}  // namespace
+
+// Pages of fewer than 128 tokens land each channel half with a copy of its own.
+Geometry tc05_geometry(int page_size) {
+    Geometry geo{Tc05Cfg<64>::kTile, 64, 1, 1, 1};
+    geo.split_halves = (page_size > 0 && page_size < Tc05Cfg<64>::kTile) ? 1 : 0;
+    return geo;
+}
+
+cudaError_t launch_split_tc05(const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& p,
+                              cudaStream_t stream) {
+    if (p.G < 1 || p.G > 64 || p.hb != 1 || p.cluster || p.box_rows < 16 || p.box_rows > Tc05Cfg<64>::kTile)
+        return cudaErrorInvalidValue;
+    if (p.block_table == nullptr && p.box_rows != Tc05Cfg<64>::kTile) return cudaErrorInvalidValue;
+    return p.G <= 32 ? launch_ncp<32>(tk, tv, p, stream) : launch_ncp<64>(tk, tv, p, stream);
 }
 
 }  // namespace ta
