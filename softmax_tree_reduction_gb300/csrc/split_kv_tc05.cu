@@ -21,10 +21,11 @@
 //             (128-byte swizzle), HBM -> shared memory by TMA, 3-stage ring
 //  warp 1     allocates TMEM (two S^T buffers, O^T) and issues every MMA
 //             from one thread; each MMA group is committed to an mbarrier
-//  warps 2-5  softmax (warps 2-9 with more than 32 columns, two threads per
-//  (2-9)      token taking 32 columns each), one token of the stage per
-//             thread: exponentials against one reference maximum per column,
-//             shared by all threads in shared memory.  The reference moves only when a column's
+//  warps 2-9  softmax: 8 warps, one token of the stage and 16 (up to 32
+//             columns in the group) or 32 of its columns per thread, so each
+//             scheduler interleaves two warps:
+//             exponentials against one reference maximum per column, shared
+//             by all threads in shared memory.  The reference moves only when a column's
 //             logits exceed it by more than 2^8 (one barrier reduction per
 //             stage tells), and then O^T in TMEM is rescaled.  Each thread
 //             keeps per-column partial denominators, summed once at the end;
@@ -48,9 +49,10 @@
 namespace ta {
 namespace {
 
-template <int NCP>
+template <int NCP, int CPT>
 struct Tc05Cfg {
     static_assert(NCP == 32 || NCP == 64, "columns per MMA");
+    static_assert(CPT == 16 || CPT == 32, "columns per softmax thread");
     static constexpr int D = 128;
     static constexpr int kTile = 128;                   // tokens per stage (M of S^T)
     static constexpr int kStages = 3;
@@ -62,12 +64,13 @@ struct Tc05Cfg {
     static constexpr int kQBytes = 2 * 64 * 128;
     static constexpr int kCtlOff = kQOff + kQBytes;
     static constexpr int kCtlBytes = 256;
-    static constexpr int kRedOff = kCtlOff + kCtlBytes;  // m_ref, alpha, shift [64]; partials [4][64];
-    static constexpr int kRedBytes = (3 * 64 + 4 * 64 + 2 * 16) * 4;  // causal column masks [2][16]
+    // m_ref, m_fin, alpha, shift [64]; per-warp partials [4][64]; causal column masks [4][16]
+    static constexpr int kRedOff = kCtlOff + kCtlBytes;
+    static constexpr int kRedBytes = (4 * 64 + 4 * 64 + 64) * 4;
     static constexpr int kSmem = 1024 + kRedOff + kRedBytes;
     static_assert(kSmem <= 227 * 1024, "shared memory per block");
     static_assert(kSmem > 114 * 1024, "one block per SM: the block's TMEM allocation never waits");
-    static constexpr int kSoftmaxWarps = NCP / 8;       // 4 or 8: each thread takes 32 columns of a token
+    static constexpr int kSoftmaxWarps = 4 * NCP / CPT;  // a thread takes CPT columns of one token
     static constexpr int kThreads = 64 + 32 * kSoftmaxWarps;
     static constexpr uint32_t kColS = NCP;              // S^T buffer x at columns x * NCP (x = 0, 1)
     static constexpr uint32_t kColO = 2 * NCP;          // O^T: [hi | lo], 2 NCP columns
@@ -147,11 +150,11 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-template <int NCP>
-__global__ void __launch_bounds__(Tc05Cfg<NCP>::kThreads, 1)
+template <int NCP, int CPT>
+__global__ void __launch_bounds__(Tc05Cfg<NCP, CPT>::kThreads, 1)
     split_kv_tc05_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                          const SplitParams p) {
-    using C = Tc05Cfg<NCP>;
+    using C = Tc05Cfg<NCP, CPT>;
     constexpr int D = C::D;
     constexpr int kS = C::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -184,11 +187,12 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP>::kThreads, 1)
     int* o_count = reinterpret_cast<int*>(tmem_slot + 1);
     static_assert(3 * kS * 8 + 16 + 8 + 11 * 8 + 32 + 8 <= C::kCtlBytes, "control block");
     float* m_ref = reinterpret_cast<float*>(smem + C::kRedOff);   // [64] reference maxima (log2 units)
-    float* alpha_s = m_ref + 64;                                   // [64] scale of a moved reference
+    float* m_fin = m_ref + 64;                                     // [64] m_ref, 0 where it is -inf
+    float* alpha_s = m_fin + 64;                                   // [64] scale of a moved reference
     float* shift_s = alpha_s + 64;                                 // [64] offset change of a moved reference
     float* wred = shift_s + 64;                                    // [4][64] per-warp partials
-    // cmask[slice][d]: bit i set iff column 32 slice + i of the group sees a
-    // token d positions into the causal diagonal, i.e. (32 slice + i) % nq >= d
+    // cmask[slice][d]: bit i set iff column CPT slice + i of the group sees a
+    // token d positions into the causal diagonal, i.e. (CPT slice + i) % nq >= d
     uint32_t* cmask = reinterpret_cast<uint32_t*>(wred + 4 * 64);
 
     const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -401,16 +405,17 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP>::kThreads, 1)
 
     // ---------------------------------------------------------- softmax
     // Softmax warp sw (of SW) reads TMEM lane quarter `quarter` = warp % 4 and
-    // owns the 32 columns [32 cs, 32 cs + 32), cs = sw / 4: its thread t =
+    // owns the CPT columns [CPT cs, CPT cs + CPT), cs = sw / 4: its thread t =
     // 32 quarter + lane handles token t of each stage and, at the end,
     // channel t of O^T for those columns.
     constexpr int SW = C::kSoftmaxWarps;
     constexpr int NT = 32 * SW;       // softmax threads
+    constexpr int NS = NCP / CPT;     // column slices
     const int quarter = warp & 3;
     const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
     const int ct = threadIdx.x - 64;  // 0 .. NT - 1
     const int cs = (warp - 2) >> 2;   // column slice
-    const int c_base = 32 * cs;
+    const int c_base = CPT * cs;
     const int t = 32 * quarter + lane;
     const int G = p.G;
 
@@ -424,21 +429,26 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP>::kThreads, 1)
             if (rr < G) v = __ldg(q16 + (static_cast<size_t>(b) * p.Hq + static_cast<size_t>(g) * G + rr) * 16 + ch);
             *reinterpret_cast<uint4*>(qs + (ch >> 3) * 8192 + rr * 128 + (((ch & 7) ^ (rr & 7)) << 4)) = v;
         }
-        if (ct < 64) m_ref[ct] = -INFINITY;
-        if (ct < 32) {
+        if (ct < 64) {
+            m_ref[ct] = -INFINITY;
+            m_fin[ct] = 0.f;
+        }
+        if (ct < 64) {  // cmask[slice][d] over slices of CPT columns, d < 16
             const int sl = ct >> 4, d = ct & 15;
             uint32_t m = 0;
-            for (int i = 0; i < 32; ++i) m |= static_cast<uint32_t>((32 * sl + i) % p.nq >= d) << i;
+            for (int i = 0; i < CPT; ++i) m |= static_cast<uint32_t>((CPT * sl + i) % p.nq >= d) << i;
             cmask[ct] = m;
         }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(q_full);
     }
-    consumer_sync(NT);  // m_ref and cmask initialised
+    consumer_sync(NT);  // m_ref, m_fin and cmask initialised
     // bit i of gmask: column c_base + i exists in the group
-    const uint32_t gmask = G >= c_base + 32 ? 0xffffffffu : (G <= c_base ? 0u : (1u << (G - c_base)) - 1u);
+    const uint32_t gmask = G >= c_base + CPT ? (CPT == 32 ? 0xffffffffu : (1u << CPT) - 1u)
+                                             : (G <= c_base ? 0u : (1u << (G - c_base)) - 1u);
     const uint32_t* cm = cmask + 16 * cs;
+    uint32_t mneg = gmask;  // bit i: column c_base + i has no reference yet (m_ref = -inf)
 
     int N = n_raw;
     const bool bad = (N < 0) || (N > p.S);
@@ -449,9 +459,9 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP>::kThreads, 1)
     // causal: query i of nq sees tokens < N - nq + 1 + i
     const int causal_from = p.causal ? N - p.nq + 1 : 0x7fffffff;
     const float sl2 = p.scale_log2;
-    float lp[32];  // this thread's partial denominators of its columns, relative to m_ref
+    float lp[CPT];  // this thread's partial denominators of its columns, relative to m_ref
 #pragma unroll
-    for (int c = 0; c < 32; ++c) lp[c] = 0.f;
+    for (int i = 0; i < CPT; ++i) lp[i] = 0.f;
     // Every exit from this loop is decided together by the softmax warps at a
     // barrier reduction (a warp leaving alone would strand the others at the
     // next named barrier); a failed wait only sets `failed`.
@@ -467,8 +477,8 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP>::kThreads, 1)
         const int tok0 = smeta[4 * x + 0], nv = smeta[4 * x + 1], s = smeta[4 * x + 2];
         if (nv < 0) break;  // every warp saw the same end-of-work event
         tc_fence_after();
-        float xs[32];  // this token's logits of the warp's columns, then their offsets from the references
-        tmem_ld32(tmem + lane_base + C::kColS * x + c_base, xs);
+        float xs[CPT];  // this token's logits of the warp's columns, then their offsets from the references
+        tmem_ld_cols<CPT>(tmem + lane_base + C::kColS * x + c_base, xs);
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
@@ -482,26 +492,27 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP>::kThreads, 1)
             const int d = tok0 + t - causal_from + 1;  // <= 0 before the diagonal (and without causality)
             if (d > 0) vmask &= cm[min(d, 15)];
         }
-        // offsets from the references; a logit past its reference by more than
-        // the margin, or a column's first logits, move the reference (rare)
-        bool over = false;
+        // offsets from the references (0 where there is none yet); a logit past
+        // its reference by more than the margin, or a column's first logits,
+        // move the reference (rare)
+        float xm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int i4 = 0; i4 < 8; ++i4) {
-            const float4 m4 = *reinterpret_cast<const float4*>(m_ref + c_base + 4 * i4);
+        for (int i4 = 0; i4 < CPT / 4; ++i4) {
+            const float4 m4 = *reinterpret_cast<const float4*>(m_fin + c_base + 4 * i4);
             const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int i = 4 * i4 + e;
-                const bool v = (vmask >> i) & 1;
-                xs[i] = fmaf(xs[i], sl2, (mv[e] == -INFINITY) ? 0.f : -mv[e]);
-                over |= v && (mv[e] == -INFINITY || xs[i] > C::kRescaleLog2);
+                xs[i] = fmaf(xs[i], sl2, -mv[e]);
+                xm[e] = fmaxf(xm[e], ((vmask >> i) & 1) ? xs[i] : -INFINITY);
             }
         }
+        const bool over = (fmaxf(fmaxf(xm[0], xm[1]), fmaxf(xm[2], xm[3])) > C::kRescaleLog2) || (vmask & mneg);
         bool rescale_o = false;  // O^T needs the moved references' scales (after P^T is written)
         if (softmax_any<NT>(over)) {
             // new references: per column, the maximum over the stage's counted tokens
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
+            for (int i = 0; i < CPT; ++i) {
                 const float wm = warp_max(((vmask >> i) & 1) ? xs[i] : -INFINITY);
                 if (lane == 0) wred[quarter * 64 + c_base + i] = wm;
             }
@@ -511,37 +522,42 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP>::kThreads, 1)
                 const int c = ct;
                 const float tx = fmaxf(fmaxf(wred[c], wred[64 + c]), fmaxf(wred[128 + c], wred[192 + c]));
                 const float m_old = m_ref[c];
-                const float base = (m_old == -INFINITY) ? 0.f : m_old;  // xs = logit - base
+                const float base = m_fin[c];  // xs = logit - base
                 float m_new = m_old;
                 if (tx != -INFINITY && (m_old == -INFINITY || tx > C::kRescaleLog2)) m_new = tx + base;
                 alpha = (m_old == -INFINITY || m_new == m_old) ? 1.f : ex2(m_old - m_new);
                 alpha_s[c] = alpha;
                 shift_s[c] = (m_new == -INFINITY) ? 0.f : base - m_new;
                 m_ref[c] = m_new;
+                m_fin[c] = (m_new == -INFINITY) ? 0.f : m_new;
             }
-            const bool resc = softmax_any<NT>(alpha != 1.f);  // also publishes alpha_s, shift_s, m_ref
+            const bool resc = softmax_any<NT>(alpha != 1.f);  // also publishes the new references
+            mneg = 0;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
+            for (int i = 0; i < CPT; ++i) {
                 lp[i] *= alpha_s[c_base + i];
                 xs[i] += shift_s[c_base + i];
+                mneg |= static_cast<uint32_t>(m_ref[c_base + i] == -INFINITY) << i;
             }
+            mneg &= gmask;
             rescale_o = resc && j > 0;  // the same decision in every thread
         }
         // P^T row t of the B operand in the stage's K half: element n of
         // [hi | lo] at block n / 64, 16-byte chunk (n % 64) / 8 (swizzled)
         uint8_t* pb = stages + s * C::kStageBytes;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {  // hi columns c_base + 8k .. + 7, lo columns NCP + the same
+        for (int k = 0; k < CPT / 8; ++k) {  // hi columns c_base + 8k .. + 7, lo columns NCP + the same
+            float pv[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) pv[e] = ((vmask >> (8 * k + e)) & 1) ? ex2(xs[8 * k + e]) : 0.f;
             uint32_t hw[4], lw[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int i = 8 * k + 2 * e;
-                const float p0 = ((vmask >> i) & 1) ? ex2(xs[i]) : 0.f;
-                const float p1 = ((vmask >> (i + 1)) & 1) ? ex2(xs[i + 1]) : 0.f;
-                lp[i] += p0;
-                lp[i + 1] += p1;
-                hw[e] = pack_bf16(p0, p1);
-                lw[e] = pack_bf16(p0 - __uint_as_float(hw[e] << 16), p1 - __uint_as_float(hw[e] & 0xffff0000u));
+                lp[8 * k + 2 * e] += pv[2 * e];
+                lp[8 * k + 2 * e + 1] += pv[2 * e + 1];
+                hw[e] = pack_bf16(pv[2 * e], pv[2 * e + 1]);
+                lw[e] = pack_bf16(pv[2 * e] - __uint_as_float(hw[e] << 16),
+                                  pv[2 * e + 1] - __uint_as_float(hw[e] & 0xffff0000u));
             }
             const int nh = c_base + 8 * k, nl = NCP + c_base + 8 * k;
             const uint32_t oh = (nh / 64) * (C::kTile * 128) + t * 128 + ((((nh % 64) / 8) ^ (t & 7)) << 4);
@@ -550,14 +566,13 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP>::kThreads, 1)
             *reinterpret_cast<uint4*>(pb + ol) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
         // V rows past the stage's valid tokens may hold anything (even NaN): zero
-        // them (with two column slices each zeroes one channel half)
+        // them, the row's 16 chunks shared among the column slices
         if (!tok_ok) {
             uint4* vr = reinterpret_cast<uint4*>(pb + C::kKBytes + t * 128);
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                if (SW == 8 && hf != cs) continue;
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) vr[hf * C::kTile * 8 + ch] = make_uint4(0u, 0u, 0u, 0u);
+            for (int q = 0; q < 16 / NS; ++q) {
+                const int ch = cs * (16 / NS) + q;  // chunk ch of the row: half ch / 8
+                vr[(ch >> 3) * C::kTile * 8 + (ch & 7)] = make_uint4(0u, 0u, 0u, 0u);
             }
         }
         if (rescale_o) {
@@ -568,13 +583,13 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP>::kThreads, 1)
                 tc_fence_after();
 #pragma unroll 1
                 for (int k = 0; k < 2; ++k) {
-                    float ov[32];
+                    float ov[CPT];
                     const uint32_t col = C::kColO + k * NCP + c_base;
-                    tmem_ld32(tmem + lane_base + col, ov);
+                    tmem_ld_cols<CPT>(tmem + lane_base + col, ov);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) ov[i] *= alpha_s[c_base + i];
-                    tmem_st32(tmem + lane_base + col, ov);
+                    for (int i = 0; i < CPT; ++i) ov[i] *= alpha_s[c_base + i];
+                    tmem_st_cols<CPT>(tmem + lane_base + col, ov);
                 }
                 tmem_wait_st();
             }
@@ -592,23 +607,23 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP>::kThreads, 1)
     // the block's state: the denominators summed over the threads, then O^T
     // (relative to m_ref) from TMEM once the last product is done
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
+    for (int i = 0; i < CPT; ++i) {
         const float ws = warp_sum(lp[i]);
         if (lane == 0) wred[quarter * 64 + c_base + i] = ws;
     }
     if (!failed && j > 0) failed = !warp_wait_count(o_count, j, p.err, abort_flag);
-    float o[32];  // channel t of the warp's columns
+    float o[CPT];  // channel t of the warp's columns
     if (!failed && j > 0) {
         tc_fence_after();
-        float lo[32];
-        tmem_ld32(tmem + lane_base + C::kColO + c_base, o);
-        tmem_ld32(tmem + lane_base + C::kColO + NCP + c_base, lo);
+        float lo[CPT];
+        tmem_ld_cols<CPT>(tmem + lane_base + C::kColO + c_base, o);
+        tmem_ld_cols<CPT>(tmem + lane_base + C::kColO + NCP + c_base, lo);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] += lo[i];
+        for (int i = 0; i < CPT; ++i) o[i] += lo[i];
     } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = 0.f;
+        for (int i = 0; i < CPT; ++i) o[i] = 0.f;
     }
     tc_fence_before();
     __syncwarp();
@@ -619,7 +634,7 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP>::kThreads, 1)
     const float nan = __int_as_float(0x7fc00000);
     const size_t hrow0 = static_cast<size_t>(b) * p.Hq + static_cast<size_t>(g) * G;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
+    for (int i = 0; i < CPT; ++i) {
         const int c = c_base + i;
         if (c >= G) break;
         const float L = (wred[c] + wred[64 + c]) + (wred[128 + c] + wred[192 + c]);
@@ -647,11 +662,11 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP>::kThreads, 1)
     allow_dependents();
 }
 
-template <int NCP>
+template <int NCP, int CPT>
 cudaError_t launch_ncp(const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& p, cudaStream_t stream) {
-    using C = Tc05Cfg<NCP>;
+    using C = Tc05Cfg<NCP, CPT>;
     static std::atomic<unsigned long long> configured{0};
-    cudaError_t e = set_smem_once(split_kv_tc05_kernel<NCP>, C::kSmem, configured);
+    cudaError_t e = set_smem_once(split_kv_tc05_kernel<NCP, CPT>, C::kSmem, configured);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.P, p.Hkv, p.B);
@@ -663,24 +678,29 @@ cudaError_t launch_ncp(const CUtensorMap& tk, const CUtensorMap& tv, const Split
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, split_kv_tc05_kernel<NCP>, tk, tv, p);
+    return cudaLaunchKernelEx(&cfg, split_kv_tc05_kernel<NCP, CPT>, tk, tv, p);
 }
 
 }  // namespace
 
 // Pages of fewer than 128 tokens land each channel half with a copy of its own.
 Geometry tc05_geometry(int page_size) {
-    Geometry geo{Tc05Cfg<64>::kTile, 64, 1, 1, 1};
-    geo.split_halves = (page_size > 0 && page_size < Tc05Cfg<64>::kTile) ? 1 : 0;
+    constexpr int kTile = Tc05Cfg<64, 16>::kTile;
+    Geometry geo{kTile, 64, 1, 1, 1};
+    geo.split_halves = (page_size > 0 && page_size < kTile) ? 1 : 0;
     return geo;
 }
 
 cudaError_t launch_split_tc05(const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& p,
                               cudaStream_t stream) {
-    if (p.G < 1 || p.G > 64 || p.hb != 1 || p.cluster || p.box_rows < 16 || p.box_rows > Tc05Cfg<64>::kTile)
+    constexpr int kTile = Tc05Cfg<64, 16>::kTile;
+    if (p.G < 1 || p.G > 64 || p.hb != 1 || p.cluster || p.box_rows < 16 || p.box_rows > kTile)
         return cudaErrorInvalidValue;
-    if (p.block_table == nullptr && p.box_rows != Tc05Cfg<64>::kTile) return cudaErrorInvalidValue;
-    return p.G <= 32 ? launch_ncp<32>(tk, tv, p, stream) : launch_ncp<64>(tk, tv, p, stream);
+    if (p.block_table == nullptr && p.box_rows != kTile) return cudaErrorInvalidValue;
+    // up to 32 columns: 8 softmax warps of 16 columns; up to 64: 8 warps of 32
+    // columns (16 warps of 16 measured slower: 112.9 vs 109.9 us on the
+    // 131072-token layer, their registers capped near 100 per thread)
+    return p.G <= 32 ? launch_ncp<32, 16>(tk, tv, p, stream) : launch_ncp<64, 32>(tk, tv, p, stream);
 }
 
 }  // namespace ta
