@@ -61,8 +61,11 @@ typedef enum {
     TA_ERR_CUDA = -7,          /* a CUDA runtime/driver call failed */
     TA_ERR_DEVICE_DATA = -8,   /* device found a sequence length outside [0, max_seqlen] */
     TA_ERR_DEVICE_TIMEOUT = -9, /* a bounded on-chip wait gave up (outputs are NaN) */
-    TA_ERR_SCRATCH_LIMIT = -10  /* tree_attn_decode_noalloc: the partial states need more than
+    TA_ERR_SCRATCH_LIMIT = -10, /* tree_attn_decode_noalloc: the partial states need more than
                                    TA_NOALLOC_SCRATCH_BYTES */
+    TA_ERR_DEVICE_BOUNDS = -11  /* bounds-checking build only (compiled with TA_DEBUG_BOUNDS):
+                                   a kernel caught an index outside its buffer and skipped
+                                   the access; the outputs are not to be trusted */
 } ta_status;
 
 /* Element types. */
@@ -326,8 +329,9 @@ int tree_attn_decode_noalloc(const ta_shape *shape, const void *q, const void *k
                              int num_splits, void *stream);
 
 /* Synchronise `stream`, then read and clear the current device's error word.
- * Returns TA_OK, TA_ERR_DEVICE_DATA or TA_ERR_DEVICE_TIMEOUT (or TA_ERR_CUDA
- * when the synchronisation itself fails).
+ * Returns TA_OK, TA_ERR_DEVICE_DATA, TA_ERR_DEVICE_TIMEOUT or (bounds-checking
+ * build) TA_ERR_DEVICE_BOUNDS, or TA_ERR_CUDA when the synchronisation itself
+ * fails.
  *
  * The error word is one per device, shared by every call and stream: it
  * reports what any call since the last read found.  The library's scheduling

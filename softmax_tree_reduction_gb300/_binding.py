@@ -16,11 +16,14 @@ from typing import Optional
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libtreeattn.so")
+# TREE_ATTN_LIBRARY selects another build of the library (e.g. the
+# bounds-checking libtreeattn_debug.so); the default is the in-tree build.
+LIB_PATH = os.environ.get("TREE_ATTN_LIBRARY") or os.path.join(_HERE, "libtreeattn.so")
 
 TA_OK = 0
 TA_ERR_DEVICE_DATA = -8      # a length or page-table entry outside its range (rows are NaN)
 TA_ERR_DEVICE_TIMEOUT = -9   # a bounded on-chip wait gave up (outputs are NaN)
+TA_ERR_DEVICE_BOUNDS = -11   # bounds-checking build: an index outside its buffer was caught
 TA_F32, TA_BF16, TA_E4M3 = 0, 1, 2
 TA_KERNEL = {"auto": 0, "fma": 1, "mma": 2, "tc05": 3}
 TA_MAX_SPLITS = 4096

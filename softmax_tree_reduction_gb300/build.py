@@ -4,7 +4,14 @@ Each translation unit under csrc/ is compiled in parallel, then linked into
 ``softmax_tree_reduction_gb300/libtreeattn.so`` (static CUDA runtime, no
 torch headers).  Objects go to ``softmax_tree_reduction_gb300/_build/``.
 
-    python -m softmax_tree_reduction_gb300.build [--verbose-ptxas] [--force]
+``build(debug=True)`` makes the bounds-checking library instead,
+``libtreeattn_debug.so`` (objects in ``_build_debug/``): the same sources
+compiled with TA_DEBUG_BOUNDS, whose kernels check computed indices against
+their buffers, skip an access that falls outside and report it through the
+device error word (TA_ERR_DEVICE_BOUNDS).  Point the binding at it with the
+TREE_ATTN_LIBRARY environment variable.
+
+    python -m softmax_tree_reduction_gb300.build [--verbose-ptxas] [--force] [--debug]
 """
 from __future__ import annotations
 
@@ -17,6 +24,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libtreeattn.so")
+LIB_DEBUG = os.path.join(HERE, "libtreeattn_debug.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 SOURCES = ["api.cu", "combine.cu", "split_kv_mma.cu", "split_kv_fma_bf16.cu", "split_kv_fma_f32.cu",
@@ -40,20 +48,24 @@ def _deps_mtime() -> float:
     return max(os.path.getmtime(f) for f in files)
 
 
-def up_to_date() -> bool:
-    return os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps_mtime()
+def up_to_date(lib: str = LIB) -> bool:
+    return os.path.exists(lib) and os.path.getmtime(lib) >= _deps_mtime()
 
 
-def build(force: bool = False, verbose_ptxas: bool = False, quiet: bool = True) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose_ptxas: bool = False, quiet: bool = True, debug: bool = False) -> str:
+    lib = LIB_DEBUG if debug else LIB
+    build_dir = BUILD + "_debug" if debug else BUILD
+    if not force and up_to_date(lib):
+        return lib
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
     extra = ["-Xptxas", "-v"] if verbose_ptxas else []
+    if debug:
+        extra.append("-DTA_DEBUG_BOUNDS")
     procs = []
     objs = []
     for src in SOURCES:
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(build_dir, src.replace(".cu", ".o"))
         objs.append(obj)
         cmd = [cc, *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         procs.append((src, cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT,
@@ -68,12 +80,13 @@ def build(force: bool = False, verbose_ptxas: bool = False, quiet: bool = True) 
     if failed:
         msg = "\n".join(f"--- {s}\n{o}" for s, o in failed)
         raise RuntimeError(f"nvcc failed:\n{msg}")
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart_static", "-ldl", "-lrt",
                     "-lpthread"], check=True)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose_ptxas="--verbose-ptxas" in sys.argv, quiet=False))
+    print(build(force="--force" in sys.argv, verbose_ptxas="--verbose-ptxas" in sys.argv, quiet=False,
+                debug="--debug" in sys.argv))

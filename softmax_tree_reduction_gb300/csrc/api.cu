@@ -21,7 +21,7 @@ namespace {
 
 using ta::Geometry;
 
-__device__ int g_error_word;  // bits ta::kErrBadSeqlen | ta::kErrTimeout | ta::kErrCounters
+__device__ int g_error_word;  // bits ta::kErrBadSeqlen | kErrTimeout | kErrCounters | kErrBounds
 
 // Scheduling counters (chunk claims and row tickets) of the split kernels.
 // Zero at load; each call reserves two consecutive slots per schedule row
@@ -605,6 +605,11 @@ int decode_impl(const ta_shape* shape, const ta_paged_kv* paged, int nq, int cau
     }
     p.out = out;
     p.lse = lse;
+    p.rows = static_cast<size_t>(shape->batch) * shape->num_q_heads;
+    p.q_elems = p.rows * shape->head_dim;
+    p.out_elems = p.q_elems;
+    p.part_rows = P > 1 ? p.rows * P : 0;
+    p.bt_elems = paged ? static_cast<size_t>(shape->batch) * paged->max_pages_per_seq : 0;
     bool fused = false;
     if (P > 1) {
         char* w = static_cast<char*>(workspace);
@@ -673,6 +678,8 @@ const char* tree_attn_status_string(int status) {
         case TA_ERR_CUDA: return "a CUDA call failed";
         case TA_ERR_DEVICE_DATA: return "a sequence length outside [0, max_seqlen] was found on the device";
         case TA_ERR_DEVICE_TIMEOUT: return "an on-chip wait timed out";
+        case TA_ERR_DEVICE_BOUNDS:
+            return "an index outside its buffer was caught on the device (bounds-checking build)";
         case TA_ERR_SCRATCH_LIMIT:
             return "the partial states need more than the no-allocation scratch buffer holds "
                    "(TA_NOALLOC_SCRATCH_BYTES); use fewer splits or tree_attn_decode with a workspace";
@@ -815,6 +822,7 @@ int tree_attn_get_device_error(void* stream) {
         if (cudaDeviceSynchronize() != cudaSuccess) return TA_ERR_CUDA;
     }
     if (h & (ta::kErrTimeout | ta::kErrCounters)) return TA_ERR_DEVICE_TIMEOUT;
+    if (h & ta::kErrBounds) return TA_ERR_DEVICE_BOUNDS;
     return TA_ERR_DEVICE_DATA;
 }
 

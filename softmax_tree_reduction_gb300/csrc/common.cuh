@@ -15,6 +15,8 @@ constexpr int kErrBadSeqlen = 1;  // a sequence length outside [0, max_seqlen], 
 constexpr int kErrTimeout = 2;    // a bounded barrier wait gave up
 constexpr int kErrCounters = 4;   // a row's copy warp outlived its bounded hand-over, so the
                                   // row's scheduling counters may not be back at zero
+constexpr int kErrBounds = 8;     // (bounds-checking builds) an index outside its buffer was
+                                  // caught and the access skipped
 
 // log2(e) and ln(2): the kernels evaluate exp(x) as 2^(x * log2 e).
 constexpr float kLog2e = 1.4426950408889634f;
@@ -54,7 +56,26 @@ struct SplitParams {
     int chunk_tiles;        // tiles per scheduled chunk
     int prefetch_tiles;     // tiles of its slice a block prefetches into L2 before its wait
     float scale_log2;       // logit scale * log2(e)
+    // buffer extents, checked by the bounds-checking build only
+    size_t q_elems;         // elements of q
+    size_t out_elems;       // elements of out (B * Hq * d)
+    size_t rows;            // rows of lse (B * Hq)
+    size_t part_rows;       // rows of the partial states (B * Hq * P; 0 when P == 1)
+    size_t bt_elems;        // entries of the block table
 };
+
+// Bounds checks of the bounds-checking build (TA_DEBUG_BOUNDS): an index
+// outside [0, n) sets kErrBounds in *err and the caller skips the access.
+// In the normal build the check is the constant true and compiles away.
+#ifdef TA_DEBUG_BOUNDS
+__device__ __forceinline__ bool in_bounds(size_t idx, size_t n, int* err) {
+    if (idx < n) return true;
+    atomicOr(err, kErrBounds);
+    return false;
+}
+#else
+__device__ __forceinline__ constexpr bool in_bounds(size_t, size_t, int*) { return true; }
+#endif
 
 __device__ __forceinline__ float ex2(float x) {
     float y;

@@ -25,10 +25,11 @@ __device__ __forceinline__ void emit_state(const SplitParams& p, int b, int hq, 
             ov = 0.f;
             lv = -INFINITY;
         }
-        p.out[row * D + dd] = ov;
-        if (dd == 0 && p.lse) p.lse[row] = lv;
+        if (in_bounds(row * D + dd, p.out_elems, p.err)) p.out[row * D + dd] = ov;
+        if (dd == 0 && p.lse && in_bounds(row, p.rows, p.err)) p.lse[row] = lv;
     } else {
         const size_t pr = row * p.P + split;
+        if (!in_bounds(pr, p.part_rows, p.err)) return;
         p.part_o[pr * D + dd] = poison ? nan : o;
         if (dd == 0) {
             p.part_m[pr] = poison ? nan : (M2 == -INFINITY ? -INFINITY : M2 * kLn2);

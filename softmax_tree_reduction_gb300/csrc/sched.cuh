@@ -51,7 +51,9 @@ __device__ __forceinline__ int load_box_page(const SplitParams& p, int b, int N,
     if (t < 0 || !p.block_table) return kNoPage;
     const int tj = t + j * p.box_rows;
     if (j >= tile / p.box_rows || tj >= N) return kNoPage;
-    return __ldg(p.block_table + static_cast<size_t>(b) * p.max_pages + (tj >> p.page_shift));
+    const size_t e = static_cast<size_t>(b) * p.max_pages + (tj >> p.page_shift);
+    if (!in_bounds(e, p.bt_elems, p.err)) return kNoPage;
+    return __ldg(p.block_table + e);
 }
 
 // The contiguous slice [*t, *t_end) that block `split` streams first, and the
@@ -96,7 +98,9 @@ __device__ int prefetch_row_head(const SplitParams& p, int b, int split, int til
         if (p.block_table) {
             const int tj = t + lane * p.box_rows;
             if (tj >= N) break;
-            page = ld_relaxed(p.block_table + static_cast<size_t>(b) * p.max_pages + (tj >> p.page_shift));
+            const size_t e = static_cast<size_t>(b) * p.max_pages + (tj >> p.page_shift);
+            if (!in_bounds(e, p.bt_elems, p.err)) break;
+            page = ld_relaxed(p.block_table + e);
             if (page < 0 || page >= p.num_pages) break;
         }
         pf(t, lane, page);
@@ -322,6 +326,7 @@ __device__ void cluster_merge_row(const SplitParams& p, size_t hq0, int nh, cons
             O = fmaf(w, oq[q], O);
         }
         const size_t r = hq0 + h;
+        if (!in_bounds(r, p.rows, p.err)) continue;
         p.out[r * D + dd] = (L == 0.f) ? 0.f : O / L;  // NaN inputs propagate
         if (dd == 0 && p.lse) p.lse[r] = (L > 0.f) ? (M + log2f(L)) * kLn2 : (L == 0.f ? -INFINITY : L);
     }
@@ -357,6 +362,8 @@ __device__ void finish_row(const SplitParams& p, int row, size_t hq0, int G, flo
         // them on its own: no block barrier on the way to the outputs.
         for (int idx = tid; idx < G * D4; idx += nthr) {
             const int h = idx / D4, d4 = idx - h * D4;
+            if (!in_bounds((row0 + h) * P + P - 1, p.part_rows, p.err) || !in_bounds(row0 + h, p.rows, p.err))
+                continue;
             const float4* o = reinterpret_cast<const float4*>(p.part_o + (row0 + h) * P * D) + d4;
             const float* mrow = p.part_m + (row0 + h) * P;
             const float* lrow = p.part_l + (row0 + h) * P;
@@ -396,6 +403,8 @@ __device__ void finish_row(const SplitParams& p, int row, size_t hq0, int G, flo
         }
         return;
     }
+    if (!in_bounds((row0 + G) * P - 1, p.part_rows, p.err) || !in_bounds(row0 + G - 1, p.rows, p.err))
+        return;  // (bounds-checking build) the row's states are not where they should be
     float* sw = scratch;           // [G][P]  maxima, then leaf weights
     float* sl = scratch + G * P;   // [G][P]  denominators
     float* sr = sl + G * P;        // [G] root maxima, [G] root denominators

@@ -180,8 +180,8 @@ __global__ void __launch_bounds__(FmaCfg<KV, D>::kThreads, 1)
 #pragma unroll
                 for (int e = 0; e < EPC; ++e) {
                     const size_t idx = (qrow + i) * D + (j + 8 * c) * EPC + e;
-                    const float qv =
-                        p.q_is_bf16
+                    const float qv = !in_bounds(idx, p.q_elems, p.err) ? 0.f
+                        : p.q_is_bf16
                             ? __bfloat162float(static_cast<const __nv_bfloat16*>(p.q)[idx])
                             : static_cast<const float*>(p.q)[idx];
                     qf[i][c * EPC + e] = qv * p.scale_log2;

@@ -159,6 +159,7 @@ __global__ void __launch_bounds__(Fp8Cfg<HB>::kThreads, 1)
             C::kStageBytes, [&](int s, int y, int j, int page) {
                 uint8_t* st = stages + s * C::kStageBytes;
                 const int off = j * box_bytes;
+                if (!in_bounds(off + box_bytes - 1, C::kKBytes, p.err)) return;
                 if (!paged) {
                     tma_load_4d(st + off, &tmK, 0, y, g0, b, &full[s], pol);
                     tma_load_4d(st + C::kKBytes + off, &tmV, 0, y, g0, b, &full[s], pol);
@@ -202,8 +203,8 @@ __global__ void __launch_bounds__(Fp8Cfg<HB>::kThreads, 1)
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         const int c = nt * 8 + gid;
-        const bool hv = c < p.G;
-        const int hq = g * p.G + (hv ? c : 0);
+        const int hq = g * p.G + (c < p.G ? c : 0);
+        const bool hv = c < p.G && in_bounds((static_cast<size_t>(b) * p.Hq + hq + 1) * D - 1, p.q_elems, p.err);
         const uint4* qh = reinterpret_cast<const uint4*>(
             static_cast<const __nv_bfloat16*>(p.q) + (static_cast<size_t>(b) * p.Hq + hq) * D + 32 * tig);
 #pragma unroll

@@ -164,6 +164,7 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, CG>::kThreads, 1)
                     // tile at j*box_bytes.
                     uint8_t* st = stages + s * C::kStageBytes;
                     const int off = j * box_bytes;
+                    if (!in_bounds(off + box_bytes - 1, C::kKBytes, p.err)) return;
                     if (!paged) {
                         tma_load_5d(st + off, &tmK, 0, y, 0, g0, b, &full[s], pol);
                         tma_load_5d(st + C::kKBytes + off, &tmV, 0, y, 0, g0, b, &full[s], pol);
@@ -210,8 +211,8 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, CG>::kThreads, 1)
         const uint32_t* q32 = static_cast<const uint32_t*>(p.q);
         for (int idx = threadIdx.x - 32; idx < 16 * CG * (D / 2); idx += C::kWarps * 32) {
             const int c = idx / (D / 2), w = idx - c * (D / 2);
-            const uint32_t v =
-                (c < p.G) ? q32[(static_cast<size_t>(b) * p.Hq + g0 * p.G + c) * (D / 2) + w] : 0u;
+            const size_t qi = (static_cast<size_t>(b) * p.Hq + g0 * p.G + c) * (D / 2) + w;
+            const uint32_t v = (c < p.G && in_bounds(2 * qi + 1, p.q_elems, p.err)) ? q32[qi] : 0u;
             *reinterpret_cast<uint32_t*>(qs + c * C::kQRowBytes + 4 * w) = v;
         }
         consumer_sync(C::kWarps * 32);
@@ -221,8 +222,8 @@ __global__ void __launch_bounds__(MmaCfg<D, HB, CG>::kThreads, 1)
 #pragma unroll
     for (int nt = 0; nt < NT && !C::kQSmem; ++nt) {
         const int c = cbase + nt * 8 + gid;
-        const bool hv = c < p.G;
-        const int hq = g * p.G + (hv ? c : 0);
+        const int hq = g * p.G + (c < p.G ? c : 0);
+        const bool hv = c < p.G && in_bounds((static_cast<size_t>(b) * p.Hq + hq + 1) * D - 1, p.q_elems, p.err);
         const __nv_bfloat16* qh =
             static_cast<const __nv_bfloat16*>(p.q) + (static_cast<size_t>(b) * p.Hq + hq) * D;
 #pragma unroll

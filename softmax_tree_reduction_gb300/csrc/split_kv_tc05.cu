@@ -268,6 +268,7 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP, CPT>::kThreads, 1)
                         return;
                     }
                     const int ty = (y + j * R) & page_mask;
+                    if (!in_bounds(static_cast<size_t>(j + 1) * R * 128 - 1, C::kTile * 128, p.err)) return;
                     if (!split_halves) {  // one box: both halves of the 128 tokens
                         tma_load_5d(st, &tmK, 0, ty, 0, g, page, &full[s], pol);
                         tma_load_5d(st + C::kKBytes, &tmV, 0, ty, 0, g, page, &full[s], pol);
@@ -426,7 +427,8 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP, CPT>::kThreads, 1)
         for (int idx = ct; idx < 64 * 16; idx += NT) {
             const int rr = idx >> 4, ch = idx & 15;
             uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (rr < G) v = __ldg(q16 + (static_cast<size_t>(b) * p.Hq + static_cast<size_t>(g) * G + rr) * 16 + ch);
+            const size_t qi = (static_cast<size_t>(b) * p.Hq + static_cast<size_t>(g) * G + rr) * 16 + ch;
+            if (rr < G && in_bounds(8 * qi + 7, p.q_elems, p.err)) v = __ldg(q16 + qi);
             *reinterpret_cast<uint4*>(qs + (ch >> 3) * 8192 + rr * 128 + (((ch & 7) ^ (rr & 7)) << 4)) = v;
         }
         if (ct < 64) {
@@ -562,8 +564,10 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP, CPT>::kThreads, 1)
             const int nh = c_base + 8 * k, nl = NCP + c_base + 8 * k;
             const uint32_t oh = (nh / 64) * (C::kTile * 128) + t * 128 + ((((nh % 64) / 8) ^ (t & 7)) << 4);
             const uint32_t ol = (nl / 64) * (C::kTile * 128) + t * 128 + ((((nl % 64) / 8) ^ (t & 7)) << 4);
-            *reinterpret_cast<uint4*>(pb + oh) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            *reinterpret_cast<uint4*>(pb + ol) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            if (in_bounds(oh + 15, C::kKBytes, p.err))
+                *reinterpret_cast<uint4*>(pb + oh) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            if (in_bounds(ol + 15, C::kKBytes, p.err))
+                *reinterpret_cast<uint4*>(pb + ol) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
         // V rows past the stage's valid tokens may hold anything (even NaN): zero
         // them, the row's 16 chunks shared among the column slices
@@ -640,8 +644,9 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP, CPT>::kThreads, 1)
         const float L = (wred[c] + wred[64 + c]) + (wred[128 + c] + wred[192 + c]);
         const size_t hrow = hrow0 + c;
         if (p.P == 1) {
-            p.out[hrow * D + t] = poison ? nan : (L > 0.f ? o[i] / L : 0.f);
-        } else {
+            if (in_bounds(hrow * D + t, p.out_elems, p.err))
+                p.out[hrow * D + t] = poison ? nan : (L > 0.f ? o[i] / L : 0.f);
+        } else if (in_bounds(hrow * p.P + split, p.part_rows, p.err)) {
             p.part_o[(hrow * p.P + split) * D + t] = poison ? nan : o[i];
         }
     }
@@ -650,8 +655,9 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP, CPT>::kThreads, 1)
         const float m = m_ref[ct];
         const size_t hrow = hrow0 + ct;
         if (p.P == 1) {
-            if (p.lse) p.lse[hrow] = poison ? nan : (L > 0.f ? (m + log2f(L)) * kLn2 : -INFINITY);
-        } else {
+            if (p.lse && in_bounds(hrow, p.rows, p.err))
+                p.lse[hrow] = poison ? nan : (L > 0.f ? (m + log2f(L)) * kLn2 : -INFINITY);
+        } else if (in_bounds(hrow * p.P + split, p.part_rows, p.err)) {
             const size_t pr = hrow * p.P + split;
             p.part_m[pr] = poison ? nan : (m == -INFINITY || L == 0.f ? -INFINITY : m * kLn2);
             p.part_l[pr] = poison ? nan : L;
