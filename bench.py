@@ -42,14 +42,17 @@ FALLBACK_HBM_GBS = 6800.0
 # workload, with the SHA-256 of the kernel source it was taken on; reported
 # only while that source is unchanged.
 NCU_TRAFFIC = {
-    # tensor-core kernel, BF16 cache, 8B-shaped layer of 131072 tokens, 19 splits
-    ("mma", "llama3.1-8b-decode-layer"): {
-        "bytes_per_launch": 537324800 + 2997504, "num_splits": 19,
-        "src_sha256": "696e23f05d8bd1508358c5982ea2f3223cce80b325e630299f2717986676f60b"},
-    # FP8 kernel, E4M3 cache, the same layer and split count
-    ("fp8", "llama3.1-8b-decode-layer"): {
-        "bytes_per_launch": 268520960 + 2965248, "num_splits": 19,
-        "src_sha256": "5f8dbf729267369e5bfa9ce20bfb4e3f67c003f9c734ae4f114ddee1765daa73"},
+    # warp-level tensor-core kernel, BF16 cache, 8B-shaped layer of 131072 tokens, 19 splits
+    ("mma", "llama3.1-8b-decode-layer", 1): {
+        "bytes_per_launch": 537313280 + 3423744, "num_splits": 19,
+        "src_sha256": "26142dfeb40e7e2f28a485ecaaaebd4bc535c9ccd7805ae58d29236cb4a282ea"},
+    # tcgen05 kernel, the same layer with 8 and 16 queries per row (32 and 64 columns per KV head)
+    ("tc05", "llama3.1-8b-decode-layer", 8): {
+        "bytes_per_launch": 537470208 + 2971136, "num_splits": 19,
+        "src_sha256": "ce522a28c1033722e14ac6b8242e6efd3822d734cec09137b920e3eb2bea1217"},
+    ("tc05", "llama3.1-8b-decode-layer", 16): {
+        "bytes_per_launch": 537434368 + 2981376, "num_splits": 19,
+        "src_sha256": "ce522a28c1033722e14ac6b8242e6efd3822d734cec09137b920e3eb2bea1217"},
 }
 
 
@@ -474,10 +477,10 @@ def run_ours(args, rank, world, local):
         return None
     peak, peak_kind = load_peaks()
     achieved = kv_bytes / (split_ms_max / 1e3) / 1e9
-    tr = NCU_TRAFFIC.get((kernel_used, w.name))
+    tr = NCU_TRAFFIC.get((kernel_used, w.name, args.queries))
     traffic = None
     if (tr and tr.get("src_sha256") == kernel_source_hash(kernel_used) and tr.get("num_splits") == P
-            and not args.paged and args.queries == 1 and not args.deterministic):
+            and not args.paged and not args.deterministic):
         traffic = tr["bytes_per_launch"]
     cpu = None
     if not args.no_cpu_baseline:
