@@ -40,6 +40,10 @@ constexpr int kChunkTokens = 128;
 // 512 / 1152 / 1792 / 2304 were slower on the 8B-shaped layer).
 constexpr int kPrefetchTokens = 1152;
 constexpr int kPrefetchTokensFp8 = 768;
+// The tcgen05 kernel's steps are longer (many columns per KV head), so less of
+// the prefetch hides behind the previous step's merge: 256 tokens measured
+// best (0 / 256 / 512 / 1152: 94.2 / 93.6 / 94.5 / 95.2 us with 32 columns).
+constexpr int kPrefetchTokensTc05 = 256;
 // The row's last block merges the partial states itself when there are few
 // of them (its merge costs about one L2 round trip per 20 states, serially);
 // more splits go to the combine kernel, which spreads the merge over (h, b)
@@ -588,8 +592,10 @@ int decode_impl(const ta_shape* shape, const ta_paged_kv* paged, int nq, int cau
                                            : 1.0f / std::sqrt(static_cast<float>(shape->head_dim));
     p.scale_log2 = scale * ta::kLog2e;
     p.chunk_tiles = std::max(1, kChunkTokens / geo.tile_tokens);
-    p.prefetch_tiles =
-        std::max(1, (kernel == kKernelFp8 ? kPrefetchTokensFp8 : kPrefetchTokens) / geo.tile_tokens);
+    p.prefetch_tiles = std::max(1, (kernel == kKernelFp8    ? kPrefetchTokensFp8
+                                    : kernel == TA_KERNEL_TC05 ? kPrefetchTokensTc05
+                                                               : kPrefetchTokens) /
+                                       geo.tile_tokens);
     p.box_rows = rows;
     p.hb = hb;
     p.stall = (options && (options->flags & TA_FLAG_DIAG_STALL)) ? 1 : 0;

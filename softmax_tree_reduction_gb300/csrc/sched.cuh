@@ -339,7 +339,8 @@ __device__ void cluster_merge_row(const SplitParams& p, size_t hq0, int nh, cons
 // last ticket resets the claim counter every claim of the row has landed --
 // also when the compute warps left the stage ring early after a timed-out
 // wait -- and a finished call leaves both counters at zero.
-template <int D>
+// kBatch: leaf numerators each thread keeps in flight (registers: 4 per leaf).
+template <int D, int kBatch = 20>
 __device__ void finish_row(const SplitParams& p, int row, size_t hq0, int G, float* scratch,
                            int* flag, uint64_t* prod_done, int tid, int nthr) {
     consumer_sync(nthr);
@@ -355,7 +356,6 @@ __device__ void finish_row(const SplitParams& p, int row, size_t hq0, int G, flo
     const int P = p.P;
     const size_t row0 = hq0;
     constexpr int D4 = D / 4;
-    constexpr int kBatch = 20;     // leaf numerators in flight per thread
     if (P <= kBatch) {
         // Few leaves: each thread loads its channel's numerators together with
         // its head's maxima and denominators (one round trip to L2) and merges

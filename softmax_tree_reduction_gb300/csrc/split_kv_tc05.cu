@@ -66,7 +66,7 @@ struct Tc05Cfg {
     static constexpr int kCtlBytes = 256;
     // m_ref, m_fin, alpha, shift [64]; per-warp partials [4][64]; causal column masks [4][16]
     static constexpr int kRedOff = kCtlOff + kCtlBytes;
-    static constexpr int kRedBytes = (4 * 64 + 4 * 64 + 64) * 4;
+    static constexpr int kRedBytes = (4 * 64 + 4 * 64 + 64 + 4) * 4;
     static constexpr int kSmem = 1024 + kRedOff + kRedBytes;
     static_assert(kSmem <= 227 * 1024, "shared memory per block");
     static_assert(kSmem > 114 * 1024, "one block per SM: the block's TMEM allocation never waits");
@@ -76,6 +76,8 @@ struct Tc05Cfg {
     static constexpr uint32_t kColO = 2 * NCP;          // O^T: [hi | lo], 2 NCP columns
     static constexpr uint32_t kTmemCols = 4 * NCP;      // 128 or 256
     static constexpr float kRescaleLog2 = 8.f;          // lazy-rescale margin (log2 units)
+    // the row merge's loads in flight per thread (4 registers each)
+    static constexpr int kMergeBatch = 20;
 };
 
 // Bounded wait that also gives up when another role of the block has aborted.
@@ -194,6 +196,7 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP, CPT>::kThreads, 1)
     // cmask[slice][d]: bit i set iff column CPT slice + i of the group sees a
     // token d positions into the causal diagonal, i.e. (CPT slice + i) % nq >= d
     uint32_t* cmask = reinterpret_cast<uint32_t*>(wred + 4 * 64);
+    int* fail_rec = reinterpret_cast<int*>(cmask + 64);            // a softmax warp's wait failed
 
     const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int row = b * p.Hkv + g;
@@ -435,6 +438,7 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP, CPT>::kThreads, 1)
             m_ref[ct] = -INFINITY;
             m_fin[ct] = 0.f;
         }
+        if (ct == 0) *fail_rec = 0;
         if (ct < 64) {  // cmask[slice][d] over slices of CPT columns, d < 16
             const int sl = ct >> 4, d = ct & 15;
             uint32_t m = 0;
@@ -464,54 +468,66 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP, CPT>::kThreads, 1)
     float lp[CPT];  // this thread's partial denominators of its columns, relative to m_ref
 #pragma unroll
     for (int i = 0; i < CPT; ++i) lp[i] = 0.f;
-    // Every exit from this loop is decided together by the softmax warps at a
-    // barrier reduction (a warp leaving alone would strand the others at the
-    // next named barrier); a failed wait only sets `failed`.
+    // Every exit from this loop is decided together by the softmax warps after
+    // the stage's one barrier reduction (a warp leaving alone would strand the
+    // others at the next named barrier): a warp whose wait failed records it in
+    // shared memory before the reduction and votes, and all warps read the
+    // record after it.
     bool failed = false;
     int j = 0;
     for (;; ++j) {
         const int x = j & 1;
-        failed |= !warp_wait(&s_full[x], (j >> 1) & 1, p.err, abort_flag);
-        if (softmax_any<NT>(failed)) {
+        const bool ok = warp_wait(&s_full[x], (j >> 1) & 1, p.err, abort_flag);
+        int tok0 = 0, nv = -1, s = 0;
+        if (ok) {
+            tok0 = smeta[4 * x + 0];
+            nv = smeta[4 * x + 1];
+            s = smeta[4 * x + 2];
+        } else if (lane == 0) {
+            *fail_rec = 1;
+        }
+        float xs[CPT];       // this token's logits of the warp's columns, then their offsets from the references
+        uint32_t vmask = 0;  // bit i: column c_base + i counts this token
+        bool over = !ok;
+        const bool tok_ok = t < nv;
+        if (ok && nv >= 0) {
+            tc_fence_after();
+            tmem_ld_cols<CPT>(tmem + lane_base + C::kColS * x + c_base, xs);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_free[x]);
+
+            // column c counts this token iff c < G, t < nv and (causal) tok0 + t <
+            // causal_from + c % nq, i.e. c % nq >= d for the token's depth d into the diagonal
+            vmask = tok_ok ? gmask : 0u;
+            const int d = tok0 + t - causal_from + 1;  // <= 0 before the diagonal (and without causality)
+            if (d > 0) vmask &= cm[min(d, 15)];
+            // offsets from the references (0 where there is none yet); a logit past
+            // its reference by more than the margin, or a column's first logits,
+            // move the reference (rare)
+            float xm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int i4 = 0; i4 < CPT / 4; ++i4) {
+                const float4 m4 = *reinterpret_cast<const float4*>(m_fin + c_base + 4 * i4);
+                const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int i = 4 * i4 + e;
+                    xs[i] = fmaf(xs[i], sl2, -mv[e]);
+                    xm[e] = fmaxf(xm[e], ((vmask >> i) & 1) ? xs[i] : -INFINITY);
+                }
+            }
+            over = (fmaxf(fmaxf(xm[0], xm[1]), fmaxf(xm[2], xm[3])) > C::kRescaleLog2) || (vmask & mneg);
+        }
+        const bool any_over = softmax_any<NT>(over);  // the stage's barrier reduction
+        if (*const_cast<volatile int*>(fail_rec)) {
             failed = true;
             break;
         }
-        const int tok0 = smeta[4 * x + 0], nv = smeta[4 * x + 1], s = smeta[4 * x + 2];
-        if (nv < 0) break;  // every warp saw the same end-of-work event
-        tc_fence_after();
-        float xs[CPT];  // this token's logits of the warp's columns, then their offsets from the references
-        tmem_ld_cols<CPT>(tmem + lane_base + C::kColS * x + c_base, xs);
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s_free[x]);
-
-        // column c counts this token iff c < G, t < nv and (causal) tok0 + t <
-        // causal_from + c % nq, i.e. c % nq >= d for the token's depth d into the diagonal
-        const bool tok_ok = t < nv;
-        uint32_t vmask = tok_ok ? gmask : 0u;  // bit i: column c_base + i counts this token
-        {
-            const int d = tok0 + t - causal_from + 1;  // <= 0 before the diagonal (and without causality)
-            if (d > 0) vmask &= cm[min(d, 15)];
-        }
-        // offsets from the references (0 where there is none yet); a logit past
-        // its reference by more than the margin, or a column's first logits,
-        // move the reference (rare)
-        float xm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int i4 = 0; i4 < CPT / 4; ++i4) {
-            const float4 m4 = *reinterpret_cast<const float4*>(m_fin + c_base + 4 * i4);
-            const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int i = 4 * i4 + e;
-                xs[i] = fmaf(xs[i], sl2, -mv[e]);
-                xm[e] = fmaxf(xm[e], ((vmask >> i) & 1) ? xs[i] : -INFINITY);
-            }
-        }
-        const bool over = (fmaxf(fmaxf(xm[0], xm[1]), fmaxf(xm[2], xm[3])) > C::kRescaleLog2) || (vmask & mneg);
+        if (nv < 0) break;  // every warp's wait succeeded and saw the same end-of-work event
         bool rescale_o = false;  // O^T needs the moved references' scales (after P^T is written)
-        if (softmax_any<NT>(over)) {
+        if (any_over) {
             // new references: per column, the maximum over the stage's counted tokens
 #pragma unroll
             for (int i = 0; i < CPT; ++i) {
@@ -583,6 +599,7 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP, CPT>::kThreads, 1)
             // every earlier O^T product must be complete before O^T is rescaled:
             // this warp's columns, hi and lo
             failed |= !warp_wait_count(o_count, j, p.err, abort_flag);
+            if (failed && lane == 0) *fail_rec = 1;  // the next stage's reduction ends the loop
             if (!failed) {
                 tc_fence_after();
 #pragma unroll 1
@@ -605,6 +622,7 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP, CPT>::kThreads, 1)
         if (j >= 2 && !failed) failed = !warp_wait_count(o_count, j - 1, p.err, abort_flag);
         __syncwarp();
         if (lane == 0 && !failed) mbar_arrive(&p_full[x]);
+        if (lane == 0 && failed) *fail_rec = 1;
     }
     if (failed && lane == 0) atomicOr(abort_flag, 1);  // the issuer stops polling too
 
@@ -664,7 +682,8 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP, CPT>::kThreads, 1)
         }
     }
     if (p.done)
-        finish_row<D>(p, row, hrow0, G, reinterpret_cast<float*>(stages), last_flag, prod_done, ct, NT);
+        finish_row<D, C::kMergeBatch>(p, row, hrow0, G, reinterpret_cast<float*>(stages), last_flag, prod_done,
+                                      ct, NT);
     allow_dependents();
 }
 
@@ -704,8 +723,8 @@ cudaError_t launch_split_tc05(const CUtensorMap& tk, const CUtensorMap& tv, cons
         return cudaErrorInvalidValue;
     if (p.block_table == nullptr && p.box_rows != kTile) return cudaErrorInvalidValue;
     // up to 32 columns: 8 softmax warps of 16 columns; up to 64: 8 warps of 32
-    // columns (16 warps of 16 measured slower: 112.9 vs 109.9 us on the
-    // 131072-token layer, their registers capped near 100 per thread)
+    // columns (16 warps of 16, 96 registers a thread, measured slower: 109.8 vs
+    // 109.6 us on the 131072-token layer, 748.8 vs 736.5 us on the 70B-shaped one)
     return p.G <= 32 ? launch_ncp<32, 16>(tk, tv, p, stream) : launch_ncp<64, 32>(tk, tv, p, stream);
 }
 
