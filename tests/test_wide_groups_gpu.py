@@ -141,3 +141,35 @@ def test_tc05_wrong_length_hint_changes_nothing(P):
     torch.cuda.synchronize()
     assert ta.tree_attn_get_device_error() == 0
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_tc05_bad_seqlen_sets_error_word_and_nan_rows():
+    """A length outside [0, max_seqlen] on the tcgen05 path: that row is NaN,
+    the others are correct, and the error word reports it."""
+    inp = _inputs(32, 2, [1000, 333, 2000], 2048, seed=8)
+    ref_o, ref_l = oracle.attention(inp["q"], inp["k"], inp["v"], inp["seqlens"])
+    q, k, v, sl = (inp[x].cuda() for x in ("q", "k", "v", "seqlens"))
+    bad = sl.clone()
+    bad[1] = 2048 + 7
+    assert ta.tree_attn_get_device_error() == 0
+    for P in (1, 4):
+        out, lse = ta.tree_attn_decode(q, k, v, bad, num_splits=P, kernel="tc05")
+        assert ta.tree_attn_get_device_error() == ta.TA_ERR_DEVICE_DATA
+        o = out.cpu()
+        assert torch.isnan(o[1]).all() and torch.isfinite(o[0]).all() and torch.isfinite(o[2]).all()
+        keep = [0, 2]
+        _check(out[keep], lse[keep], ref_o[keep], ref_l[keep], f"good rows P={P}")
+
+
+def test_tc05_bad_page_entry_poisons_only_its_row():
+    inp = _inputs(48, 2, [700, 1500], 1536, seed=9)
+    ref_o, ref_l = oracle.attention(inp["q"], inp["k"], inp["v"], inp["seqlens"])
+    kp, vp, bt = workloads.page_pool(inp["k"], inp["v"], inp["seqlens"], 64, seed=3)
+    bt = bt.clone()
+    bt[1, 5] = kp.shape[0] + 3        # a page past the pool for a valid token of row 1
+    out, lse = ta.tree_attn_decode_paged(inp["q"].cuda(), kp.cuda(), vp.cuda(), bt.cuda(), inp["seqlens"].cuda(),
+                                         num_splits=3, max_seqlen=1536, kernel="tc05")
+    assert ta.tree_attn_get_device_error() == ta.TA_ERR_DEVICE_DATA
+    o = out.cpu()
+    assert torch.isnan(o[1]).all()
+    _check(out[:1], lse[:1], ref_o[:1], ref_l[:1], "row 0")
