@@ -92,6 +92,10 @@ def parse_args(argv=None):
                     help="FP8 E4M3 caches (the workload's K and V rounded with one scale per KV head)")
     ap.add_argument("--cluster-merge", action="store_true",
                     help="each row's (2..8) blocks merge through a thread-block cluster's shared memory")
+    ap.add_argument("--merge", choices=["auto", "ticket", "cluster"], default="auto",
+                    help="context sweep: the library's choice of split count and merge (auto), the "
+                         "heuristic's split count merged by the last-arriving block (ticket), or "
+                         "--cluster-merge (cluster)")
     ap.add_argument("--deterministic", action="store_true",
                     help="fixed chunk assignment (bitwise reproducible) instead of run-time balancing")
     return ap.parse_args(argv)
@@ -645,7 +649,8 @@ def run_sweeps(args):
             copies = draw(N)
             shape = ta.make_shape(copies[0]["q"], copies[0]["k"])
             P = ta.tree_attn_pick_splits(shape)
-            if args.cluster_merge:
+            merge = "cluster" if args.cluster_merge else args.merge
+            if merge == "cluster":
                 P = min(P, 8)  # one cluster per row: at most 8 blocks
             kv_bytes = w.kv_bytes(np.full(w.batch, N))
             B, Hq, d = copies[0]["q"].shape
@@ -653,10 +658,11 @@ def run_sweeps(args):
             lse = torch.empty(B, Hq, device="cuda")
             ws = torch.empty(max(16, ta.tree_attn_workspace_bytes(shape, P)), dtype=torch.uint8,
                              device="cuda")
-            ms, split = _time_steps(ta, torch, copies, P, args.kernel, args.steps, args.warmup, out, lse, ws,
-                                    args.deterministic, args.graph, args.cluster_merge)
+            ms, split = _time_steps(ta, torch, copies, 0 if merge == "auto" else P, args.kernel, args.steps,
+                                    args.warmup, out, lse, ws, args.deterministic, args.graph,
+                                    merge == "cluster")
             lines.append({"sweep": "context", "workload": w.name, "kv": "e4m3" if args.fp8 else "bf16",
-                          "cluster_merge": args.cluster_merge,
+                          "merge": merge,
                           "context": N, "num_splits": P,
                           "graph": args.graph, "l2": "fits" if w.kv_bytes(np.full(w.batch, N)) * len(copies)
                           < L2_BYTES else "exceeds",

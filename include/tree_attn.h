@@ -142,7 +142,9 @@ typedef enum {
                                     through the cluster's distributed shared memory instead
                                     of the last-arriving block reading them back from L2:
                                     a shorter step end for short contexts.  Tensor-core and
-                                    FP8 kernels; a heuristic split count is capped at 8 */
+                                    FP8 kernels; a heuristic split count is capped at 8.
+                                    Chosen without the flag for short rows when num_splits
+                                    <= 0 (see tree_attn_decode) */
 #define TA_FLAG_DIAG_MISHINT 4   /* diagnostic, for testing: the copy warps' length hint
                                     (used to start the first copies before the row length
                                     is read) is made wrong, so those copies are discarded
@@ -208,7 +210,14 @@ int tree_attn_pick_splits_paged(const ta_shape *shape, int page_size, const int3
  *  seqlens     device int32 [batch], each in [0, max_seqlen]
  *  out         device float32 [batch][num_q_heads][head_dim]
  *  lse         device float32 [batch][num_q_heads], or NULL to skip it
- *  num_splits  P >= 1, or <= 0 to use tree_attn_pick_splits(shape, NULL, 0)
+ *  num_splits  P >= 1, or <= 0 to use tree_attn_pick_splits(shape, NULL, 0).
+ *              With <= 0 the library also picks the merge: when P >= 2, the
+ *              kernel has the cluster merge (BF16 tensor-core kernel up to 16
+ *              columns, FP8 kernel), slices of min(P, 8) blocks would hold at
+ *              most 640 tokens (768 for FP8 caches) and every row's cluster
+ *              fits on the device at once, the row's min(P, 8) blocks merge as
+ *              with TA_FLAG_CLUSTER_MERGE (not with the diagnostic flags).  The
+ *              workspace for the heuristic's P is then more than enough.
  *  workspace   device, >= tree_attn_workspace_bytes(shape, P) bytes, 16-byte
  *              aligned; may be NULL when P == 1.  Contents on entry are
  *              ignored; calls sharing one workspace must be ordered on the GPU.

@@ -217,6 +217,13 @@ def tree_attn_check_shape(shape: TaShape) -> int:
     return int(load().tree_attn_check_shape(ctypes.byref(shape)))
 
 
+def _splits_arg(num_splits: int, P: int, kernel: str, cluster_merge: bool) -> int:
+    """The split count passed to the library once the workspace is sized for P:
+    0 when the caller left the choice to the library (it then picks the same P,
+    and for short rows may merge through a thread-block cluster), else P."""
+    return 0 if int(num_splits) <= 0 and kernel == "auto" and not cluster_merge else P
+
+
 def tree_attn_workspace_bytes(shape: TaShape, num_splits: int) -> int:
     return int(load().tree_attn_workspace_bytes(ctypes.byref(shape), int(num_splits)))
 
@@ -282,7 +289,10 @@ def tree_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
         lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=q.device)
     P = int(num_splits)
     if P <= 0:
-        P = tree_attn_pick_splits(shape)
+        pick_key = ("pick", q.device.index)  # the heuristic's count depends on the device's SMs
+        P = ws_sizes.get(pick_key)
+        if P is None:
+            P = ws_sizes[pick_key] = tree_attn_pick_splits(shape)
         if cluster_merge:
             P = min(P, TA_CLUSTER_MAX_SPLITS)  # one cluster per row
     nbytes = ws_sizes.get(P)
@@ -295,7 +305,8 @@ def tree_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
     if (kernel == "auto" and split_events is None and not deterministic and k_scale is None and not diag_stall
             and not diag_mishint and not cluster_merge):
         rc = lib.tree_attn_decode(shape_ref, _ptr(q), _ptr(k_cache), _ptr(v_cache),
-                                  _ptr(seqlens), _ptr(out), _ptr(lse), P, _ptr(workspace),
+                                  _ptr(seqlens), _ptr(out), _ptr(lse), _splits_arg(num_splits, P, kernel, False),
+                                  _ptr(workspace),
                                   ws_bytes, st)
     else:
         if split_events is not None:
@@ -307,7 +318,8 @@ def tree_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
         opts = _options(kernel, deterministic, k_scale, v_scale, split_events, diag_stall, diag_mishint,
                         cluster_merge)
         rc = lib.tree_attn_decode_ex(ctypes.byref(shape), _ptr(q), _ptr(k_cache), _ptr(v_cache),
-                                     _ptr(seqlens), _ptr(out), _ptr(lse), P, _ptr(workspace),
+                                     _ptr(seqlens), _ptr(out), _ptr(lse),
+                                     _splits_arg(num_splits, P, kernel, cluster_merge), _ptr(workspace),
                                      ws_bytes, ctypes.byref(opts), st)
     if rc != TA_OK:
         raise TreeAttnError(rc, "tree_attn_decode")
@@ -412,7 +424,8 @@ def tree_attn_decode_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torc
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     opts = _options(kernel, deterministic, k_scale, v_scale, cluster_merge=cluster_merge)
     rc = lib.tree_attn_decode_paged(ctypes.byref(shape), ctypes.byref(paged), _ptr(q), _ptr(k_pages),
-                                    _ptr(v_pages), _ptr(seqlens), _ptr(out), _ptr(lse), P,
+                                    _ptr(v_pages), _ptr(seqlens), _ptr(out), _ptr(lse),
+                                    _splits_arg(num_splits, P, kernel, cluster_merge),
                                     _ptr(workspace), ws_bytes, ctypes.byref(opts), _stream(stream))
     if rc != TA_OK:
         raise TreeAttnError(rc, "tree_attn_decode_paged")
@@ -474,7 +487,8 @@ def tree_attn_decode_multi(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
     opts = _options(kernel, deterministic, k_scale, v_scale, cluster_merge=cluster_merge)
     rc = lib.tree_attn_decode_multi(ctypes.byref(base), ctypes.byref(paged) if paged is not None else None,
                                     nq, int(bool(causal)), _ptr(q), _ptr(k_cache), _ptr(v_cache),
-                                    _ptr(seqlens), _ptr(out), _ptr(lse), P, _ptr(workspace), ws_bytes,
+                                    _ptr(seqlens), _ptr(out), _ptr(lse),
+                                    _splits_arg(num_splits, P, kernel, cluster_merge), _ptr(workspace), ws_bytes,
                                     ctypes.byref(opts), _stream(stream))
     if rc != TA_OK:
         raise TreeAttnError(rc, "tree_attn_decode_multi")

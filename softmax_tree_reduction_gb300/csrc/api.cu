@@ -8,6 +8,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <iterator>
 #include <memory>
 #include <mutex>
 #include <new>
@@ -72,6 +73,16 @@ constexpr int kMmaHeadsPage16 = 2;   // BF16 tensor-core kernel, token-major poo
 constexpr int kKnownFlags =
     TA_FLAG_DETERMINISTIC | TA_FLAG_DIAG_STALL | TA_FLAG_DIAG_MISHINT | TA_FLAG_CLUSTER_MERGE;
 constexpr int kClusterMaxSplits = 8;  // portable cluster size
+// With the split count left to the library, rows whose slices are at most this
+// many tokens merge through a thread-block cluster (TA_FLAG_CLUSTER_MERGE):
+// there the step is mostly its fixed start and end, and the cluster merge
+// drops the ticket and the last block's L2 round trips (about 3 us).  Measured
+// on GB300 with CUDA-graph replay: 9-14 % shorter steps on the 8B-shaped layer
+// (8 rows) at 1024-4096 tokens, 6-8 % on the 70B-shaped one (32 rows of 4
+// slices) at 1024-2048, 1 % at 640 tokens per slice (BF16), and slower from
+// 768 tokens per slice (BF16) or 1024 (FP8) on, where 16 slices beat 8.
+constexpr int kClusterAutoTokens = 640;
+constexpr int kClusterAutoTokensFp8 = 768;
 
 constexpr int kMaxDevices = 64;
 
@@ -82,6 +93,7 @@ struct DeviceState {
     unsigned* ring = nullptr;  // device address of g_sched_ring on this device
     unsigned cursor = 0;       // next free ring slot
     int device = 0;            // this entry's CUDA device
+    int cluster_cap[kClusterMaxSplits + 1];  // co-resident clusters per size; -1: not queried
 };
 
 std::mutex g_mu;
@@ -105,10 +117,18 @@ int device_state(DeviceState** out) {
         s.device = dev;
         s.err = static_cast<int*>(p);
         s.ring = static_cast<unsigned*>(r);
+        std::fill(std::begin(s.cluster_cap), std::end(s.cluster_cap), -1);
         s.ready = true;
     }
     *out = &s;
     return TA_OK;
+}
+
+// Clusters of `size` split-kernel blocks that fit on the device at once.
+int cluster_capacity(DeviceState* s, int size) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (s->cluster_cap[size] < 0) s->cluster_cap[size] = ta::mma_cluster_capacity(size);
+    return s->cluster_cap[size];
 }
 
 // Reserve `n` consecutive counter slots for one call (nullptr if n exceeds the ring).
@@ -385,6 +405,21 @@ int pick_splits_impl(const ta_shape* s, const int32_t* host_seqlens, int num_sms
                           heads_per_block(s, kernel, page_size, num_sms));
 }
 
+// Whether a call whose split count the library picked (P) merges each row
+// through a cluster of min(P, 8) blocks instead: short slices, a kernel with
+// the cluster merge, and every row's cluster resident in one wave.
+bool auto_cluster(DeviceState* ds, const ta_shape* s, int kernel, int P, int page_size,
+                  const ta_options* options) {
+    if (P < 2 || (kernel != TA_KERNEL_MMA && kernel != kKernelFp8)) return false;
+    if (options && (options->flags & (TA_FLAG_DIAG_STALL | TA_FLAG_DIAG_MISHINT))) return false;
+    const int pc = std::min(P, kClusterMaxSplits);
+    const int limit = s->kv_dtype == TA_E4M3 ? kClusterAutoTokensFp8 : kClusterAutoTokens;
+    if (ceil_div(s->max_seqlen, pc) > limit) return false;
+    const int64_t rows = static_cast<int64_t>(s->batch) *
+                         (s->num_kv_heads / heads_per_block(s, kernel, page_size, ds->num_sms));
+    return rows <= cluster_capacity(ds, pc);
+}
+
 // 4-D map over (channel, token, KV head, batch row) -- or, for a page pool,
 // (channel, token in page, KV head, physical page).  Box: box_x channels x
 // `rows` tokens.
@@ -525,7 +560,7 @@ int decode_impl(const ta_shape* shape, const ta_paged_kv* paged, int nq, int cau
         return TA_ERR_ALIGN;
     if (options && (options->flags & ~kKnownFlags) != 0) return TA_ERR_SHAPE;
     const bool deterministic = options && (options->flags & TA_FLAG_DETERMINISTIC);
-    const bool cluster = options && (options->flags & TA_FLAG_CLUSTER_MERGE);
+    bool cluster = options && (options->flags & TA_FLAG_CLUSTER_MERGE);
     const int kernel = resolve_kernel(shape, options ? options->kernel : TA_KERNEL_AUTO, cluster);
     if (kernel < 0) return kernel;
     if (cluster && kernel != TA_KERNEL_MMA && kernel != kKernelFp8) return TA_ERR_SHAPE;
@@ -554,6 +589,8 @@ int decode_impl(const ta_shape* shape, const ta_paged_kv* paged, int nq, int cau
     int P = num_splits;
     if (P <= 0) {
         P = pick_splits_impl(shape, nullptr, ds->num_sms, kernel, paged ? paged->page_size : 0);
+        if (!cluster && auto_cluster(ds, shape, kernel, P, paged ? paged->page_size : 0, options))
+            cluster = true;
         if (cluster) P = std::min(P, kClusterMaxSplits);
         if (P < 1 || P > TA_MAX_SPLITS) return TA_ERR_SPLITS;
         if ((rc = check_ws(P)) != TA_OK) return rc;

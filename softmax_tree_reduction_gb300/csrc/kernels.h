@@ -44,6 +44,10 @@ Geometry fp8_geometry(int heads_per_block);
 // Geometry (hb = p.hb KV heads per box).
 cudaError_t launch_split_mma(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv,
                              const SplitParams& p, cudaStream_t stream);
+// Clusters of `cluster_size` blocks of the BF16 tensor-core kernel that can be
+// resident at once on the current device (the GPCs bound it; the FP8 kernel's
+// blocks, also one per SM, fit the same way).  0 if the query fails.
+int mma_cluster_capacity(int cluster_size);
 cudaError_t launch_split_fma_bf16(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv,
                                   const SplitParams& p, cudaStream_t stream);
 cudaError_t launch_split_fma_f32(int head_dim, const CUtensorMap& tk, const CUtensorMap& tv,

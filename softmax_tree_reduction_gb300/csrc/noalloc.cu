@@ -49,6 +49,8 @@ extern "C" int tree_attn_decode_noalloc(const ta_shape* shape, const void* q, co
     if (need > TA_NOALLOC_SCRATCH_BYTES) return TA_ERR_SCRATCH_LIMIT;
     void* scratch = nullptr;
     if (P > 1 && (rc = scratch_address(&scratch)) != TA_OK) return rc;
-    return tree_attn_decode(shape, q, k_cache, v_cache, seqlens, out, lse, P, scratch,
+    // A split count left to the library stays 0: tree_attn_decode then picks the
+    // same P (and may merge short rows through a thread-block cluster).
+    return tree_attn_decode(shape, q, k_cache, v_cache, seqlens, out, lse, num_splits <= 0 ? 0 : P, scratch,
                             P > 1 ? static_cast<size_t>(TA_NOALLOC_SCRATCH_BYTES) : 0, stream);
 }

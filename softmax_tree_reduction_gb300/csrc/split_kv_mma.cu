@@ -542,6 +542,29 @@ cudaError_t launch_impl(const CUtensorMap& tk, const CUtensorMap& tv, const Spli
 
 }  // namespace
 
+int mma_cluster_capacity(int cluster_size) {
+    using C = MmaCfg<128, 1>;
+    static std::atomic<unsigned long long> configured{0};
+    if (set_smem_once(split_kv_mma_kernel<128, 1, 1, 1>, C::kSmem, configured) != cudaSuccess) return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cluster_size, 1, 1);
+    cfg.blockDim = dim3(C::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = static_cast<unsigned>(cluster_size);
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, split_kv_mma_kernel<128, 1, 1, 1>, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
 // Several KV heads per block only at head_dim 128 (small pages).
 Geometry mma_geometry(int head_dim, int heads_per_block) {
     const int hb = (head_dim == 128 && heads_per_block == 2) ? 2 : 1;
