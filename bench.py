@@ -84,6 +84,8 @@ def parse_args(argv=None):
                     help="run through the paged-KV entry point with this page size (pages shuffled in a pool)")
     ap.add_argument("--queries", type=int, default=1,
                     help="queries per sequence (causal over the last positions, as when verifying draft tokens)")
+    ap.add_argument("--paged-order", choices=["shuffled", "sequential"], default="shuffled",
+                    help="physical page order: a random permutation of the pool, or each row's pages in order")
     ap.add_argument("--paged-layout", choices=["NHD", "HND"], default="NHD",
                     help="page layout: [pages][page][heads][d] (NHD) or [pages][heads][page][d] (HND)")
     ap.add_argument("--graph", action="store_true",
@@ -312,7 +314,7 @@ def run_ours(args, rank, world, local):
     scales = dict(k_scale=dev.get("k_scale"), v_scale=dev.get("v_scale"), cluster_merge=args.cluster_merge)
     if args.paged:
         kp, vp, bt = workloads.page_pool(inp["k"], inp["v"], inp["seqlens"], args.paged, seed=w.seed,
-                                         layout=args.paged_layout)
+                                         layout=args.paged_layout, shuffle=args.paged_order == "shuffled")
         dev.update(k=kp.cuda(), v=vp.cuda(), block_table=bt.cuda())
         del kp, vp
     # two copies of the KV cache, alternated step to step (each far larger than L2)
@@ -505,7 +507,8 @@ def run_ours(args, rank, world, local):
                    "cluster_merge": args.cluster_merge,
                    "kv_dtype": "e4m3 (per-KV-head scales)" if args.fp8 else str(w.kv_dtype).replace("torch.", ""),
                    "queries_per_sequence": args.queries,
-                   "kv_layout": f"paged ({args.paged_layout}), {args.paged}-token pages shuffled in a pool"
+                   "kv_layout": f"paged ({args.paged_layout}), {args.paged}-token pages "
+                                f"{'shuffled in' if args.paged_order == 'shuffled' else 'in row order in'} a pool"
                    if args.paged
                    else "dense [B][Hkv][S][d]",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",

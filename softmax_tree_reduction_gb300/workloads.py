@@ -187,8 +187,10 @@ def seqlens_of(w: Workload, seed: Optional[int] = None):
                          dtype=torch.int64).numpy()
 
 
-def page_pool(k, v, seqlens, page_size, layout="NHD", extra_pages=3, seed=0):
-    """Scatter dense caches [B, Hkv, S, d] into shuffled page pools.
+def page_pool(k, v, seqlens, page_size, layout="NHD", extra_pages=3, seed=0, shuffle=True):
+    """Scatter dense caches [B, Hkv, S, d] into shuffled page pools (``shuffle``
+    False: each row's pages in order, one after another, as a fresh allocator
+    would hand them out).
 
     Returns (k_pool, v_pool, block_table): pools of shape [num_pages, page_size,
     Hkv, d] ("NHD") or [num_pages, Hkv, page_size, d] ("HND", returned as a
@@ -201,7 +203,7 @@ def page_pool(k, v, seqlens, page_size, layout="NHD", extra_pages=3, seed=0):
     max_pages = max(1, (S + page_size - 1) // page_size)
     num_pages = sum(pages) + extra_pages
     g = torch.Generator().manual_seed(seed)
-    perm = torch.randperm(num_pages, generator=g)
+    perm = torch.randperm(num_pages, generator=g) if shuffle else torch.arange(num_pages)
     shape = (num_pages, page_size, Hkv, d) if layout == "NHD" else (num_pages, Hkv, page_size, d)
     kp = torch.full(shape, float("nan"), dtype=k.dtype)
     vp = torch.full(shape, float("nan"), dtype=v.dtype)
