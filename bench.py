@@ -123,7 +123,7 @@ def load_peaks():
 
 def kernel_source_hash(kernel):
     name = {"mma": "split_kv_mma.cu", "fma": "split_kv_fma.cuh", "fp8": "split_kv_fp8.cu",
-            "tc05": "split_kv_tc05.cu"}[kernel]
+            "tc05": "split_kv_tc05.cu", "fp8tc05": "split_kv_tc05_fp8.cu"}[kernel]
     h = hashlib.sha256()
     for f in (name, "common.cuh", "emit.cuh", "sched.cuh", "warp_mma.cuh", "tc05.cuh", "api.cu"):
         with open(os.path.join(ROOT, "softmax_tree_reduction_gb300", "csrc", f), "rb") as fh:
@@ -335,7 +335,11 @@ def run_ours(args, rank, world, local):
         P = min(P, 8)  # one cluster per row: at most 8 blocks
     kernel_used = args.kernel
     if args.fp8:
-        kernel_used = "fp8"
+        # the library's choice for E4M3 caches: tcgen05 above 16 columns per KV
+        # head (not with the cluster merge), else the warp-level FP8 kernel
+        cols = w.group * args.queries
+        tc = args.kernel == "tc05" or (args.kernel == "auto" and cols > 16 and not args.cluster_merge)
+        kernel_used = "fp8tc05" if tc else "fp8"
     elif kernel_used == "auto":
         # the library's choice: warp-level tensor cores for BF16 with up to 16
         # columns per KV head; tcgen05 for 17..64 columns at head_dim 128 (the
@@ -516,7 +520,7 @@ def run_ours(args, rank, world, local):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
-                     "kernel": f"split_kv_{kernel_used}",
+                     "kernel": "split_kv_tc05_fp8" if kernel_used == "fp8tc05" else f"split_kv_{kernel_used}",
                      # time per launch over the timed region, steps back to back: a launch
                      # starts its L2 prefetch while the previous one merges, so launches overlap
                      "launch_us_back_to_back": round(split_ms_max * 1e3, 3),

@@ -112,16 +112,18 @@ typedef struct {
 /* Kernel family for the per-slice step. */
 typedef enum {
     TA_KERNEL_AUTO = 0,  /* tensor-core path when it applies, else FMA: TA_KERNEL_TC05 for
-                            BF16 q and kv at head_dim 128 with more than 16 columns (query
-                            heads x queries) per KV head, unless TA_FLAG_CLUSTER_MERGE is
-                            set; else TA_KERNEL_MMA where it applies */
+                            BF16 q at head_dim 128 with more than 16 columns (query heads x
+                            queries) per KV head, unless TA_FLAG_CLUSTER_MERGE is set; else
+                            TA_KERNEL_MMA where it applies */
     TA_KERNEL_FMA = 1,   /* FP32 FMA on CUDA cores; every dtype combination */
     TA_KERNEL_MMA = 2,   /* warp-level tensor-core mma: BF16 q and kv (Hq/Hkv <= 16, or <= 64
                             at head_dim 128), or BF16 q with an E4M3 cache (Hq/Hkv <= 16,
                             head_dim 128) */
     TA_KERNEL_TC05 = 3   /* fifth-generation tensor cores (tcgen05.mma, accumulators in
-                            tensor memory): BF16 q and kv, head_dim 128, Hq/Hkv <= 64 (x
-                            queries); not with TA_FLAG_CLUSTER_MERGE */
+                            tensor memory), BF16 q, head_dim 128: BF16 kv with Hq/Hkv <= 64
+                            (x queries), or an E4M3 cache with Hq/Hkv <= 32 (x queries;
+                            K used as E4M3 against q split into two E4M3 terms, V widened
+                            to FP16); not with TA_FLAG_CLUSTER_MERGE */
 } ta_kernel;
 
 /* Bits of ta_options.flags. */

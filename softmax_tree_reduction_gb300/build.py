@@ -28,7 +28,7 @@ LIB_DEBUG = os.path.join(HERE, "libtreeattn_debug.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 SOURCES = ["api.cu", "combine.cu", "split_kv_mma.cu", "split_kv_fma_bf16.cu", "split_kv_fma_f32.cu",
-           "noalloc.cu", "split_kv_fp8.cu", "split_kv_tc05.cu"]
+           "noalloc.cu", "split_kv_fp8.cu", "split_kv_tc05.cu", "split_kv_tc05_fp8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", "-I", CSRC, "-I", INCLUDE]

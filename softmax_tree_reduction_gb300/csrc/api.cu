@@ -159,11 +159,17 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int elem_bytes(int dtype) { return dtype == TA_BF16 ? 2 : (dtype == TA_E4M3 ? 1 : 4); }
 
-// Internal kernel family for FP8 caches (selected by TA_KERNEL_AUTO / TA_KERNEL_MMA).
+// Internal kernel families for FP8 caches: the warp-level tensor-core kernel
+// (TA_KERNEL_MMA) and the tcgen05 kernel (TA_KERNEL_TC05).
 constexpr int kKernelFp8 = 4;
+constexpr int kKernelTc05Fp8 = 5;
 static_assert(kKernelFp8 != TA_KERNEL_AUTO && kKernelFp8 != TA_KERNEL_FMA && kKernelFp8 != TA_KERNEL_MMA &&
-                  kKernelFp8 != TA_KERNEL_TC05,
+                  kKernelFp8 != TA_KERNEL_TC05 && kKernelTc05Fp8 > kKernelFp8,
               "internal kernel id");
+// FP8 caches with more than this many columns per KV head take the tcgen05
+// kernel by default (up to 16 the warp-level kernel is faster: 59.8 against
+// 66.2 us with 16 columns on the 131072-token 8B-shaped layer).
+constexpr int kFp8Tc05MinCols = 16;
 
 struct Strides {
     int64_t b, h, t;
@@ -222,10 +228,16 @@ int check_shape(const ta_shape* s, Strides* st, int page_size = 0) {
 int resolve_kernel(const ta_shape* s, int requested, bool cluster = false) {
     const int G = s->num_q_heads / s->num_kv_heads;
     if (s->kv_dtype == TA_E4M3) {
-        const bool ok = s->q_dtype == TA_BF16 && s->head_dim == 128 && G <= 16;
-        if (requested == TA_KERNEL_FMA || requested == TA_KERNEL_TC05) return TA_ERR_DTYPE;
-        if (requested != TA_KERNEL_AUTO && requested != TA_KERNEL_MMA) return TA_ERR_SHAPE;
-        return ok ? kKernelFp8 : static_cast<int>(TA_ERR_DTYPE);
+        if (s->q_dtype != TA_BF16 || s->head_dim != 128 || requested == TA_KERNEL_FMA) return TA_ERR_DTYPE;
+        const bool mma_ok = G <= 16, tc05_ok = G <= 32 && !cluster;
+        switch (requested) {
+            case TA_KERNEL_AUTO:
+                if (tc05_ok && G > kFp8Tc05MinCols) return kKernelTc05Fp8;
+                return mma_ok ? kKernelFp8 : static_cast<int>(TA_ERR_SHAPE);
+            case TA_KERNEL_MMA: return mma_ok ? kKernelFp8 : static_cast<int>(TA_ERR_SHAPE);
+            case TA_KERNEL_TC05: return tc05_ok ? kKernelTc05Fp8 : static_cast<int>(TA_ERR_SHAPE);
+            default: return TA_ERR_SHAPE;
+        }
     }
     const bool bf16 = s->q_dtype == TA_BF16 && s->kv_dtype == TA_BF16;
     const bool mma_ok = bf16 && (G <= 16 || (G <= 64 && s->head_dim == 128));
@@ -247,7 +259,8 @@ int resolve_kernel(const ta_shape* s, int requested, bool cluster = false) {
 
 Geometry geometry_hb(const ta_shape* s, int kernel, int hb) {
     if (kernel == kKernelFp8) return ta::fp8_geometry(hb);
-    if (kernel == TA_KERNEL_TC05) return ta::tc05_geometry(0);  // one KV head per block
+    if (kernel == kKernelTc05Fp8) return ta::tc05_fp8_geometry();  // one KV head per block
+    if (kernel == TA_KERNEL_TC05) return ta::tc05_geometry(0);    // one KV head per block
     return kernel == TA_KERNEL_MMA ? ta::mma_geometry(s->head_dim, hb)
                                    : ta::fma_geometry(elem_bytes(s->kv_dtype), s->head_dim);
 }
@@ -286,6 +299,7 @@ int heads_per_block(const ta_shape* s, int kernel, int page_size, int num_sms) {
 
 Geometry geometry_of(const ta_shape* s, int kernel, int page_size, int num_sms) {
     if (kernel == TA_KERNEL_TC05) return ta::tc05_geometry(page_size);
+    if (kernel == kKernelTc05Fp8) return ta::tc05_fp8_geometry();
     return geometry_hb(s, kernel, heads_per_block(s, kernel, page_size, num_sms));
 }
 
@@ -629,7 +643,7 @@ int decode_impl(const ta_shape* shape, const ta_paged_kv* paged, int nq, int cau
                                            : 1.0f / std::sqrt(static_cast<float>(shape->head_dim));
     p.scale_log2 = scale * ta::kLog2e;
     p.chunk_tiles = std::max(1, kChunkTokens / geo.tile_tokens);
-    p.prefetch_tiles = std::max(1, (kernel == kKernelFp8    ? kPrefetchTokensFp8
+    p.prefetch_tiles = std::max(1, (kernel == kKernelFp8 || kernel == kKernelTc05Fp8 ? kPrefetchTokensFp8
                                     : kernel == TA_KERNEL_TC05 ? kPrefetchTokensTc05
                                                                : kPrefetchTokens) /
                                        geo.tile_tokens);
@@ -687,6 +701,8 @@ int decode_impl(const ta_shape* shape, const ta_paged_kv* paged, int nq, int cau
         e = ta::launch_split_fp8(tk, tv, p, stream);
     else if (kernel == TA_KERNEL_TC05)
         e = ta::launch_split_tc05(tk, tv, p, stream);
+    else if (kernel == kKernelTc05Fp8)
+        e = ta::launch_split_tc05_fp8(tk, tv, p, stream);
     else if (kernel == TA_KERNEL_MMA)
         e = ta::launch_split_mma(shape->head_dim, tk, tv, p, stream);
     else if (shape->kv_dtype == TA_BF16)

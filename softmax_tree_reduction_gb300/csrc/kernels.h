@@ -57,6 +57,11 @@ cudaError_t launch_split_fma_f32(int head_dim, const CUtensorMap& tk, const CUte
 Geometry tc05_geometry(int page_size);
 cudaError_t launch_split_tc05(const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& p,
                               cudaStream_t stream);
+// FP8 (E4M3) caches on the tcgen05 tensor cores: head_dim 128, BF16 q, up to
+// 32 columns per KV head, one KV head per block.
+Geometry tc05_fp8_geometry();
+cudaError_t launch_split_tc05_fp8(const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& p,
+                                  cudaStream_t stream);
 // FP8 (E4M3) caches, head_dim 128, BF16 q, up to 16 columns per KV head.
 cudaError_t launch_split_fp8(const CUtensorMap& tk, const CUtensorMap& tv, const SplitParams& p,
                              cudaStream_t stream);

@@ -19,9 +19,11 @@
 //
 //  warp 0     copies: K and V tiles of 128 tokens, [half][128 tokens][128 B]
 //             (128-byte swizzle), HBM -> shared memory by TMA, 3-stage ring
-//  warp 1     allocates TMEM (two S^T buffers, O^T) and issues every MMA
-//             from one thread; each MMA group is committed to an mbarrier
-//  warps 2-9  softmax: 8 warps, one token of the stage and 16 (up to 32
+//  warp 1     allocates TMEM (two S^T buffers, O^T) and issues the O^T
+//             products from one thread
+//  warp 2     issues the S^T products from one thread; each MMA group is
+//             committed to an mbarrier
+//  warps 3-10 softmax: 8 warps, one token of the stage and 16 (up to 32
 //             columns in the group) or 32 of its columns per thread, so each
 //             scheduler interleaves two warps:
 //             exponentials against one reference maximum per column, shared
@@ -71,7 +73,8 @@ struct Tc05Cfg {
     static_assert(kSmem <= 227 * 1024, "shared memory per block");
     static_assert(kSmem > 114 * 1024, "one block per SM: the block's TMEM allocation never waits");
     static constexpr int kSoftmaxWarps = 4 * NCP / CPT;  // a thread takes CPT columns of one token
-    static constexpr int kThreads = 64 + 32 * kSoftmaxWarps;
+    static constexpr int kSoftmax0 = 3;                  // first softmax warp
+    static constexpr int kThreads = 32 * (kSoftmax0 + kSoftmaxWarps);
     static constexpr uint32_t kColS = NCP;              // S^T buffer x at columns x * NCP (x = 0, 1)
     static constexpr uint32_t kColO = 2 * NCP;          // O^T: [hi | lo], 2 NCP columns
     static constexpr uint32_t kTmemCols = 4 * NCP;      // 128 or 256
@@ -80,76 +83,9 @@ struct Tc05Cfg {
     static constexpr int kMergeBatch = 20;
 };
 
-// Bounded wait that also gives up when another role of the block has aborted.
-__device__ bool wait_or_abort(uint64_t* bar, unsigned parity, int* err, const volatile int* abort_flag) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = globaltimer();
-    while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (globaltimer() - t0 > kWaitLimitNs) {
-            atomicOr(err, kErrTimeout);
-            return false;
-        }
-    }
-}
-
-// Lane 0 waits, the warp follows (warp-uniform outcome).
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, unsigned parity, int* err, const volatile int* abort_flag) {
-    int ok = 1;
-    if ((threadIdx.x & 31) == 0) ok = wait_or_abort(bar, parity, err, abort_flag) ? 1 : 0;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    __syncwarp();
-    return ok != 0;
-}
-
-// Lane 0 waits until *count >= target (a counter published with release
-// semantics by another warp of the block), the warp follows.
-__device__ __forceinline__ bool warp_wait_count(int* count, int target, int* err, const volatile int* abort_flag) {
-    int ok = 1;
-    if ((threadIdx.x & 31) == 0 && ld_acquire_smem(count) < target) {
-        const unsigned long long t0 = globaltimer();
-        while (ld_acquire_smem(count) < target) {
-            if (*abort_flag || globaltimer() - t0 > kWaitLimitNs) {
-                if (!*abort_flag) atomicOr(err, kErrTimeout);
-                ok = 0;
-                break;
-            }
-        }
-    }
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    __syncwarp();
-    return ok != 0;
-}
-
-// OR of `pred` over the NT softmax threads (named barrier 1), which also
-// synchronises them.
-template <int NT>
-__device__ __forceinline__ bool softmax_any(bool pred) {
-    uint32_t out;
-    asm volatile(
-        "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\t"
-        "bar.red.or.pred po, 1, %2, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
-        : "=r"(out)
-        : "r"(pred ? 1u : 0u), "n"(NT)
-        : "memory");
-    return out != 0;
-}
-
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&h);
-}
-
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-    return v;
-}
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-    return v;
 }
 
 template <int NCP, int CPT>
@@ -187,7 +123,9 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP, CPT>::kThreads, 1)
     // when they must touch O^T, instead of waiting on a barrier phase that may
     // have moved on.
     int* o_count = reinterpret_cast<int*>(tmem_slot + 1);
-    static_assert(3 * kS * 8 + 16 + 8 + 11 * 8 + 32 + 8 <= C::kCtlBytes, "control block");
+    int* ev_total = o_count + 1;          // events of the block (-1 until known)
+    volatile int* ev_stage = ev_total + 1;  // [4] stage of each event whose O^T product is outstanding
+    static_assert(3 * kS * 8 + 16 + 8 + 11 * 8 + 32 + 8 + 4 + 16 <= C::kCtlBytes, "control block");
     float* m_ref = reinterpret_cast<float*>(smem + C::kRedOff);   // [64] reference maxima (log2 units)
     float* m_fin = m_ref + 64;                                     // [64] m_ref, 0 where it is -inf
     float* alpha_s = m_fin + 64;                                   // [64] scale of a moved reference
@@ -216,9 +154,10 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP, CPT>::kThreads, 1)
             mbar_init(&o_done[x], 1);
         }
         mbar_init(tmem_free, C::kSoftmaxWarps);
-        mbar_init(final_bar, 1);
+        mbar_init(final_bar, 2);  // both issuing threads' MMAs have completed
         mbar_init(q_full, C::kSoftmaxWarps);
         *o_count = 0;
+        *ev_total = -1;
         *abort_flag = 0;
         *bad_page = 0;
         fence_barrier_init();
@@ -290,25 +229,81 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP, CPT>::kThreads, 1)
         return;
     }
 
-    // ---------------------------------------------------------- MMA issuer
-    if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuers
+    // Lane 0 of warp 2 issues the S^T products, lane 0 of warp 1 the O^T
+    // products: one thread issuing both would keep either waiting while it
+    // issues the other.
+    if (warp == 2) {
         if (lane == 0) {
             bool ok = wait_or_abort(q_full, 0, p.err, abort_flag);
-            constexpr uint32_t id_s = idesc_bf16(128, NCP, 0, 0);      // S^T = K Q^T: both K-major
+            constexpr uint32_t id_s = idesc_bf16(128, NCP, 0, 0);  // S^T = K Q^T: both K-major
+            // Descriptors of the buffers' first bytes; an operand's descriptor is its
+            // buffer's plus the byte offset / 16 (start-address field; no carry, as
+            // every shared address is below 256 KB).
+            const uint64_t dq = smem_desc_sw128(smem_u32(qs), 16, 1024);
+            const uint64_t dk0 = smem_desc_sw128(smem_u32(stages), 16, 1024);
+            int j1 = 0;  // next event
+            for (int it = 0; ok; ++it) {
+                const int s = it % kS;
+                if (!wait_or_abort(&full[s], (it / kS) & 1, p.err, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const int nv = meta[s].nvalid;
+                if (nv == 0) {  // a discarded speculative stage
+                    mbar_arrive(&empty[s]);
+                    continue;
+                }
+                // S^T buffer j1 % 2 is free once the softmax warps have read event j1 - 2
+                const int x = j1 & 1;
+                if (j1 >= 2 && !wait_or_abort(&s_free[x], ((j1 >> 1) - 1) & 1, p.err, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (nv < 0) {  // the end-of-work event for the softmax warps, the count for the O^T issuer
+                    smeta[4 * x + 1] = -1;
+                    mbar_arrive(&s_full[x]);
+                    mbar_arrive(&s_full[x]);
+                    st_release_smem(ev_total, j1);
+                    break;
+                }
+                tc_fence_after();
+                smeta[4 * x + 0] = meta[s].tok0;
+                smeta[4 * x + 1] = nv;
+                smeta[4 * x + 2] = s;
+                ev_stage[j1 & 3] = s;  // read by the O^T issuer after P^T of event j1 is written
+                mbar_arrive(&s_full[x]);
+                const uint64_t dk = dk0 + static_cast<uint64_t>((s * C::kStageBytes) >> 4);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t koff = (kk >> 2) * (C::kTile * 128) + (kk & 3) * 32;
+                    const uint32_t qoff = (kk >> 2) * 8192 + (kk & 3) * 32;
+                    umma_f16(tmem + C::kColS * x, dk + (koff >> 4), dq + (qoff >> 4), id_s, kk > 0 ? 1u : 0u);
+                }
+                umma_commit(&s_full[x]);
+                ++j1;
+            }
+            if (!ok) atomicOr(abort_flag, 1);
+            umma_commit(final_bar);  // completes once its S^T products have
+        }
+        allow_dependents();
+        return;
+    }
+    if (warp == 1) {
+        if (lane == 0) {
+            bool ok = true;
             constexpr uint32_t id_o = idesc_bf16(128, 2 * NCP, 1, 1);  // O^T += V^T P^T: both MN-major
-            const uint32_t q_addr = smem_u32(qs), st_addr = smem_u32(stages);
-            int it = 0;          // copy stage sequence
-            int j1 = 0, j2 = 0;  // next event for S^T; next event for O^T
-            int o_seen = 0;      // events whose O^T completion was observed and published
-            int ev_stage[4];     // stage of each event whose O^T product is outstanding (<= kS)
-            bool end = false;
+            const uint64_t dst0 = smem_desc_sw128(smem_u32(stages), C::kTile * 128, 1024);
+            int j2 = 0;      // next event for O^T
+            int o_seen = 0;  // events whose O^T completion was observed and published
+            int n_ev = -1;   // the block's events, once the S^T issuer has seen the end of work
             unsigned long long idle_since = 0;
             // Every barrier is polled without blocking, so that whichever becomes
             // ready first is served.  No barrier can run two phases ahead of its
             // poll: o_done[x] because at most two O^T products are in flight,
             // p_full because the softmax warps arrive on P^T of event j only after
-            // event j - 2's O^T product has completed (o_count), s_full / s_free
-            // as the events alternate.
+            // event j - 2's O^T product has completed (o_count).  P^T of event j
+            // exists only after its S^T.
             while (ok) {
                 bool progress = false;
                 // publish completed O^T products, in order
@@ -317,62 +312,29 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP, CPT>::kThreads, 1)
                     st_release_smem(o_count, o_seen);
                     progress = true;
                 }
-                // S^T = K Q^T for the next stage once its copies landed and its buffer is free
-                if (!end && mbar_test_wait(&full[it % kS], (it / kS) & 1)) {
-                    const int s = it % kS;
-                    const int nv = meta[s].nvalid;
-                    if (nv < 0) {
-                        end = true;
-                        progress = true;
-                    } else if (nv == 0) {  // a discarded speculative stage
-                        mbar_arrive(&empty[s]);
-                        ++it;
-                        progress = true;
-                    } else if (j1 < 2 || mbar_test_wait(&s_free[j1 & 1], ((j1 >> 1) - 1) & 1)) {
-                        tc_fence_after();
-                        const int x = j1 & 1;
-                        smeta[4 * x + 0] = meta[s].tok0;
-                        smeta[4 * x + 1] = nv;
-                        smeta[4 * x + 2] = s;
-                        mbar_arrive(&s_full[x]);
-                        const uint32_t kb = st_addr + s * C::kStageBytes;
-#pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t koff = (kk >> 2) * (C::kTile * 128) + (kk & 3) * 32;
-                            const uint32_t qoff = (kk >> 2) * 8192 + (kk & 3) * 32;
-                            umma_bf16(tmem + C::kColS * x, smem_desc_sw128(kb + koff, 16, 1024),
-                                      smem_desc_sw128(q_addr + qoff, 16, 1024), id_s, kk > 0 ? 1u : 0u);
-                        }
-                        umma_commit(&s_full[x]);
-                        ev_stage[j1 & 3] = s;
-                        ++j1;
-                        ++it;
-                        progress = true;
-                    }
-                }
+                if (n_ev < 0) n_ev = ld_acquire_smem(ev_total);
                 // O^T += V^T P^T for the oldest event whose P^T is written (at most two in flight)
-                if (j2 < j1 && o_seen >= j2 - 1 && mbar_test_wait(&p_full[j2 & 1], (j2 >> 1) & 1)) {
+                if ((n_ev < 0 || j2 < n_ev) && o_seen >= j2 - 1 && mbar_test_wait(&p_full[j2 & 1], (j2 >> 1) & 1)) {
                     tc_fence_after();
                     const int s = ev_stage[j2 & 3];
-                    const uint32_t pb = st_addr + s * C::kStageBytes, vb = pb + C::kKBytes;
+                    const uint64_t pd = dst0 + static_cast<uint64_t>((s * C::kStageBytes) >> 4);
+                    const uint64_t vd = pd + (C::kKBytes >> 4);
 #pragma unroll
                     for (int kk = 0; kk < C::kTile / 16; ++kk) {
                         // 16 tokens: two groups of 8 rows; V's channel halves and
                         // P^T's 64-column blocks are 16 KB apart
-                        umma_bf16(tmem + C::kColO, smem_desc_sw128(vb + kk * 2048, C::kTile * 128, 1024),
-                                  smem_desc_sw128(pb + kk * 2048, C::kTile * 128, 1024), id_o,
-                                  (j2 > 0 || kk > 0) ? 1u : 0u);
+                        umma_f16(tmem + C::kColO, vd + 128 * kk, pd + 128 * kk, id_o, (j2 > 0 || kk > 0) ? 1u : 0u);
                     }
                     umma_commit(&empty[s]);
                     umma_commit(&o_done[j2 & 1]);
                     ++j2;
                     progress = true;
                 }
-                if (end && j2 == j1 && o_seen == j2) break;
+                if (n_ev >= 0 && j2 == n_ev && o_seen == j2) break;
                 if (progress) {
                     idle_since = 0;
                 } else {
-                    // leave the issue slots of this sub-partition to the softmax warp
+                    // leave the issue slots of this sub-partition to the softmax warps
                     __nanosleep(20);
                     if (*const_cast<volatile int*>(abort_flag)) {
                         ok = false;
@@ -382,16 +344,6 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP, CPT>::kThreads, 1)
                         atomicOr(p.err, kErrTimeout);
                         ok = false;
                     }
-                }
-            }
-            if (ok) {  // the end-of-work event for the softmax warps
-                const int x = j1 & 1;
-                if (j1 < 2 || wait_or_abort(&s_free[x], ((j1 >> 1) - 1) & 1, p.err, abort_flag)) {
-                    smeta[4 * x + 1] = -1;
-                    mbar_arrive(&s_full[x]);
-                    mbar_arrive(&s_full[x]);
-                } else {
-                    ok = false;
                 }
             }
             if (!ok) atomicOr(abort_flag, 1);
@@ -417,8 +369,8 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP, CPT>::kThreads, 1)
     constexpr int NS = NCP / CPT;     // column slices
     const int quarter = warp & 3;
     const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
-    const int ct = threadIdx.x - 64;  // 0 .. NT - 1
-    const int cs = (warp - 2) >> 2;   // column slice
+    const int ct = threadIdx.x - 32 * C::kSoftmax0;  // 0 .. NT - 1
+    const int cs = (warp - C::kSoftmax0) >> 2;       // column slice
     const int c_base = CPT * cs;
     const int t = 32 * quarter + lane;
     const int G = p.G;

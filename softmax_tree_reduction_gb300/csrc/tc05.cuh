@@ -1,7 +1,9 @@
 // Fifth-generation tensor-core building blocks (tcgen05): tensor-memory
 // allocation, loads and stores, shared-memory matrix descriptors, the
-// instruction descriptor of BF16 x BF16 -> FP32 products, the MMA itself and
-// its commit to an mbarrier.  sm_100-family only.
+// instruction descriptors of BF16, FP16 and E4M3 products with FP32
+// accumulators, the MMAs and their commit to an mbarrier, and the bounded
+// waits and barrier reductions the kernels' roles synchronise with.
+// sm_100-family only.
 #pragma once
 
 #include <stdint.h>
@@ -100,16 +102,39 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) 
         : "memory");
 }
 
-// N (16 or 32) consecutive columns of the warp's lanes, one lane per thread.
+// 8 consecutive 32-bit columns of one TMEM lane per thread (as tmem_ld32).
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr)
+                 : "memory");
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const float (&v)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+                 "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+                 "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+                 "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
+                 : "memory");
+}
+
+// N (8, 16 or 32) consecutive columns of the warp's lanes, one lane per thread.
 template <int N>
 __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[N]) {
-    static_assert(N == 16 || N == 32, "columns per load");
-    if constexpr (N == 16) tmem_ld16(taddr, v); else tmem_ld32(taddr, v);
+    static_assert(N == 8 || N == 16 || N == 32, "columns per load");
+    if constexpr (N == 8) tmem_ld8(taddr, v);
+    else if constexpr (N == 16) tmem_ld16(taddr, v);
+    else tmem_ld32(taddr, v);
 }
 template <int N>
 __device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const float (&v)[N]) {
-    static_assert(N == 16 || N == 32, "columns per store");
-    if constexpr (N == 16) tmem_st16(taddr, v); else tmem_st32(taddr, v);
+    static_assert(N == 8 || N == 16 || N == 32, "columns per store");
+    if constexpr (N == 8) tmem_st8(taddr, v);
+    else if constexpr (N == 16) tmem_st16(taddr, v);
+    else tmem_st32(taddr, v);
 }
 
 // Two half-warps on the same 16 lanes: thread i < 16 reads lane (lane base +
@@ -195,20 +220,43 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
            (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
-// Instruction descriptor: D FP32, A and B BF16, dense, M x N, each operand
-// K-major (0) or MN-major (1).
+// Instruction descriptor: D FP32, dense, M x N, each operand K-major (0) or
+// MN-major (1), A and B of format code `fmt`: under kind::f16, 0 = FP16 and
+// 1 = BF16; under kind::f8f6f4, 0 = E4M3.
+__host__ __device__ constexpr uint32_t idesc_fmt(int fmt, int M, int N, int a_mn, int b_mn) {
+    return (1u << 4) | (static_cast<uint32_t>(fmt) << 7) | (static_cast<uint32_t>(fmt) << 10) |
+           (static_cast<uint32_t>(a_mn) << 15) | (static_cast<uint32_t>(b_mn) << 16) |
+           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
-           (static_cast<uint32_t>(b_mn) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
-           (static_cast<uint32_t>(M >> 4) << 24);
+    return idesc_fmt(1, M, N, a_mn, b_mn);
+}
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int a_mn, int b_mn) {
+    return idesc_fmt(0, M, N, a_mn, b_mn);
+}
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N, int a_mn, int b_mn) {
+    return idesc_fmt(0, M, N, a_mn, b_mn);
 }
 
-// D (TMEM) = A (smem) x B (smem) [+ D when `accumulate`], issued by one thread.
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                          uint32_t accumulate) {
+// D (TMEM) = A (smem) x B (smem) [+ D when `accumulate`], issued by one
+// thread: 16-bit operands (kind::f16, FP16 or BF16 per the descriptor), K
+// steps of 16 elements.
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// The same with 8-bit operands (kind::f8f6f4, E4M3 per the descriptor), K
+// steps of 32 elements.
+__device__ __forceinline__ void umma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
@@ -218,6 +266,74 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))
                  : "memory");
+}
+
+// ------------------------------------------------ role synchronisation
+// Bounded wait that also gives up when another role of the block has aborted.
+__device__ inline bool wait_or_abort(uint64_t* bar, unsigned parity, int* err, const volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > kWaitLimitNs) {
+            atomicOr(err, kErrTimeout);
+            return false;
+        }
+    }
+}
+
+// Lane 0 waits, the warp follows (warp-uniform outcome).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, unsigned parity, int* err, const volatile int* abort_flag) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = wait_or_abort(bar, parity, err, abort_flag) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    return ok != 0;
+}
+
+// Lane 0 waits until *count >= target (a counter published with release
+// semantics by another warp of the block), the warp follows.
+__device__ __forceinline__ bool warp_wait_count(int* count, int target, int* err, const volatile int* abort_flag) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0 && ld_acquire_smem(count) < target) {
+        const unsigned long long t0 = globaltimer();
+        while (ld_acquire_smem(count) < target) {
+            if (*abort_flag || globaltimer() - t0 > kWaitLimitNs) {
+                if (!*abort_flag) atomicOr(err, kErrTimeout);
+                ok = 0;
+                break;
+            }
+        }
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    return ok != 0;
+}
+
+// OR of `pred` over the NT softmax threads (named barrier 1), which also
+// synchronises them.
+template <int NT>
+__device__ __forceinline__ bool softmax_any(bool pred) {
+    uint32_t out;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.or.pred po, 1, %2, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(out)
+        : "r"(pred ? 1u : 0u), "n"(NT)
+        : "memory");
+    return out != 0;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
 }
 
 }  // namespace ta

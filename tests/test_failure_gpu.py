@@ -29,15 +29,19 @@ def _inputs(kv, d, fp8=False):
     return inp
 
 
-@pytest.mark.parametrize("family", ["mma", "fma", "fp8"])
+def _kernel(family):
+    return {"fp8": "mma", "fp8tc05": "tc05"}.get(family, family)
+
+
+@pytest.mark.parametrize("family", ["mma", "fma", "fp8", "fp8tc05"])
 @pytest.mark.parametrize("P", [1, 5])
 def test_stalled_waits_report_timeout_and_leave_the_device_usable(family, P):
-    fp8 = family == "fp8"
+    fp8 = family.startswith("fp8")
     kv = torch.float32 if family == "fma" else torch.bfloat16
     inp = _inputs(kv, 128 if family != "fma" else 64, fp8=fp8)
     q, k, v, sl = (inp[x].cuda() for x in ("q", "k", "v", "seqlens"))
     kw = dict(k_scale=inp["ks"].cuda(), v_scale=inp["vs"].cuda()) if fp8 else {}
-    kern = "auto" if fp8 else family
+    kern = _kernel(family)
     assert ta.tree_attn_get_device_error() == 0
     out, lse = ta.tree_attn_decode(q, k, v, sl, num_splits=P, kernel=kern, diag_stall=True, **kw)
     assert ta.tree_attn_get_device_error() == ta.TA_ERR_DEVICE_TIMEOUT
@@ -56,15 +60,15 @@ def test_stalled_waits_report_timeout_and_leave_the_device_usable(family, P):
     assert np.max(np.abs(lse.double().cpu().numpy() - ref_l)) <= max(tol, 1e-3)
 
 
-@pytest.mark.parametrize("family", ["mma", "fma", "fp8"])
+@pytest.mark.parametrize("family", ["mma", "fma", "fp8", "fp8tc05"])
 @pytest.mark.parametrize("P", [1, 5, 19])
 def test_wrong_length_hint_changes_nothing(family, P):
-    fp8 = family == "fp8"
+    fp8 = family.startswith("fp8")
     kv = torch.float32 if family == "fma" else torch.bfloat16
     inp = _inputs(kv, 128 if family != "fma" else 64, fp8=fp8)
     q, k, v, sl = (inp[x].cuda() for x in ("q", "k", "v", "seqlens"))
     kw = dict(k_scale=inp["ks"].cuda(), v_scale=inp["vs"].cuda()) if fp8 else {}
-    kern = "auto" if fp8 else family
+    kern = _kernel(family)
     o1, l1 = ta.tree_attn_decode(q, k, v, sl, num_splits=P, kernel=kern, deterministic=True, **kw)
     o2, l2 = ta.tree_attn_decode(q, k, v, sl, num_splits=P, kernel=kern, deterministic=True, diag_mishint=True, **kw)
     o3, l3 = ta.tree_attn_decode(q, k, v, sl, num_splits=P, kernel=kern, diag_mishint=True, **kw)

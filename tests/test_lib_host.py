@@ -73,6 +73,8 @@ def shape(ta, **kw):
     (dict(kv_dtype=2, q_dtype=0), -4),                # FP8 needs BF16 q
     (dict(kv_dtype=2, head_dim=64), -4),              # FP8 path is d = 128
     (dict(kv_dtype=2, num_q_heads=128), 0),           # FP8 path: G = 16 (two n-tiles)
+    (dict(kv_dtype=2, num_q_heads=256), 0),           # FP8 on tcgen05: G = 32
+    (dict(kv_dtype=2, num_q_heads=512), -3),          # FP8: G = 64 unsupported
     (dict(scale=-1.0), -3),
     (dict(scale=float("nan")), -3),
     (dict(kv_stride_b=131072 * 8 * 128, kv_stride_h=128, kv_stride_t=8 * 128), 0),  # token-major
@@ -332,16 +334,21 @@ def test_binding_constants_match_the_header(ta):
 
 
 def test_tc05_kernel_choice_and_limits(ta):
-    """The tcgen05 kernel takes BF16 q and cache at head_dim 128 with up to 64
-    columns per KV head; it is the automatic choice above 16 columns, and
-    refused (before any CUDA call) for other dtypes, head_dim 64, an E4M3
-    cache, or together with the cluster merge."""
+    """The tcgen05 kernels take BF16 q at head_dim 128 with up to 64 columns per
+    KV head over a BF16 cache and up to 32 over an E4M3 cache (the automatic
+    choice above 16 columns for both); they are refused
+    (before any CUDA call) for other dtypes, head_dim 64, more columns, or
+    together with the cluster merge."""
     wide = shape(ta, num_q_heads=256, num_kv_heads=8)       # 32 columns per KV head
     assert ta.tree_attn_launch_count(wide, 19, kernel="tc05") == 1
     assert ta.tree_attn_launch_count(wide, 64, kernel="tc05") == 2
     assert ta.tree_attn_launch_count(shape(ta), 19, kernel="tc05") == 1   # 4 columns, asked for
+    fp8 = shape(ta, kv_dtype=ta.TA_E4M3)
+    assert ta.tree_attn_launch_count(fp8, 19, kernel="tc05") == 1
+    assert ta.tree_attn_launch_count(shape(ta, kv_dtype=ta.TA_E4M3, num_q_heads=256), 19) == 1   # 32 columns
     for bad, code in ((shape(ta, q_dtype=ta.TA_F32), -4), (shape(ta, head_dim=64), -3),
-                      (shape(ta, kv_dtype=ta.TA_E4M3), -4)):
+                      (shape(ta, kv_dtype=ta.TA_E4M3, q_dtype=ta.TA_F32), -4),
+                      (shape(ta, kv_dtype=ta.TA_E4M3, num_q_heads=512), -3)):
         with pytest.raises(ta.TreeAttnError) as ei:
             ta.tree_attn_launch_count(bad, 8, kernel="tc05")
         assert ei.value.status == code
