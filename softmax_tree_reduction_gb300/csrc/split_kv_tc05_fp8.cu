@@ -24,23 +24,22 @@
 // shared memory and P is FP16, scaled by 2^6 and split into hi + lo parts.
 //
 //  warp 0       copies: K and V tiles of 128 tokens x 128 B (E4M3, 128-byte
-//               swizzle), HBM -> shared memory by TMA, 3-stage ring
+//               swizzle), HBM -> shared memory by TMA, 5-stage ring
 //  warp 1       allocates TMEM (two S^T buffers, O^T accumulators) and issues
-//               the O^T products from one thread
-//  warps 2-5    issue the S^T products (one thread of warp 2) and widen V:
-//               one token row each, E4M3 -> FP16 into one of two
-//               [half][128 tokens][128 B] buffers; a ring stage is released
-//               once its S^T product is done and its V rows are in the
-//               widening threads' registers, so the ring stays in flight
-//               while the products and softmax run
-//  warps 6-     softmax: one token of the stage and CPT columns per thread,
+//               the O^T products from one thread; each releases its stage
+//  warp 2       issues the S^T products from one thread
+//  warps 3-6    widen V in place: one token row each, E4M3 -> FP16, written
+//               over the stage once its S^T product is done -- channel half
+//               0 over the K tile (no longer needed), half 1 over the
+//               thread's own V row (already in its registers)
+//  warps 7-     softmax: one token of the stage and CPT columns per thread,
 //               with lazily moved per-column reference maxima as in the BF16
 //               tcgen05 kernel; P^T goes into one of three 16 KB buffers
 //
 // Operands in shared memory (128-byte swizzle, 1024-byte atoms of 8 rows):
 //   K8   [128 tokens][128 B]          A of S^T, K-major (as TMA left it)
 //   Q8   [2 terms][NC rows][128 B]    B of S^T, K-major
-//   V16  [half][128 tokens][128 B]    A of O^T, MN-major
+//   V16  [half][128 tokens][128 B]    A of O^T, MN-major (the whole stage)
 //   P^T  [128 tokens][128 B]          B of O^T, MN-major: N = 64 columns,
 //                                     hi at [0, NC), lo at [NC, 2 NC)
 #include <cuda_bf16.h>
@@ -60,14 +59,12 @@ struct Tc05F8Cfg {
     static_assert(CPT == 8 || CPT == 16, "columns per softmax thread");
     static constexpr int D = 128;
     static constexpr int kTile = 128;                   // tokens per stage
-    static constexpr int kStages = 3;
+    static constexpr int kStages = 5;
     static constexpr int kK8Bytes = kTile * 128;        // K (or V) of a stage: [128 tokens][128 B]
     static constexpr int kStageBytes = 2 * kK8Bytes;
-    static constexpr int kV16Bytes = 2 * kTile * 128;   // [half][128 tokens][128 B]
     static constexpr int kPBytes = kTile * 128;         // [128 tokens][64 FP16 columns]
     static constexpr int kPBufs = 3;
-    static constexpr int kV16Off = kStages * kStageBytes;
-    static constexpr int kPOff = kV16Off + 2 * kV16Bytes;
+    static constexpr int kPOff = kStages * kStageBytes;
     static constexpr int kQOff = kPOff + kPBufs * kPBytes;
     static constexpr int kQBytes = 2 * NCP * 128;       // [2 terms][NCP rows][128 B]
     static constexpr int kCtlOff = kQOff + kQBytes;
@@ -79,8 +76,9 @@ struct Tc05F8Cfg {
     static_assert(kSmem <= 227 * 1024, "shared memory per block");
     static_assert(kSmem > 114 * 1024, "one block per SM: the block's TMEM allocation never waits");
     static constexpr int kWidenWarps = 4;
+    static constexpr int kWiden0 = 3;                   // first widening warp
     static constexpr int kSoftmaxWarps = 4 * NCP / CPT;
-    static constexpr int kSoftmax0 = 2 + kWidenWarps;   // first softmax warp
+    static constexpr int kSoftmax0 = kWiden0 + kWidenWarps;  // first softmax warp
     static constexpr int kThreads = 32 * (kSoftmax0 + kSoftmaxWarps);
     static constexpr uint32_t kColS = 2 * NCP;          // S^T buffer x at columns x * 2 NCP: [term 1 | term 2]
     // O^T in kOAcc accumulators of 64 columns ([hi | lo] in the first 2 NCP),
@@ -130,32 +128,36 @@ __global__ void __launch_bounds__(Tc05F8Cfg<NCP, CPT>::kThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* stages = smem;
-    uint8_t* v16 = smem + C::kV16Off;
     uint8_t* pbuf = smem + C::kPOff;
     uint8_t* qs = smem + C::kQOff;
     uint8_t* ctl = smem + C::kCtlOff;
     uint64_t* full = reinterpret_cast<uint64_t*>(ctl);             // [kS] copies landed
-    uint64_t* empty = full + kS;                                    // [kS] S^T done and V widened
+    uint64_t* empty = full + kS;                                    // [kS] the stage's O^T product done
     volatile StageMeta* meta = reinterpret_cast<volatile StageMeta*>(empty + kS);
     int* abort_flag = const_cast<int*>(reinterpret_cast<volatile int*>(meta + kS));
     int* last_flag = abort_flag + 1;
     volatile unsigned* claim_sink = reinterpret_cast<volatile unsigned*>(abort_flag + 2);
     volatile int* bad_page = reinterpret_cast<volatile int*>(abort_flag + 3);
     uint64_t* prod_done = reinterpret_cast<uint64_t*>(abort_flag + 4);  // the copy warp's last claim is made
-    uint64_t* s_full = prod_done + 1;                               // [2] S^T of an event computed
+    uint64_t* k_done = prod_done + 1;                               // [kS] the stage's S^T product done
+    uint64_t* v_full = k_done + kS;                                 // [kS] the stage's V widened in place
+    uint64_t* s_full = v_full + kS;                                 // [2] S^T of an event computed
     uint64_t* s_free = s_full + 2;                                  // [2] S^T read by the softmax warps
     uint64_t* p_full = s_full + 4;                                  // [3] P^T of an event written
     uint64_t* o_done = s_full + 7;                                  // [2] O^T += ... of an event done
-    uint64_t* v_full = s_full + 9;                                  // [2] V16 of an event widened
-    uint64_t* v_free = s_full + 11;                                 // [2] V16 buffer read by its product
-    uint64_t* tmem_free = s_full + 13;                              // softmax warps are done with TMEM
-    uint64_t* final_bar = s_full + 14;                              // every MMA has completed
-    uint64_t* q_full = s_full + 15;                                 // Q8 is in shared memory
-    volatile int* smeta = reinterpret_cast<volatile int*>(s_full + 16);  // [2][4]: tok0, nvalid
+    uint64_t* tmem_free = s_full + 9;                               // softmax warps are done with TMEM
+    uint64_t* final_bar = s_full + 10;                              // every MMA has completed
+    uint64_t* q_full = s_full + 11;                                 // Q8 is in shared memory
+    volatile int* smeta = reinterpret_cast<volatile int*>(s_full + 12);  // [2][4]: tok0, nvalid
     uint32_t* tmem_slot = const_cast<uint32_t*>(reinterpret_cast<volatile uint32_t*>(smeta + 8));
     int* o_count = reinterpret_cast<int*>(tmem_slot + 1);           // O^T products completed (O^T issuer)
     int* ev_total = o_count + 1;                                    // events of the block (-1 until known)
-    static_assert(3 * kS * 8 + 16 + 8 + 16 * 8 + 32 + 8 <= C::kCtlBytes, "control block");
+    // [8] each event's stage and the parity of that stage's use, until its O^T
+    // product is issued (at most kS events are outstanding: a stage is reused
+    // only after its product)
+    volatile int* ev_stage = ev_total + 1;
+    volatile int* ev_par = ev_stage + 8;
+    static_assert(3 * kS * 8 + 16 + 8 + 2 * kS * 8 + 12 * 8 + 32 + 12 + 64 <= C::kCtlBytes, "control block");
     float* m_ref = reinterpret_cast<float*>(smem + C::kRedOff);    // [64] reference maxima (log2 units)
     float* m_fin = m_ref + 64;                                      // [64] m_ref, 0 where it is -inf
     float* alpha_s = m_fin + 64;                                    // [64] scale of a moved reference
@@ -171,15 +173,15 @@ __global__ void __launch_bounds__(Tc05F8Cfg<NCP, CPT>::kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kS; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1 + C::kWidenWarps);
+            mbar_init(&empty[s], 1);
+            mbar_init(&k_done[s], 1);
+            mbar_init(&v_full[s], C::kWidenWarps);
         }
         mbar_init(prod_done, 1);
         for (int x = 0; x < 2; ++x) {
             mbar_init(&s_full[x], 2);  // the issuer's release of the event, and the MMA commit
             mbar_init(&s_free[x], C::kSoftmaxWarps);
             mbar_init(&o_done[x], 1);
-            mbar_init(&v_full[x], C::kWidenWarps);
-            mbar_init(&v_free[x], 1);
         }
         for (int x = 0; x < C::kPBufs; ++x) mbar_init(&p_full[x], C::kSoftmaxWarps);
         mbar_init(tmem_free, C::kSoftmaxWarps);
@@ -252,18 +254,69 @@ __global__ void __launch_bounds__(Tc05F8Cfg<NCP, CPT>::kThreads, 1)
         return;
     }
 
-    // ---------------------------------------------------------- O^T issuer
-    // The S^T products are issued by the first widening warp (below), the O^T
-    // products by lane 0 of warp 1, so that neither product waits for the
-    // other's issue.
+    // ---------------------------------------------------------- MMA issuers
+    // Lane 0 of warp 2 issues the S^T products, lane 0 of warp 1 the O^T
+    // products: one thread issuing both would keep either waiting while it
+    // issues the other.  Descriptors are those of the buffers' first bytes plus
+    // the byte offset / 16 (start-address field; no carry, as every shared
+    // address is below 256 KB).
+    if (warp == 2) {
+        if (lane == 0) {
+            bool ok = wait_or_abort(q_full, 0, p.err, abort_flag);
+            constexpr uint32_t id_s = idesc_e4m3(128, 2 * NCP, 0, 0);  // S^T = K8 Q8^T: both K-major
+            const uint64_t dq = smem_desc_sw128(smem_u32(qs), 16, 1024);
+            const uint64_t dk0 = smem_desc_sw128(smem_u32(stages), 16, 1024);
+            int j1 = 0;  // next event
+            for (int it = 0; ok; ++it) {
+                const int s = it % kS;
+                if (!wait_or_abort(&full[s], (it / kS) & 1, p.err, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const int nv = meta[s].nvalid;
+                if (nv == 0) {  // a discarded speculative stage: its barriers still move one phase
+                    mbar_arrive(&k_done[s]);
+                    mbar_arrive(&empty[s]);
+                    continue;
+                }
+                // S^T buffer j1 % 2 is free once the softmax warps have read event j1 - 2
+                const int x = j1 & 1;
+                if (j1 >= 2 && !wait_or_abort(&s_free[x], ((j1 >> 1) - 1) & 1, p.err, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (nv < 0) {  // the count for the O^T issuer, the end-of-work event for the softmax warps
+                    st_release_smem(ev_total, j1);
+                    smeta[4 * x + 1] = -1;
+                    mbar_arrive(&s_full[x]);
+                    mbar_arrive(&s_full[x]);
+                    break;
+                }
+                tc_fence_after();
+                smeta[4 * x + 0] = meta[s].tok0;
+                smeta[4 * x + 1] = nv;
+                ev_stage[j1 & 7] = s;  // read by the O^T issuer once P^T of event j1 is written
+                ev_par[j1 & 7] = (it / kS) & 1;
+                mbar_arrive(&s_full[x]);
+                const uint64_t dk = dk0 + static_cast<uint64_t>((s * C::kStageBytes) >> 4);
+#pragma unroll
+                for (int kk = 0; kk < D / 32; ++kk)  // 32 channels (32 B) per K step
+                    umma_e4m3(tmem + C::kColS * x, dk + 2 * kk, dq + 2 * kk, id_s, kk > 0 ? 1u : 0u);
+                umma_commit(&s_full[x]);
+                umma_commit(&k_done[s]);
+                ++j1;
+            }
+            if (!ok) atomicOr(abort_flag, 1);
+            umma_commit(final_bar);  // completes once its S^T products have
+        }
+        allow_dependents();
+        return;
+    }
     if (warp == 1) {
         if (lane == 0) {
             bool ok = true;
             constexpr uint32_t id_o = idesc_f16(128, 64, 1, 1);  // O^T += V16^T P^T: both MN-major
-            // Descriptors of the buffers' first bytes; an operand's descriptor is its
-            // buffer's plus the byte offset / 16 (start-address field; no carry, as
-            // every shared address is below 256 KB).
-            const uint64_t dv0 = smem_desc_sw128(smem_u32(v16), C::kTile * 128, 1024);
+            const uint64_t dst0 = smem_desc_sw128(smem_u32(stages), C::kTile * 128, 1024);
             const uint64_t dp0 = smem_desc_sw128(smem_u32(pbuf), C::kTile * 128, 1024);
             int j2 = 0;      // next event for O^T
             int o_seen = 0;  // events whose O^T completion was observed and published
@@ -272,9 +325,9 @@ __global__ void __launch_bounds__(Tc05F8Cfg<NCP, CPT>::kThreads, 1)
             // Every barrier is polled without blocking.  None can run two phases
             // ahead of its poll: o_done[x] because at most two O^T products are in
             // flight; p_full because the softmax warps write P^T of event j only
-            // after event j - 3's product has completed (o_count); v_full because
-            // the widening warps wait for v_free of event j - 2 (whose product
-            // consumed v_full first).  P^T of event j exists only after its S^T.
+            // after event j - 3's product has completed (o_count); v_full[s]
+            // because a stage is refilled only after its product.  P^T of event j
+            // exists only after its S^T (which recorded the event's stage).
             while (ok) {
                 bool progress = false;
                 // publish completed O^T products, in order
@@ -286,23 +339,26 @@ __global__ void __launch_bounds__(Tc05F8Cfg<NCP, CPT>::kThreads, 1)
                 if (n_ev < 0) n_ev = ld_acquire_smem(ev_total);
                 // O^T += V16^T P^T for the oldest event whose P^T and V16 are ready (at most two in flight)
                 if ((n_ev < 0 || j2 < n_ev) && o_seen >= j2 - 1 &&
-                    mbar_test_wait(&p_full[j2 % C::kPBufs], (j2 / C::kPBufs) & 1) &&
-                    mbar_test_wait(&v_full[j2 & 1], (j2 >> 1) & 1)) {
-                    tc_fence_after();
-                    const uint64_t dp = dp0 + static_cast<uint64_t>(((j2 % C::kPBufs) * C::kPBytes) >> 4);
-                    const uint64_t dv = dv0 + static_cast<uint64_t>(((j2 & 1) * C::kV16Bytes) >> 4);
+                    mbar_test_wait(&p_full[j2 % C::kPBufs], (j2 / C::kPBufs) & 1)) {
+                    const int s = ev_stage[j2 & 7];
+                    if (mbar_test_wait(&v_full[s], static_cast<unsigned>(ev_par[j2 & 7]))) {
+                        tc_fence_after();
+                        const uint64_t dp = dp0 + static_cast<uint64_t>(((j2 % C::kPBufs) * C::kPBytes) >> 4);
+                        const uint64_t dv = dst0 + static_cast<uint64_t>((s * C::kStageBytes) >> 4);
 #pragma unroll
-                    for (int i = 0; i < C::kTile / 16; ++i) {
-                        // 16 tokens: two groups of 8 rows; V16's channel halves are 16 KB
-                        // apart.  The two token halves alternate between two accumulators.
-                        const int h = i & 1, kk = 4 * h + (i >> 1);
-                        const uint32_t acc = C::kColO + 64 * (2 * (j2 & 1) + h);
-                        umma_f16(tmem + acc, dv + 128 * kk, dp + 128 * kk, id_o, (j2 >= 2 || (kk & 3) > 0) ? 1u : 0u);
+                        for (int i = 0; i < C::kTile / 16; ++i) {
+                            // 16 tokens: two groups of 8 rows; V16's channel halves are 16 KB
+                            // apart.  The two token halves alternate between two accumulators.
+                            const int h = i & 1, kk = 4 * h + (i >> 1);
+                            const uint32_t acc = C::kColO + 64 * (2 * (j2 & 1) + h);
+                            umma_f16(tmem + acc, dv + 128 * kk, dp + 128 * kk, id_o,
+                                     (j2 >= 2 || (kk & 3) > 0) ? 1u : 0u);
+                        }
+                        umma_commit(&empty[s]);
+                        umma_commit(&o_done[j2 & 1]);
+                        ++j2;
+                        progress = true;
                     }
-                    umma_commit(&v_free[j2 & 1]);
-                    umma_commit(&o_done[j2 & 1]);
-                    ++j2;
-                    progress = true;
                 }
                 if (n_ev >= 0 && j2 == n_ev && o_seen == j2) break;
                 if (progress) {
@@ -333,87 +389,43 @@ __global__ void __launch_bounds__(Tc05F8Cfg<NCP, CPT>::kThreads, 1)
     }
 
     // ---------------------------------------------------------- widening
-    // Thread tw widens token row tw of each stage's V: 16-byte chunk c of the
-    // E4M3 row (channels 16c .. 16c + 15) becomes chunks 2 (c % 4) and
-    // 2 (c % 4) + 1 of channel half c / 4 in FP16.  The row is first copied
-    // to registers, so the ring stage is released (with the S^T product's
-    // commit) before the wait for a free V16 buffer.  Rows past the stage's
-    // valid tokens may hold anything (even NaN) and are written as zeros.
+    // Thread tw widens token row tw of each stage's V in place: 16-byte chunk c
+    // of the E4M3 row (channels 16c .. 16c + 15) becomes chunks 2 (c % 4) and
+    // 2 (c % 4) + 1 of channel half c / 4 in FP16; half 0 goes over the K tile
+    // (free once the stage's S^T product is done), half 1 over the thread's own
+    // E4M3 row, read beforehand.  Rows past the stage's valid tokens may hold
+    // anything (even NaN) and are written as zeros.
     if (warp < C::kSoftmax0) {
-        const int tw = threadIdx.x - 64;  // 0 .. 127
+        const int tw = threadIdx.x - 32 * C::kWiden0;  // 0 .. 127
         const uint32_t sw = static_cast<uint32_t>(tw & 7);
-        const bool s_issuer = warp == 2 && lane == 0;
-        constexpr uint32_t id_s = idesc_e4m3(128, 2 * NCP, 0, 0);  // S^T = K8 Q8^T: both K-major
-        const uint64_t dq = smem_desc_sw128(smem_u32(qs), 16, 1024);
-        const uint64_t dk0 = smem_desc_sw128(smem_u32(stages), 16, 1024);
-        int j1 = 0;  // next event for S^T (the issuing thread's count)
-        // The issuing thread's share of stage s (nv valid tokens, nv < 0: end of
-        // work): S^T = K8 Q8^T into buffer j1 % 2 once the softmax warps have read
-        // event j1 - 2 from it, committed to s_full and to the stage's release;
-        // at the end of work, the end event for the softmax warps and the event
-        // count for the O^T issuer.  False if a wait gave up.
-        auto issue_s = [&](int s, int nv) -> bool {
-            const int x = j1 & 1;
-            if (nv == 0) {  // a discarded speculative stage
-                mbar_arrive(&empty[s]);
-                return true;
-            }
-            if (j1 >= 2 && !wait_or_abort(&s_free[x], ((j1 >> 1) - 1) & 1, p.err, abort_flag)) return false;
-            if (nv < 0) {
-                smeta[4 * x + 1] = -1;
-                mbar_arrive(&s_full[x]);
-                mbar_arrive(&s_full[x]);
-                st_release_smem(ev_total, j1);
-                return true;
-            }
-            tc_fence_after();
-            smeta[4 * x + 0] = meta[s].tok0;
-            smeta[4 * x + 1] = nv;
-            mbar_arrive(&s_full[x]);
-            const uint64_t dk = dk0 + static_cast<uint64_t>((s * C::kStageBytes) >> 4);
-#pragma unroll
-            for (int kk = 0; kk < D / 32; ++kk)  // 32 channels (32 B) per K step
-                umma_e4m3(tmem + C::kColS * x, dk + 2 * kk, dq + 2 * kk, id_s, kk > 0 ? 1u : 0u);
-            umma_commit(&s_full[x]);
-            umma_commit(&empty[s]);
-            ++j1;
-            return true;
-        };
-        bool ok = s_issuer ? wait_or_abort(q_full, 0, p.err, abort_flag) : true;
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        int jv = 0;
-        for (int it = 0; ok; ++it) {
+        bool ok = true;
+        for (int it = 0;; ++it) {
             const int s = it % kS;
-            if (!warp_wait(&full[s], (it / kS) & 1, p.err, abort_flag)) {
+            const unsigned par = (it / kS) & 1;
+            if (!warp_wait(&full[s], par, p.err, abort_flag)) {
                 ok = false;
                 break;
             }
             const int nv = meta[s].nvalid;
-            if (warp == 2) {
-                int res = 1;
-                if (lane == 0) res = issue_s(s, nv) ? 1 : 0;
-                if (!__shfl_sync(0xffffffffu, res, 0)) {
-                    ok = false;
-                    break;
-                }
-            }
             if (nv < 0) break;
-            uint4 raw[8];
+            if (nv == 0) {  // a discarded speculative stage: no event, but v_full[s] moves one phase
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&v_full[s]);
+                continue;
+            }
+            uint8_t* st = stages + s * C::kStageBytes;
             const bool row_ok = tw < nv;
+            uint4 raw[8];
             if (row_ok) {
-                const uint8_t* v8 = stages + s * C::kStageBytes + C::kK8Bytes + tw * 128;
+                const uint8_t* v8 = st + C::kK8Bytes + tw * 128;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) raw[c] = *reinterpret_cast<const uint4*>(v8 + ((c ^ sw) << 4));
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
-            if (nv == 0) continue;  // a discarded speculative stage: no event
-            const int y = jv & 1;
-            if (jv >= 2 && !warp_wait(&v_free[y], ((jv >> 1) - 1) & 1, p.err, abort_flag)) {
+            if (!warp_wait(&k_done[s], par, p.err, abort_flag)) {
                 ok = false;
                 break;
             }
-            uint8_t* vd = v16 + y * C::kV16Bytes + tw * 128;
+            uint8_t* vd = st + tw * 128;
             if (row_ok) {
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
@@ -422,7 +434,7 @@ __global__ void __launch_bounds__(Tc05F8Cfg<NCP, CPT>::kThreads, 1)
                                                  e4m3x2_to_f16x2(w.y), e4m3x2_to_f16x2(w.y >> 16));
                     const uint4 hi4 = make_uint4(e4m3x2_to_f16x2(w.z), e4m3x2_to_f16x2(w.z >> 16),
                                                  e4m3x2_to_f16x2(w.w), e4m3x2_to_f16x2(w.w >> 16));
-                    uint8_t* half_row = vd + (c >> 2) * (C::kTile * 128);
+                    uint8_t* half_row = vd + (c >> 2) * C::kK8Bytes;
                     const uint32_t c0 = 2 * (c & 3);
                     *reinterpret_cast<uint4*>(half_row + ((c0 ^ sw) << 4)) = lo4;
                     *reinterpret_cast<uint4*>(half_row + (((c0 + 1) ^ sw) << 4)) = hi4;
@@ -430,16 +442,13 @@ __global__ void __launch_bounds__(Tc05F8Cfg<NCP, CPT>::kThreads, 1)
             } else {
 #pragma unroll
                 for (int c = 0; c < 16; ++c)
-                    *reinterpret_cast<uint4*>(vd + (c >> 3) * (C::kTile * 128) + (c & 7) * 16) =
-                        make_uint4(0u, 0u, 0u, 0u);
+                    *reinterpret_cast<uint4*>(vd + (c >> 3) * C::kK8Bytes + (c & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
             }
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&v_full[y]);
-            ++jv;
+            if (lane == 0) mbar_arrive(&v_full[s]);
         }
         if (!ok && lane == 0) atomicOr(abort_flag, 1);
-        if (s_issuer) umma_commit(final_bar);  // completes once its S^T products have
         allow_dependents();
         return;
     }
