@@ -44,15 +44,19 @@ FALLBACK_HBM_GBS = 6800.0
 NCU_TRAFFIC = {
     # warp-level tensor-core kernel, BF16 cache, 8B-shaped layer of 131072 tokens, 19 splits
     ("mma", "llama3.1-8b-decode-layer", 1): {
-        "bytes_per_launch": 537313280 + 3423744, "num_splits": 19,
-        "src_sha256": "26142dfeb40e7e2f28a485ecaaaebd4bc535c9ccd7805ae58d29236cb4a282ea"},
+        "bytes_per_launch": 537316608 + 2760192, "num_splits": 19,
+        "src_sha256": "f7a82f7f47667c959ecbe121213fb598015141733f20d36a6708e380c006ba5b"},
     # tcgen05 kernel, the same layer with 8 and 16 queries per row (32 and 64 columns per KV head)
     ("tc05", "llama3.1-8b-decode-layer", 8): {
-        "bytes_per_launch": 537470208 + 2971136, "num_splits": 19,
-        "src_sha256": "ce522a28c1033722e14ac6b8242e6efd3822d734cec09137b920e3eb2bea1217"},
+        "bytes_per_launch": 537073408 + 2994176, "num_splits": 19,
+        "src_sha256": "edcc13b57bc4b5a90be8e31d84f32ef0fca3889784c826a4159d4d80c92ee0f9"},
     ("tc05", "llama3.1-8b-decode-layer", 16): {
-        "bytes_per_launch": 537434368 + 2981376, "num_splits": 19,
-        "src_sha256": "ce522a28c1033722e14ac6b8242e6efd3822d734cec09137b920e3eb2bea1217"},
+        "bytes_per_launch": 537161728 + 2981632, "num_splits": 19,
+        "src_sha256": "edcc13b57bc4b5a90be8e31d84f32ef0fca3889784c826a4159d4d80c92ee0f9"},
+    # tcgen05 FP8 kernel, the same layer's E4M3 cache with 8 queries per row (32 columns per KV head)
+    ("fp8tc05", "llama3.1-8b-decode-layer", 8): {
+        "bytes_per_launch": 268626688 + 2908928, "num_splits": 19,
+        "src_sha256": "c9abbc972f7e280a5b6330060c5fb84dccfd8c83a54995c2339d737172394316"},
 }
 
 
