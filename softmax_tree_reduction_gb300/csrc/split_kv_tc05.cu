@@ -23,9 +23,9 @@
 //             products from one thread
 //  warp 2     issues the S^T products from one thread; each MMA group is
 //             committed to an mbarrier
-//  warps 3-10 softmax: 8 warps, one token of the stage and 16 (up to 32
-//             columns in the group) or 32 of its columns per thread, so each
-//             scheduler interleaves two warps:
+//  warps 3-   softmax: 4 warps per 16 columns (8 up to 32 columns in the
+//             group, 16 up to 64), one token of the stage and 16 of its
+//             columns per thread:
 //             exponentials against one reference maximum per column, shared
 //             by all threads in shared memory.  The reference moves only when a column's
 //             logits exceed it by more than 2^8 (one barrier reduction per
@@ -79,8 +79,9 @@ struct Tc05Cfg {
     static constexpr uint32_t kColO = 2 * NCP;          // O^T: [hi | lo], 2 NCP columns
     static constexpr uint32_t kTmemCols = 4 * NCP;      // 128 or 256
     static constexpr float kRescaleLog2 = 8.f;          // lazy-rescale margin (log2 units)
-    // the row merge's loads in flight per thread (4 registers each)
-    static constexpr int kMergeBatch = 20;
+    // the row merge's loads in flight per thread (4 registers each; fewer when
+    // the block's threads leave about 100 registers each)
+    static constexpr int kMergeBatch = kThreads > 400 ? 8 : 20;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
@@ -674,10 +675,10 @@ cudaError_t launch_split_tc05(const CUtensorMap& tk, const CUtensorMap& tv, cons
     if (p.G < 1 || p.G > 64 || p.hb != 1 || p.cluster || p.box_rows < 16 || p.box_rows > kTile)
         return cudaErrorInvalidValue;
     if (p.block_table == nullptr && p.box_rows != kTile) return cudaErrorInvalidValue;
-    // up to 32 columns: 8 softmax warps of 16 columns; up to 64: 8 warps of 32
-    // columns (16 warps of 16, 96 registers a thread, measured slower: 109.8 vs
-    // 109.6 us on the 131072-token layer, 748.8 vs 736.5 us on the 70B-shaped one)
-    return p.G <= 32 ? launch_ncp<32, 16>(tk, tv, p, stream) : launch_ncp<64, 32>(tk, tv, p, stream);
+    // up to 32 columns: 8 softmax warps of 16 columns (16 warps of 8 measured
+    // slower: 92.2 vs 91.2 us on the 131072-token layer); up to 64: 16 warps of
+    // 16 columns (8 warps of 32: 105.7 vs 104.0 us)
+    return p.G <= 32 ? launch_ncp<32, 16>(tk, tv, p, stream) : launch_ncp<64, 16>(tk, tv, p, stream);
 }
 
 }  // namespace ta
