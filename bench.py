@@ -48,11 +48,11 @@ NCU_TRAFFIC = {
         "src_sha256": "f7a82f7f47667c959ecbe121213fb598015141733f20d36a6708e380c006ba5b"},
     # tcgen05 kernel, the same layer with 8 and 16 queries per row (32 and 64 columns per KV head)
     ("tc05", "llama3.1-8b-decode-layer", 8): {
-        "bytes_per_launch": 537073408 + 2994176, "num_splits": 19,
-        "src_sha256": "edcc13b57bc4b5a90be8e31d84f32ef0fca3889784c826a4159d4d80c92ee0f9"},
+        "bytes_per_launch": 537064192 + 2746368, "num_splits": 19,
+        "src_sha256": "bf5b30293c608a090b420cef96952ad58c141b7aba81be8da02e0afeb7d6af1e"},
     ("tc05", "llama3.1-8b-decode-layer", 16): {
-        "bytes_per_launch": 537161728 + 2981632, "num_splits": 19,
-        "src_sha256": "edcc13b57bc4b5a90be8e31d84f32ef0fca3889784c826a4159d4d80c92ee0f9"},
+        "bytes_per_launch": 537132288 + 2721536, "num_splits": 19,
+        "src_sha256": "bf5b30293c608a090b420cef96952ad58c141b7aba81be8da02e0afeb7d6af1e"},
     # tcgen05 FP8 kernel, the same layer's E4M3 cache with 8 queries per row (32 columns per KV head)
     ("fp8tc05", "llama3.1-8b-decode-layer", 8): {
         "bytes_per_launch": 268626688 + 2908928, "num_splits": 19,
