@@ -113,20 +113,19 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP, CPT>::kThreads, 1)
     uint64_t* s_full = prod_done + 1;                              // [2] S^T of an event computed
     uint64_t* s_free = s_full + 2;                                 // [2] S^T read by the softmax warps
     uint64_t* p_full = s_full + 4;                                 // [2] P^T of an event written
-    uint64_t* o_done = s_full + 6;                                 // [2] O^T += ... of an event done
-    uint64_t* tmem_free = s_full + 8;                              // softmax warps are done with TMEM
-    uint64_t* final_bar = s_full + 9;                              // every MMA has completed
-    uint64_t* q_full = s_full + 10;                                // Q is in shared memory
-    volatile int* smeta = reinterpret_cast<volatile int*>(s_full + 11);  // [2][4]: tok0, nvalid, stage
+    // o_done[j % 4]: event j's O^T product done.  The softmax warps wait on it
+    // for an event at most two behind theirs, and a barrier can only move on
+    // past that event once they have written P^T of an event four later, so
+    // the phase they wait for is never overtaken.
+    uint64_t* o_done = s_full + 6;                                 // [4]
+    uint64_t* tmem_free = s_full + 10;                             // softmax warps are done with TMEM
+    uint64_t* final_bar = s_full + 11;                             // every MMA has completed
+    uint64_t* q_full = s_full + 12;                                // Q is in shared memory
+    volatile int* smeta = reinterpret_cast<volatile int*>(s_full + 13);  // [2][4]: tok0, nvalid, stage
     uint32_t* tmem_slot = const_cast<uint32_t*>(reinterpret_cast<volatile uint32_t*>(smeta + 8));
-    // Number of events whose O^T product has completed, published by the
-    // issuer (it alone waits on o_done, in order); the softmax warps read it
-    // when they must touch O^T, instead of waiting on a barrier phase that may
-    // have moved on.
-    int* o_count = reinterpret_cast<int*>(tmem_slot + 1);
-    int* ev_total = o_count + 1;          // events of the block (-1 until known)
+    int* ev_total = reinterpret_cast<int*>(tmem_slot + 1);  // events of the block (-1 until known)
     volatile int* ev_stage = ev_total + 1;  // [4] stage of each event whose O^T product is outstanding
-    static_assert(3 * kS * 8 + 16 + 8 + 11 * 8 + 32 + 8 + 4 + 16 <= C::kCtlBytes, "control block");
+    static_assert(3 * kS * 8 + 16 + 8 + 13 * 8 + 32 + 4 + 4 + 16 <= C::kCtlBytes, "control block");
     float* m_ref = reinterpret_cast<float*>(smem + C::kRedOff);   // [64] reference maxima (log2 units)
     float* m_fin = m_ref + 64;                                     // [64] m_ref, 0 where it is -inf
     float* alpha_s = m_fin + 64;                                   // [64] scale of a moved reference
@@ -152,12 +151,11 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP, CPT>::kThreads, 1)
             mbar_init(&s_full[x], 2);  // the issuer's release of the event, and the MMA commit
             mbar_init(&s_free[x], C::kSoftmaxWarps);
             mbar_init(&p_full[x], C::kSoftmaxWarps);
-            mbar_init(&o_done[x], 1);
         }
+        for (int x = 0; x < 4; ++x) mbar_init(&o_done[x], 1);
         mbar_init(tmem_free, C::kSoftmaxWarps);
         mbar_init(final_bar, 2);  // both issuing threads' MMAs have completed
         mbar_init(q_full, C::kSoftmaxWarps);
-        *o_count = 0;
         *ev_total = -1;
         *abort_flag = 0;
         *bad_page = 0;
@@ -295,57 +293,27 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP, CPT>::kThreads, 1)
             bool ok = true;
             constexpr uint32_t id_o = idesc_bf16(128, 2 * NCP, 1, 1);  // O^T += V^T P^T: both MN-major
             const uint64_t dst0 = smem_desc_sw128(smem_u32(stages), C::kTile * 128, 1024);
-            int j2 = 0;      // next event for O^T
-            int o_seen = 0;  // events whose O^T completion was observed and published
-            int n_ev = -1;   // the block's events, once the S^T issuer has seen the end of work
-            unsigned long long idle_since = 0;
-            // Every barrier is polled without blocking, so that whichever becomes
-            // ready first is served.  No barrier can run two phases ahead of its
-            // poll: o_done[x] because at most two O^T products are in flight,
-            // p_full because the softmax warps arrive on P^T of event j only after
-            // event j - 2's O^T product has completed (o_count).  P^T of event j
-            // exists only after its S^T.
-            while (ok) {
-                bool progress = false;
-                // publish completed O^T products, in order
-                if (o_seen < j2 && mbar_test_wait(&o_done[o_seen & 1], (o_seen >> 1) & 1)) {
-                    ++o_seen;
-                    st_release_smem(o_count, o_seen);
-                    progress = true;
+            // Event by event: P^T of event j2 written (or, at the end of work, the
+            // softmax warps' last arrival, after which the event count is known)
+            for (int j2 = 0;; ++j2) {
+                if (!wait_or_abort(&p_full[j2 & 1], (j2 >> 1) & 1, p.err, abort_flag)) {
+                    ok = false;
+                    break;
                 }
-                if (n_ev < 0) n_ev = ld_acquire_smem(ev_total);
-                // O^T += V^T P^T for the oldest event whose P^T is written (at most two in flight)
-                if ((n_ev < 0 || j2 < n_ev) && o_seen >= j2 - 1 && mbar_test_wait(&p_full[j2 & 1], (j2 >> 1) & 1)) {
-                    tc_fence_after();
-                    const int s = ev_stage[j2 & 3];
-                    const uint64_t pd = dst0 + static_cast<uint64_t>((s * C::kStageBytes) >> 4);
-                    const uint64_t vd = pd + (C::kKBytes >> 4);
+                const int n_ev = ld_acquire_smem(ev_total);
+                if (n_ev >= 0 && j2 >= n_ev) break;
+                tc_fence_after();
+                const int s = ev_stage[j2 & 3];
+                const uint64_t pd = dst0 + static_cast<uint64_t>((s * C::kStageBytes) >> 4);
+                const uint64_t vd = pd + (C::kKBytes >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < C::kTile / 16; ++kk) {
-                        // 16 tokens: two groups of 8 rows; V's channel halves and
-                        // P^T's 64-column blocks are 16 KB apart
-                        umma_f16(tmem + C::kColO, vd + 128 * kk, pd + 128 * kk, id_o, (j2 > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    umma_commit(&empty[s]);
-                    umma_commit(&o_done[j2 & 1]);
-                    ++j2;
-                    progress = true;
+                for (int kk = 0; kk < C::kTile / 16; ++kk) {
+                    // 16 tokens: two groups of 8 rows; V's channel halves and
+                    // P^T's 64-column blocks are 16 KB apart
+                    umma_f16(tmem + C::kColO, vd + 128 * kk, pd + 128 * kk, id_o, (j2 > 0 || kk > 0) ? 1u : 0u);
                 }
-                if (n_ev >= 0 && j2 == n_ev && o_seen == j2) break;
-                if (progress) {
-                    idle_since = 0;
-                } else {
-                    // leave the issue slots of this sub-partition to the softmax warps
-                    __nanosleep(20);
-                    if (*const_cast<volatile int*>(abort_flag)) {
-                        ok = false;
-                    } else if (idle_since == 0) {
-                        idle_since = globaltimer();
-                    } else if (globaltimer() - idle_since > kWaitLimitNs) {
-                        atomicOr(p.err, kErrTimeout);
-                        ok = false;
-                    }
-                }
+                umma_commit(&empty[s]);
+                umma_commit(&o_done[j2 & 3]);
             }
             if (!ok) atomicOr(abort_flag, 1);
             // TMEM is freed only once no MMA is in flight and the softmax warps are done with it
@@ -478,7 +446,12 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP, CPT>::kThreads, 1)
             failed = true;
             break;
         }
-        if (nv < 0) break;  // every warp's wait succeeded and saw the same end-of-work event
+        if (nv < 0) {  // every warp's wait succeeded and saw the same end-of-work event
+            // a last arrival wakes the O^T issuer (after event j - 2's product, as for any event)
+            if (j >= 2) failed = !warp_wait(&o_done[(j - 2) & 3], ((j - 2) >> 2) & 1, p.err, abort_flag);
+            if (lane == 0 && !failed) mbar_arrive(&p_full[x]);
+            break;
+        }
         bool rescale_o = false;  // O^T needs the moved references' scales (after P^T is written)
         if (any_over) {
             // new references: per column, the maximum over the stage's counted tokens
@@ -551,7 +524,7 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP, CPT>::kThreads, 1)
         if (rescale_o) {
             // every earlier O^T product must be complete before O^T is rescaled:
             // this warp's columns, hi and lo
-            failed |= !warp_wait_count(o_count, j, p.err, abort_flag);
+            failed |= !warp_wait(&o_done[(j - 1) & 3], ((j - 1) >> 2) & 1, p.err, abort_flag);
             if (failed && lane == 0) *fail_rec = 1;  // the next stage's reduction ends the loop
             if (!failed) {
                 tc_fence_after();
@@ -572,7 +545,7 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP, CPT>::kThreads, 1)
         tc_fence_before();
         // event j - 2's P^T must have been taken (its O^T product completed)
         // before p_full[x] gets event j's arrivals
-        if (j >= 2 && !failed) failed = !warp_wait_count(o_count, j - 1, p.err, abort_flag);
+        if (j >= 2 && !failed) failed = !warp_wait(&o_done[(j - 2) & 3], ((j - 2) >> 2) & 1, p.err, abort_flag);
         __syncwarp();
         if (lane == 0 && !failed) mbar_arrive(&p_full[x]);
         if (lane == 0 && failed) *fail_rec = 1;
@@ -586,7 +559,7 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP, CPT>::kThreads, 1)
         const float ws = warp_sum(lp[i]);
         if (lane == 0) wred[quarter * 64 + c_base + i] = ws;
     }
-    if (!failed && j > 0) failed = !warp_wait_count(o_count, j, p.err, abort_flag);
+    if (!failed && j > 0) failed = !warp_wait(&o_done[(j - 1) & 3], ((j - 1) >> 2) & 1, p.err, abort_flag);
     float o[CPT];  // channel t of the warp's columns
     if (!failed && j > 0) {
         tc_fence_after();

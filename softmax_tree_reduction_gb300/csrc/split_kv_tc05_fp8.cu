@@ -144,20 +144,22 @@ __global__ void __launch_bounds__(Tc05F8Cfg<NCP, CPT>::kThreads, 1)
     uint64_t* s_full = v_full + kS;                                 // [2] S^T of an event computed
     uint64_t* s_free = s_full + 2;                                  // [2] S^T read by the softmax warps
     uint64_t* p_full = s_full + 4;                                  // [3] P^T of an event written
-    uint64_t* o_done = s_full + 7;                                  // [2] O^T += ... of an event done
-    uint64_t* tmem_free = s_full + 9;                               // softmax warps are done with TMEM
-    uint64_t* final_bar = s_full + 10;                              // every MMA has completed
-    uint64_t* q_full = s_full + 11;                                 // Q8 is in shared memory
-    volatile int* smeta = reinterpret_cast<volatile int*>(s_full + 12);  // [2][4]: tok0, nvalid
+    // o_done[j % 4]: event j's O^T product done.  The softmax warps wait on it
+    // for an event at most three behind theirs, and a barrier can only move on
+    // past that event once they have written P^T of an event four later.
+    uint64_t* o_done = s_full + 7;                                  // [4]
+    uint64_t* tmem_free = s_full + 11;                              // softmax warps are done with TMEM
+    uint64_t* final_bar = s_full + 12;                              // every MMA has completed
+    uint64_t* q_full = s_full + 13;                                 // Q8 is in shared memory
+    volatile int* smeta = reinterpret_cast<volatile int*>(s_full + 14);  // [2][4]: tok0, nvalid
     uint32_t* tmem_slot = const_cast<uint32_t*>(reinterpret_cast<volatile uint32_t*>(smeta + 8));
-    int* o_count = reinterpret_cast<int*>(tmem_slot + 1);           // O^T products completed (O^T issuer)
-    int* ev_total = o_count + 1;                                    // events of the block (-1 until known)
+    int* ev_total = reinterpret_cast<int*>(tmem_slot + 1);         // events of the block (-1 until known)
     // [8] each event's stage and the parity of that stage's use, until its O^T
     // product is issued (at most kS events are outstanding: a stage is reused
     // only after its product)
     volatile int* ev_stage = ev_total + 1;
     volatile int* ev_par = ev_stage + 8;
-    static_assert(3 * kS * 8 + 16 + 8 + 2 * kS * 8 + 12 * 8 + 32 + 12 + 64 <= C::kCtlBytes, "control block");
+    static_assert(3 * kS * 8 + 16 + 8 + 2 * kS * 8 + 14 * 8 + 32 + 8 + 64 <= C::kCtlBytes, "control block");
     float* m_ref = reinterpret_cast<float*>(smem + C::kRedOff);    // [64] reference maxima (log2 units)
     float* m_fin = m_ref + 64;                                      // [64] m_ref, 0 where it is -inf
     float* alpha_s = m_fin + 64;                                    // [64] scale of a moved reference
@@ -181,13 +183,12 @@ __global__ void __launch_bounds__(Tc05F8Cfg<NCP, CPT>::kThreads, 1)
         for (int x = 0; x < 2; ++x) {
             mbar_init(&s_full[x], 2);  // the issuer's release of the event, and the MMA commit
             mbar_init(&s_free[x], C::kSoftmaxWarps);
-            mbar_init(&o_done[x], 1);
         }
+        for (int x = 0; x < 4; ++x) mbar_init(&o_done[x], 1);
         for (int x = 0; x < C::kPBufs; ++x) mbar_init(&p_full[x], C::kSoftmaxWarps);
         mbar_init(tmem_free, C::kSoftmaxWarps);
         mbar_init(final_bar, 2);  // both issuing threads' MMAs have completed
         mbar_init(q_full, C::kSoftmaxWarps);
-        *o_count = 0;
         *ev_total = -1;
         *abort_flag = 0;
         *bad_page = 0;
@@ -318,62 +319,34 @@ __global__ void __launch_bounds__(Tc05F8Cfg<NCP, CPT>::kThreads, 1)
             constexpr uint32_t id_o = idesc_f16(128, 64, 1, 1);  // O^T += V16^T P^T: both MN-major
             const uint64_t dst0 = smem_desc_sw128(smem_u32(stages), C::kTile * 128, 1024);
             const uint64_t dp0 = smem_desc_sw128(smem_u32(pbuf), C::kTile * 128, 1024);
-            int j2 = 0;      // next event for O^T
-            int o_seen = 0;  // events whose O^T completion was observed and published
-            int n_ev = -1;   // the block's events, once the S^T issuer has seen the end of work
-            unsigned long long idle_since = 0;
-            // Every barrier is polled without blocking.  None can run two phases
-            // ahead of its poll: o_done[x] because at most two O^T products are in
-            // flight; p_full because the softmax warps write P^T of event j only
-            // after event j - 3's product has completed (o_count); v_full[s]
-            // because a stage is refilled only after its product.  P^T of event j
-            // exists only after its S^T (which recorded the event's stage).
-            while (ok) {
-                bool progress = false;
-                // publish completed O^T products, in order
-                if (o_seen < j2 && mbar_test_wait(&o_done[o_seen & 1], (o_seen >> 1) & 1)) {
-                    ++o_seen;
-                    st_release_smem(o_count, o_seen);
-                    progress = true;
+            // Event by event: P^T of event j2 written (or, at the end of work, the
+            // softmax warps' last arrival, after which the event count is known),
+            // then the event's stage widened
+            for (int j2 = 0;; ++j2) {
+                if (!wait_or_abort(&p_full[j2 % C::kPBufs], (j2 / C::kPBufs) & 1, p.err, abort_flag)) {
+                    ok = false;
+                    break;
                 }
-                if (n_ev < 0) n_ev = ld_acquire_smem(ev_total);
-                // O^T += V16^T P^T for the oldest event whose P^T and V16 are ready (at most two in flight)
-                if ((n_ev < 0 || j2 < n_ev) && o_seen >= j2 - 1 &&
-                    mbar_test_wait(&p_full[j2 % C::kPBufs], (j2 / C::kPBufs) & 1)) {
-                    const int s = ev_stage[j2 & 7];
-                    if (mbar_test_wait(&v_full[s], static_cast<unsigned>(ev_par[j2 & 7]))) {
-                        tc_fence_after();
-                        const uint64_t dp = dp0 + static_cast<uint64_t>(((j2 % C::kPBufs) * C::kPBytes) >> 4);
-                        const uint64_t dv = dst0 + static_cast<uint64_t>((s * C::kStageBytes) >> 4);
+                const int n_ev = ld_acquire_smem(ev_total);
+                if (n_ev >= 0 && j2 >= n_ev) break;
+                const int s = ev_stage[j2 & 7];
+                if (!wait_or_abort(&v_full[s], static_cast<unsigned>(ev_par[j2 & 7]), p.err, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t dp = dp0 + static_cast<uint64_t>(((j2 % C::kPBufs) * C::kPBytes) >> 4);
+                const uint64_t dv = dst0 + static_cast<uint64_t>((s * C::kStageBytes) >> 4);
 #pragma unroll
-                        for (int i = 0; i < C::kTile / 16; ++i) {
-                            // 16 tokens: two groups of 8 rows; V16's channel halves are 16 KB
-                            // apart.  The two token halves alternate between two accumulators.
-                            const int h = i & 1, kk = 4 * h + (i >> 1);
-                            const uint32_t acc = C::kColO + 64 * (2 * (j2 & 1) + h);
-                            umma_f16(tmem + acc, dv + 128 * kk, dp + 128 * kk, id_o,
-                                     (j2 >= 2 || (kk & 3) > 0) ? 1u : 0u);
-                        }
-                        umma_commit(&empty[s]);
-                        umma_commit(&o_done[j2 & 1]);
-                        ++j2;
-                        progress = true;
-                    }
+                for (int i = 0; i < C::kTile / 16; ++i) {
+                    // 16 tokens: two groups of 8 rows; V16's channel halves are 16 KB
+                    // apart.  The two token halves alternate between two accumulators.
+                    const int h = i & 1, kk = 4 * h + (i >> 1);
+                    const uint32_t acc = C::kColO + 64 * (2 * (j2 & 1) + h);
+                    umma_f16(tmem + acc, dv + 128 * kk, dp + 128 * kk, id_o, (j2 >= 2 || (kk & 3) > 0) ? 1u : 0u);
                 }
-                if (n_ev >= 0 && j2 == n_ev && o_seen == j2) break;
-                if (progress) {
-                    idle_since = 0;
-                } else {
-                    __nanosleep(20);
-                    if (*const_cast<volatile int*>(abort_flag)) {
-                        ok = false;
-                    } else if (idle_since == 0) {
-                        idle_since = globaltimer();
-                    } else if (globaltimer() - idle_since > kWaitLimitNs) {
-                        atomicOr(p.err, kErrTimeout);
-                        ok = false;
-                    }
-                }
+                umma_commit(&empty[s]);
+                umma_commit(&o_done[j2 & 3]);
             }
             if (!ok) atomicOr(abort_flag, 1);
             // TMEM is freed only once no MMA is in flight and the softmax warps are done with it
@@ -608,7 +581,13 @@ __global__ void __launch_bounds__(Tc05F8Cfg<NCP, CPT>::kThreads, 1)
             failed = true;
             break;
         }
-        if (nv < 0) break;  // every warp's wait succeeded and saw the same end-of-work event
+        if (nv < 0) {  // every warp's wait succeeded and saw the same end-of-work event
+            // a last arrival wakes the O^T issuer (after event j - 3's product, as for any event)
+            if (j >= C::kPBufs)
+                failed = !warp_wait(&o_done[(j - C::kPBufs) & 3], ((j - C::kPBufs) >> 2) & 1, p.err, abort_flag);
+            if (lane == 0 && !failed) mbar_arrive(&p_full[j % C::kPBufs]);
+            break;
+        }
         bool rescale_o = false;
         if (any_over) {
 #pragma unroll
@@ -643,7 +622,8 @@ __global__ void __launch_bounds__(Tc05F8Cfg<NCP, CPT>::kThreads, 1)
             rescale_o = resc && j > 0;
         }
         // P^T buffer j % 3 was last read by event j - 3's product
-        if (j >= C::kPBufs && !failed) failed = !warp_wait_count(o_count, j - C::kPBufs + 1, p.err, abort_flag);
+        if (j >= C::kPBufs && !failed)
+            failed = !warp_wait(&o_done[(j - C::kPBufs) & 3], ((j - C::kPBufs) >> 2) & 1, p.err, abort_flag);
         if (!failed) {
             // P^T row t: element n of [hi | lo] at 16-byte chunk n / 8 (swizzled)
             uint8_t* pb = pbuf + (j % C::kPBufs) * C::kPBytes + t * 128;
@@ -670,7 +650,7 @@ __global__ void __launch_bounds__(Tc05F8Cfg<NCP, CPT>::kThreads, 1)
         }
         if (rescale_o && !failed) {
             // every earlier O^T product must be complete before O^T is rescaled
-            failed = !warp_wait_count(o_count, j, p.err, abort_flag);
+            failed = !warp_wait(&o_done[(j - 1) & 3], ((j - 1) >> 2) & 1, p.err, abort_flag);
             if (!failed) {
                 tc_fence_after();
 #pragma unroll 1
@@ -701,7 +681,7 @@ __global__ void __launch_bounds__(Tc05F8Cfg<NCP, CPT>::kThreads, 1)
         const float ws = warp_sum(lp[i]);
         if (lane == 0) wred[quarter * 64 + c_base + i] = ws;
     }
-    if (!failed && j > 0) failed = !warp_wait_count(o_count, j, p.err, abort_flag);
+    if (!failed && j > 0) failed = !warp_wait(&o_done[(j - 1) & 3], ((j - 1) >> 2) & 1, p.err, abort_flag);
     float o[CPT];  // channel t of the warp's columns
     if (!failed && j > 0) {
         tc_fence_after();

@@ -292,25 +292,6 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, unsigned parity, int* e
     return ok != 0;
 }
 
-// Lane 0 waits until *count >= target (a counter published with release
-// semantics by another warp of the block), the warp follows.
-__device__ __forceinline__ bool warp_wait_count(int* count, int target, int* err, const volatile int* abort_flag) {
-    int ok = 1;
-    if ((threadIdx.x & 31) == 0 && ld_acquire_smem(count) < target) {
-        const unsigned long long t0 = globaltimer();
-        while (ld_acquire_smem(count) < target) {
-            if (*abort_flag || globaltimer() - t0 > kWaitLimitNs) {
-                if (!*abort_flag) atomicOr(err, kErrTimeout);
-                ok = 0;
-                break;
-            }
-        }
-    }
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    __syncwarp();
-    return ok != 0;
-}
-
 // OR of `pred` over the NT softmax threads (named barrier 1), which also
 // synchronises them.
 template <int NT>
