@@ -65,7 +65,7 @@ struct Tc05Cfg {
     static constexpr int kQOff = kStages * kStageBytes;
     static constexpr int kQBytes = 2 * 64 * 128;
     static constexpr int kCtlOff = kQOff + kQBytes;
-    static constexpr int kCtlBytes = 256;
+    static constexpr int kCtlBytes = 384;
     // m_ref, m_fin, alpha, shift [64]; per-warp partials [4][64]; causal column masks [4][16]
     static constexpr int kRedOff = kCtlOff + kCtlBytes;
     static constexpr int kRedBytes = (4 * 64 + 4 * 64 + 64 + 4) * 4;
@@ -112,20 +112,24 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP, CPT>::kThreads, 1)
     uint64_t* prod_done = reinterpret_cast<uint64_t*>(abort_flag + 4);  // the copy warp's last claim is made
     uint64_t* s_full = prod_done + 1;                              // [2] S^T of an event computed
     uint64_t* s_free = s_full + 2;                                 // [2] S^T read by the softmax warps
-    uint64_t* p_full = s_full + 4;                                 // [2] P^T of an event written
+    // p_full[j % 4]: P^T of event j written.  The O^T issuer has waited on the
+    // same barrier for event j - 4 before the softmax warps arrive for event j:
+    // event j's stage was last used by event j - 3 and released by its O^T
+    // product, issued after event j - 4's.
+    uint64_t* p_full = s_full + 4;                                 // [4]
     // o_done[j % 4]: event j's O^T product done.  The softmax warps wait on it
-    // for an event at most two behind theirs, and a barrier can only move on
-    // past that event once they have written P^T of an event four later, so
-    // the phase they wait for is never overtaken.
-    uint64_t* o_done = s_full + 6;                                 // [4]
-    uint64_t* tmem_free = s_full + 10;                             // softmax warps are done with TMEM
-    uint64_t* final_bar = s_full + 11;                             // every MMA has completed
-    uint64_t* q_full = s_full + 12;                                // Q is in shared memory
-    volatile int* smeta = reinterpret_cast<volatile int*>(s_full + 13);  // [2][4]: tok0, nvalid, stage
+    // for the event just before theirs, and a barrier can only move on past
+    // that event once they have written P^T of an event four later, so the
+    // phase they wait for is never overtaken.
+    uint64_t* o_done = s_full + 8;                                 // [4]
+    uint64_t* tmem_free = s_full + 12;                             // softmax warps are done with TMEM
+    uint64_t* final_bar = s_full + 13;                             // every MMA has completed
+    uint64_t* q_full = s_full + 14;                                // Q is in shared memory
+    volatile int* smeta = reinterpret_cast<volatile int*>(s_full + 15);  // [2][4]: tok0, nvalid, stage
     uint32_t* tmem_slot = const_cast<uint32_t*>(reinterpret_cast<volatile uint32_t*>(smeta + 8));
     int* ev_total = reinterpret_cast<int*>(tmem_slot + 1);  // events of the block (-1 until known)
     volatile int* ev_stage = ev_total + 1;  // [4] stage of each event whose O^T product is outstanding
-    static_assert(3 * kS * 8 + 16 + 8 + 13 * 8 + 32 + 4 + 4 + 16 <= C::kCtlBytes, "control block");
+    static_assert(3 * kS * 8 + 16 + 8 + 15 * 8 + 32 + 4 + 4 + 16 <= C::kCtlBytes, "control block");
     float* m_ref = reinterpret_cast<float*>(smem + C::kRedOff);   // [64] reference maxima (log2 units)
     float* m_fin = m_ref + 64;                                     // [64] m_ref, 0 where it is -inf
     float* alpha_s = m_fin + 64;                                   // [64] scale of a moved reference
@@ -150,9 +154,11 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP, CPT>::kThreads, 1)
         for (int x = 0; x < 2; ++x) {
             mbar_init(&s_full[x], 2);  // the issuer's release of the event, and the MMA commit
             mbar_init(&s_free[x], C::kSoftmaxWarps);
-            mbar_init(&p_full[x], C::kSoftmaxWarps);
         }
-        for (int x = 0; x < 4; ++x) mbar_init(&o_done[x], 1);
+        for (int x = 0; x < 4; ++x) {
+            mbar_init(&p_full[x], C::kSoftmaxWarps);
+            mbar_init(&o_done[x], 1);
+        }
         mbar_init(tmem_free, C::kSoftmaxWarps);
         mbar_init(final_bar, 2);  // both issuing threads' MMAs have completed
         mbar_init(q_full, C::kSoftmaxWarps);
@@ -296,7 +302,7 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP, CPT>::kThreads, 1)
             // Event by event: P^T of event j2 written (or, at the end of work, the
             // softmax warps' last arrival, after which the event count is known)
             for (int j2 = 0;; ++j2) {
-                if (!wait_or_abort(&p_full[j2 & 1], (j2 >> 1) & 1, p.err, abort_flag)) {
+                if (!wait_or_abort(&p_full[j2 & 3], (j2 >> 2) & 1, p.err, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -447,9 +453,7 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP, CPT>::kThreads, 1)
             break;
         }
         if (nv < 0) {  // every warp's wait succeeded and saw the same end-of-work event
-            // a last arrival wakes the O^T issuer (after event j - 2's product, as for any event)
-            if (j >= 2) failed = !warp_wait(&o_done[(j - 2) & 3], ((j - 2) >> 2) & 1, p.err, abort_flag);
-            if (lane == 0 && !failed) mbar_arrive(&p_full[x]);
+            if (lane == 0) mbar_arrive(&p_full[j & 3]);  // a last arrival wakes the O^T issuer
             break;
         }
         bool rescale_o = false;  // O^T needs the moved references' scales (after P^T is written)
@@ -543,11 +547,8 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP, CPT>::kThreads, 1)
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        // event j - 2's P^T must have been taken (its O^T product completed)
-        // before p_full[x] gets event j's arrivals
-        if (j >= 2 && !failed) failed = !warp_wait(&o_done[(j - 2) & 3], ((j - 2) >> 2) & 1, p.err, abort_flag);
         __syncwarp();
-        if (lane == 0 && !failed) mbar_arrive(&p_full[x]);
+        if (lane == 0 && !failed) mbar_arrive(&p_full[j & 3]);
         if (lane == 0 && failed) *fail_rec = 1;
     }
     if (failed && lane == 0) atomicOr(abort_flag, 1);  // the issuer stops polling too
