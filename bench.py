@@ -45,18 +45,18 @@ NCU_TRAFFIC = {
     # warp-level tensor-core kernel, BF16 cache, 8B-shaped layer of 131072 tokens, 19 splits
     ("mma", "llama3.1-8b-decode-layer", 1): {
         "bytes_per_launch": 537316608 + 2760192, "num_splits": 19,
-        "src_sha256": "f7a82f7f47667c959ecbe121213fb598015141733f20d36a6708e380c006ba5b"},
+        "src_sha256": "59386695fba4fc9262837d650de324d47d9e706eacf4aa39fcf9eb83df155df7"},
     # tcgen05 kernel, the same layer with 8 and 16 queries per row (32 and 64 columns per KV head)
     ("tc05", "llama3.1-8b-decode-layer", 8): {
-        "bytes_per_launch": 537064192 + 2746368, "num_splits": 19,
-        "src_sha256": "bf5b30293c608a090b420cef96952ad58c141b7aba81be8da02e0afeb7d6af1e"},
+        "bytes_per_launch": 537058816 + 3119104, "num_splits": 19,
+        "src_sha256": "efbbf4ccd646a86c9145e5f433ff91f6e4e5c4dd215004c8a7787460c120d531"},
     ("tc05", "llama3.1-8b-decode-layer", 16): {
-        "bytes_per_launch": 537132288 + 2721536, "num_splits": 19,
-        "src_sha256": "bf5b30293c608a090b420cef96952ad58c141b7aba81be8da02e0afeb7d6af1e"},
+        "bytes_per_launch": 537133568 + 2754048, "num_splits": 19,
+        "src_sha256": "efbbf4ccd646a86c9145e5f433ff91f6e4e5c4dd215004c8a7787460c120d531"},
     # tcgen05 FP8 kernel, the same layer's E4M3 cache with 8 queries per row (32 columns per KV head)
     ("fp8tc05", "llama3.1-8b-decode-layer", 8): {
-        "bytes_per_launch": 268626688 + 2908928, "num_splits": 19,
-        "src_sha256": "c9abbc972f7e280a5b6330060c5fb84dccfd8c83a54995c2339d737172394316"},
+        "bytes_per_launch": 268630016 + 3099392, "num_splits": 19,
+        "src_sha256": "5a36c3ee5674bdec33faaf6802177ab69a39fc187404b08f1ab499744c1dd875"},
 }
 
 
@@ -126,10 +126,17 @@ def load_peaks():
 
 
 def kernel_source_hash(kernel):
-    name = {"mma": "split_kv_mma.cu", "fma": "split_kv_fma.cuh", "fp8": "split_kv_fp8.cu",
-            "tc05": "split_kv_tc05.cu", "fp8tc05": "split_kv_tc05_fp8.cu"}[kernel]
+    """SHA-256 of the sources a kernel family is compiled from (its own file and
+    the headers it includes) and of the host code that configures its launch."""
+    warp_level = ("common.cuh", "emit.cuh", "kernels.h", "sched.cuh", "warp_mma.cuh")
+    tcgen05 = ("common.cuh", "kernels.h", "sched.cuh", "tc05.cuh")
+    files = {"mma": ("split_kv_mma.cu",) + warp_level,
+             "fp8": ("split_kv_fp8.cu",) + warp_level,
+             "fma": ("split_kv_fma.cuh", "common.cuh", "emit.cuh", "kernels.h", "sched.cuh"),
+             "tc05": ("split_kv_tc05.cu",) + tcgen05,
+             "fp8tc05": ("split_kv_tc05_fp8.cu",) + tcgen05}[kernel]
     h = hashlib.sha256()
-    for f in (name, "common.cuh", "emit.cuh", "sched.cuh", "warp_mma.cuh", "tc05.cuh", "api.cu"):
+    for f in files + ("api.cu",):
         with open(os.path.join(ROOT, "softmax_tree_reduction_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
