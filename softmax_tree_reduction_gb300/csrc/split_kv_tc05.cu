@@ -441,8 +441,9 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP, CPT>::kThreads, 1)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int i = 4 * i4 + e;
-                    xs[i] = fmaf(xs[i], sl2, -mv[e]);
-                    xm[e] = fmaxf(xm[e], ((vmask >> i) & 1) ? xs[i] : -INFINITY);
+                    // columns that do not count this token get -inf (exponential 0)
+                    xs[i] = ((vmask >> i) & 1) ? fmaf(xs[i], sl2, -mv[e]) : -INFINITY;
+                    xm[e] = fmaxf(xm[e], xs[i]);
                 }
             }
             over = (fmaxf(fmaxf(xm[0], xm[1]), fmaxf(xm[2], xm[3])) > C::kRescaleLog2) || (vmask & mneg);
@@ -461,7 +462,7 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP, CPT>::kThreads, 1)
             // new references: per column, the maximum over the stage's counted tokens
 #pragma unroll
             for (int i = 0; i < CPT; ++i) {
-                const float wm = warp_max(((vmask >> i) & 1) ? xs[i] : -INFINITY);
+                const float wm = warp_max(xs[i]);
                 if (lane == 0) wred[quarter * 64 + c_base + i] = wm;
             }
             consumer_sync(NT);
@@ -497,7 +498,7 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP, CPT>::kThreads, 1)
         for (int k = 0; k < CPT / 8; ++k) {  // hi columns c_base + 8k .. + 7, lo columns NCP + the same
             float pv[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) pv[e] = ((vmask >> (8 * k + e)) & 1) ? ex2(xs[8 * k + e]) : 0.f;
+            for (int e = 0; e < 8; ++e) pv[e] = ex2(xs[8 * k + e]);
             uint32_t hw[4], lw[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
