@@ -438,11 +438,14 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP, CPT>::kThreads, 1)
             for (int i4 = 0; i4 < CPT / 4; ++i4) {
                 const float4 m4 = *reinterpret_cast<const float4*>(m_fin + c_base + 4 * i4);
                 const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
+                float y[4];
+                fma2(y[0], y[1], xs[4 * i4], xs[4 * i4 + 1], sl2, sl2, -mv[0], -mv[1]);
+                fma2(y[2], y[3], xs[4 * i4 + 2], xs[4 * i4 + 3], sl2, sl2, -mv[2], -mv[3]);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int i = 4 * i4 + e;
                     // columns that do not count this token get -inf (exponential 0)
-                    xs[i] = ((vmask >> i) & 1) ? fmaf(xs[i], sl2, -mv[e]) : -INFINITY;
+                    xs[i] = ((vmask >> i) & 1) ? y[e] : -INFINITY;
                     xm[e] = fmaxf(xm[e], xs[i]);
                 }
             }
@@ -502,11 +505,13 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP, CPT>::kThreads, 1)
             uint32_t hw[4], lw[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                lp[8 * k + 2 * e] += pv[2 * e];
-                lp[8 * k + 2 * e + 1] += pv[2 * e + 1];
+                add2(lp[8 * k + 2 * e], lp[8 * k + 2 * e + 1], lp[8 * k + 2 * e], lp[8 * k + 2 * e + 1], pv[2 * e],
+                     pv[2 * e + 1]);
                 hw[e] = pack_bf16(pv[2 * e], pv[2 * e + 1]);
-                lw[e] = pack_bf16(pv[2 * e] - __uint_as_float(hw[e] << 16),
-                                  pv[2 * e + 1] - __uint_as_float(hw[e] & 0xffff0000u));
+                float l0, l1;
+                sub2(l0, l1, pv[2 * e], pv[2 * e + 1], __uint_as_float(hw[e] << 16),
+                     __uint_as_float(hw[e] & 0xffff0000u));
+                lw[e] = pack_bf16(l0, l1);
             }
             const int nh = c_base + 8 * k, nl = NCP + c_base + 8 * k;
             const uint32_t oh = (nh / 64) * (C::kTile * 128) + t * 128 + ((((nh % 64) / 8) ^ (t & 7)) << 4);

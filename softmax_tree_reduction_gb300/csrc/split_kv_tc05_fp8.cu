@@ -557,7 +557,7 @@ __global__ void __launch_bounds__(Tc05F8Cfg<NCP, CPT>::kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&s_free[x]);
 #pragma unroll
-            for (int i = 0; i < CPT; ++i) xs[i] = fmaf(s2[i], 0.0625f, xs[i]);
+            for (int i = 0; i < CPT; i += 2) fma2(xs[i], xs[i + 1], s2[i], s2[i + 1], 0.0625f, 0.0625f, xs[i], xs[i + 1]);
 
             vmask = tok_ok ? gmask : 0u;
             const int d = tok0 + t - causal_from + 1;  // <= 0 before the diagonal (and without causality)
@@ -567,11 +567,14 @@ __global__ void __launch_bounds__(Tc05F8Cfg<NCP, CPT>::kThreads, 1)
             for (int i4 = 0; i4 < CPT / 4; ++i4) {
                 const float4 m4 = *reinterpret_cast<const float4*>(m_fin + c_base + 4 * i4);
                 const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
+                float y[4];
+                fma2(y[0], y[1], xs[4 * i4], xs[4 * i4 + 1], sl2, sl2, -mv[0], -mv[1]);
+                fma2(y[2], y[3], xs[4 * i4 + 2], xs[4 * i4 + 3], sl2, sl2, -mv[2], -mv[3]);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int i = 4 * i4 + e;
                     // columns that do not count this token get -inf (exponential 0)
-                    xs[i] = ((vmask >> i) & 1) ? fmaf(xs[i], sl2, -mv[e]) : -INFINITY;
+                    xs[i] = ((vmask >> i) & 1) ? y[e] : -INFINITY;
                     xm[e] = fmaxf(xm[e], xs[i]);
                 }
             }
@@ -636,12 +639,15 @@ __global__ void __launch_bounds__(Tc05F8Cfg<NCP, CPT>::kThreads, 1)
                 uint32_t hw[4], lw[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    lp[8 * k + 2 * e] += pv[2 * e];
-                    lp[8 * k + 2 * e + 1] += pv[2 * e + 1];
-                    const float a = pv[2 * e] * C::kPScale, c = pv[2 * e + 1] * C::kPScale;
+                    add2(lp[8 * k + 2 * e], lp[8 * k + 2 * e + 1], lp[8 * k + 2 * e], lp[8 * k + 2 * e + 1],
+                         pv[2 * e], pv[2 * e + 1]);
+                    float a, c;
+                    mul2(a, c, pv[2 * e], pv[2 * e + 1], C::kPScale, C::kPScale);
                     hw[e] = pack_f16(a, c);
                     const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hw[e]));
-                    lw[e] = pack_f16(a - hf.x, c - hf.y);
+                    float l0, l1;
+                    sub2(l0, l1, a, c, hf.x, hf.y);
+                    lw[e] = pack_f16(l0, l1);
                 }
                 const int nh = c_base + 8 * k, nl = NCP + c_base + 8 * k;
                 const uint32_t oh = ((nh / 8) ^ (t & 7)) << 4, ol = ((nl / 8) ^ (t & 7)) << 4;
