@@ -48,15 +48,15 @@ NCU_TRAFFIC = {
         "src_sha256": "59386695fba4fc9262837d650de324d47d9e706eacf4aa39fcf9eb83df155df7"},
     # tcgen05 kernel, the same layer with 8 and 16 queries per row (32 and 64 columns per KV head)
     ("tc05", "llama3.1-8b-decode-layer", 8): {
-        "bytes_per_launch": 537058816 + 3119104, "num_splits": 19,
-        "src_sha256": "efbbf4ccd646a86c9145e5f433ff91f6e4e5c4dd215004c8a7787460c120d531"},
+        "bytes_per_launch": 537053952 + 2729216, "num_splits": 19,
+        "src_sha256": "4e80c86264a90901f84252c725cb7cc2f4e95a1a86b7d87693c965a085a763de"},
     ("tc05", "llama3.1-8b-decode-layer", 16): {
-        "bytes_per_launch": 537133568 + 2754048, "num_splits": 19,
-        "src_sha256": "efbbf4ccd646a86c9145e5f433ff91f6e4e5c4dd215004c8a7787460c120d531"},
+        "bytes_per_launch": 537137920 + 3182592, "num_splits": 19,
+        "src_sha256": "4e80c86264a90901f84252c725cb7cc2f4e95a1a86b7d87693c965a085a763de"},
     # tcgen05 FP8 kernel, the same layer's E4M3 cache with 8 queries per row (32 columns per KV head)
     ("fp8tc05", "llama3.1-8b-decode-layer", 8): {
-        "bytes_per_launch": 268630016 + 3099392, "num_splits": 19,
-        "src_sha256": "5a36c3ee5674bdec33faaf6802177ab69a39fc187404b08f1ab499744c1dd875"},
+        "bytes_per_launch": 268622848 + 2941696, "num_splits": 19,
+        "src_sha256": "ac856a1d1ec171fac9f81390d4f499a8cb11536ad6db60788094c76c2afb0db9"},
 }
 
 
