@@ -571,13 +571,18 @@ __global__ void __launch_bounds__(Tc05F8Cfg<NCP, CPT>::kThreads, 1)
                 fma2(y[0], y[1], xs[4 * i4], xs[4 * i4 + 1], sl2, sl2, -mv[0], -mv[1]);
                 fma2(y[2], y[3], xs[4 * i4 + 2], xs[4 * i4 + 3], sl2, sl2, -mv[2], -mv[3]);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int i = 4 * i4 + e;
-                    // columns that do not count this token get -inf (exponential 0)
-                    xs[i] = ((vmask >> i) & 1) ? y[e] : -INFINITY;
-                    xm[e] = fmaxf(xm[e], xs[i]);
-                }
+                for (int e = 0; e < 4; ++e) xs[4 * i4 + e] = y[e];
             }
+            // columns that do not count this token get -inf (exponential 0); with 16
+            // columns a thread, a stage whose tokens all count in every column (the
+            // usual one) skips this (with 8 the warp vote measured slower than the selects)
+            constexpr uint32_t kAll = CPT == 32 ? 0xffffffffu : (1u << CPT) - 1u;
+            if (CPT < 16 || !__all_sync(0xffffffffu, vmask == kAll)) {
+#pragma unroll
+                for (int i = 0; i < CPT; ++i) xs[i] = ((vmask >> i) & 1) ? xs[i] : -INFINITY;
+            }
+#pragma unroll
+            for (int i = 0; i < CPT; ++i) xm[i & 3] = fmaxf(xm[i & 3], xs[i]);
             over = (fmaxf(fmaxf(xm[0], xm[1]), fmaxf(xm[2], xm[3])) > C::kRescaleLog2) || (vmask & mneg);
         }
         const bool any_over = softmax_any<NT>(over);  // the stage's barrier reduction
