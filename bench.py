@@ -48,15 +48,15 @@ NCU_TRAFFIC = {
         "src_sha256": "59386695fba4fc9262837d650de324d47d9e706eacf4aa39fcf9eb83df155df7"},
     # tcgen05 kernel, the same layer with 8 and 16 queries per row (32 and 64 columns per KV head)
     ("tc05", "llama3.1-8b-decode-layer", 8): {
-        "bytes_per_launch": 537053952 + 2729216, "num_splits": 19,
-        "src_sha256": "4e80c86264a90901f84252c725cb7cc2f4e95a1a86b7d87693c965a085a763de"},
+        "bytes_per_launch": 537053184 + 2904576, "num_splits": 19,
+        "src_sha256": "6b42c244e43dffc6cee419098b96a94dbf6d22e6014f23faf9cf8d66e4df2a7c"},
     ("tc05", "llama3.1-8b-decode-layer", 16): {
-        "bytes_per_launch": 537137920 + 3182592, "num_splits": 19,
-        "src_sha256": "4e80c86264a90901f84252c725cb7cc2f4e95a1a86b7d87693c965a085a763de"},
+        "bytes_per_launch": 537136896 + 3225600, "num_splits": 19,
+        "src_sha256": "6b42c244e43dffc6cee419098b96a94dbf6d22e6014f23faf9cf8d66e4df2a7c"},
     # tcgen05 FP8 kernel, the same layer's E4M3 cache with 8 queries per row (32 columns per KV head)
     ("fp8tc05", "llama3.1-8b-decode-layer", 8): {
-        "bytes_per_launch": 268622848 + 2941696, "num_splits": 19,
-        "src_sha256": "ac856a1d1ec171fac9f81390d4f499a8cb11536ad6db60788094c76c2afb0db9"},
+        "bytes_per_launch": 268623616 + 3101184, "num_splits": 19,
+        "src_sha256": "03c9e5841447fc6e62bcba4e5ee62501fc12c96adc71f126dbbe7477e222b964"},
 }
 
 
