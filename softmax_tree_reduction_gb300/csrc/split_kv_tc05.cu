@@ -433,7 +433,7 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP, CPT>::kThreads, 1)
             // offsets from the references (0 where there is none yet); a logit past
             // its reference by more than the margin, or a column's first logits,
             // move the reference (rare)
-            float xm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            float xm[2] = {-INFINITY, -INFINITY};
 #pragma unroll
             for (int i4 = 0; i4 < CPT / 4; ++i4) {
                 const float4 m4 = *reinterpret_cast<const float4*>(m_fin + c_base + 4 * i4);
@@ -452,8 +452,8 @@ __global__ void __launch_bounds__(Tc05Cfg<NCP, CPT>::kThreads, 1)
                 for (int i = 0; i < CPT; ++i) xs[i] = ((vmask >> i) & 1) ? xs[i] : -INFINITY;
             }
 #pragma unroll
-            for (int i = 0; i < CPT; ++i) xm[i & 3] = fmaxf(xm[i & 3], xs[i]);
-            over = (fmaxf(fmaxf(xm[0], xm[1]), fmaxf(xm[2], xm[3])) > C::kRescaleLog2) || (vmask & mneg);
+            for (int i = 0; i < CPT; i += 2) xm[(i >> 1) & 1] = max3(xm[(i >> 1) & 1], xs[i], xs[i + 1]);
+            over = (fmaxf(xm[0], xm[1]) > C::kRescaleLog2) || (vmask & mneg);
         }
         const bool any_over = softmax_any<NT>(over);  // the stage's barrier reduction
         if (*const_cast<volatile int*>(fail_rec)) {

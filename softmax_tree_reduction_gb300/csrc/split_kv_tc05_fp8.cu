@@ -562,7 +562,7 @@ __global__ void __launch_bounds__(Tc05F8Cfg<NCP, CPT>::kThreads, 1)
             vmask = tok_ok ? gmask : 0u;
             const int d = tok0 + t - causal_from + 1;  // <= 0 before the diagonal (and without causality)
             if (d > 0) vmask &= cm[min(d, 15)];
-            float xm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            float xm[2] = {-INFINITY, -INFINITY};
 #pragma unroll
             for (int i4 = 0; i4 < CPT / 4; ++i4) {
                 const float4 m4 = *reinterpret_cast<const float4*>(m_fin + c_base + 4 * i4);
@@ -582,8 +582,8 @@ __global__ void __launch_bounds__(Tc05F8Cfg<NCP, CPT>::kThreads, 1)
                 for (int i = 0; i < CPT; ++i) xs[i] = ((vmask >> i) & 1) ? xs[i] : -INFINITY;
             }
 #pragma unroll
-            for (int i = 0; i < CPT; ++i) xm[i & 3] = fmaxf(xm[i & 3], xs[i]);
-            over = (fmaxf(fmaxf(xm[0], xm[1]), fmaxf(xm[2], xm[3])) > C::kRescaleLog2) || (vmask & mneg);
+            for (int i = 0; i < CPT; i += 2) xm[(i >> 1) & 1] = max3(xm[(i >> 1) & 1], xs[i], xs[i + 1]);
+            over = (fmaxf(xm[0], xm[1]) > C::kRescaleLog2) || (vmask & mneg);
         }
         const bool any_over = softmax_any<NT>(over);  // the stage's barrier reduction
         if (*const_cast<volatile int*>(fail_rec)) {

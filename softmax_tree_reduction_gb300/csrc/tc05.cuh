@@ -292,6 +292,13 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, unsigned parity, int* e
     return ok != 0;
 }
 
+// Maximum of three values (NaN inputs are ignored, as by fmaxf).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // Packed two-lane FP32 arithmetic (f32x2: one instruction for two values, each
 // rounded as the scalar operation would be).
 __device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0, float c1) {
