@@ -48,15 +48,15 @@ NCU_TRAFFIC = {
         "src_sha256": "59386695fba4fc9262837d650de324d47d9e706eacf4aa39fcf9eb83df155df7"},
     # tcgen05 kernel, the same layer with 8 and 16 queries per row (32 and 64 columns per KV head)
     ("tc05", "llama3.1-8b-decode-layer", 8): {
-        "bytes_per_launch": 537053184 + 2904576, "num_splits": 19,
-        "src_sha256": "6b42c244e43dffc6cee419098b96a94dbf6d22e6014f23faf9cf8d66e4df2a7c"},
+        "bytes_per_launch": 537053696 + 2923008, "num_splits": 19,
+        "src_sha256": "7b2271b50877b0922013af7bf995687381b9919b45172c56d16581a9ad887131"},
     ("tc05", "llama3.1-8b-decode-layer", 16): {
-        "bytes_per_launch": 537136896 + 3225600, "num_splits": 19,
-        "src_sha256": "6b42c244e43dffc6cee419098b96a94dbf6d22e6014f23faf9cf8d66e4df2a7c"},
+        "bytes_per_launch": 537125632 + 3222016, "num_splits": 19,
+        "src_sha256": "7b2271b50877b0922013af7bf995687381b9919b45172c56d16581a9ad887131"},
     # tcgen05 FP8 kernel, the same layer's E4M3 cache with 8 queries per row (32 columns per KV head)
     ("fp8tc05", "llama3.1-8b-decode-layer", 8): {
-        "bytes_per_launch": 268623616 + 3101184, "num_splits": 19,
-        "src_sha256": "03c9e5841447fc6e62bcba4e5ee62501fc12c96adc71f126dbbe7477e222b964"},
+        "bytes_per_launch": 268646656 + 3003904, "num_splits": 19,
+        "src_sha256": "5e686e4a74a3e0766f61d2ad2a9009fcea89ac37da8bc5e2c0252ec89b010c34"},
 }
 
 
