@@ -125,18 +125,22 @@ def load_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+_WARP_LEVEL = ("common.cuh", "emit.cuh", "kernels.h", "sched.cuh", "warp_mma.cuh")
+_TCGEN05 = ("common.cuh", "kernels.h", "sched.cuh", "tc05.cuh")
+# Per kernel family: its own source first, then every header it includes
+# (directly or through another header), under softmax_tree_reduction_gb300/csrc.
+KERNEL_SOURCES = {"mma": ("split_kv_mma.cu",) + _WARP_LEVEL,
+                  "fp8": ("split_kv_fp8.cu",) + _WARP_LEVEL,
+                  "fma": ("split_kv_fma.cuh", "common.cuh", "emit.cuh", "kernels.h", "sched.cuh"),
+                  "tc05": ("split_kv_tc05.cu",) + _TCGEN05,
+                  "fp8tc05": ("split_kv_tc05_fp8.cu",) + _TCGEN05}
+
+
 def kernel_source_hash(kernel):
     """SHA-256 of the sources a kernel family is compiled from (its own file and
     the headers it includes) and of the host code that configures its launch."""
-    warp_level = ("common.cuh", "emit.cuh", "kernels.h", "sched.cuh", "warp_mma.cuh")
-    tcgen05 = ("common.cuh", "kernels.h", "sched.cuh", "tc05.cuh")
-    files = {"mma": ("split_kv_mma.cu",) + warp_level,
-             "fp8": ("split_kv_fp8.cu",) + warp_level,
-             "fma": ("split_kv_fma.cuh", "common.cuh", "emit.cuh", "kernels.h", "sched.cuh"),
-             "tc05": ("split_kv_tc05.cu",) + tcgen05,
-             "fp8tc05": ("split_kv_tc05_fp8.cu",) + tcgen05}[kernel]
     h = hashlib.sha256()
-    for f in files + ("api.cu",):
+    for f in KERNEL_SOURCES[kernel] + ("api.cu",):
         with open(os.path.join(ROOT, "softmax_tree_reduction_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
