@@ -113,8 +113,9 @@ typedef struct {
 typedef enum {
     TA_KERNEL_AUTO = 0,  /* tensor-core path when it applies, else FMA: TA_KERNEL_TC05 for
                             BF16 q at head_dim 128 with more than 16 columns (query heads x
-                            queries) per KV head, unless TA_FLAG_CLUSTER_MERGE is set; else
-                            TA_KERNEL_MMA where it applies */
+                            queries) per KV head, on a BF16 cache (up to 64 columns) or an
+                            E4M3 cache (up to 32), unless TA_FLAG_CLUSTER_MERGE is set;
+                            else TA_KERNEL_MMA where it applies */
     TA_KERNEL_FMA = 1,   /* FP32 FMA on CUDA cores; every dtype combination */
     TA_KERNEL_MMA = 2,   /* warp-level tensor-core mma: BF16 q and kv (Hq/Hkv <= 16, or <= 64
                             at head_dim 128), or BF16 q with an E4M3 cache (Hq/Hkv <= 16,
