@@ -180,11 +180,24 @@ def test_combine_argument_errors(ta):
 
 
 def test_binding_refuses_cpu_tensors(ta):
+    """Every entry point refuses host tensors before any work: there is no CPU
+    fallback on the product path."""
     import torch
     q = torch.zeros(1, 1, 64)
     k = torch.zeros(1, 1, 8, 64)
-    with pytest.raises(ValueError):
-        ta.tree_attn_decode(q, k, k, torch.zeros(1, dtype=torch.int32))
+    sl = torch.zeros(1, dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA device"):
+        ta.tree_attn_decode(q, k, k, sl)
+    with pytest.raises(ValueError, match="CUDA device"):
+        ta.tree_attn_decode_multi(q[:, :, None, :], k, k, sl)
+    pages = torch.zeros(4, 16, 1, 64)
+    bt = torch.zeros(1, 4, dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA device"):
+        ta.tree_attn_decode_paged(q, pages, pages, bt, sl)
+    with pytest.raises(ValueError, match="CUDA device"):
+        ta.tree_attn_decode_noalloc(q, k, k, sl, torch.zeros(1, 1, 64))
+    with pytest.raises(ValueError, match="CUDA device"):
+        ta.tree_attn_combine(torch.zeros(1, 1, 2, 64), torch.zeros(1, 1, 2), torch.zeros(1, 1, 2))
 
 
 def test_launch_count(ta):
